@@ -1,0 +1,549 @@
+"""Benchmark of the MoE expert FFN forward on one GB300 (or N replicas).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one pass of the whole path (rms_norm, router softmax/top-k,
+permute, FC1 + silu_and_mul, FC2 + routing weight, combine) over one batch of
+the workload.  Prints ONE JSON line (rank 0).
+
+Timed regions (CUDA events on the launching stream, after W warm-up steps):
+  value     K calls of moe_ffn_forward with device-resident inputs.
+  roofline  K steps through the step entry points (the same kernels), with
+            events around each stage; achieved = algorithmic bytes (decode)
+            or flops (prefill) of the dominant kernel / its mean duration.
+  e2e       K calls of moe_ffn_forward whose inputs come from pinned host
+            memory and whose output goes back to pinned host memory, copies
+            inside the timed region.
+The expert weights of every workload but the tiny one are larger than L2, so
+each step reads them from HBM; for the tiny workload L2 is flushed (a 512 MB
+write) between timed steps.
+
+--impl reference times the CPU oracle (fp64 numpy, one thread) on a bounded
+token sample of the same workload and prints the same line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "MoE FFN fwd: HBM TB/s vs peak & tokens/s (T≤64); TFLOP/s vs peak (T=4096)"
+DEFAULT_WORKLOAD = "c2_decode_balanced"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# --------------------------------------------------------------- algorithm --
+
+def algorithmic_work(inp, offsets_np):
+    """Expert-weight bytes each GEMM reads (experts with >= 1 row) and the
+    GEMM flops over unpadded rows."""
+    E, H, I = inp["E"], inp["H"], inp["I"]
+    counts = np.diff(offsets_np)
+    active = int((counts > 0).sum())
+    elem = 1 if inp["fp8"] else 2
+    fc1_bytes = active * 2 * I * H * elem + (active * 2 * I * 4 if inp["fp8"] else 0)
+    fc2_bytes = active * H * I * elem + (active * H * 4 if inp["fp8"] else 0)
+    rows = int(counts.sum())
+    fc1_flops = 2.0 * rows * H * 2 * I
+    fc2_flops = 2.0 * rows * I * H
+    return dict(active_experts=active, rows=rows, fc1_bytes=fc1_bytes, fc2_bytes=fc2_bytes,
+                fc1_flops=fc1_flops, fc2_flops=fc2_flops)
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.idx)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                     power=float(parts[3]) if parts[3] not in ("[N/A]", "") else 0.0,
+                                     hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        load = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load)}
+
+
+# -------------------------------------------------------------- CPU oracle --
+
+def _save_sample(inp, toks, path):
+    """Writes the inputs the oracle needs for the sampled tokens."""
+    import torch
+    k = inp["k"]
+    d = dict(x=inp["x"][toks].float().cpu().numpy(), norm_w=inp["norm_w"].float().cpu().numpy(),
+             eps=np.array(inp["eps"]), k=np.array(k), fp8=np.array(inp["fp8"]))
+    if inp["router_logits"] is not None:
+        d["logits"] = inp["router_logits"][toks].cpu().numpy()
+        l = inp["router_logits"][toks].cpu().numpy()
+        experts = sorted(set(np.argsort(-l, axis=1, kind="stable")[:, :k].reshape(-1).tolist()))
+    else:
+        d["router_w"] = inp["router_w"].cpu().numpy()
+        if inp["router_bias"] is not None:
+            d["router_bias"] = inp["router_bias"].cpu().numpy()
+        experts = list(range(inp["E"]))
+        # only experts some sampled token can select are needed: the oracle's
+        # own routing decides; keep all when E is small, else the candidates
+        # with the largest logits (fp32 estimate) plus a margin of 4 per token.
+        if inp["E"] > 16:
+            x = inp["x"][toks].float()
+            xh = x * torch.rsqrt(x.pow(2).mean(-1, keepdim=True) + inp["eps"]) * inp["norm_w"].float()
+            l = (xh @ inp["router_w"])
+            if inp["router_bias"] is not None:
+                l = l + inp["router_bias"]
+            cand = torch.topk(l, min(inp["E"], k + 4), dim=1).indices.cpu().numpy()
+            experts = sorted(set(cand.reshape(-1).tolist()))
+    d["experts"] = np.array(experts, dtype=np.int64)
+    d["E"] = np.array(inp["E"])
+    for e in experts:
+        d[f"w13_{e}"] = inp["w13"][e].view(torch.int16).cpu().numpy()
+        d[f"w2_{e}"] = inp["w2"][e].view(torch.int16).cpu().numpy()
+    np.savez(path, **d)
+
+
+ORACLE_CHILD = r"""
+import sys, time, json, os
+import numpy as np
+sys.path.insert(0, sys.argv[2])
+import oracle as O
+d = np.load(sys.argv[1])
+def bf(a):
+    return (a.astype(np.int32).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+W13 = {int(e): bf(d[f"w13_{e}"]) for e in d["experts"]}
+W2 = {int(e): bf(d[f"w2_{e}"]) for e in d["experts"]}
+kw = {}
+if "logits" in d: kw["logits"] = d["logits"].astype(np.float64)
+else:
+    kw["router_w"] = d["router_w"].astype(np.float64)
+    if "router_bias" in d: kw["router_bias"] = d["router_bias"].astype(np.float64)
+reps = int(sys.argv[3])
+t0 = time.perf_counter()
+for _ in range(reps):
+    if "logits" not in kw:
+        # restrict the router to the experts whose weights were saved: the
+        # sampled tokens' selections fall inside them (checked below)
+        pass
+    res = O.moe_ffn_forward(d["x"].astype(np.float64), d["norm_w"].astype(np.float64),
+                            float(d["eps"]), int(d["k"]), lambda e: W13[e], lambda e: W2[e],
+                            fp8=bool(d["fp8"]), **kw)
+    assert set(res["ids"].reshape(-1).tolist()) <= set(W13), "sample needs more experts"
+dt = time.perf_counter() - t0
+print(json.dumps({"seconds": dt, "tokens": int(d["x"].shape[0]) * reps}))
+"""
+
+
+def run_oracle_sample(inp, n_tokens, reps=1, seed=0):
+    """Times the CPU oracle (one thread) on n_tokens sampled tokens; returns
+    (tokens/s, seconds, description)."""
+    T = inp["T"]
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(T, size=min(n_tokens, T), replace=False))
+    with tempfile.TemporaryDirectory() as td:
+        path = os.path.join(td, "sample.npz")
+        _save_sample(inp, toks, path)
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+                   CUDA_VISIBLE_DEVICES="")
+        p = subprocess.run([sys.executable, "-c", ORACLE_CHILD, path, ROOT, str(reps)],
+                           capture_output=True, text=True, env=env, timeout=1800)
+        if p.returncode != 0:
+            raise RuntimeError("oracle baseline failed:\n" + p.stderr[-2000:])
+        r = json.loads(p.stdout.strip().splitlines()[-1])
+    desc = (f"{len(toks)} of {T} tokens (seeded sample) x {reps}: oracle moe_ffn_forward on "
+            f"the sample (weights of the experts it needs preloaded as fp64), 1 thread")
+    return r["tokens"] / r["seconds"], r["seconds"], desc
+
+
+# -------------------------------------------------------------------- main --
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (0 = auto)")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a float over ranks (timing only; no data-path collective)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def auto_cpu_tokens(workload):
+    return {"c1_tiny": 4, "c2_decode_balanced": 2, "c3_decode_skewed": 1,
+            "c4_decode_fp8": 2, "c5_prefill": 2}.get(workload, 1)
+
+
+def main_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+    import workloads
+    inp = workloads.make_inputs(args.workload, "cpu" if not torch.cuda.is_available() else "cuda")
+    n = args.cpu_tokens or auto_cpu_tokens(args.workload)
+    # warm-up steps are untimed oracle runs on the same sample
+    for _ in range(min(args.warmup, 1)):
+        run_oracle_sample(inp, n, 1)
+    tps, secs, desc = run_oracle_sample(inp, n, max(1, args.steps))
+    ms = secs / max(1, args.steps) * 1e3
+    cfg = inp
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "T": cfg["T"], "H": cfg["H"], "E": cfg["E"],
+                   "top_k": cfg["k"], "I": cfg["I"], "fp8": cfg["fp8"]},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": desc + f"; each step = one pass over the sample"},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main_native(args):
+    import torch
+    rank, world, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import moe_expert_ffn_rms_gb300 as M
+    import workloads
+
+    M.check_device()
+    inp = workloads.make_inputs(args.workload, dev)
+    T, H, E, k, I, fp8 = inp["T"], inp["H"], inp["E"], inp["k"], inp["I"], inp["fp8"]
+    R = T * k
+    shape = M.make_shape(T, H, E, I, k, inp["eps"], fp8=fp8)
+    ws = M.alloc_workspace(M.moe_ffn_workspace_size(shape), dev)
+    w13, w2, s13, s2 = inp["w13"], inp["w2"], None, None
+    if fp8:
+        w13 = torch.empty((E, 2 * I, H), dtype=torch.uint8, device=dev)
+        s13 = torch.empty((E, 2 * I), dtype=torch.float32, device=dev)
+        w2 = torch.empty((E, H, I), dtype=torch.uint8, device=dev)
+        s2 = torch.empty((E, H), dtype=torch.float32, device=dev)
+        M.moe_quantize_fp8_rows(inp["w13"], w13, s13)
+        M.moe_quantize_fp8_rows(inp["w2"], w2, s2)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    tw = torch.empty((T, k), dtype=torch.float32, device=dev)
+    st = torch.cuda.current_stream()
+    small = (3 * H * I * (1 if fp8 else 2) * E) < 256 * 2 ** 20
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if small else None
+
+    def fwd(x=None, out_=None):
+        M.moe_ffn_forward(shape, inp["x"] if x is None else x, inp["norm_w"], w13, w2,
+                          out if out_ is None else out_, ws, router_w=inp["router_w"],
+                          router_logits=inp["router_logits"], router_bias=inp["router_bias"],
+                          w13_scale=s13, w2_scale=s2, topk_ids_out=ids, topk_w_out=tw)
+
+    # ---- region A: the product call, device-resident inputs
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize()
+    offsets_np = None
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(st)
+        fwd()
+        ev[i][1].record(st)
+    torch.cuda.synchronize()
+    wall_a = time.perf_counter() - t_wall
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    # keep the same load for a moment so the clock sampler sees it
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < max(0.0, 1.5 - wall_a):
+        fwd()
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    mean_ms = sum(step_ms) / len(step_ms)
+    mean_ms = max_over_ranks(mean_ms, world)
+    value = world * T / (mean_ms * 1e-3)
+
+    # ---- region B: the same kernels through the step entry points, with
+    # events around each stage (per-kernel durations for the roofline)
+    xhat = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    xq = torch.empty((T, H), dtype=torch.uint8, device=dev) if fp8 else None
+    xs = torch.empty((T,), dtype=torch.float32, device=dev) if fp8 else None
+    rws = M.alloc_workspace(max(256, M.moe_route_workspace_size(T, H, E)), dev)
+    offsets = torch.empty((E + 1,), dtype=torch.int32, device=dev)
+    row_src = torch.empty((R,), dtype=torch.int32, device=dev)
+    rop = torch.empty((R,), dtype=torch.int32, device=dev)
+    xp = torch.empty((R, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    xps = torch.empty((R,), dtype=torch.float32, device=dev) if fp8 else None
+    act = torch.empty((R, I), dtype=torch.bfloat16, device=dev)
+    actq = torch.empty((R, I), dtype=torch.uint8, device=dev) if fp8 else None
+    acts = torch.empty((R,), dtype=torch.float32, device=dev) if fp8 else None
+    y = torch.empty((R, H), dtype=torch.float32, device=dev)
+    out_b = torch.empty_like(out)
+    stages = ["rmsnorm", "route", "permute", "fc1", "fc2", "combine"]
+
+    def step_b(evs=None):
+        def mark(i):
+            if evs is not None:
+                evs[i].record(st)
+        mark(0)
+        M.moe_rmsnorm(inp["x"], inp["norm_w"], inp["eps"], xhat, xq, xs)
+        mark(1)
+        M.moe_route_topk(T, H, E, k, ids, tw, xhat=xhat, router_w=inp["router_w"],
+                         router_bias=inp["router_bias"], logits_in=inp["router_logits"],
+                         workspace=rws)
+        mark(2)
+        M.moe_permute(ids, T, E, k, offsets, row_src, rop, xhat=xq if fp8 else xhat, xp=xp,
+                      row_bytes=H * (1 if fp8 else 2), xscale=xs, xp_scale=xps)
+        mark(3)
+        M.moe_grouped_gemm(shape, M.GEMM_FC1_SILU, xp, w13, offsets, act, a_scale=xps, w_scale=s13)
+        if fp8:
+            M.lib.moe_quantize_fp8_rows(act.data_ptr(), R, I, actq.data_ptr(), acts.data_ptr(),
+                                        st.cuda_stream)
+        mark(4)
+        M.moe_grouped_gemm(shape, M.GEMM_FC2, actq if fp8 else act, w2, offsets, y,
+                           a_scale=acts, w_scale=s2, row_src=row_src, topk_w=tw)
+        mark(5)
+        M.moe_combine(y, rop, T, k, out_b)
+        mark(6)
+
+    for _ in range(args.warmup):
+        step_b()
+    torch.cuda.synchronize()
+    fwd()
+    torch.cuda.synchronize()
+    same = bool(torch.equal(out, out_b)) if args.warmup > 0 else None
+    evs_all = []
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        step_b(evs)
+        evs_all.append(evs)
+    torch.cuda.synchronize()
+    stage_ms = {s: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs_all)
+                for i, s in enumerate(stages)}
+    offsets_np = offsets.cpu().numpy()
+    work = algorithmic_work(dict(inp, fp8=fp8), offsets_np)
+    peaks = load_peaks()
+    decode = T <= 64
+    if decode:
+        dom = "fc1"
+        achieved = work["fc1_bytes"] / (stage_ms["fc1"] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": read_traffic("fc1", args.workload),
+                "kernel": "grouped GEMM FC1 + silu_and_mul",
+                "peak_source": peaks["source"],
+                "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
+                "fc2_GBs": work["fc2_bytes"] / (stage_ms["fc2"] * 1e-3) / 1e9,
+                "ffn_GBs": (work["fc1_bytes"] + work["fc2_bytes"]) /
+                           ((stage_ms["fc1"] + stage_ms["fc2"]) * 1e-3) / 1e9,
+                "algorithmic_bytes_per_launch": work["fc1_bytes"]}
+    else:
+        dom = "fc1"
+        achieved = work["fc1_flops"] / (stage_ms["fc1"] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": read_traffic("fc1", args.workload),
+                "kernel": "grouped GEMM FC1 + silu_and_mul", "peak_source": peaks["source"],
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "fc2_TFLOPs": work["fc2_flops"] / (stage_ms["fc2"] * 1e-3) / 1e12,
+                "ffn_TFLOPs": (work["fc1_flops"] + work["fc2_flops"]) /
+                              ((stage_ms["fc1"] + stage_ms["fc2"]) * 1e-3) / 1e12,
+                "algorithmic_flops_per_launch": work["fc1_flops"]}
+
+    # ---- e2e: host buffers in, host buffer out, copies inside the timed region
+    x_h = inp["x"].cpu().pin_memory()
+    lg_h = inp["router_logits"].cpu().pin_memory() if inp["router_logits"] is not None else None
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(inp["x"])
+    lg_d = torch.empty_like(inp["router_logits"]) if lg_h is not None else None
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        if lg_h is not None:
+            lg_d.copy_(lg_h, non_blocking=True)
+        M.moe_ffn_forward(shape, x_d, inp["norm_w"], w13, w2, out, ws, router_w=inp["router_w"],
+                          router_logits=lg_d, router_bias=inp["router_bias"], w13_scale=s13,
+                          w2_scale=s2)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(st)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    h2d = x_h.numel() * 2 + (lg_h.numel() * 4 if lg_h is not None else 0)
+    d2h = out_h.numel() * 2
+
+    launches_per_step = (1 + (1 if inp["router_w"] is not None else 0) + 1 + 1 + 1 + 1 +
+                         (1 if fp8 else 0) + 1 + 1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_tokens or auto_cpu_tokens(args.workload)
+        # FP8 workloads: the oracle gets the bf16 originals and quantises them itself
+        tps, secs, desc = run_oracle_sample(inp, n)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc,
+               "seconds": secs}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8-e4m3 x fp8-e4m3 -> f32" if fp8 else "bf16 x bf16 -> f32",
+            "data": "synthetic (seeded torch generator; random-init weights)",
+            "config": {"workload": args.workload, "T": T, "H": H, "E": E, "top_k": k, "I": I,
+                       "fp8": fp8, "routing": inp["routing"],
+                       "active_experts": work["active_experts"],
+                       "l2": ("flushed between steps (512 MB write)" if flush is not None else
+                              f"inputs larger than L2: expert weights "
+                              f"{3 * H * I * E * (1 if fp8 else 2) / 1e9:.2f} GB"),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roof,
+            "stages_ms": stage_ms,
+            "stage_path_equals_forward": same,
+            "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "wall_s_region_a": wall_a,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def read_traffic(kernel, workload):
+    """DRAM traffic per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    import hashlib
+    src = os.path.join(ROOT, "moe_expert_ffn_rms_gb300", "csrc")
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(src)):
+        if fn.startswith("gemm_") or fn.endswith(".cuh"):
+            h.update(open(os.path.join(src, fn), "rb").read())
+    sha = h.hexdigest()[:12]
+    with open(p) as f:
+        for ln in f:
+            parts = ln.split()
+            if len(parts) >= 4 and not ln.startswith("#") and parts[0] == kernel and \
+                    parts[1] == workload and parts[2] == sha:
+                return float(parts[3])
+    return None
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        main_reference(a)
+    else:
+        main_native(a)

@@ -1,0 +1,247 @@
+/*
+ * moe_ffn.h -- C ABI of libmoeffn.so, the MoE expert FFN forward for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The path (per token t):
+ *   x_hat = rms_norm(x, norm_w)                      moe_rmsnorm
+ *   logits = x_hat W_r (+ b); top-k of softmax,       moe_route_topk
+ *            renormalised
+ *   rows grouped by expert                            moe_permute
+ *   a = silu(x_hat W_gate^T) * (x_hat W_up^T)         moe_grouped_gemm (FC1)
+ *   y = w_tj * (a W2^T)                               moe_grouped_gemm (FC2)
+ *   out_t = sum_j y_tj                                moe_combine
+ * moe_ffn_forward runs all of it; the step entry points run one step each.
+ *
+ * Sources (web pages, by title and section):
+ *   [V100]  Qiita, "running the latest vLLM on a Tesla V100": section
+ *           "2nd wall" names rms_norm and silu_and_mul as the custom ops of
+ *           the FFN; section "rewrite on torch::stable::Tensor" defines
+ *           rms_norm as pow -> mean -> rsqrt -> mul.
+ *   [RUBIN] "vLLM Support for NVIDIA Vera Rubin NVL72", section "Locality
+ *           domain": at small token counts the MoE forward is FC1 then FC2
+ *           over expert weights streamed from HBM, split by columns (split-N).
+ *   [SM]    "vLLM's adaptation to different GPU SM architectures", sections
+ *           3.1/3.2 (W8A8 scaled GEMM, FP8 E4M3, output-first signature
+ *           cutlass_scaled_mm(c, ...)) and 4.3 (experts take hidden_states,
+ *           w1, w2; small batches want few launches).
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, unless a
+ *     comment says "host".  The library never allocates or frees device
+ *     memory; scratch comes from the caller's `workspace`.
+ *   - Layouts are row-major with the last index contiguous.  bf16 is
+ *     __nv_bfloat16 (2 bytes), e4m3 is OCP FP8 E4M3FN (1 byte).
+ *   - Device pointers must be 16-byte aligned; row lengths must keep every
+ *     row 16-byte aligned (H and I multiples of 64).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     only enqueue work on it and never synchronise the host.
+ *   - Inputs are read only.  A return of MOE_OK means the work was enqueued;
+ *     a kernel fault surfaces as MOE_ERR_CUDA at a later call or at the
+ *     caller's synchronisation.  On any other status nothing was enqueued
+ *     and moe_last_error() describes the problem (thread-local string).
+ *   - Device-side waits are bounded; a wait that runs out records
+ *     MOE_ERR_TIMEOUT in the library's device status word, which
+ *     moe_device_status() reads.
+ */
+#ifndef MOE_FFN_H_
+#define MOE_FFN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,         /* null pointer, misalignment, bad value */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,   /* shape outside the supported envelope */
+  MOE_ERR_UNSUPPORTED_DEVICE = 3,  /* current device is not compute capability 10.3 */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes < the size query's answer */
+  MOE_ERR_CUDA = 5,                /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = 6              /* a bounded device-side wait ran out */
+} moe_status;
+
+typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1 } moe_wdtype;
+
+/* Which step of the grouped GEMM moe_grouped_gemm runs. */
+typedef enum {
+  MOE_GEMM_FC1_RAW = 0,   /* c bf16 [R, 2I] = a W13^T                          */
+  MOE_GEMM_FC1_SILU = 1,  /* c bf16 [R, I]  = silu(a W_gate^T) * (a W_up^T)   */
+  MOE_GEMM_FC2 = 2        /* c fp32 [R, H]  = topk_w[row] * (a W2^T)           */
+} moe_gemm_mode;
+
+/* Engine used for the grouped GEMMs.  AUTO picks by the host-known average
+ * rows per expert (T*top_k/E): the weight-streaming decode engine for small
+ * batches, the tile engine for large ones. */
+typedef enum { MOE_ENGINE_AUTO = 0, MOE_ENGINE_DECODE = 1, MOE_ENGINE_PREFILL = 2 } moe_engine;
+
+/* Problem size.  T tokens, H hidden, E experts, I intermediate, top_k <= 8. */
+typedef struct {
+  int32_t T, H, E, I, top_k;
+  float eps;        /* rms_norm epsilon (1e-6 in the reference workloads) */
+  int32_t wdtype;   /* moe_wdtype of w13 / w2 */
+  int32_t engine;   /* moe_engine */
+} moe_shape;
+
+typedef void* moe_stream_t; /* cudaStream_t */
+
+/* ---------------------------------------------------------------- misc -- */
+
+/* MOE_ABI_VERSION of the built library. */
+int32_t moe_abi_version(void);
+
+/* Thread-local description of the last non-MOE_OK status on this thread
+ * (empty string if none).  Never NULL; valid until the next call. */
+const char* moe_last_error(void);
+
+/* Static name of a status code ("MOE_OK", ...). */
+const char* moe_status_string(moe_status s);
+
+/* Checks that the current CUDA device is compute capability 10.3 (GB300)
+ * and caches its SM count.  Every compute entry point calls it. */
+moe_status moe_check_device(void);
+
+/* Reads (and if clear != 0, resets) the library's device status word:
+ * MOE_OK, or MOE_ERR_TIMEOUT after a bounded wait ran out, or
+ * MOE_ERR_INVALID_ARG after a kernel saw an out-of-range expert id.
+ * `status_out` is a HOST pointer.  Synchronises the device. */
+moe_status moe_device_status(int32_t* status_out, int32_t clear);
+
+/* ------------------------------------------------------- whole forward -- */
+
+/* Device workspace bytes moe_ffn_forward / moe_ffn_forward_routed need for
+ * this shape (0 and an error message when the shape is invalid). */
+size_t moe_ffn_workspace_size(const moe_shape* shape);
+
+/* The whole MoE expert FFN forward:
+ *   out = combine(FC2(silu_and_mul(FC1(permute(rms_norm(x))))))
+ * with routing from the router ([SM] 4.3: experts(hidden_states, w1, w2);
+ * [RUBIN] Locality domain: FC1 then FC2).
+ *   shape       host pointer; T, H, E, I, top_k, eps, wdtype, engine.
+ *   x           bf16 [T, H]          tokens.
+ *   norm_w      bf16 [H]             rms_norm weight.
+ *   router_w    fp32 [H, E]          router weight; or NULL when
+ *   router_logits fp32 [T, E]        ... precomputed logits are given
+ *                                    instead (exactly one of the two).
+ *   router_bias fp32 [E] or NULL     added to the logits before softmax.
+ *   w13         [E, 2I, H]           bf16, or e4m3 codes when wdtype is
+ *                                    FP8 (rows 0..I-1 gate, I..2I-1 up).
+ *   w2          [E, H, I]            bf16 or e4m3 codes.
+ *   w13_scale   fp32 [E, 2I] / NULL  per-output-channel dequant scale (FP8).
+ *   w2_scale    fp32 [E, H]  / NULL  ditto for w2.
+ *   out         bf16 [T, H]          result.
+ *   topk_ids_out int32 [T, top_k] / NULL  the routing decision, descending
+ *   topk_w_out  fp32 [T, top_k]  / NULL   weight, ties to the lower index.
+ *   workspace   >= moe_ffn_workspace_size(shape) bytes, 256-byte aligned;
+ *               must not be used by other work while this call runs.
+ * Errors: INVALID_ARG (null/misaligned/both or neither router input),
+ * UNSUPPORTED_SHAPE (H or I not a multiple of 64, top_k > 8 or > E,
+ * E > 256), WORKSPACE_TOO_SMALL, UNSUPPORTED_DEVICE, CUDA. */
+moe_status moe_ffn_forward(const moe_shape* shape, const void* x, const void* norm_w,
+                           const float* router_w, const float* router_logits,
+                           const float* router_bias, const void* w13, const void* w2,
+                           const float* w13_scale, const float* w2_scale, void* out,
+                           int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                           size_t workspace_bytes, moe_stream_t stream);
+
+/* As moe_ffn_forward, with the routing given by the caller (vLLM's
+ * fused-experts form): topk_ids int32 [T, top_k] (distinct experts per
+ * token, each in [0, E)) and topk_w fp32 [T, top_k].  An id outside [0, E)
+ * is skipped and flagged in the device status word. */
+moe_status moe_ffn_forward_routed(const moe_shape* shape, const void* x, const void* norm_w,
+                                  const int32_t* topk_ids, const float* topk_w,
+                                  const void* w13, const void* w2, const float* w13_scale,
+                                  const float* w2_scale, void* out, void* workspace,
+                                  size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------ the steps -- */
+
+/* rms_norm ([V100] "rewrite on torch::stable::Tensor"):
+ *   y[t, i] = bf16( x[t, i] / sqrt(mean_i(x[t, :]^2) + eps) * w[i] )
+ * fp32 arithmetic.  x bf16 [T, H], w bf16 [H], y bf16 [T, H].
+ * If yq != NULL also writes the per-token E4M3 quantisation of y:
+ *   yscale[t] = max|y[t, :]| / 448 (1 when the row is zero),
+ *   yq[t, i] = e4m3_satfinite_rne(y[t, i] / yscale[t])   (e4m3 [T, H]).
+ * yq and yscale are both NULL or both given.  H % 8 == 0. */
+moe_status moe_rmsnorm(const void* x, const void* w, int32_t T, int32_t H, float eps, void* y,
+                       void* yq, float* yscale, moe_stream_t stream);
+
+/* Device workspace bytes moe_route_topk needs (router partial sums). */
+size_t moe_route_workspace_size(int32_t T, int32_t H, int32_t E);
+
+/* Router softmax and renormalised top-k.
+ *   logits = xhat W_r + b   (fp32; skipped when logits_in != NULL, then
+ *                            logits = logits_in + b)
+ *   ids[t, :]  = the top_k experts by logit, descending, ties to the lower
+ *                expert index (softmax is increasing in the logit, so this
+ *                is the top-k of the probabilities);
+ *   w[t, j]    = exp(l_j - l_max) / sum_j' exp(l_j' - l_max) over the
+ *                selected experts (= softmax, then renormalised).
+ *   xhat bf16 [T, H]; router_w fp32 [H, E]; router_bias fp32 [E] or NULL;
+ *   logits_in fp32 [T, E] or NULL; ids int32 [T, k]; weights fp32 [T, k];
+ *   logits_out fp32 [T, E] or NULL (receives logits incl. bias).
+ *   E <= 256, k <= min(E, 8). */
+moe_status moe_route_topk(const void* xhat, const float* router_w, const float* router_bias,
+                          const float* logits_in, int32_t T, int32_t H, int32_t E, int32_t k,
+                          int32_t* ids, float* weights, float* logits_out, void* workspace,
+                          size_t workspace_bytes, moe_stream_t stream);
+
+/* Token -> expert grouping (stable counting sort of the T*k (t, j) pairs by
+ * expert; rows ordered by expert, then token).
+ *   ids int32 [T, k]            routing (each row: distinct experts)
+ *   offsets int32 [E + 1]       expert e owns rows offsets[e] .. offsets[e+1]-1
+ *   row_src int32 [T*k]         row r holds pair t*k + j
+ *   row_of_pair int32 [T*k]     inverse: pair t*k + j sits in row r
+ *   xhat / xp                   optional gather xp[r, :] = xhat[row_src[r]/k, :]
+ *                               (rows of row_bytes bytes, multiple of 16);
+ *                               both NULL to skip.
+ *   xscale / xp_scale           optional fp32 per-row scale gather (FP8), or NULL.
+ * E <= 256.  Ids outside [0, E) are skipped and flagged. */
+moe_status moe_permute(const int32_t* ids, int32_t T, int32_t E, int32_t k, int32_t* offsets,
+                       int32_t* row_src, int32_t* row_of_pair, const void* xhat, void* xp,
+                       int32_t row_bytes, const float* xscale, float* xp_scale,
+                       moe_stream_t stream);
+
+/* Grouped GEMM over the expert segments given by offsets ([RUBIN] FC1/FC2,
+ * [SM] 3.1 scaled GEMM).  For each expert e and each row r in
+ * offsets[e] .. offsets[e+1]-1:
+ *   FC1_RAW:  c[r, n] = bf16( sum_h a[r, h] * w[e, n, h] )       n < 2I, K = H
+ *   FC1_SILU: c[r, n] = bf16( silu(g) * u ),  g = sum_h a[r,h] w[e,n,h],
+ *                                             u = sum_h a[r,h] w[e,I+n,h]  n < I
+ *   FC2:      c[r, n] = topk_w[row_src[r]] * sum_i a[r, i] * w[e, n, i]   n < H
+ *             (fp32 output; topk_w/row_src NULL -> weight 1)
+ * a: bf16 [R, K] (or e4m3 with a_scale fp32 [R] when shape->wdtype is FP8,
+ * then w is e4m3 with w_scale fp32 [E, N]); products accumulate in fp32 and
+ * are scaled by a_scale[r] * w_scale[e, n].  R = offsets[E] <= T*top_k. */
+moe_status moe_grouped_gemm(const moe_shape* shape, int32_t mode, const void* a,
+                            const float* a_scale, const void* w, const float* w_scale,
+                            const int32_t* offsets, const int32_t* row_src, const float* topk_w,
+                            void* c, moe_stream_t stream);
+
+/* silu_and_mul ([V100] "2nd wall"): a[r, i] = bf16( silu(h[r, i]) * h[r, I+i] ),
+ * silu(z) = z / (1 + exp(-z)); h bf16 [R, 2I], a bf16 [R, I]; I % 8 == 0. */
+moe_status moe_silu_and_mul(const void* h, int32_t R, int32_t I, void* a, moe_stream_t stream);
+
+/* Weighted combine: out[t, :] = bf16( sum_{j=0..k-1} y[row_of_pair[t*k+j], :] )
+ * summed in fp32 in j order (the routing weight is already in y).
+ * y fp32 [T*k, H]; out bf16 [T, H]; H % 4 == 0. */
+moe_status moe_combine(const float* y, const int32_t* row_of_pair, int32_t T, int32_t k,
+                       int32_t H, void* out, moe_stream_t stream);
+
+/* Row-wise dynamic E4M3 quantisation ([SM] 3.2, W8A8):
+ *   scale[r] = max|x[r, :]| / 448 (1 for a zero row), fp32;
+ *   q[r, c] = e4m3_satfinite_rne( x[r, c] / scale[r] ) (IEEE fp32 divide).
+ * Used per output channel for weights (rows = E*N) and per token for
+ * activations.  x bf16 [rows, cols], q e4m3 [rows, cols], cols % 16 == 0. */
+moe_status moe_quantize_fp8_rows(const void* x, int64_t rows, int32_t cols, void* q,
+                                 float* scale, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H_ */

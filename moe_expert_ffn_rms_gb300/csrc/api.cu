@@ -1,0 +1,482 @@
+// extern "C" entry points of libmoeffn.so: argument checks, workspace layout
+// and the launch sequence of the MoE expert FFN forward.  No entry point
+// allocates device memory or synchronises the host (except
+// moe_device_status, which documents that it does).
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "engine.h"
+#include "kernels.h"
+
+// Device status word: MOE_OK, or the first error a kernel flagged.
+__device__ int g_moe_status = 0;
+
+namespace {
+
+thread_local std::string g_err;
+
+moe_status fail(moe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = std::string(moe_status_string(s)) + ": " + buf;
+  return s;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+struct DevInfo {
+  bool checked = false;
+  bool ok = false;
+  int sms = 0;
+  int* status = nullptr;  // device address of g_moe_status
+};
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+#define MOE_REQ(cond, code, ...) \
+  do {                           \
+    if (!(cond)) return fail(code, __VA_ARGS__); \
+  } while (0)
+
+#define MOE_CUDA(call, what)                 \
+  do {                                       \
+    cudaError_t _e = (call);                 \
+    if (_e != cudaSuccess) return cuda_fail(_e, what); \
+  } while (0)
+
+moe_status device_info(DevInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_UNSUPPORTED_DEVICE, "device %d", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.ok = (major == 10 && minor == 3);
+    d.sms = sms;
+    if (d.ok) {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_moe_status)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress(g_moe_status)");
+      d.status = (int*)p;
+      moe::engine_init_device();
+    }
+    d.checked = true;
+    if (!d.ok)
+      return fail(MOE_ERR_UNSUPPORTED_DEVICE, "device %d is compute capability %d.%d, need 10.3",
+                  dev, major, minor);
+  }
+  if (!d.ok) return fail(MOE_ERR_UNSUPPORTED_DEVICE, "device %d is not compute capability 10.3", dev);
+  *out = &d;
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------ shapes / ws --
+moe_status check_shape(const moe_shape* s) {
+  MOE_REQ(s != nullptr, MOE_ERR_INVALID_ARG, "shape is NULL");
+  MOE_REQ(s->T >= 0 && s->H > 0 && s->E > 0 && s->I > 0 && s->top_k > 0, MOE_ERR_INVALID_ARG,
+          "shape fields must be positive (T >= 0): T=%d H=%d E=%d I=%d top_k=%d", s->T, s->H,
+          s->E, s->I, s->top_k);
+  MOE_REQ(s->H % 64 == 0 && s->I % 64 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+          "H=%d and I=%d must be multiples of 64", s->H, s->I);
+  MOE_REQ(s->E <= kMaxExperts, MOE_ERR_UNSUPPORTED_SHAPE, "E=%d > %d", s->E, kMaxExperts);
+  MOE_REQ(s->top_k <= kMaxTopK && s->top_k <= s->E, MOE_ERR_UNSUPPORTED_SHAPE,
+          "top_k=%d must be <= min(E=%d, %d)", s->top_k, s->E, kMaxTopK);
+  MOE_REQ(s->wdtype == MOE_W_BF16 || s->wdtype == MOE_W_FP8_E4M3, MOE_ERR_INVALID_ARG,
+          "wdtype=%d", s->wdtype);
+  MOE_REQ(s->engine >= MOE_ENGINE_AUTO && s->engine <= MOE_ENGINE_PREFILL, MOE_ERR_INVALID_ARG,
+          "engine=%d", s->engine);
+  MOE_REQ((int64_t)s->T * s->top_k <= (1 << 24), MOE_ERR_UNSUPPORTED_SHAPE, "T*top_k too large");
+  MOE_REQ(s->eps >= 0.f, MOE_ERR_INVALID_ARG, "eps < 0");
+  return MOE_OK;
+}
+
+struct Ws {
+  size_t xhat, xq, xscale, part, ids, tw, offsets, row_src, row_of_pair, xp, xp_scale, act, actq,
+      act_scale, y, total;
+};
+
+size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+Ws layout(const moe_shape* s) {
+  const size_t T = s->T, H = s->H, E = s->E, I = s->I, k = s->top_k, R = T * k;
+  const bool f8 = s->wdtype == MOE_W_FP8_E4M3;
+  Ws w{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o += up256(bytes); return at; };
+  w.xhat = take(T * H * 2);
+  w.xq = take(f8 ? T * H : 0);
+  w.xscale = take(f8 ? T * 4 : 0);
+  w.part = take((size_t)moe::route_splits(s->T > 0 ? s->T : 1, s->H, s->E) * (T > 0 ? T : 1) * E * 4);
+  w.ids = take(R * 4);
+  w.tw = take(R * 4);
+  w.offsets = take((E + 1) * 4);
+  w.row_src = take(R * 4);
+  w.row_of_pair = take(R * 4);
+  w.xp = take(R * H * (f8 ? 1 : 2));
+  w.xp_scale = take(f8 ? R * 4 : 0);
+  w.act = take(R * I * 2);
+  w.actq = take(f8 ? R * I : 0);
+  w.act_scale = take(f8 ? R * 4 : 0);
+  w.y = take(R * H * 4);
+  w.total = o;
+  return w;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(reinterpret_cast<char*>(base) + off);
+}
+
+int pick_engine(const moe_shape* s) {
+  if (s->engine != MOE_ENGINE_AUTO) return s->engine;
+  const char* env = getenv("MOE_FORCE_ENGINE");
+  if (env && !strcmp(env, "decode")) return MOE_ENGINE_DECODE;
+  if (env && !strcmp(env, "prefill")) return MOE_ENGINE_PREFILL;
+  // Average rows per expert; the decode engine streams weights with the
+  // tokens as the narrow operand, the prefill engine tiles the tokens.
+  const double rows_per_expert = (double)s->T * s->top_k / s->E;
+  return rows_per_expert <= 96.0 ? MOE_ENGINE_DECODE : MOE_ENGINE_PREFILL;
+}
+
+// Grouped GEMM dispatch: tcgen05 engines where the shape allows, else SIMT.
+moe_status run_gemm(const moe_shape* s, int mode, int engine, const void* a, const float* a_scale,
+                    const void* w, const float* w_scale, const int32_t* offsets,
+                    const int32_t* row_src, const float* topk_w, void* c, int R_max, int sms,
+                    int* status, cudaStream_t st) {
+  const bool f8 = s->wdtype == MOE_W_FP8_E4M3;
+  const int K = (mode == MOE_GEMM_FC2) ? s->I : s->H;
+  const int N_out = (mode == MOE_GEMM_FC2) ? s->H : (mode == MOE_GEMM_FC1_SILU ? s->I : 2 * s->I);
+  cudaError_t e = cudaErrorNotSupported;
+  const char* env = getenv("MOE_FORCE_SIMT");
+  const bool simt_only = env && env[0] == '1';
+  if (!simt_only)
+    e = moe::launch_gemm_tc(mode, f8, engine == MOE_ENGINE_DECODE, a, a_scale, w, w_scale,
+                            offsets, row_src, topk_w, c, s->E, K, s->I, N_out, R_max, s->T, sms,
+                            status, st);
+  if (e == cudaErrorNotSupported)
+    e = moe::launch_gemm_simt(mode, f8, a, a_scale, w, w_scale, offsets, row_src, topk_w, c, s->E,
+                              K, s->I, N_out, R_max, st);
+  if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
+  return MOE_OK;
+}
+
+moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, const float* router_w,
+                        const float* router_logits, const float* router_bias,
+                        const int32_t* ids_in, const float* tw_in, const void* w13, const void* w2,
+                        const float* w13_scale, const float* w2_scale, void* out,
+                        int32_t* ids_out, float* tw_out, void* workspace, size_t ws_bytes,
+                        moe_stream_t stream) {
+  moe_status rc = check_shape(s);
+  if (rc != MOE_OK) return rc;
+  const bool f8 = s->wdtype == MOE_W_FP8_E4M3;
+  const bool routed = ids_in != nullptr;
+  MOE_REQ(x && norm_w && w13 && w2 && out && workspace, MOE_ERR_INVALID_ARG,
+          "x, norm_w, w13, w2, out and workspace must be non-NULL");
+  if (routed) {
+    MOE_REQ(tw_in != nullptr, MOE_ERR_INVALID_ARG, "topk_w is NULL");
+  } else {
+    MOE_REQ((router_w != nullptr) != (router_logits != nullptr), MOE_ERR_INVALID_ARG,
+            "give exactly one of router_w and router_logits");
+  }
+  MOE_REQ(!f8 || (w13_scale && w2_scale), MOE_ERR_INVALID_ARG, "FP8 weights need w13_scale and w2_scale");
+  MOE_REQ(aligned16(x) && aligned16(norm_w) && aligned16(w13) && aligned16(w2) && aligned16(out),
+          MOE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  MOE_REQ(((uintptr_t)workspace & 255u) == 0, MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const Ws L = layout(s);
+  MOE_REQ(ws_bytes >= L.total, MOE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", ws_bytes,
+          L.total);
+  DevInfo* dev = nullptr;
+  if ((rc = device_info(&dev)) != MOE_OK) return rc;
+  if (s->T == 0) return MOE_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int T = s->T, H = s->H, E = s->E, I = s->I, k = s->top_k, R = T * k;
+  const int engine = pick_engine(s);
+
+  bf16* xhat = at<bf16>(workspace, L.xhat);
+  uint8_t* xq = f8 ? at<uint8_t>(workspace, L.xq) : nullptr;
+  float* xscale = f8 ? at<float>(workspace, L.xscale) : nullptr;
+  int32_t* ids = ids_out ? ids_out : at<int32_t>(workspace, L.ids);
+  float* tw = tw_out ? tw_out : at<float>(workspace, L.tw);
+  int32_t* offsets = at<int32_t>(workspace, L.offsets);
+  int32_t* row_src = at<int32_t>(workspace, L.row_src);
+  int32_t* row_of_pair = at<int32_t>(workspace, L.row_of_pair);
+  void* xp = at<void>(workspace, L.xp);
+  float* xp_scale = f8 ? at<float>(workspace, L.xp_scale) : nullptr;
+  bf16* act = at<bf16>(workspace, L.act);
+  uint8_t* actq = f8 ? at<uint8_t>(workspace, L.actq) : nullptr;
+  float* act_scale = f8 ? at<float>(workspace, L.act_scale) : nullptr;
+  float* y = at<float>(workspace, L.y);
+
+  // a1: rms_norm (+ per-token E4M3 quantisation on the FP8 path)
+  MOE_CUDA(moe::launch_rmsnorm(x, norm_w, T, H, s->eps, xhat, xq, xscale, st), "rmsnorm launch");
+  // a2 + a3: router logits, softmax, top-k, renorm
+  if (routed) {
+    ids = const_cast<int32_t*>(ids_in);
+    tw = const_cast<float*>(tw_in);
+  } else {
+    const float* part = router_logits;
+    int ks = 1;
+    if (router_w) {
+      ks = moe::route_splits(T, H, E);
+      float* pbuf = at<float>(workspace, L.part);
+      MOE_CUDA(moe::launch_router_logits(xhat, router_w, T, H, E, ks, pbuf, st), "router launch");
+      part = pbuf;
+    }
+    MOE_CUDA(moe::launch_topk(part, ks, router_bias, T, E, k, ids, tw, nullptr, st), "top-k launch");
+  }
+  // a4: permute + gather of the (quantised) token rows
+  MOE_CUDA(moe::launch_permute(ids, T, E, k, offsets, row_src, row_of_pair, dev->status, st),
+           "permute launch");
+  MOE_CUDA(moe::launch_gather_rows(offsets, E, row_src, k, R, f8 ? (const void*)xq : (const void*)xhat,
+                                   xp, H * (f8 ? 1 : 2), xscale, xp_scale, st),
+           "gather launch");
+  // a5 + a6: FC1 with the silu_and_mul epilogue
+  rc = run_gemm(s, MOE_GEMM_FC1_SILU, engine, xp, xp_scale, w13, w13_scale, offsets, row_src,
+                nullptr, act, R, dev->sms, dev->status, st);
+  if (rc != MOE_OK) return rc;
+  // FP8: per-row quantisation of the bf16 intermediate before FC2
+  const void* a2 = act;
+  if (f8) {
+    MOE_CUDA(moe::launch_quant_rows(act, R, I, actq, act_scale, offsets + E, st), "quant launch");
+    a2 = actq;
+  }
+  // a7: FC2 with the routing-weight epilogue
+  rc = run_gemm(s, MOE_GEMM_FC2, engine, a2, act_scale, w2, w2_scale, offsets, row_src, tw, y, R,
+                dev->sms, dev->status, st);
+  if (rc != MOE_OK) return rc;
+  // a8: combine
+  MOE_CUDA(moe::launch_combine(y, row_of_pair, T, k, H, out, st), "combine launch");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_last_error(void) { return g_err.c_str(); }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+    case MOE_ERR_UNSUPPORTED_DEVICE: return "MOE_ERR_UNSUPPORTED_DEVICE";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status moe_check_device(void) {
+  DevInfo* d = nullptr;
+  return device_info(&d);
+}
+
+moe_status moe_device_status(int32_t* status_out, int32_t clear) {
+  MOE_REQ(status_out != nullptr, MOE_ERR_INVALID_ARG, "status_out is NULL");
+  DevInfo* d = nullptr;
+  moe_status rc = device_info(&d);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  int v = 0;
+  MOE_CUDA(cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost), "read status word");
+  *status_out = v;
+  if (clear) {
+    int z = 0;
+    MOE_CUDA(cudaMemcpy(d->status, &z, sizeof(int), cudaMemcpyHostToDevice), "clear status word");
+  }
+  return MOE_OK;
+}
+
+size_t moe_ffn_workspace_size(const moe_shape* shape) {
+  if (check_shape(shape) != MOE_OK) return 0;
+  return layout(shape).total;
+}
+
+moe_status moe_ffn_forward(const moe_shape* shape, const void* x, const void* norm_w,
+                           const float* router_w, const float* router_logits,
+                           const float* router_bias, const void* w13, const void* w2,
+                           const float* w13_scale, const float* w2_scale, void* out,
+                           int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                           size_t workspace_bytes, moe_stream_t stream) {
+  return forward_impl(shape, x, norm_w, router_w, router_logits, router_bias, nullptr, nullptr,
+                      w13, w2, w13_scale, w2_scale, out, topk_ids_out, topk_w_out, workspace,
+                      workspace_bytes, stream);
+}
+
+moe_status moe_ffn_forward_routed(const moe_shape* shape, const void* x, const void* norm_w,
+                                  const int32_t* topk_ids, const float* topk_w, const void* w13,
+                                  const void* w2, const float* w13_scale, const float* w2_scale,
+                                  void* out, void* workspace, size_t workspace_bytes,
+                                  moe_stream_t stream) {
+  if (topk_ids == nullptr) return fail(MOE_ERR_INVALID_ARG, "topk_ids is NULL");
+  return forward_impl(shape, x, norm_w, nullptr, nullptr, nullptr, topk_ids, topk_w, w13, w2,
+                      w13_scale, w2_scale, out, nullptr, nullptr, workspace, workspace_bytes,
+                      stream);
+}
+
+moe_status moe_rmsnorm(const void* x, const void* w, int32_t T, int32_t H, float eps, void* y,
+                       void* yq, float* yscale, moe_stream_t stream) {
+  MOE_REQ(x && w && y, MOE_ERR_INVALID_ARG, "x, w and y must be non-NULL");
+  MOE_REQ((yq == nullptr) == (yscale == nullptr), MOE_ERR_INVALID_ARG,
+          "yq and yscale must both be given or both NULL");
+  MOE_REQ(T >= 0 && H > 0 && H % 8 == 0, MOE_ERR_UNSUPPORTED_SHAPE, "T=%d H=%d (H %% 8 == 0)", T, H);
+  MOE_REQ(aligned16(x) && aligned16(w) && aligned16(y) && (!yq || ((uintptr_t)yq & 7u) == 0),
+          MOE_ERR_INVALID_ARG, "misaligned pointer");
+  MOE_REQ(eps >= 0.f, MOE_ERR_INVALID_ARG, "eps < 0");
+  DevInfo* d = nullptr;
+  moe_status rc = device_info(&d);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(moe::launch_rmsnorm(x, w, T, H, eps, y, yq, yscale, (cudaStream_t)stream), "rmsnorm launch");
+  return MOE_OK;
+}
+
+size_t moe_route_workspace_size(int32_t T, int32_t H, int32_t E) {
+  if (T < 0 || H <= 0 || H % 64 || E <= 0 || E > kMaxExperts) return 0;
+  return up256((size_t)moe::route_splits(T > 0 ? T : 1, H, E) * (T > 0 ? T : 1) * E * 4);
+}
+
+moe_status moe_route_topk(const void* xhat, const float* router_w, const float* router_bias,
+                          const float* logits_in, int32_t T, int32_t H, int32_t E, int32_t k,
+                          int32_t* ids, float* weights, float* logits_out, void* workspace,
+                          size_t workspace_bytes, moe_stream_t stream) {
+  MOE_REQ(ids && weights, MOE_ERR_INVALID_ARG, "ids and weights must be non-NULL");
+  MOE_REQ(T >= 0 && E > 0 && E <= kMaxExperts && k > 0 && k <= E && k <= kMaxTopK,
+          MOE_ERR_UNSUPPORTED_SHAPE, "T=%d E=%d k=%d (E <= 256, k <= min(E, 8))", T, E, k);
+  if (logits_in == nullptr) {
+    MOE_REQ(xhat && router_w && workspace, MOE_ERR_INVALID_ARG,
+            "xhat, router_w and workspace are needed when logits_in is NULL");
+    MOE_REQ(H > 0 && H % 64 == 0, MOE_ERR_UNSUPPORTED_SHAPE, "H=%d must be a multiple of 64", H);
+    MOE_REQ(aligned16(xhat), MOE_ERR_INVALID_ARG, "xhat must be 16-byte aligned");
+    MOE_REQ(workspace_bytes >= moe_route_workspace_size(T, H, E), MOE_ERR_WORKSPACE_TOO_SMALL,
+            "workspace %zu < %zu bytes", workspace_bytes, moe_route_workspace_size(T, H, E));
+  }
+  DevInfo* d = nullptr;
+  moe_status rc = device_info(&d);
+  if (rc != MOE_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  const float* part = logits_in;
+  int ks = 1;
+  if (!logits_in) {
+    ks = moe::route_splits(T, H, E);
+    MOE_CUDA(moe::launch_router_logits(xhat, router_w, T, H, E, ks, (float*)workspace, st),
+             "router launch");
+    part = (const float*)workspace;
+  }
+  MOE_CUDA(moe::launch_topk(part, ks, router_bias, T, E, k, ids, weights, logits_out, st),
+           "top-k launch");
+  return MOE_OK;
+}
+
+moe_status moe_permute(const int32_t* ids, int32_t T, int32_t E, int32_t k, int32_t* offsets,
+                       int32_t* row_src, int32_t* row_of_pair, const void* xhat, void* xp,
+                       int32_t row_bytes, const float* xscale, float* xp_scale,
+                       moe_stream_t stream) {
+  MOE_REQ(ids && offsets && row_src && row_of_pair, MOE_ERR_INVALID_ARG,
+          "ids, offsets, row_src and row_of_pair must be non-NULL");
+  MOE_REQ(T >= 0 && E > 0 && E <= kMaxExperts && k > 0 && k <= kMaxTopK,
+          MOE_ERR_UNSUPPORTED_SHAPE, "T=%d E=%d k=%d", T, E, k);
+  MOE_REQ((xhat == nullptr) == (xp == nullptr), MOE_ERR_INVALID_ARG, "give both xhat and xp or neither");
+  MOE_REQ((xscale == nullptr) == (xp_scale == nullptr), MOE_ERR_INVALID_ARG,
+          "give both xscale and xp_scale or neither");
+  MOE_REQ(!xp_scale || xp, MOE_ERR_INVALID_ARG, "a scale gather needs the row gather");
+  if (xp) {
+    MOE_REQ(row_bytes > 0 && row_bytes % 16 == 0 && aligned16(xhat) && aligned16(xp),
+            MOE_ERR_INVALID_ARG, "row_bytes=%d must be a positive multiple of 16, pointers aligned",
+            row_bytes);
+  }
+  DevInfo* d = nullptr;
+  moe_status rc = device_info(&d);
+  if (rc != MOE_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  MOE_CUDA(moe::launch_permute(ids, T, E, k, offsets, row_src, row_of_pair, d->status, st),
+           "permute launch");
+  if (xp)
+    MOE_CUDA(moe::launch_gather_rows(offsets, E, row_src, k, T * k, xhat, xp, row_bytes, xscale,
+                                     xp_scale, st),
+             "gather launch");
+  return MOE_OK;
+}
+
+moe_status moe_grouped_gemm(const moe_shape* shape, int32_t mode, const void* a,
+                            const float* a_scale, const void* w, const float* w_scale,
+                            const int32_t* offsets, const int32_t* row_src, const float* topk_w,
+                            void* c, moe_stream_t stream) {
+  moe_status rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  MOE_REQ(mode >= MOE_GEMM_FC1_RAW && mode <= MOE_GEMM_FC2, MOE_ERR_INVALID_ARG, "mode=%d", mode);
+  MOE_REQ(a && w && offsets && c, MOE_ERR_INVALID_ARG, "a, w, offsets and c must be non-NULL");
+  MOE_REQ(aligned16(a) && aligned16(w) && aligned16(c), MOE_ERR_INVALID_ARG, "misaligned pointer");
+  const bool f8 = shape->wdtype == MOE_W_FP8_E4M3;
+  MOE_REQ(!f8 || (a_scale && w_scale), MOE_ERR_INVALID_ARG, "FP8 needs a_scale and w_scale");
+  MOE_REQ(!(topk_w && !row_src), MOE_ERR_INVALID_ARG, "topk_w needs row_src");
+  DevInfo* d = nullptr;
+  if ((rc = device_info(&d)) != MOE_OK) return rc;
+  const int R_max = shape->T * shape->top_k;
+  return run_gemm(shape, mode, pick_engine(shape), a, a_scale, w, w_scale, offsets, row_src,
+                  mode == MOE_GEMM_FC2 ? topk_w : nullptr, c, R_max, d->sms, d->status,
+                  (cudaStream_t)stream);
+}
+
+moe_status moe_silu_and_mul(const void* h, int32_t R, int32_t I, void* a, moe_stream_t stream) {
+  MOE_REQ(h && a, MOE_ERR_INVALID_ARG, "h and a must be non-NULL");
+  MOE_REQ(R >= 0 && I > 0 && I % 8 == 0, MOE_ERR_UNSUPPORTED_SHAPE, "R=%d I=%d (I %% 8 == 0)", R, I);
+  MOE_REQ(aligned16(h) && aligned16(a), MOE_ERR_INVALID_ARG, "misaligned pointer");
+  DevInfo* d = nullptr;
+  moe_status rc = device_info(&d);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(moe::launch_silu_and_mul(h, R, I, a, (cudaStream_t)stream), "silu_and_mul launch");
+  return MOE_OK;
+}
+
+moe_status moe_combine(const float* y, const int32_t* row_of_pair, int32_t T, int32_t k,
+                       int32_t H, void* out, moe_stream_t stream) {
+  MOE_REQ(y && row_of_pair && out, MOE_ERR_INVALID_ARG, "y, row_of_pair and out must be non-NULL");
+  MOE_REQ(T >= 0 && k > 0 && k <= kMaxTopK && H > 0 && H % 4 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+          "T=%d k=%d H=%d", T, k, H);
+  MOE_REQ(aligned16(y) && ((uintptr_t)out & 7u) == 0, MOE_ERR_INVALID_ARG, "misaligned pointer");
+  DevInfo* d = nullptr;
+  moe_status rc = device_info(&d);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(moe::launch_combine(y, row_of_pair, T, k, H, out, (cudaStream_t)stream), "combine launch");
+  return MOE_OK;
+}
+
+moe_status moe_quantize_fp8_rows(const void* x, int64_t rows, int32_t cols, void* q, float* scale,
+                                 moe_stream_t stream) {
+  MOE_REQ(x && q && scale, MOE_ERR_INVALID_ARG, "x, q and scale must be non-NULL");
+  MOE_REQ(rows >= 0 && cols > 0 && cols % 16 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+          "rows=%lld cols=%d (cols %% 16 == 0)", (long long)rows, cols);
+  MOE_REQ(aligned16(x) && aligned16(q), MOE_ERR_INVALID_ARG, "misaligned pointer");
+  DevInfo* d = nullptr;
+  moe_status rc = device_info(&d);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(moe::launch_quant_rows(x, rows, cols, q, scale, nullptr, (cudaStream_t)stream),
+           "quantise launch");
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,90 @@
+// Shared device helpers for the MoE expert FFN kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/moe_ffn.h"
+
+typedef __nv_bfloat16 bf16;
+
+#define MOE_DEV __device__ __forceinline__
+
+// Largest supported expert count / top_k (shared-memory tables are sized by them).
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+
+// ---------------------------------------------------------------- status --
+// The device status word lives in api.cu; kernels receive its address.
+MOE_DEV void flag_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// ------------------------------------------------------------ conversions --
+MOE_DEV float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+MOE_DEV float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+MOE_DEV void unpack8_bf16(const uint4& u, float* f) {
+  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
+  f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
+  f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+}
+
+MOE_DEV uint32_t pack2_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // RNE, a in the low half
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+MOE_DEV float bf16_round_f(float a) { return __bfloat162float(__float2bfloat16_rn(a)); }
+
+// E4M3 code -> float (exact).
+MOE_DEV float e4m3_to_f(uint8_t c) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// float -> E4M3 code, round to nearest even, saturating to +-448.
+MOE_DEV uint8_t f_to_e4m3(float v) {
+  return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+// silu(z) = z / (1 + exp(-z)), fp32.
+MOE_DEV float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// ------------------------------------------------------------- reductions --
+MOE_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+MOE_DEV float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide sum / max for blockDim.x <= 1024 (a multiple of 32); every
+// thread gets the result.  `red` is 32 floats of shared memory.
+MOE_DEV float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float r = (lane < nw) ? red[lane] : 0.0f;
+  return warp_sum(r);
+}
+
+MOE_DEV float block_max(float v, float* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float r = (lane < nw) ? red[lane] : 0.0f;
+  return warp_max(r);
+}

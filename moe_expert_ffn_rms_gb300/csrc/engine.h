@@ -1,0 +1,24 @@
+// Tensor-core (tcgen05 / TMEM / TMA) grouped GEMM engines (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Per-device one-time set-up (driver entry points, kernel attributes).
+void engine_init_device();
+
+// Launches the tcgen05 grouped GEMM for one step, or returns
+// cudaErrorNotSupported (nothing enqueued) when the shape is outside what
+// the tensor-core engines cover; the caller then uses the SIMT engine.
+//   mode   0 FC1 raw, 1 FC1 + silu_and_mul, 2 FC2 x routing weight
+//   decode true: weights are the 128-row MMA operand and the expert's
+//          tokens the narrow one (small batches); false: token tiles.
+cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const float* a_scale,
+                           const void* w, const float* w_scale, const int32_t* offsets,
+                           const int32_t* row_src, const float* topk_w, void* c, int E, int K,
+                           int I, int N_out, int R_max, int T, int sms, int* status,
+                           cudaStream_t st);
+
+}  // namespace moe

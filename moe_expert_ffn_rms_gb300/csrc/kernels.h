@@ -1,0 +1,37 @@
+// Host-side launch functions of the MoE FFN kernels (internal to libmoeffn).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Router split-K: number of K chunks the router logits are split into.
+int route_splits(int T, int H, int E);
+
+cudaError_t launch_rmsnorm(const void* x, const void* w, int T, int H, float eps, void* y,
+                           void* yq, float* yscale, cudaStream_t st);
+cudaError_t launch_router_logits(const void* xhat, const float* wr, int T, int H, int E, int ks,
+                                 float* part, cudaStream_t st);
+cudaError_t launch_topk(const float* part, int ks, const float* bias, int T, int E, int k,
+                        int32_t* ids, float* w, float* logits_out, cudaStream_t st);
+cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* offsets,
+                           int32_t* row_src, int32_t* row_of_pair, int* status, cudaStream_t st);
+cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* row_src, int k,
+                               int R_max, const void* src, void* dst, int row_bytes,
+                               const float* sscale, float* dscale, cudaStream_t st);
+cudaError_t launch_silu_and_mul(const void* h, int R, int I, void* a, cudaStream_t st);
+cudaError_t launch_combine(const float* y, const int32_t* row_of_pair, int T, int k, int H,
+                           void* out, cudaStream_t st);
+cudaError_t launch_quant_rows(const void* x, int64_t rows, int cols, void* q, float* scale,
+                              const int32_t* nrows_dev, cudaStream_t st);
+
+// Grouped GEMM, SIMT tile engine (any supported shape).
+// mode: 0 FC1 raw, 1 FC1 silu, 2 FC2.  fp8: A/W are e4m3 codes with scales.
+cudaError_t launch_gemm_simt(int mode, bool fp8, const void* a, const float* a_scale,
+                             const void* w, const float* w_scale, const int32_t* offsets,
+                             const int32_t* row_src, const float* topk_w, void* c, int E, int K,
+                             int I, int N_out, int R_max, cudaStream_t st);
+
+}  // namespace moe

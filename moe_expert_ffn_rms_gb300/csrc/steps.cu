@@ -1,0 +1,481 @@
+// The non-GEMM steps of the MoE expert FFN forward: rms_norm, router logits,
+// softmax/top-k/renorm, permute (+ row gather), silu_and_mul, combine and
+// row-wise E4M3 quantisation.  All are HBM- or latency-bound; they use
+// 16-byte vector accesses and warp-shuffle reductions.
+#include "common.cuh"
+#include "kernels.h"
+
+#include <float.h>
+
+namespace moe {
+
+// ===================================================================== rms_norm
+// One CTA per token row.  y = bf16((x * r) * w), r = 1 / sqrt(mean(x^2) + eps)
+// (the pow -> mean -> rsqrt -> mul composite, fp32).  With FP8 the bf16 row is
+// also quantised per token: s = absmax / 448, q = e4m3(y / s).
+template <bool FP8>
+__global__ void __launch_bounds__(512) rmsnorm_kernel(const bf16* __restrict__ x,
+                                                      const bf16* __restrict__ w, int H, float eps,
+                                                      bf16* __restrict__ y, uint8_t* __restrict__ yq,
+                                                      float* __restrict__ yscale) {
+  __shared__ float red[32];
+  const int t = blockIdx.x;
+  const int nv = H >> 3;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  uint4* yr = reinterpret_cast<uint4*>(y + (size_t)t * H);
+  float ss = 0.f;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float f[8];
+    unpack8_bf16(xr[v], f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+  }
+  ss = block_sum(ss, red);
+  const float r = 1.0f / sqrtf(ss / (float)H + eps);
+  float amax = 0.f;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float f[8], g[8];
+    unpack8_bf16(xr[v], f);
+    unpack8_bf16(wr[v], g);
+    uint4 o;
+    o.x = pack2_bf16((f[0] * r) * g[0], (f[1] * r) * g[1]);
+    o.y = pack2_bf16((f[2] * r) * g[2], (f[3] * r) * g[3]);
+    o.z = pack2_bf16((f[4] * r) * g[4], (f[5] * r) * g[5]);
+    o.w = pack2_bf16((f[6] * r) * g[6], (f[7] * r) * g[7]);
+    yr[v] = o;
+    if (FP8) {
+      float h[8];
+      unpack8_bf16(o, h);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
+    }
+  }
+  if (FP8) {
+    amax = block_max(amax, red);
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    uint2* qr = reinterpret_cast<uint2*>(yq + (size_t)t * H);
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      float h[8];
+      unpack8_bf16(yr[v], h);  // this thread wrote yr[v] above
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) lo |= (uint32_t)f_to_e4m3(__fdiv_rn(h[i], s)) << (8 * i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hi |= (uint32_t)f_to_e4m3(__fdiv_rn(h[4 + i], s)) << (8 * i);
+      qr[v] = make_uint2(lo, hi);
+    }
+    if (threadIdx.x == 0) yscale[t] = s;
+  }
+}
+
+cudaError_t launch_rmsnorm(const void* x, const void* w, int T, int H, float eps, void* y,
+                           void* yq, float* yscale, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  int nv = H / 8;
+  int threads = nv >= 512 ? 512 : ((nv + 31) / 32) * 32;
+  if (yq)
+    rmsnorm_kernel<true><<<T, threads, 0, st>>>((const bf16*)x, (const bf16*)w, H, eps, (bf16*)y,
+                                                (uint8_t*)yq, yscale);
+  else
+    rmsnorm_kernel<false><<<T, threads, 0, st>>>((const bf16*)x, (const bf16*)w, H, eps, (bf16*)y,
+                                                 nullptr, nullptr);
+  return cudaGetLastError();
+}
+
+// ================================================================ router logits
+// part[z, t, e] = sum over the z-th K chunk of xhat[t, h] * Wr[h, e]  (fp32,
+// h ascending).  The chunks are summed in order by the top-k kernel, so the
+// logits are deterministic.  CTA tile: 16 tokens x 64 experts, K step 64.
+constexpr int RT_T = 16, RT_E = 64, RT_K = 64;
+
+__global__ void __launch_bounds__(256) router_logits_kernel(const bf16* __restrict__ xhat,
+                                                            const float* __restrict__ wr, int T,
+                                                            int H, int E, int kchunk,
+                                                            float* __restrict__ part) {
+  __shared__ float xs[RT_T][RT_K + 1];
+  __shared__ float ws[RT_K][RT_E];
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E;
+  const int kb0 = blockIdx.z * kchunk;
+  const int kb1 = min(H, kb0 + kchunk);
+  const int tx = tid & 63, ty = tid >> 6;  // expert column, token group
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int kb = kb0; kb < kb1; kb += RT_K) {
+    {  // xhat tile: 16 tokens x 64 k, 4 consecutive k per thread
+      const int tt = tid >> 4, kk = (tid & 15) * 4;
+      const int t = t0 + tt;
+      float f0 = 0.f, f1 = 0.f, f2 = 0.f, f3 = 0.f;
+      if (t < T) {
+        uint2 u = *reinterpret_cast<const uint2*>(xhat + (size_t)t * H + kb + kk);
+        f0 = bf16_lo(u.x); f1 = bf16_hi(u.x); f2 = bf16_lo(u.y); f3 = bf16_hi(u.y);
+      }
+      xs[tt][kk] = f0; xs[tt][kk + 1] = f1; xs[tt][kk + 2] = f2; xs[tt][kk + 3] = f3;
+    }
+#pragma unroll
+    for (int i = 0; i < (RT_K * RT_E) / 256; ++i) {  // Wr tile: 64 k x 64 experts
+      const int idx = tid + i * 256;
+      const int kk = idx >> 6, ee = idx & 63;
+      const int e = e0 + ee;
+      ws[kk][ee] = (e < E) ? wr[(size_t)(kb + kk) * E + e] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < RT_K; ++kk) {
+      const float wv = ws[kk][tx];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = fmaf(xs[ty + 4 * i][kk], wv, acc[i]);
+    }
+    __syncthreads();
+  }
+  const int e = e0 + tx;
+  if (e < E) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = t0 + ty + 4 * i;
+      if (t < T) part[((size_t)blockIdx.z * T + t) * E + e] = acc[i];
+    }
+  }
+}
+
+int route_splits(int T, int H, int E) {
+  const int tiles = ((T + RT_T - 1) / RT_T) * ((E + RT_E - 1) / RT_E);
+  const int steps = H / RT_K;
+  int ks = (2 * 152 + tiles - 1) / tiles;
+  if (ks > steps) ks = steps;
+  if (ks < 1) ks = 1;
+  const int per = (steps + ks - 1) / ks;  // K steps per chunk
+  return (steps + per - 1) / per;         // chunks actually needed
+}
+
+cudaError_t launch_router_logits(const void* xhat, const float* wr, int T, int H, int E, int ks,
+                                 float* part, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  // K chunk: a multiple of RT_K covering H in ks pieces.
+  int steps = H / RT_K;
+  int per = (steps + ks - 1) / ks;
+  int kchunk = per * RT_K;
+  int ks_eff = (H + kchunk - 1) / kchunk;
+  if (ks_eff != ks) return cudaErrorInvalidValue;  // route_splits() keeps these equal
+  dim3 grid((T + RT_T - 1) / RT_T, (E + RT_E - 1) / RT_E, ks);
+  router_logits_kernel<<<grid, 256, 0, st>>>((const bf16*)xhat, wr, T, H, E, kchunk, part);
+  return cudaGetLastError();
+}
+
+// ==================================================== softmax / top-k / renorm
+// One warp per token.  Logit of expert e = sum_z part[z, t, e] (+ bias[e]);
+// lane l holds experts l, l+32, ...  The k winners are taken one at a time by
+// a warp arg-max (larger logit first, lower index on ties); the weights are
+// the softmax over the selected logits (= full softmax renormalised).
+__global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ part, int ks,
+                                                   const float* __restrict__ bias, int T, int E,
+                                                   int k, int32_t* __restrict__ ids,
+                                                   float* __restrict__ wout,
+                                                   float* __restrict__ logits_out) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  constexpr int PER = kMaxExperts / 32;
+  float v[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = -FLT_MAX;
+    if (e < E) {
+      float s = 0.f;
+      for (int z = 0; z < ks; ++z) s += part[((size_t)z * T + t) * E + e];
+      if (bias) s += bias[e];
+      v[i] = s;
+      if (logits_out) logits_out[(size_t)t * E + e] = s;
+    }
+  }
+  unsigned taken = 0;
+  float sel_v[kMaxTopK];
+  int sel_e[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j >= k) break;
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !(taken & (1u << i)) && (v[i] > bv || (v[i] == bv && e < be))) {
+        bv = v[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    sel_v[j] = bv;
+    sel_e[j] = be;
+  }
+  if (lane == 0) {
+    const float m = sel_v[0];
+    float p[kMaxTopK];
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j >= k) break;
+      p[j] = expf(sel_v[j] - m);
+      s += p[j];
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j >= k) break;
+      ids[(size_t)t * k + j] = sel_e[j];
+      wout[(size_t)t * k + j] = p[j] / s;
+    }
+  }
+}
+
+cudaError_t launch_topk(const float* part, int ks, const float* bias, int T, int E, int k,
+                        int32_t* ids, float* w, float* logits_out, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  topk_kernel<<<(T + 3) / 4, 128, 0, st>>>(part, ks, bias, T, E, k, ids, w, logits_out);
+  return cudaGetLastError();
+}
+
+// ====================================================================== permute
+// Stable counting sort of the T*k pairs by expert in one CTA of 32 warps.
+// Warp w owns a contiguous chunk of tokens.  Pass 1 counts per (warp, expert);
+// pass 2 turns the counts into each warp's first row per expert (expert-major
+// exclusive prefix, then warp order); pass 3 walks each chunk in pair order in
+// batches of 32 and ranks equal experts inside a batch with __match_any_sync.
+constexpr int PERM_WARPS = 32;
+
+__global__ void __launch_bounds__(PERM_WARPS * 32) permute_kernel(
+    const int32_t* __restrict__ ids, int T, int E, int k, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ row_src, int32_t* __restrict__ row_of_pair, int* status) {
+  extern __shared__ int sm[];
+  int* cnt = sm;                         // [PERM_WARPS][E]
+  int* tot = sm + PERM_WARPS * E;        // [E + 1]
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < PERM_WARPS * E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int chunk = (T + PERM_WARPS - 1) / PERM_WARPS;
+  const int tb = min(T, w * chunk), te = min(T, (w + 1) * chunk);
+  const int p0 = tb * k, p1 = te * k;
+  for (int p = p0 + lane; p < p1; p += 32) {
+    const int e = ids[p];
+    if (e >= 0 && e < E) atomicAdd(&cnt[w * E + e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int s = 0;
+    for (int ww = 0; ww < PERM_WARPS; ++ww) s += cnt[ww * E + e];
+    tot[e] = s;
+  }
+  __syncthreads();
+  if (w == 0) {  // exclusive scan of tot[0..E) by warp 0
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int v = (e < E) ? tot[e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e < E) tot[e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tot[E] = carry;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    offsets[e] = tot[e];
+    if (e < E) {
+      int run = tot[e];
+      for (int ww = 0; ww < PERM_WARPS; ++ww) {
+        const int c = cnt[ww * E + e];
+        cnt[ww * E + e] = run;
+        run += c;
+      }
+    }
+  }
+  __syncthreads();
+  bool bad = false;
+  for (int pb = p0; pb < p1; pb += 32) {
+    const int p = pb + lane;
+    const bool valid = p < p1;
+    int e = valid ? ids[p] : -1;
+    const bool ok = valid && e >= 0 && e < E;
+    if (valid && !ok) bad = true;
+    const int key = ok ? e : -1 - lane;  // invalid lanes form singleton groups
+    const unsigned grp = __match_any_sync(0xffffffffu, key);
+    if (ok) {
+      const int rank = __popc(grp & ((1u << lane) - 1u));
+      const int r = cnt[w * E + e] + rank;
+      row_src[r] = p;
+      row_of_pair[p] = r;
+    } else if (valid) {
+      row_of_pair[p] = -1;
+    }
+    __syncwarp();
+    if (ok && (grp & ((1u << lane) - 1u)) == 0) cnt[w * E + e] += __popc(grp);
+    __syncwarp();
+  }
+  if (bad) flag_status(status, MOE_ERR_INVALID_ARG);
+}
+
+cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* offsets,
+                           int32_t* row_src, int32_t* row_of_pair, int* status, cudaStream_t st) {
+  size_t smem = (size_t)(PERM_WARPS * E + E + 1) * sizeof(int);
+  permute_kernel<<<1, PERM_WARPS * 32, smem, st>>>(ids, T, E, k, offsets, row_src, row_of_pair,
+                                                   status);
+  return cudaGetLastError();
+}
+
+// Row gather dst[r, :] = src[row_src[r] / k, :] for r < offsets[E]
+// (row_bytes a multiple of 16); optional per-row scale gather.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restrict__ offsets,
+                                                          int E, const int32_t* __restrict__ row_src,
+                                                          int k, int R_max,
+                                                          const uint4* __restrict__ src,
+                                                          uint4* __restrict__ dst, int row_vec,
+                                                          const float* __restrict__ sscale,
+                                                          float* __restrict__ dscale) {
+  const int R = min(offsets[E], R_max);
+  const int warps = blockDim.x >> 5, lane = threadIdx.x & 31;
+  for (int r = blockIdx.x * warps + (threadIdx.x >> 5); r < R; r += gridDim.x * warps) {
+    const int t = row_src[r] / k;
+    const uint4* s = src + (size_t)t * row_vec;
+    uint4* d = dst + (size_t)r * row_vec;
+    for (int v = lane; v < row_vec; v += 32) d[v] = s[v];
+    if (dscale && lane == 0) dscale[r] = sscale[t];
+  }
+}
+
+cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* row_src, int k,
+                               int R_max, const void* src, void* dst, int row_bytes,
+                               const float* sscale, float* dscale, cudaStream_t st) {
+  if (R_max == 0) return cudaSuccess;
+  int blocks = (R_max + 7) / 8;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  gather_rows_kernel<<<blocks, 256, 0, st>>>(offsets, E, row_src, k, R_max, (const uint4*)src,
+                                             (uint4*)dst, row_bytes / 16, sscale, dscale);
+  return cudaGetLastError();
+}
+
+// ================================================================ silu_and_mul
+__global__ void __launch_bounds__(256) silu_and_mul_kernel(const bf16* __restrict__ h, int R,
+                                                           int I, bf16* __restrict__ a) {
+  const int vpr = I >> 3;  // 8-element vectors per output row
+  const size_t n = (size_t)R * vpr;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / vpr, c = i % vpr;
+    const uint4 g = reinterpret_cast<const uint4*>(h + r * 2 * I)[c];
+    const uint4 u = reinterpret_cast<const uint4*>(h + r * 2 * I + I)[c];
+    float gf[8], uf[8];
+    unpack8_bf16(g, gf);
+    unpack8_bf16(u, uf);
+    uint4 o;
+    o.x = pack2_bf16(silu_f(gf[0]) * uf[0], silu_f(gf[1]) * uf[1]);
+    o.y = pack2_bf16(silu_f(gf[2]) * uf[2], silu_f(gf[3]) * uf[3]);
+    o.z = pack2_bf16(silu_f(gf[4]) * uf[4], silu_f(gf[5]) * uf[5]);
+    o.w = pack2_bf16(silu_f(gf[6]) * uf[6], silu_f(gf[7]) * uf[7]);
+    reinterpret_cast<uint4*>(a + r * I)[c] = o;
+  }
+}
+
+cudaError_t launch_silu_and_mul(const void* h, int R, int I, void* a, cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  size_t n = (size_t)R * (I / 8);
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  silu_and_mul_kernel<<<blocks, 256, 0, st>>>((const bf16*)h, R, I, (bf16*)a);
+  return cudaGetLastError();
+}
+
+// ===================================================================== combine
+// out[t, :] = bf16( sum_j y[row_of_pair[t*k + j], :] ), fp32, j ascending.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
+                                                      const int32_t* __restrict__ row_of_pair,
+                                                      int T, int k, int H, bf16* __restrict__ out) {
+  const int t = blockIdx.y;
+  const int h4 = blockIdx.x * blockDim.x + threadIdx.x;  // float4 index
+  if (h4 * 4 >= H) return;
+  int rows[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) rows[j] = (j < k) ? row_of_pair[(size_t)t * k + j] : -1;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j >= k) break;
+    if (rows[j] < 0) continue;
+    const float4 v = reinterpret_cast<const float4*>(y + (size_t)rows[j] * H)[h4];
+    s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+  }
+  uint2 o;
+  o.x = pack2_bf16(s.x, s.y);
+  o.y = pack2_bf16(s.z, s.w);
+  reinterpret_cast<uint2*>(out + (size_t)t * H)[h4] = o;
+}
+
+cudaError_t launch_combine(const float* y, const int32_t* row_of_pair, int T, int k, int H,
+                           void* out, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const int h4 = H / 4;
+  dim3 grid((h4 + 255) / 256, T);
+  combine_kernel<<<grid, 256, 0, st>>>(y, row_of_pair, T, k, H, (bf16*)out);
+  return cudaGetLastError();
+}
+
+// ========================================================== row E4M3 quantiser
+// One CTA per row: s = absmax / 448 (1 for a zero row); q = e4m3(x / s).
+// Rows at or beyond *nrows_dev (when given) are skipped.
+__global__ void __launch_bounds__(256) quant_rows_kernel(const bf16* __restrict__ x, int64_t rows,
+                                                         int cols, uint8_t* __restrict__ q,
+                                                         float* __restrict__ scale,
+                                                         const int32_t* __restrict__ nrows_dev) {
+  __shared__ float red[32];
+  const int64_t nr = nrows_dev ? min(rows, (int64_t)*nrows_dev) : rows;
+  const int nv = cols >> 3;
+  for (int64_t r = blockIdx.x; r < nr; r += gridDim.x) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + r * cols);
+    float amax = 0.f;
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      float f[8];
+      unpack8_bf16(xr[v], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    }
+    amax = block_max(amax, red);
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    uint2* qr = reinterpret_cast<uint2*>(q + r * cols);
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      float f[8];
+      unpack8_bf16(xr[v], f);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) lo |= (uint32_t)f_to_e4m3(__fdiv_rn(f[i], s)) << (8 * i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hi |= (uint32_t)f_to_e4m3(__fdiv_rn(f[4 + i], s)) << (8 * i);
+      qr[v] = make_uint2(lo, hi);
+    }
+    if (threadIdx.x == 0) scale[r] = s;
+    __syncthreads();  // red[] is reused by the next row
+  }
+}
+
+cudaError_t launch_quant_rows(const void* x, int64_t rows, int cols, void* q, float* scale,
+                              const int32_t* nrows_dev, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  int64_t blocks = rows < 152 * 64 ? rows : 152 * 64;
+  quant_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>((const bf16*)x, rows, cols, (uint8_t*)q,
+                                                      scale, nrows_dev);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

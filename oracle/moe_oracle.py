@@ -305,7 +305,7 @@ def moe_ffn_forward(x, norm_w, eps, k, w13, w2, router_w=None, router_bias=None,
     offsets, row_src = permute(ids, E)
     tok = row_src // k
     row_w = topk_w.reshape(-1)[row_src]
-    I = np.asarray(w2_of(0)).shape[1]
+    I = np.asarray(w2_of(int(ids.flat[0]))).shape[1]  # any expert in use gives I
     if not fp8:
         xp = xhat[tok]
         A = grouped_fc1(xp, offsets, w13_of, I)
