@@ -182,24 +182,24 @@ else:
     kw["router_w"] = d["router_w"].astype(np.float64)
     if "router_bias" in d: kw["router_bias"] = d["router_bias"].astype(np.float64)
 reps = int(sys.argv[3])
+min_seconds = float(sys.argv[4])
 t0 = time.perf_counter()
-for _ in range(reps):
-    if "logits" not in kw:
-        # restrict the router to the experts whose weights were saved: the
-        # sampled tokens' selections fall inside them (checked below)
-        pass
+done = 0
+while done < reps or time.perf_counter() - t0 < min_seconds:
     res = O.moe_ffn_forward(d["x"].astype(np.float64), d["norm_w"].astype(np.float64),
                             float(d["eps"]), int(d["k"]), lambda e: W13[e], lambda e: W2[e],
                             fp8=bool(d["fp8"]), **kw)
     assert set(res["ids"].reshape(-1).tolist()) <= set(W13), "sample needs more experts"
+    done += 1
 dt = time.perf_counter() - t0
-print(json.dumps({"seconds": dt, "tokens": int(d["x"].shape[0]) * reps}))
+print(json.dumps({"seconds": dt, "tokens": int(d["x"].shape[0]) * done, "passes": done}))
 """
 
 
-def run_oracle_sample(inp, n_tokens, reps=1, seed=0):
-    """Times the CPU oracle (one thread) on n_tokens sampled tokens; returns
-    (tokens/s, seconds, description)."""
+def run_oracle_sample(inp, n_tokens, reps=1, seed=0, min_seconds=10.0):
+    """Times the CPU oracle (one thread) on n_tokens sampled tokens, repeated
+    for at least `reps` passes and `min_seconds`; returns (tokens/s, seconds,
+    description)."""
     T = inp["T"]
     rng = np.random.default_rng(seed)
     toks = np.sort(rng.choice(T, size=min(n_tokens, T), replace=False))
@@ -208,13 +208,15 @@ def run_oracle_sample(inp, n_tokens, reps=1, seed=0):
         _save_sample(inp, toks, path)
         env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                    CUDA_VISIBLE_DEVICES="")
-        p = subprocess.run([sys.executable, "-c", ORACLE_CHILD, path, ROOT, str(reps)],
+        p = subprocess.run([sys.executable, "-c", ORACLE_CHILD, path, ROOT, str(reps),
+                            str(min_seconds)],
                            capture_output=True, text=True, env=env, timeout=1800)
         if p.returncode != 0:
             raise RuntimeError("oracle baseline failed:\n" + p.stderr[-2000:])
         r = json.loads(p.stdout.strip().splitlines()[-1])
-    desc = (f"{len(toks)} of {T} tokens (seeded sample) x {reps}: oracle moe_ffn_forward on "
-            f"the sample (weights of the experts it needs preloaded as fp64), 1 thread")
+    desc = (f"{len(toks)} of {T} tokens (seeded sample) x {r['passes']} passes: oracle "
+            f"moe_ffn_forward on the sample (weights of the experts it needs preloaded as "
+            f"fp64), 1 thread")
     return r["tokens"] / r["seconds"], r["seconds"], desc
 
 
@@ -276,8 +278,8 @@ def main_reference(args):
     n = args.cpu_tokens or auto_cpu_tokens(args.workload)
     # warm-up steps are untimed oracle runs on the same sample
     for _ in range(min(args.warmup, 1)):
-        run_oracle_sample(inp, n, 1)
-    tps, secs, desc = run_oracle_sample(inp, n, max(1, args.steps))
+        run_oracle_sample(inp, n, 1, min_seconds=0.0)
+    tps, secs, desc = run_oracle_sample(inp, n, max(1, args.steps), min_seconds=0.0)
     ms = secs / max(1, args.steps) * 1e3
     cfg = inp
     line = {
