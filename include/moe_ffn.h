@@ -158,6 +158,32 @@ moe_status moe_ffn_forward_routed(const moe_shape* shape, const void* x, const v
                                   const float* w2_scale, void* out, void* workspace,
                                   size_t workspace_bytes, moe_stream_t stream);
 
+/* moe_ffn_forward without a caller workspace, for callers that cannot
+ * allocate device memory: a plug-in inside a host program that owns the
+ * device-memory budget, a latency-critical path that must not pay for an
+ * allocation, or plain C / FFI code that holds only the buffers it was
+ * handed.  The pages describe no such entry point; it has no counterpart
+ * there.
+ *   Arguments and results are those of moe_ffn_forward, minus workspace.
+ *   Scratch: a file-scope device array of 32 MiB inside the library, held on
+ *   every device where the library's device code is loaded until the
+ *   process exits.  Shapes whose moe_ffn_workspace_size() exceeds 32 MiB
+ *   (large prefill batches) are rejected with MOE_ERR_WORKSPACE_TOO_SMALL
+ *   and nothing is enqueued.  No call allocates or frees device memory.
+ *   Set-up: the first call on a device (with that device current) looks up
+ *   the array's device address; make that first call before any stream
+ *   capture.
+ *   All calls on a device share the one array and it keeps the last call's
+ *   contents (nothing in it needs to start at zero).  Calls whose work
+ *   overlaps on the GPU (other streams, other host threads) race on it:
+ *   serialise them, e.g. on one stream. */
+moe_status moe_ffn_forward_static_ws(const moe_shape* shape, const void* x, const void* norm_w,
+                                     const float* router_w, const float* router_logits,
+                                     const float* router_bias, const void* w13, const void* w2,
+                                     const float* w13_scale, const float* w2_scale, void* out,
+                                     int32_t* topk_ids_out, float* topk_w_out,
+                                     moe_stream_t stream);
+
 /* ------------------------------------------------------------ the steps -- */
 
 /* rms_norm ([V100] "rewrite on torch::stable::Tensor"):

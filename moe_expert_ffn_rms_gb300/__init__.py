@@ -61,6 +61,8 @@ _SIGS = {
                                        _P, _P, _P, _P, _SZ, _P]),
     "moe_ffn_forward_routed": (ctypes.c_int, [ctypes.POINTER(MoeShape), _P, _P, _P, _P, _P, _P, _P,
                                               _P, _P, _P, _SZ, _P]),
+    "moe_ffn_forward_static_ws": (ctypes.c_int, [ctypes.POINTER(MoeShape), _P, _P, _P, _P, _P, _P,
+                                                 _P, _P, _P, _P, _P, _P, _P]),
     "moe_rmsnorm": (ctypes.c_int, [_P, _P, _I32, _I32, ctypes.c_float, _P, _P, _P, _P]),
     "moe_route_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "moe_route_topk": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ,
@@ -154,6 +156,18 @@ def moe_ffn_forward(shape: MoeShape, x, norm_w, w13, w2, out, workspace, router_
                                _ptr(w13_scale), _ptr(w2_scale), _ptr(out), _ptr(topk_ids_out),
                                _ptr(topk_w_out), _ws_ptr(workspace), _ws_bytes(workspace),
                                _stream(stream)))
+    return out
+
+
+def moe_ffn_forward_static_ws(shape: MoeShape, x, norm_w, w13, w2, out, router_w=None,
+                              router_logits=None, router_bias=None, w13_scale=None,
+                              w2_scale=None, topk_ids_out=None, topk_w_out=None, stream=None):
+    """moe_ffn_forward with the library's fixed 32 MiB device scratch instead
+    of a caller workspace (for callers that cannot allocate device memory)."""
+    _check(lib.moe_ffn_forward_static_ws(ctypes.byref(shape), _ptr(x), _ptr(norm_w), _ptr(router_w),
+                                         _ptr(router_logits), _ptr(router_bias), _ptr(w13),
+                                         _ptr(w2), _ptr(w13_scale), _ptr(w2_scale), _ptr(out),
+                                         _ptr(topk_ids_out), _ptr(topk_w_out), _stream(stream)))
     return out
 
 

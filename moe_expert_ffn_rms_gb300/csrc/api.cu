@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "engine.h"
 #include "kernels.h"
+#include "api_internal.h"
 
 // Device status word: MOE_OK, or the first error a kernel flagged.
 __device__ int g_moe_status = 0;
@@ -270,6 +271,11 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
 }
 
 }  // namespace
+
+namespace moe {
+moe_status api_fail(moe_status s, const char* msg) { return fail(s, "%s", msg); }
+moe_status api_check_shape(const moe_shape* shape) { return check_shape(shape); }
+}  // namespace moe
 
 extern "C" {
 
