@@ -16,6 +16,15 @@ typedef __nv_bfloat16 bf16;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 
+// ------------------------------------------------ programmatic dependent launch --
+// Every kernel of the path is launched with programmatic stream serialisation:
+// it lets the next kernel in the stream start (prologue only) once this one
+// calls pdl_trigger(), and waits in pdl_wait() until the previous kernel has
+// completed and its writes are visible.  Each kernel calls pdl_wait() before
+// its first global-memory access.  Both are no-ops for a normal launch.
+MOE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- status --
 // The device status word lives in api.cu; kernels receive its address.
 MOE_DEV void flag_status(int* status, int code) {
@@ -53,6 +62,27 @@ MOE_DEV uint8_t f_to_e4m3(float v) {
 
 // silu(z) = z / (1 + exp(-z)), fp32.
 MOE_DEV float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// Host: launch `kern` on `st`, with programmatic stream serialisation unless
+// the environment sets MOE_PDL=0.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 // ------------------------------------------------------------- reductions --
 MOE_DEV float warp_sum(float v) {

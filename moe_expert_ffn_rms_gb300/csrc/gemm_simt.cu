@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(
   __shared__ int s_e, s_row0;
 
   const int tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
   for (int e = tid; e <= E; e += blockDim.x) s_off[e] = offsets[e];
   __syncthreads();
   if (tid < 32) {  // prefix of M tiles per expert
@@ -169,14 +171,13 @@ cudaError_t launch_gemm_simt(int mode, bool fp8, const void* a, const float* a_s
   // N_w: rows of one expert's weight matrix.
   const int N_w = (mode == 2) ? N_out : 2 * I;
   dim3 grid(N_out / BN, (R_max + BM - 1) / BM + E);
-#define MOE_SIMT_LAUNCH(MD, F8)                                                               \
-  gemm_simt_kernel<MD, F8><<<grid, 256, 0, st>>>(a, a_scale, w, w_scale, offsets, row_src, \
-                                                  topk_w, c, E, K, I, N_out, N_w)
+#define MOE_SIMT_LAUNCH(MD, F8)                                                             \
+  return launch_kernel(gemm_simt_kernel<MD, F8>, grid, dim3(256), 0, st, a, a_scale, w, w_scale, \
+                       offsets, row_src, topk_w, c, E, K, I, N_out, N_w)
   if (mode == 0) { if (fp8) MOE_SIMT_LAUNCH(0, true); else MOE_SIMT_LAUNCH(0, false); }
   else if (mode == 1) { if (fp8) MOE_SIMT_LAUNCH(1, true); else MOE_SIMT_LAUNCH(1, false); }
   else { if (fp8) MOE_SIMT_LAUNCH(2, true); else MOE_SIMT_LAUNCH(2, false); }
 #undef MOE_SIMT_LAUNCH
-  return cudaGetLastError();
 }
 
 }  // namespace moe

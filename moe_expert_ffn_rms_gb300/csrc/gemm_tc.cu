@@ -113,7 +113,29 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~(uintptr_t)1023);
 
-  // ---- set-up: unit table, barriers, TMEM
+  // ---- set-up: barriers and TMEM first (no global memory), then wait for
+  // the previous kernel and build the unit table from the expert offsets
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 128);
+    }
+    mbar_init(&drain_bar, 1);
+    mbar_init(&xch_bar, 128);
+    s_abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_x);
+  } else if (warp == 1) {
+    tmem_alloc(&s_tmem, 2 * kAccCols);
+    tmem_relinquish();
+  }
+  pdl_trigger();
+  pdl_wait();
   for (int e = threadIdx.x; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
   __syncthreads();
   if (threadIdx.x == 0) {  // offsets must be monotone within [0, R_max]
@@ -148,25 +170,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) s_up[p.E] = carry;
-    if (lane == 0) {
-      for (int s = 0; s < p.stages; ++s) {
-        mbar_init(&full_bar[s], 1);
-        mbar_init(&empty_bar[s], 1);
-      }
-      for (int a = 0; a < 2; ++a) {
-        mbar_init(&tfull_bar[a], 1);
-        mbar_init(&tempty_bar[a], 128);
-      }
-      mbar_init(&drain_bar, 1);
-      mbar_init(&xch_bar, 128);
-      s_abort = 0;
-      fence_mbar_init();
-      prefetch_tmap(&tm_w);
-      prefetch_tmap(&tm_x);
-    }
-  } else if (warp == 1) {
-    tmem_alloc(&s_tmem, 2 * kAccCols);
-    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -481,8 +484,7 @@ cudaError_t launch_one(const CUtensorMap& tw, const CUtensorMap& tx, const Param
   auto k = moe_tc_gemm_kernel<SWAP, MODE, FP8>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, smem, st>>>(tw, tx, p);
-  return cudaGetLastError();
+  return launch_kernel(k, dim3(grid), dim3(kThreads), smem, st, tw, tx, p);
 }
 
 template <bool SWAP, bool FP8>

@@ -6,6 +6,15 @@
 #include "kernels.h"
 
 #include <float.h>
+#include <stdlib.h>
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("MOE_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
 
 namespace moe {
 
@@ -18,6 +27,8 @@ __global__ void __launch_bounds__(512) rmsnorm_kernel(const bf16* __restrict__ x
                                                       const bf16* __restrict__ w, int H, float eps,
                                                       bf16* __restrict__ y, uint8_t* __restrict__ yq,
                                                       float* __restrict__ yscale) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int t = blockIdx.x;
   const int nv = H >> 3;
@@ -75,65 +86,91 @@ cudaError_t launch_rmsnorm(const void* x, const void* w, int T, int H, float eps
   int nv = H / 8;
   int threads = nv >= 512 ? 512 : ((nv + 31) / 32) * 32;
   if (yq)
-    rmsnorm_kernel<true><<<T, threads, 0, st>>>((const bf16*)x, (const bf16*)w, H, eps, (bf16*)y,
-                                                (uint8_t*)yq, yscale);
-  else
-    rmsnorm_kernel<false><<<T, threads, 0, st>>>((const bf16*)x, (const bf16*)w, H, eps, (bf16*)y,
-                                                 nullptr, nullptr);
-  return cudaGetLastError();
+    return launch_kernel(rmsnorm_kernel<true>, dim3(T), dim3(threads), 0, st, (const bf16*)x,
+                         (const bf16*)w, H, eps, (bf16*)y, (uint8_t*)yq, yscale);
+  return launch_kernel(rmsnorm_kernel<false>, dim3(T), dim3(threads), 0, st, (const bf16*)x,
+                       (const bf16*)w, H, eps, (bf16*)y, (uint8_t*)nullptr, (float*)nullptr);
 }
 
 // ================================================================ router logits
 // part[z, t, e] = sum over the z-th K chunk of xhat[t, h] * Wr[h, e]  (fp32,
-// h ascending).  The chunks are summed in order by the top-k kernel, so the
-// logits are deterministic.  CTA tile: 16 tokens x 64 experts, K step 64.
-constexpr int RT_T = 16, RT_E = 64, RT_K = 64;
+// h ascending within the chunk).  The chunks are summed in order by the
+// top-k kernel, so the logits are deterministic.  CTA tile: 64 tokens x 64
+// experts, K step 32, 256 threads with a 4 x 4 register tile each (float4
+// shared-memory reads: 2 loads per 16 FMA).
+constexpr int RT_T = 64, RT_E = 64, RT_K = 32;
 
 __global__ void __launch_bounds__(256) router_logits_kernel(const bf16* __restrict__ xhat,
                                                             const float* __restrict__ wr, int T,
                                                             int H, int E, int kchunk,
                                                             float* __restrict__ part) {
-  __shared__ float xs[RT_T][RT_K + 1];
-  __shared__ float ws[RT_K][RT_E];
+  pdl_trigger();
+  pdl_wait();
+  __shared__ __align__(16) float xs[RT_K][RT_T + 4];  // [k][token]
+  __shared__ __align__(16) float ws[RT_K][RT_E];      // [k][expert]
   const int tid = threadIdx.x;
   const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E;
   const int kb0 = blockIdx.z * kchunk;
   const int kb1 = min(H, kb0 + kchunk);
-  const int tx = tid & 63, ty = tid >> 6;  // expert column, token group
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const int tx = tid & 15, ty = tid >> 4;  // experts tx*4.., tokens ty*4..
+  const bool e_vec = (E % 4 == 0);
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   for (int kb = kb0; kb < kb1; kb += RT_K) {
-    {  // xhat tile: 16 tokens x 64 k, 4 consecutive k per thread
-      const int tt = tid >> 4, kk = (tid & 15) * 4;
+    {  // x_hat tile: 64 tokens x 32 k; thread loads 8 consecutive k of one token
+      const int tt = tid >> 2, kk = (tid & 3) * 8;
       const int t = t0 + tt;
-      float f0 = 0.f, f1 = 0.f, f2 = 0.f, f3 = 0.f;
+      float f[8];
       if (t < T) {
-        uint2 u = *reinterpret_cast<const uint2*>(xhat + (size_t)t * H + kb + kk);
-        f0 = bf16_lo(u.x); f1 = bf16_hi(u.x); f2 = bf16_lo(u.y); f3 = bf16_hi(u.y);
+        unpack8_bf16(*reinterpret_cast<const uint4*>(xhat + (size_t)t * H + kb + kk), f);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = 0.f;
       }
-      xs[tt][kk] = f0; xs[tt][kk + 1] = f1; xs[tt][kk + 2] = f2; xs[tt][kk + 3] = f3;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xs[kk + i][tt] = f[i];
     }
 #pragma unroll
-    for (int i = 0; i < (RT_K * RT_E) / 256; ++i) {  // Wr tile: 64 k x 64 experts
+    for (int i = 0; i < 2; ++i) {  // W_r tile: 32 k x 64 experts, float4 per thread
       const int idx = tid + i * 256;
-      const int kk = idx >> 6, ee = idx & 63;
-      const int e = e0 + ee;
-      ws[kk][ee] = (e < E) ? wr[(size_t)(kb + kk) * E + e] : 0.f;
+      const int kk = idx >> 4, e4 = (idx & 15) * 4;
+      const int e = e0 + e4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float* src = wr + (size_t)(kb + kk) * E + e;
+      if (e_vec && e + 3 < E) {
+        v = *reinterpret_cast<const float4*>(src);
+      } else {
+        if (e < E) v.x = src[0];
+        if (e + 1 < E) v.y = src[1];
+        if (e + 2 < E) v.z = src[2];
+        if (e + 3 < E) v.w = src[3];
+      }
+      *reinterpret_cast<float4*>(&ws[kk][e4]) = v;
     }
     __syncthreads();
 #pragma unroll 8
     for (int kk = 0; kk < RT_K; ++kk) {
-      const float wv = ws[kk][tx];
+      const float4 a = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = fmaf(xs[ty + 4 * i][kk], wv, acc[i]);
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
-  const int e = e0 + tx;
-  if (e < E) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = t0 + ty + 4 * i;
-      if (t < T) part[((size_t)blockIdx.z * T + t) * E + e] = acc[i];
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) part[((size_t)blockIdx.z * T + t) * E + e] = acc[i][j];
     }
   }
 }
@@ -142,7 +179,8 @@ int route_splits(int T, int H, int E) {
   const int tiles = ((T + RT_T - 1) / RT_T) * ((E + RT_E - 1) / RT_E);
   const int steps = H / RT_K;
   int ks = (2 * 152 + tiles - 1) / tiles;
-  if (ks > steps) ks = steps;
+  const int min_steps = 8;  // at least 256 K per chunk
+  if (ks > steps / min_steps) ks = steps / min_steps;
   if (ks < 1) ks = 1;
   const int per = (steps + ks - 1) / ks;  // K steps per chunk
   return (steps + per - 1) / per;         // chunks actually needed
@@ -152,14 +190,14 @@ cudaError_t launch_router_logits(const void* xhat, const float* wr, int T, int H
                                  float* part, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   // K chunk: a multiple of RT_K covering H in ks pieces.
-  int steps = H / RT_K;
-  int per = (steps + ks - 1) / ks;
-  int kchunk = per * RT_K;
-  int ks_eff = (H + kchunk - 1) / kchunk;
+  const int steps = H / RT_K;
+  const int per = (steps + ks - 1) / ks;
+  const int kchunk = per * RT_K;
+  const int ks_eff = (H + kchunk - 1) / kchunk;
   if (ks_eff != ks) return cudaErrorInvalidValue;  // route_splits() keeps these equal
   dim3 grid((T + RT_T - 1) / RT_T, (E + RT_E - 1) / RT_E, ks);
-  router_logits_kernel<<<grid, 256, 0, st>>>((const bf16*)xhat, wr, T, H, E, kchunk, part);
-  return cudaGetLastError();
+  return launch_kernel(router_logits_kernel, grid, dim3(256), 0, st, (const bf16*)xhat, wr, T, H, E,
+                       kchunk, part);
 }
 
 // ==================================================== softmax / top-k / renorm
@@ -172,6 +210,8 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
                                                    int k, int32_t* __restrict__ ids,
                                                    float* __restrict__ wout,
                                                    float* __restrict__ logits_out) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -183,7 +223,18 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
     v[i] = -FLT_MAX;
     if (e < E) {
       float s = 0.f;
-      for (int z = 0; z < ks; ++z) s += part[((size_t)z * T + t) * E + e];
+      const float* pz = part + (size_t)t * E + e;
+      const size_t zstride = (size_t)T * E;
+      int z = 0;
+      for (; z + 4 <= ks; z += 4) {  // four loads in flight, summed in z order
+        const float a = pz[z * zstride], b = pz[(z + 1) * zstride];
+        const float c = pz[(z + 2) * zstride], d = pz[(z + 3) * zstride];
+        s += a;
+        s += b;
+        s += c;
+        s += d;
+      }
+      for (; z < ks; ++z) s += pz[z * zstride];
       if (bias) s += bias[e];
       v[i] = s;
       if (logits_out) logits_out[(size_t)t * E + e] = s;
@@ -240,8 +291,8 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
 cudaError_t launch_topk(const float* part, int ks, const float* bias, int T, int E, int k,
                         int32_t* ids, float* w, float* logits_out, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  topk_kernel<<<(T + 3) / 4, 128, 0, st>>>(part, ks, bias, T, E, k, ids, w, logits_out);
-  return cudaGetLastError();
+  return launch_kernel(topk_kernel, dim3((T + 3) / 4), dim3(128), 0, st, part, ks, bias, T, E, k,
+                       ids, w, logits_out);
 }
 
 // ====================================================================== permute
@@ -255,6 +306,8 @@ constexpr int PERM_WARPS = 32;
 __global__ void __launch_bounds__(PERM_WARPS * 32) permute_kernel(
     const int32_t* __restrict__ ids, int T, int E, int k, int32_t* __restrict__ offsets,
     int32_t* __restrict__ row_src, int32_t* __restrict__ row_of_pair, int* status) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int sm[];
   int* cnt = sm;                         // [PERM_WARPS][E]
   int* tot = sm + PERM_WARPS * E;        // [E + 1]
@@ -331,9 +384,8 @@ __global__ void __launch_bounds__(PERM_WARPS * 32) permute_kernel(
 cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* offsets,
                            int32_t* row_src, int32_t* row_of_pair, int* status, cudaStream_t st) {
   size_t smem = (size_t)(PERM_WARPS * E + E + 1) * sizeof(int);
-  permute_kernel<<<1, PERM_WARPS * 32, smem, st>>>(ids, T, E, k, offsets, row_src, row_of_pair,
-                                                   status);
-  return cudaGetLastError();
+  return launch_kernel(permute_kernel, dim3(1), dim3(PERM_WARPS * 32), smem, st, ids, T, E, k,
+                       offsets, row_src, row_of_pair, status);
 }
 
 // Row gather dst[r, :] = src[row_src[r] / k, :] for r < offsets[E]
@@ -345,6 +397,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restr
                                                           uint4* __restrict__ dst, int row_vec,
                                                           const float* __restrict__ sscale,
                                                           float* __restrict__ dscale) {
+  pdl_trigger();
+  pdl_wait();
   const int R = min(offsets[E], R_max);
   const int warps = blockDim.x >> 5, lane = threadIdx.x & 31;
   for (int r = blockIdx.x * warps + (threadIdx.x >> 5); r < R; r += gridDim.x * warps) {
@@ -362,14 +416,15 @@ cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* row
   if (R_max == 0) return cudaSuccess;
   int blocks = (R_max + 7) / 8;
   if (blocks > 152 * 8) blocks = 152 * 8;
-  gather_rows_kernel<<<blocks, 256, 0, st>>>(offsets, E, row_src, k, R_max, (const uint4*)src,
-                                             (uint4*)dst, row_bytes / 16, sscale, dscale);
-  return cudaGetLastError();
+  return launch_kernel(gather_rows_kernel, dim3(blocks), dim3(256), 0, st, offsets, E, row_src, k,
+                       R_max, (const uint4*)src, (uint4*)dst, row_bytes / 16, sscale, dscale);
 }
 
 // ================================================================ silu_and_mul
 __global__ void __launch_bounds__(256) silu_and_mul_kernel(const bf16* __restrict__ h, int R,
                                                            int I, bf16* __restrict__ a) {
+  pdl_trigger();
+  pdl_wait();
   const int vpr = I >> 3;  // 8-element vectors per output row
   const size_t n = (size_t)R * vpr;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
@@ -394,8 +449,8 @@ cudaError_t launch_silu_and_mul(const void* h, int R, int I, void* a, cudaStream
   size_t n = (size_t)R * (I / 8);
   int blocks = (int)((n + 255) / 256);
   if (blocks > 152 * 16) blocks = 152 * 16;
-  silu_and_mul_kernel<<<blocks, 256, 0, st>>>((const bf16*)h, R, I, (bf16*)a);
-  return cudaGetLastError();
+  return launch_kernel(silu_and_mul_kernel, dim3(blocks), dim3(256), 0, st, (const bf16*)h, R, I,
+                       (bf16*)a);
 }
 
 // ===================================================================== combine
@@ -403,6 +458,8 @@ cudaError_t launch_silu_and_mul(const void* h, int R, int I, void* a, cudaStream
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
                                                       const int32_t* __restrict__ row_of_pair,
                                                       int T, int k, int H, bf16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.y;
   const int h4 = blockIdx.x * blockDim.x + threadIdx.x;  // float4 index
   if (h4 * 4 >= H) return;
@@ -428,8 +485,7 @@ cudaError_t launch_combine(const float* y, const int32_t* row_of_pair, int T, in
   if (T == 0) return cudaSuccess;
   const int h4 = H / 4;
   dim3 grid((h4 + 255) / 256, T);
-  combine_kernel<<<grid, 256, 0, st>>>(y, row_of_pair, T, k, H, (bf16*)out);
-  return cudaGetLastError();
+  return launch_kernel(combine_kernel, grid, dim3(256), 0, st, y, row_of_pair, T, k, H, (bf16*)out);
 }
 
 // ========================================================== row E4M3 quantiser
@@ -439,6 +495,8 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const bf16* __restrict_
                                                          int cols, uint8_t* __restrict__ q,
                                                          float* __restrict__ scale,
                                                          const int32_t* __restrict__ nrows_dev) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int64_t nr = nrows_dev ? min(rows, (int64_t)*nrows_dev) : rows;
   const int nv = cols >> 3;
@@ -473,9 +531,8 @@ cudaError_t launch_quant_rows(const void* x, int64_t rows, int cols, void* q, fl
                               const int32_t* nrows_dev, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   int64_t blocks = rows < 152 * 64 ? rows : 152 * 64;
-  quant_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>((const bf16*)x, rows, cols, (uint8_t*)q,
-                                                      scale, nrows_dev);
-  return cudaGetLastError();
+  return launch_kernel(quant_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, (const bf16*)x,
+                       rows, cols, (uint8_t*)q, scale, nrows_dev);
 }
 
 }  // namespace moe

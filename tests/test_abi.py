@@ -36,6 +36,12 @@ def test_every_declared_symbol_is_exported(M):
     assert set(M.EXPORTED) >= set(declared)
 
 
+def test_library_resolves_every_symbol_at_load(M):
+    # RTLD_NOW binds every undefined symbol immediately: a missing definition
+    # fails here instead of at the first call on a GPU machine.
+    ctypes.CDLL(M.LIB_PATH, mode=os.RTLD_NOW)
+
+
 def test_abi_version_and_status_strings(M):
     assert M.abi_version() == 1
     assert M.lib.moe_status_string(0) == b"MOE_OK"
