@@ -378,7 +378,8 @@ def main_native(args):
     act = torch.empty((R, I), dtype=torch.bfloat16, device=dev)
     actq = torch.empty((R, I), dtype=torch.uint8, device=dev) if fp8 else None
     acts = torch.empty((R,), dtype=torch.float32, device=dev) if fp8 else None
-    y = torch.empty((R, H), dtype=torch.float32, device=dev)
+    y = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    pws = M.alloc_workspace(max(256, M.moe_permute_workspace_size(T, E, k)), dev)
     out_b = torch.empty_like(out)
     stages = ["rmsnorm", "route", "permute", "fc1", "fc2", "combine"]
 
@@ -394,14 +395,14 @@ def main_native(args):
                          workspace=rws)
         mark(2)
         M.moe_permute(ids, T, E, k, offsets, row_src, rop, xhat=xq if fp8 else xhat, xp=xp,
-                      row_bytes=H * (1 if fp8 else 2), xscale=xs, xp_scale=xps)
+                      row_bytes=H * (1 if fp8 else 2), xscale=xs, xp_scale=xps, workspace=pws)
         mark(3)
         M.moe_grouped_gemm(shape, M.GEMM_FC1_SILU, xp, w13, offsets, act, a_scale=xps, w_scale=s13)
         if fp8:
             M.lib.moe_quantize_fp8_rows(act.data_ptr(), R, I, actq.data_ptr(), acts.data_ptr(),
                                         st.cuda_stream)
         mark(4)
-        M.moe_grouped_gemm(shape, M.GEMM_FC2, actq if fp8 else act, w2, offsets, y,
+        M.moe_grouped_gemm(shape, M.GEMM_FC2_BF16, actq if fp8 else act, w2, offsets, y,
                            a_scale=acts, w_scale=s2, row_src=row_src, topk_w=tw)
         mark(5)
         M.moe_combine(y, rop, T, k, out_b)

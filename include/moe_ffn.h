@@ -71,7 +71,8 @@ typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1 } moe_wdtype;
 typedef enum {
   MOE_GEMM_FC1_RAW = 0,   /* c bf16 [R, 2I] = a W13^T                          */
   MOE_GEMM_FC1_SILU = 1,  /* c bf16 [R, I]  = silu(a W_gate^T) * (a W_up^T)   */
-  MOE_GEMM_FC2 = 2        /* c fp32 [R, H]  = topk_w[row] * (a W2^T)           */
+  MOE_GEMM_FC2 = 2,       /* c fp32 [R, H]  = topk_w[row] * (a W2^T)           */
+  MOE_GEMM_FC2_BF16 = 3   /* c bf16 [R, H]  = bf16(topk_w[row] * (a W2^T))     */
 } moe_gemm_mode;
 
 /* Engine used for the grouped GEMMs.  AUTO picks by the host-known average
@@ -216,6 +217,10 @@ moe_status moe_route_topk(const void* xhat, const float* router_w, const float* 
                           int32_t* ids, float* weights, float* logits_out, void* workspace,
                           size_t workspace_bytes, moe_stream_t stream);
 
+/* Device workspace bytes moe_permute needs (0 for small batches, which use a
+ * single-CTA sort; larger ones use a parallel count / scan / scatter). */
+size_t moe_permute_workspace_size(int32_t T, int32_t E, int32_t k);
+
 /* Token -> expert grouping (stable counting sort of the T*k (t, j) pairs by
  * expert; rows ordered by expert, then token).
  *   ids int32 [T, k]            routing (each row: distinct experts)
@@ -226,11 +231,13 @@ moe_status moe_route_topk(const void* xhat, const float* router_w, const float* 
  *                               (rows of row_bytes bytes, multiple of 16);
  *                               both NULL to skip.
  *   xscale / xp_scale           optional fp32 per-row scale gather (FP8), or NULL.
+ *   workspace                   >= moe_permute_workspace_size(T, E, k) bytes
+ *                               (may be NULL when that is 0).
  * E <= 256.  Ids outside [0, E) are skipped and flagged. */
 moe_status moe_permute(const int32_t* ids, int32_t T, int32_t E, int32_t k, int32_t* offsets,
                        int32_t* row_src, int32_t* row_of_pair, const void* xhat, void* xp,
-                       int32_t row_bytes, const float* xscale, float* xp_scale,
-                       moe_stream_t stream);
+                       int32_t row_bytes, const float* xscale, float* xp_scale, void* workspace,
+                       size_t workspace_bytes, moe_stream_t stream);
 
 /* Grouped GEMM over the expert segments given by offsets ([RUBIN] FC1/FC2,
  * [SM] 3.1 scaled GEMM).  For each expert e and each row r in
@@ -239,7 +246,8 @@ moe_status moe_permute(const int32_t* ids, int32_t T, int32_t E, int32_t k, int3
  *   FC1_SILU: c[r, n] = bf16( silu(g) * u ),  g = sum_h a[r,h] w[e,n,h],
  *                                             u = sum_h a[r,h] w[e,I+n,h]  n < I
  *   FC2:      c[r, n] = topk_w[row_src[r]] * sum_i a[r, i] * w[e, n, i]   n < H
- *             (fp32 output; topk_w/row_src NULL -> weight 1)
+ *             (fp32 output; FC2_BF16: the same rounded to bf16;
+ *             topk_w/row_src NULL -> weight 1)
  * a: bf16 [R, K] (or e4m3 with a_scale fp32 [R] when shape->wdtype is FP8,
  * then w is e4m3 with w_scale fp32 [E, N]); products accumulate in fp32 and
  * are scaled by a_scale[r] * w_scale[e, n].  R = offsets[E] <= T*top_k. */
@@ -254,9 +262,10 @@ moe_status moe_silu_and_mul(const void* h, int32_t R, int32_t I, void* a, moe_st
 
 /* Weighted combine: out[t, :] = bf16( sum_{j=0..k-1} y[row_of_pair[t*k+j], :] )
  * summed in fp32 in j order (the routing weight is already in y).
- * y fp32 [T*k, H]; out bf16 [T, H]; H % 4 == 0. */
-moe_status moe_combine(const float* y, const int32_t* row_of_pair, int32_t T, int32_t k,
-                       int32_t H, void* out, moe_stream_t stream);
+ * y [T*k, H], fp32 (y_bf16 = 0) or bf16 (y_bf16 = 1); out bf16 [T, H];
+ * H % 8 == 0.  Rows whose row_of_pair is -1 are skipped. */
+moe_status moe_combine(const void* y, int32_t y_bf16, const int32_t* row_of_pair, int32_t T,
+                       int32_t k, int32_t H, void* out, moe_stream_t stream);
 
 /* Row-wise dynamic E4M3 quantisation ([SM] 3.2, W8A8):
  *   scale[r] = max|x[r, :]| / 448 (1 for a zero row), fp32;

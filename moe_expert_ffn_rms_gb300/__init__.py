@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_S
                 3: "MOE_ERR_UNSUPPORTED_DEVICE", 4: "MOE_ERR_WORKSPACE_TOO_SMALL",
                 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT"}
 W_BF16, W_FP8_E4M3 = 0, 1
-GEMM_FC1_RAW, GEMM_FC1_SILU, GEMM_FC2 = 0, 1, 2
+GEMM_FC1_RAW, GEMM_FC1_SILU, GEMM_FC2, GEMM_FC2_BF16 = 0, 1, 2, 3
 ENGINE_AUTO, ENGINE_DECODE, ENGINE_PREFILL = 0, 1, 2
 
 
@@ -67,11 +67,13 @@ _SIGS = {
     "moe_route_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "moe_route_topk": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ,
                                       _P]),
-    "moe_permute": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P, _P, _P]),
+    "moe_permute_workspace_size": (_SZ, [_I32, _I32, _I32]),
+    "moe_permute": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _SZ,
+                                   _P]),
     "moe_grouped_gemm": (ctypes.c_int, [ctypes.POINTER(MoeShape), _I32, _P, _P, _P, _P, _P, _P, _P,
                                         _P, _P]),
     "moe_silu_and_mul": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
-    "moe_combine": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P]),
+    "moe_combine": (ctypes.c_int, [_P, _I32, _P, _I32, _I32, _I32, _P, _P]),
     "moe_quantize_fp8_rows": (ctypes.c_int, [_P, ctypes.c_int64, _I32, _P, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -200,11 +202,17 @@ def moe_route_topk(T, H, E, k, ids, weights, xhat=None, router_w=None, router_bi
                               _stream(stream)))
 
 
+def moe_permute_workspace_size(T, E, k) -> int:
+    return lib.moe_permute_workspace_size(T, E, k)
+
+
 def moe_permute(ids, T, E, k, offsets, row_src, row_of_pair, xhat=None, xp=None, row_bytes=0,
-                xscale=None, xp_scale=None, stream=None):
+                xscale=None, xp_scale=None, workspace=None, stream=None):
+    wsp = _ws_ptr(workspace) if workspace is not None else None
+    wsb = _ws_bytes(workspace) if workspace is not None else 0
     _check(lib.moe_permute(_ptr(ids), T, E, k, _ptr(offsets), _ptr(row_src), _ptr(row_of_pair),
-                           _ptr(xhat), _ptr(xp), row_bytes, _ptr(xscale), _ptr(xp_scale),
-                           _stream(stream)))
+                           _ptr(xhat), _ptr(xp), row_bytes, _ptr(xscale), _ptr(xp_scale), wsp,
+                           wsb, _stream(stream)))
 
 
 def moe_grouped_gemm(shape: MoeShape, mode, a, w, offsets, c, a_scale=None, w_scale=None,
@@ -223,7 +231,8 @@ def moe_silu_and_mul(h, a, stream=None):
 
 def moe_combine(y, row_of_pair, T, k, out, stream=None):
     H = y.shape[1]
-    _check(lib.moe_combine(_ptr(y), _ptr(row_of_pair), T, k, H, _ptr(out), _stream(stream)))
+    y_bf16 = 1 if y.dtype == torch.bfloat16 else 0
+    _check(lib.moe_combine(_ptr(y), y_bf16, _ptr(row_of_pair), T, k, H, _ptr(out), _stream(stream)))
     return out
 
 

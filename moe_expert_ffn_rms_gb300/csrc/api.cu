@@ -112,8 +112,8 @@ moe_status check_shape(const moe_shape* s) {
 }
 
 struct Ws {
-  size_t xhat, xq, xscale, part, ids, tw, offsets, row_src, row_of_pair, xp, xp_scale, act, actq,
-      act_scale, y, total;
+  size_t xhat, xq, xscale, part, ids, tw, offsets, row_src, row_of_pair, perm_cnt, xp, xp_scale,
+      act, actq, act_scale, y, total;
 };
 
 size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -133,12 +133,13 @@ Ws layout(const moe_shape* s) {
   w.offsets = take((E + 1) * 4);
   w.row_src = take(R * 4);
   w.row_of_pair = take(R * 4);
+  w.perm_cnt = take(moe::permute_workspace_bytes(s->T, s->E, s->top_k));
   w.xp = take(R * H * (f8 ? 1 : 2));
   w.xp_scale = take(f8 ? R * 4 : 0);
   w.act = take(R * I * 2);
   w.actq = take(f8 ? R * I : 0);
   w.act_scale = take(f8 ? R * 4 : 0);
-  w.y = take(R * H * 4);
+  w.y = take(R * H * 2);  // FC2 output in bf16
   w.total = o;
   return w;
 }
@@ -165,8 +166,9 @@ moe_status run_gemm(const moe_shape* s, int mode, int engine, const void* a, con
                     const int32_t* row_src, const float* topk_w, void* c, int R_max, int sms,
                     int* status, cudaStream_t st) {
   const bool f8 = s->wdtype == MOE_W_FP8_E4M3;
-  const int K = (mode == MOE_GEMM_FC2) ? s->I : s->H;
-  const int N_out = (mode == MOE_GEMM_FC2) ? s->H : (mode == MOE_GEMM_FC1_SILU ? s->I : 2 * s->I);
+  const bool fc2 = mode >= MOE_GEMM_FC2;
+  const int K = fc2 ? s->I : s->H;
+  const int N_out = fc2 ? s->H : (mode == MOE_GEMM_FC1_SILU ? s->I : 2 * s->I);
   cudaError_t e = cudaErrorNotSupported;
   const char* env = getenv("MOE_FORCE_SIMT");
   const bool simt_only = env && env[0] == '1';
@@ -226,7 +228,8 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   bf16* act = at<bf16>(workspace, L.act);
   uint8_t* actq = f8 ? at<uint8_t>(workspace, L.actq) : nullptr;
   float* act_scale = f8 ? at<float>(workspace, L.act_scale) : nullptr;
-  float* y = at<float>(workspace, L.y);
+  bf16* y = at<bf16>(workspace, L.y);
+  int32_t* perm_cnt = at<int32_t>(workspace, L.perm_cnt);
 
   // a1: rms_norm (+ per-token E4M3 quantisation on the FP8 path)
   MOE_CUDA(moe::launch_rmsnorm(x, norm_w, T, H, s->eps, xhat, xq, xscale, st), "rmsnorm launch");
@@ -246,7 +249,8 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
     MOE_CUDA(moe::launch_topk(part, ks, router_bias, T, E, k, ids, tw, nullptr, st), "top-k launch");
   }
   // a4: permute + gather of the (quantised) token rows
-  MOE_CUDA(moe::launch_permute(ids, T, E, k, offsets, row_src, row_of_pair, dev->status, st),
+  MOE_CUDA(moe::launch_permute_any(ids, T, E, k, offsets, row_src, row_of_pair, perm_cnt,
+                                   dev->status, st),
            "permute launch");
   MOE_CUDA(moe::launch_gather_rows(offsets, E, row_src, k, R, f8 ? (const void*)xq : (const void*)xhat,
                                    xp, H * (f8 ? 1 : 2), xscale, xp_scale, st),
@@ -261,12 +265,12 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
     MOE_CUDA(moe::launch_quant_rows(act, R, I, actq, act_scale, offsets + E, st), "quant launch");
     a2 = actq;
   }
-  // a7: FC2 with the routing-weight epilogue
-  rc = run_gemm(s, MOE_GEMM_FC2, engine, a2, act_scale, w2, w2_scale, offsets, row_src, tw, y, R,
-                dev->sms, dev->status, st);
+  // a7: FC2 with the routing-weight epilogue (bf16 output rows)
+  rc = run_gemm(s, MOE_GEMM_FC2_BF16, engine, a2, act_scale, w2, w2_scale, offsets, row_src, tw, y,
+                R, dev->sms, dev->status, st);
   if (rc != MOE_OK) return rc;
-  // a8: combine
-  MOE_CUDA(moe::launch_combine(y, row_of_pair, T, k, H, out, st), "combine launch");
+  // a8: combine (fp32 sum in slot order, one bf16 rounding)
+  MOE_CUDA(moe::launch_combine(y, true, row_of_pair, T, k, H, out, st), "combine launch");
   return MOE_OK;
 }
 
@@ -397,10 +401,15 @@ moe_status moe_route_topk(const void* xhat, const float* router_w, const float* 
   return MOE_OK;
 }
 
+size_t moe_permute_workspace_size(int32_t T, int32_t E, int32_t k) {
+  if (T < 0 || E <= 0 || E > kMaxExperts || k <= 0 || k > kMaxTopK) return 0;
+  return moe::permute_workspace_bytes(T, E, k);
+}
+
 moe_status moe_permute(const int32_t* ids, int32_t T, int32_t E, int32_t k, int32_t* offsets,
                        int32_t* row_src, int32_t* row_of_pair, const void* xhat, void* xp,
-                       int32_t row_bytes, const float* xscale, float* xp_scale,
-                       moe_stream_t stream) {
+                       int32_t row_bytes, const float* xscale, float* xp_scale, void* workspace,
+                       size_t workspace_bytes, moe_stream_t stream) {
   MOE_REQ(ids && offsets && row_src && row_of_pair, MOE_ERR_INVALID_ARG,
           "ids, offsets, row_src and row_of_pair must be non-NULL");
   MOE_REQ(T >= 0 && E > 0 && E <= kMaxExperts && k > 0 && k <= kMaxTopK,
@@ -414,11 +423,17 @@ moe_status moe_permute(const int32_t* ids, int32_t T, int32_t E, int32_t k, int3
             MOE_ERR_INVALID_ARG, "row_bytes=%d must be a positive multiple of 16, pointers aligned",
             row_bytes);
   }
+  const size_t need = moe::permute_workspace_bytes(T, E, k);
+  MOE_REQ(workspace_bytes >= need && (need == 0 || workspace != nullptr),
+          MOE_ERR_WORKSPACE_TOO_SMALL, "permute workspace %zu < %zu bytes", workspace_bytes, need);
+  MOE_REQ(need == 0 || ((uintptr_t)workspace & 15u) == 0, MOE_ERR_INVALID_ARG,
+          "workspace must be 16-byte aligned");
   DevInfo* d = nullptr;
   moe_status rc = device_info(&d);
   if (rc != MOE_OK) return rc;
   cudaStream_t st = (cudaStream_t)stream;
-  MOE_CUDA(moe::launch_permute(ids, T, E, k, offsets, row_src, row_of_pair, d->status, st),
+  MOE_CUDA(moe::launch_permute_any(ids, T, E, k, offsets, row_src, row_of_pair, (int32_t*)workspace,
+                                   d->status, st),
            "permute launch");
   if (xp)
     MOE_CUDA(moe::launch_gather_rows(offsets, E, row_src, k, T * k, xhat, xp, row_bytes, xscale,
@@ -433,7 +448,7 @@ moe_status moe_grouped_gemm(const moe_shape* shape, int32_t mode, const void* a,
                             void* c, moe_stream_t stream) {
   moe_status rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
-  MOE_REQ(mode >= MOE_GEMM_FC1_RAW && mode <= MOE_GEMM_FC2, MOE_ERR_INVALID_ARG, "mode=%d", mode);
+  MOE_REQ(mode >= MOE_GEMM_FC1_RAW && mode <= MOE_GEMM_FC2_BF16, MOE_ERR_INVALID_ARG, "mode=%d", mode);
   MOE_REQ(a && w && offsets && c, MOE_ERR_INVALID_ARG, "a, w, offsets and c must be non-NULL");
   MOE_REQ(aligned16(a) && aligned16(w) && aligned16(c), MOE_ERR_INVALID_ARG, "misaligned pointer");
   const bool f8 = shape->wdtype == MOE_W_FP8_E4M3;
@@ -443,7 +458,7 @@ moe_status moe_grouped_gemm(const moe_shape* shape, int32_t mode, const void* a,
   if ((rc = device_info(&d)) != MOE_OK) return rc;
   const int R_max = shape->T * shape->top_k;
   return run_gemm(shape, mode, pick_engine(shape), a, a_scale, w, w_scale, offsets, row_src,
-                  mode == MOE_GEMM_FC2 ? topk_w : nullptr, c, R_max, d->sms, d->status,
+                  mode >= MOE_GEMM_FC2 ? topk_w : nullptr, c, R_max, d->sms, d->status,
                   (cudaStream_t)stream);
 }
 
@@ -458,16 +473,17 @@ moe_status moe_silu_and_mul(const void* h, int32_t R, int32_t I, void* a, moe_st
   return MOE_OK;
 }
 
-moe_status moe_combine(const float* y, const int32_t* row_of_pair, int32_t T, int32_t k,
-                       int32_t H, void* out, moe_stream_t stream) {
+moe_status moe_combine(const void* y, int32_t y_bf16, const int32_t* row_of_pair, int32_t T,
+                       int32_t k, int32_t H, void* out, moe_stream_t stream) {
   MOE_REQ(y && row_of_pair && out, MOE_ERR_INVALID_ARG, "y, row_of_pair and out must be non-NULL");
-  MOE_REQ(T >= 0 && k > 0 && k <= kMaxTopK && H > 0 && H % 4 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
-          "T=%d k=%d H=%d", T, k, H);
-  MOE_REQ(aligned16(y) && ((uintptr_t)out & 7u) == 0, MOE_ERR_INVALID_ARG, "misaligned pointer");
+  MOE_REQ(T >= 0 && k > 0 && k <= kMaxTopK && H > 0 && H % 8 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+          "T=%d k=%d H=%d (H %% 8 == 0)", T, k, H);
+  MOE_REQ(aligned16(y) && aligned16(out), MOE_ERR_INVALID_ARG, "misaligned pointer");
   DevInfo* d = nullptr;
   moe_status rc = device_info(&d);
   if (rc != MOE_OK) return rc;
-  MOE_CUDA(moe::launch_combine(y, row_of_pair, T, k, H, out, (cudaStream_t)stream), "combine launch");
+  MOE_CUDA(moe::launch_combine(y, y_bf16 != 0, row_of_pair, T, k, H, out, (cudaStream_t)stream),
+           "combine launch");
   return MOE_OK;
 }
 

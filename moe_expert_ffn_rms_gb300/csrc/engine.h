@@ -12,7 +12,8 @@ void engine_init_device();
 // Launches the tcgen05 grouped GEMM for one step, or returns
 // cudaErrorNotSupported (nothing enqueued) when the shape is outside what
 // the tensor-core engines cover; the caller then uses the SIMT engine.
-//   mode   0 FC1 raw, 1 FC1 + silu_and_mul, 2 FC2 x routing weight
+//   mode   0 FC1 raw, 1 FC1 + silu_and_mul, 2 FC2 x routing weight (fp32 out),
+//          3 the same with bf16 out
 //   decode true: weights are the 128-row MMA operand and the expert's
 //          tokens the narrow one (small batches); false: token tiles.
 cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const float* a_scale,

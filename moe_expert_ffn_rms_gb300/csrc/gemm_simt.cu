@@ -33,6 +33,7 @@ MOE_DEV void load8(const void* base, size_t elem_off, float* f) {
 // MODE 0: FC1 raw (W rows n of [2I]), out bf16 [R, 2I]
 // MODE 1: FC1 silu (gate rows n, up rows I+n), out bf16 [R, I]
 // MODE 2: FC2 (W rows n of [H]), out fp32 [R, H] x topk_w
+// MODE 3: FC2, out bf16 [R, H] x topk_w
 template <int MODE, bool FP8>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(
     const void* __restrict__ A, const float* __restrict__ a_scale, const void* __restrict__ W,
@@ -157,7 +158,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(
         float v = acc[0][i][c];
         if (FP8) v = v * sa * w_scale[(size_t)e * N_w + n];
         const float tw = topk_w ? topk_w[row_src[r]] : 1.f;
-        reinterpret_cast<float*>(C)[(size_t)r * N_out + n] = tw * v;
+        if (MODE == 2) reinterpret_cast<float*>(C)[(size_t)r * N_out + n] = tw * v;
+        else reinterpret_cast<bf16*>(C)[(size_t)r * N_out + n] = __float2bfloat16_rn(tw * v);
       }
     }
   }
@@ -169,14 +171,15 @@ cudaError_t launch_gemm_simt(int mode, bool fp8, const void* a, const float* a_s
                              int I, int N_out, int R_max, cudaStream_t st) {
   if (R_max == 0) return cudaSuccess;
   // N_w: rows of one expert's weight matrix.
-  const int N_w = (mode == 2) ? N_out : 2 * I;
+  const int N_w = (mode >= 2) ? N_out : 2 * I;
   dim3 grid(N_out / BN, (R_max + BM - 1) / BM + E);
 #define MOE_SIMT_LAUNCH(MD, F8)                                                             \
   return launch_kernel(gemm_simt_kernel<MD, F8>, grid, dim3(256), 0, st, a, a_scale, w, w_scale, \
                        offsets, row_src, topk_w, c, E, K, I, N_out, N_w)
   if (mode == 0) { if (fp8) MOE_SIMT_LAUNCH(0, true); else MOE_SIMT_LAUNCH(0, false); }
   else if (mode == 1) { if (fp8) MOE_SIMT_LAUNCH(1, true); else MOE_SIMT_LAUNCH(1, false); }
-  else { if (fp8) MOE_SIMT_LAUNCH(2, true); else MOE_SIMT_LAUNCH(2, false); }
+  else if (mode == 2) { if (fp8) MOE_SIMT_LAUNCH(2, true); else MOE_SIMT_LAUNCH(2, false); }
+  else { if (fp8) MOE_SIMT_LAUNCH(3, true); else MOE_SIMT_LAUNCH(3, false); }
 #undef MOE_SIMT_LAUNCH
 }
 

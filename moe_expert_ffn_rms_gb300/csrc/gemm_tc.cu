@@ -1,7 +1,8 @@
 // Tensor-core grouped GEMM engines for the MoE FFN (tcgen05 + TMEM + TMA).
 //
 // One persistent, warp-specialised kernel template covers FC1 (raw, or with
-// the silu_and_mul epilogue) and FC2 (with the routing-weight epilogue), on
+// the silu_and_mul epilogue) and FC2 (with the routing-weight epilogue,
+// fp32 or bf16 output), on
 // bf16 (kind::f16) or E4M3 (kind::f8f6f4) operands, in two orientations:
 //
 //  decode  (SWAP = true)   the MMA's 128-row operand is a slice of one
@@ -109,6 +110,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
   __shared__ volatile int s_abort;
   __shared__ float s_xch[SWAP && MODE == 1 ? 64 * 17 : 1];  // decode FC1: up values
 
+  constexpr bool IS_FC2 = (MODE == 2 || MODE == 3);  // routing-weight epilogue
+  constexpr bool OUT_F32 = (MODE == 2);              // fp32 output (else bf16)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~(uintptr_t)1023);
@@ -349,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
                 const int r = un.row0 + c + t;
                 if (c + t < un.rows) {
                   float x = v[t] * ws * (FP8 ? p.a_scale[r] : 1.f);
-                  if (MODE == 2) {
-                    if (p.topk_w) x *= p.topk_w[p.row_src[r]];
+                  if (IS_FC2 && p.topk_w) x *= p.topk_w[p.row_src[r]];
+                  if (OUT_F32) {
                     reinterpret_cast<float*>(p.out)[(size_t)r * p.ldo + n] = x;
                   } else {
                     reinterpret_cast<bf16*>(p.out)[(size_t)r * p.ldo + n] = __float2bfloat16_rn(x);
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
             }
           }
         } else {
-          const float tw = (MODE == 2 && rvalid && p.topk_w) ? p.topk_w[p.row_src[r]] : 1.f;
+          const float tw = (IS_FC2 && rvalid && p.topk_w) ? p.topk_w[p.row_src[r]] : 1.f;
           for (int c = 0; c < 256; c += 16) {
             float v[16];
             tmem_ld16(tbase + c, v);
@@ -412,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
                 const float ws = FP8 ? p.w_scale[wrow0 + min(n0 + t, p.n_out - 1)] : 1.f;
                 v[t] = v[t] * ws * sa * tw;
               }
-              if (MODE == 2) {
+              if (OUT_F32) {
                 float* dst = reinterpret_cast<float*>(p.out) + (size_t)r * p.ldo + n0;
                 if (n0 + 16 <= p.n_out) {
 #pragma unroll
@@ -492,7 +495,8 @@ cudaError_t launch_mode(int mode, const CUtensorMap& tw, const CUtensorMap& tx, 
                         int grid, size_t smem, cudaStream_t st) {
   if (mode == 0) return launch_one<SWAP, 0, FP8>(tw, tx, p, grid, smem, st);
   if (mode == 1) return launch_one<SWAP, 1, FP8>(tw, tx, p, grid, smem, st);
-  return launch_one<SWAP, 2, FP8>(tw, tx, p, grid, smem, st);
+  if (mode == 2) return launch_one<SWAP, 2, FP8>(tw, tx, p, grid, smem, st);
+  return launch_one<SWAP, 3, FP8>(tw, tx, p, grid, smem, st);
 }
 
 }  // namespace
@@ -508,7 +512,7 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
   if (!g_encode || R_max == 0) return R_max == 0 ? cudaSuccess : cudaErrorNotSupported;
   if (E > kMaxExperts || K % 64 != 0) return cudaErrorNotSupported;
   const int elem = fp8 ? 1 : 2;
-  const int N_w = (mode == 2) ? N_out : 2 * I;  // weight rows per expert
+  const int N_w = (mode >= 2) ? N_out : 2 * I;  // weight rows per expert
   Params p{};
   p.offsets = offsets;
   p.row_src = row_src;

@@ -119,27 +119,21 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const bf16* __restri
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int kb = kb0; kb < kb1; kb += RT_K) {
-    {  // x_hat tile: 64 tokens x 32 k; thread loads 8 consecutive k of one token
-      const int tt = tid >> 2, kk = (tid & 3) * 8;
-      const int t = t0 + tt;
-      float f[8];
-      if (t < T) {
-        unpack8_bf16(*reinterpret_cast<const uint4*>(xhat + (size_t)t * H + kb + kk), f);
-      } else {
+  // Global loads of the next K slice go to registers while the current one
+  // is multiplied out of shared memory (software pipelining).
+  const int xt = tid >> 2, xk = (tid & 3) * 8;  // x_hat: token, first k of 8
+  uint4 xr = make_uint4(0u, 0u, 0u, 0u);
+  float4 wv[2];
+  auto gload = [&](int kb) {
+    const int t = t0 + xt;
+    xr = (t < T) ? *reinterpret_cast<const uint4*>(xhat + (size_t)t * H + kb + xk)
+                 : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xs[kk + i][tt] = f[i];
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {  // W_r tile: 32 k x 64 experts, float4 per thread
+    for (int i = 0; i < 2; ++i) {  // W_r: 32 k x 64 experts, a float4 per thread per i
       const int idx = tid + i * 256;
-      const int kk = idx >> 4, e4 = (idx & 15) * 4;
-      const int e = e0 + e4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int kk = idx >> 4, e = e0 + (idx & 15) * 4;
       const float* src = wr + (size_t)(kb + kk) * E + e;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (e_vec && e + 3 < E) {
         v = *reinterpret_cast<const float4*>(src);
       } else {
@@ -148,9 +142,24 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const bf16* __restri
         if (e + 2 < E) v.z = src[2];
         if (e + 3 < E) v.w = src[3];
       }
-      *reinterpret_cast<float4*>(&ws[kk][e4]) = v;
+      wv[i] = v;
+    }
+  };
+  if (kb0 < kb1) gload(kb0);
+  for (int kb = kb0; kb < kb1; kb += RT_K) {
+    {
+      float f[8];
+      unpack8_bf16(xr, f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xs[xk + i][xt] = f[i];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int idx = tid + i * 256;
+        *reinterpret_cast<float4*>(&ws[idx >> 4][(idx & 15) * 4]) = wv[i];
+      }
     }
     __syncthreads();
+    if (kb + RT_K < kb1) gload(kb + RT_K);
 #pragma unroll 8
     for (int kk = 0; kk < RT_K; ++kk) {
       const float4 a = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
@@ -218,26 +227,26 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
   constexpr int PER = kMaxExperts / 32;
   float v[PER];
 #pragma unroll
+  for (int i = 0; i < PER; ++i) v[i] = 0.f;
+  // Partial sums: chunk z outer, experts inner, so a lane has up to PER loads
+  // in flight; each logit is still summed in z order.
+  const size_t zstride = (size_t)T * E;
+  const float* pt = part + (size_t)t * E;
+  for (int z = 0; z < ks; ++z) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) v[i] += pt[z * zstride + e];
+    }
+  }
+#pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
-    v[i] = -FLT_MAX;
     if (e < E) {
-      float s = 0.f;
-      const float* pz = part + (size_t)t * E + e;
-      const size_t zstride = (size_t)T * E;
-      int z = 0;
-      for (; z + 4 <= ks; z += 4) {  // four loads in flight, summed in z order
-        const float a = pz[z * zstride], b = pz[(z + 1) * zstride];
-        const float c = pz[(z + 2) * zstride], d = pz[(z + 3) * zstride];
-        s += a;
-        s += b;
-        s += c;
-        s += d;
-      }
-      for (; z < ks; ++z) s += pz[z * zstride];
-      if (bias) s += bias[e];
-      v[i] = s;
-      if (logits_out) logits_out[(size_t)t * E + e] = s;
+      if (bias) v[i] += bias[e];
+      if (logits_out) logits_out[(size_t)t * E + e] = v[i];
+    } else {
+      v[i] = -FLT_MAX;
     }
   }
   unsigned taken = 0;
@@ -388,6 +397,131 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* off
                        offsets, row_src, row_of_pair, status);
 }
 
+// Parallel form of the same stable counting sort, for large batches: chunks
+// of PC_TOK tokens.  (1) per-chunk expert counts; (2) one CTA turns them into
+// each chunk's first row per expert (expert-major prefix, then chunk order)
+// and the expert offsets; (3) one warp per chunk ranks its pairs in pair
+// order exactly as permute_kernel's pass 3.
+constexpr int PC_TOK = 32;
+
+int permute_chunks(int T) { return (T + PC_TOK - 1) / PC_TOK; }
+
+bool permute_parallel(int T, int k) { return (int64_t)T * k > 4096; }
+
+__global__ void __launch_bounds__(256) permute_count_kernel(const int32_t* __restrict__ ids, int T,
+                                                            int E, int k, int32_t* __restrict__ cnt,
+                                                            int* status) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int c[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) c[e] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * PC_TOK * k, p1 = min(T, (blockIdx.x + 1) * PC_TOK) * k;
+  bool bad = false;
+  for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    const int e = ids[p];
+    if (e >= 0 && e < E) atomicAdd(&c[e], 1);
+    else bad = true;
+  }
+  if (bad) flag_status(status, MOE_ERR_INVALID_ARG);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[(size_t)blockIdx.x * E + e] = c[e];
+}
+
+__global__ void __launch_bounds__(256) permute_scan_kernel(int nch, int E,
+                                                           int32_t* __restrict__ cnt,
+                                                           int32_t* __restrict__ offsets) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int tot[kMaxExperts + 1];
+  const int e = threadIdx.x;
+  if (e < E) {
+    int s = 0;
+    for (int ch = 0; ch < nch; ++ch) s += cnt[(size_t)ch * E + e];
+    tot[e] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {  // exclusive scan over experts by warp 0
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int ee = base + lane;
+      const int v = (ee < E) ? tot[ee] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (ee < E) tot[ee] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tot[E] = carry;
+  }
+  __syncthreads();
+  if (e < E) offsets[e] = tot[e];
+  if (threadIdx.x == 0) offsets[E] = tot[E];
+  if (e < E) {
+    int run = tot[e];
+    for (int ch = 0; ch < nch; ++ch) {
+      const int c = cnt[(size_t)ch * E + e];
+      cnt[(size_t)ch * E + e] = run;
+      run += c;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(32) permute_scatter_kernel(const int32_t* __restrict__ ids,
+                                                             int T, int E, int k,
+                                                             const int32_t* __restrict__ base,
+                                                             int32_t* __restrict__ row_src,
+                                                             int32_t* __restrict__ row_of_pair) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int nxt[kMaxExperts];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) nxt[e] = base[(size_t)blockIdx.x * E + e];
+  __syncwarp();
+  const int p0 = blockIdx.x * PC_TOK * k, p1 = min(T, (blockIdx.x + 1) * PC_TOK) * k;
+  for (int pb = p0; pb < p1; pb += 32) {
+    const int p = pb + lane;
+    const bool valid = p < p1;
+    const int e = valid ? ids[p] : -1;
+    const bool ok = valid && e >= 0 && e < E;
+    const int key = ok ? e : -1 - lane;
+    const unsigned grp = __match_any_sync(0xffffffffu, key);
+    if (ok) {
+      const int r = nxt[e] + __popc(grp & ((1u << lane) - 1u));
+      row_src[r] = p;
+      row_of_pair[p] = r;
+    } else if (valid) {
+      row_of_pair[p] = -1;
+    }
+    __syncwarp();
+    if (ok && (grp & ((1u << lane) - 1u)) == 0) nxt[e] += __popc(grp);
+    __syncwarp();
+  }
+}
+
+size_t permute_workspace_bytes(int T, int E, int k) {
+  return permute_parallel(T, k) ? (size_t)permute_chunks(T) * E * sizeof(int32_t) : 0;
+}
+
+cudaError_t launch_permute_any(const int32_t* ids, int T, int E, int k, int32_t* offsets,
+                               int32_t* row_src, int32_t* row_of_pair, int32_t* cnt_ws,
+                               int* status, cudaStream_t st) {
+  if (!permute_parallel(T, k))
+    return launch_permute(ids, T, E, k, offsets, row_src, row_of_pair, status, st);
+  const int nch = permute_chunks(T);
+  cudaError_t e = launch_kernel(permute_count_kernel, dim3(nch), dim3(256), 0, st, ids, T, E, k,
+                                cnt_ws, status);
+  if (e != cudaSuccess) return e;
+  e = launch_kernel(permute_scan_kernel, dim3(1), dim3(256), 0, st, nch, E, cnt_ws, offsets);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(permute_scatter_kernel, dim3(nch), dim3(32), 0, st, ids, T, E, k,
+                       (const int32_t*)cnt_ws, row_src, row_of_pair);
+}
+
 // Row gather dst[r, :] = src[row_src[r] / k, :] for r < offsets[E]
 // (row_bytes a multiple of 16); optional per-row scale gather.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restrict__ offsets,
@@ -454,38 +588,67 @@ cudaError_t launch_silu_and_mul(const void* h, int R, int I, void* a, cudaStream
 }
 
 // ===================================================================== combine
-// out[t, :] = bf16( sum_j y[row_of_pair[t*k + j], :] ), fp32, j ascending.
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
+// out[t, :] = bf16( sum_j y[row_of_pair[t*k + j], :] ), fp32, j ascending;
+// y is fp32 or bf16.  Each thread handles 8 consecutive columns.
+template <bool YBF16>
+__global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y,
                                                       const int32_t* __restrict__ row_of_pair,
                                                       int T, int k, int H, bf16* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.y;
-  const int h4 = blockIdx.x * blockDim.x + threadIdx.x;  // float4 index
-  if (h4 * 4 >= H) return;
+  const int h8 = blockIdx.x * blockDim.x + threadIdx.x;  // 8-column group
+  if (h8 * 8 >= H) return;
   int rows[kMaxTopK];
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) rows[j] = (j < k) ? row_of_pair[(size_t)t * k + j] : -1;
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  float v[kMaxTopK][8];
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    if (j >= k) break;
-    if (rows[j] < 0) continue;
-    const float4 v = reinterpret_cast<const float4*>(y + (size_t)rows[j] * H)[h4];
-    s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+  for (int j = 0; j < kMaxTopK; ++j) {  // all loads first (up to 8 rows in flight)
+    if (j < k && rows[j] >= 0) {
+      if (YBF16) {
+        unpack8_bf16(reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(y) +
+                                                    (size_t)rows[j] * H)[h8], v[j]);
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(y) +
+                                                            (size_t)rows[j] * H) + 2 * h8;
+        const float4 a = src[0], b = src[1];
+        v[j][0] = a.x; v[j][1] = a.y; v[j][2] = a.z; v[j][3] = a.w;
+        v[j][4] = b.x; v[j][5] = b.y; v[j][6] = b.z; v[j][7] = b.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
+    }
   }
-  uint2 o;
-  o.x = pack2_bf16(s.x, s.y);
-  o.y = pack2_bf16(s.z, s.w);
-  reinterpret_cast<uint2*>(out + (size_t)t * H)[h4] = o;
+  float s[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s[i] = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {  // summed in j order
+    if (j < k) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s[i] += v[j][i];
+    }
+  }
+  uint4 o;
+  o.x = pack2_bf16(s[0], s[1]);
+  o.y = pack2_bf16(s[2], s[3]);
+  o.z = pack2_bf16(s[4], s[5]);
+  o.w = pack2_bf16(s[6], s[7]);
+  reinterpret_cast<uint4*>(out + (size_t)t * H)[h8] = o;
 }
 
-cudaError_t launch_combine(const float* y, const int32_t* row_of_pair, int T, int k, int H,
-                           void* out, cudaStream_t st) {
+cudaError_t launch_combine(const void* y, bool y_bf16, const int32_t* row_of_pair, int T, int k,
+                           int H, void* out, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  const int h4 = H / 4;
-  dim3 grid((h4 + 255) / 256, T);
-  return launch_kernel(combine_kernel, grid, dim3(256), 0, st, y, row_of_pair, T, k, H, (bf16*)out);
+  const int h8 = H / 8;
+  dim3 grid((h8 + 255) / 256, T);
+  if (y_bf16)
+    return launch_kernel(combine_kernel<true>, grid, dim3(256), 0, st, y, row_of_pair, T, k, H,
+                         (bf16*)out);
+  return launch_kernel(combine_kernel<false>, grid, dim3(256), 0, st, y, row_of_pair, T, k, H,
+                       (bf16*)out);
 }
 
 // ========================================================== row E4M3 quantiser

@@ -51,9 +51,9 @@ def test_abi_version_and_status_strings(M):
 def test_workspace_size_host_logic(M):
     ok = M.make_shape(16, 4096, 64, 1536, 8)
     n = M.moe_ffn_workspace_size(ok)
-    # at least x_hat, x_p, the intermediate and the fp32 FC2 output
+    # at least x_hat, x_p, the intermediate and the bf16 FC2 output rows
     R = 16 * 8
-    assert n >= 16 * 4096 * 2 + R * 4096 * 2 + R * 1536 * 2 + R * 4096 * 4
+    assert n >= 16 * 4096 * 2 + R * 4096 * 2 + R * 1536 * 2 + R * 4096 * 2
     n8 = M.moe_ffn_workspace_size(M.make_shape(16, 4096, 64, 1536, 8, fp8=True))
     assert n8 > 0
     for bad in (M.make_shape(16, 100, 64, 1536, 8),   # H not a multiple of 64
@@ -101,12 +101,18 @@ def test_step_entry_points_reject_bad_arguments_on_host(M):
                                 None) == 2
     assert M.lib.moe_route_topk(None, None, None, None, 4, 256, 8, 2, fake, fake, None, None, 0,
                                 None) == 1
-    assert M.lib.moe_permute(fake, 4, 300, 2, fake, fake, fake, None, None, 0, None, None,
+    assert M.lib.moe_permute(fake, 4, 300, 2, fake, fake, fake, None, None, 0, None, None, None, 0,
                              None) == 2
-    assert M.lib.moe_permute(fake, 4, 8, 2, fake, fake, fake, fake, None, 0, None, None,
+    assert M.lib.moe_permute(fake, 4, 8, 2, fake, fake, fake, fake, None, 0, None, None, None, 0,
                              None) == 1
+    # a large batch needs the parallel sort's workspace
+    assert M.lib.moe_permute_workspace_size(4096, 64, 8) == 128 * 64 * 4
+    assert M.lib.moe_permute_workspace_size(16, 64, 8) == 0
+    assert M.lib.moe_permute(fake, 4096, 64, 8, fake, fake, fake, None, None, 0, None, None, None,
+                             0, None) == 4
     assert M.lib.moe_silu_and_mul(fake, 4, 12, fake, None) == 2
-    assert M.lib.moe_combine(fake, fake, 4, 9, 256, fake, None) == 2
+    assert M.lib.moe_combine(fake, 0, fake, 4, 9, 256, fake, None) == 2
+    assert M.lib.moe_combine(fake, 1, fake, 4, 2, 252, fake, None) == 2
     assert M.lib.moe_quantize_fp8_rows(fake, 4, 20, fake, fake, None) == 2
     shape = M.make_shape(4, 256, 8, 512, 2)
     assert M.lib.moe_grouped_gemm(ctypes.byref(shape), 7, fake, None, fake, None, fake, None,

@@ -144,7 +144,8 @@ def test_route_topk_router(M, cfg):
     print(f"{cfg}: {ndiff} near-tie tokens routed differently")
 
 
-@pytest.mark.parametrize("T,E,k", [(1, 4, 1), (37, 6, 2), (64, 256, 8), (4096, 64, 8), (333, 7, 7)])
+@pytest.mark.parametrize("T,E,k", [(1, 4, 1), (37, 6, 2), (64, 256, 8), (4096, 64, 8), (333, 7, 7),
+                                   (1000, 256, 8), (600, 3, 2)])
 def test_permute_bit_exact(M, T, E, k):
     g = torch.Generator().manual_seed(T * 7 + E)
     ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
@@ -157,7 +158,9 @@ def test_permute_bit_exact(M, T, E, k):
     row_src = torch.empty((T * k,), dtype=torch.int32, device=DEV)
     rop = torch.empty((T * k,), dtype=torch.int32, device=DEV)
     xp = torch.empty((T * k, H), dtype=torch.bfloat16, device=DEV)
-    M.moe_permute(ids_d, T, E, k, offsets, row_src, rop, xhat=xhat, xp=xp, row_bytes=H * 2)
+    ws = M.alloc_workspace(max(16, M.moe_permute_workspace_size(T, E, k)), DEV)
+    M.moe_permute(ids_d, T, E, k, offsets, row_src, rop, xhat=xhat, xp=xp, row_bytes=H * 2,
+                  workspace=ws)
     off_ref, rs_ref = O.permute(ids.numpy(), E)
     np.testing.assert_array_equal(offsets.cpu().numpy(), off_ref)
     np.testing.assert_array_equal(row_src.cpu().numpy(), rs_ref)
@@ -168,14 +171,18 @@ def test_permute_bit_exact(M, T, E, k):
     assert M.device_status() == 0
 
 
-def test_permute_flags_out_of_range_ids(M):
-    ids = torch.tensor([[0, 1], [2, 9], [1, -1]], dtype=torch.int32, device=DEV)
+@pytest.mark.parametrize("T", [3, 1500])
+def test_permute_flags_out_of_range_ids(M, T):
+    base = torch.tensor([[0, 1], [2, 9], [1, -1]], dtype=torch.int32)
+    ids = base.repeat((T + 2) // 3, 1)[:T].contiguous().to(DEV)
     offsets = torch.empty((5,), dtype=torch.int32, device=DEV)
-    rs = torch.empty((6,), dtype=torch.int32, device=DEV)
-    rop = torch.empty((6,), dtype=torch.int32, device=DEV)
-    M.moe_permute(ids, 3, 4, 2, offsets, rs, rop)
+    rs = torch.empty((2 * T,), dtype=torch.int32, device=DEV)
+    rop = torch.empty((2 * T,), dtype=torch.int32, device=DEV)
+    ws = M.alloc_workspace(max(16, M.moe_permute_workspace_size(T, 4, 2)), DEV)
+    M.moe_permute(ids, T, 4, 2, offsets, rs, rop, workspace=ws)
     assert M.device_status(clear=True) == 1        # MOE_ERR_INVALID_ARG recorded
-    assert offsets.cpu().tolist() == [0, 1, 3, 4, 4]
+    n = T // 3
+    assert offsets.cpu().tolist() == [0, n, 3 * n, 4 * n, 4 * n]
     assert rop.cpu().tolist()[3] == -1 and rop.cpu().tolist()[5] == -1
     assert M.device_status() == 0
 
@@ -193,10 +200,11 @@ def test_silu_and_mul(M):
     assert np.mean(got == ref) > 0.99
 
 
-def test_combine(M):
+@pytest.mark.parametrize("ydtype", [torch.float32, torch.bfloat16])
+def test_combine(M, ydtype):
     g = torch.Generator(device=DEV).manual_seed(12)
     T, k, H = 29, 3, 192
-    y = torch.randn((T * k, H), generator=g, device=DEV)
+    y = torch.randn((T * k, H), generator=g, device=DEV).to(ydtype)
     perm = torch.randperm(T * k, generator=torch.Generator().manual_seed(3)).to(torch.int32)
     rop = torch.empty_like(perm)
     rop[perm.long()] = torch.arange(T * k, dtype=torch.int32)
@@ -260,6 +268,12 @@ def test_grouped_gemm_modes(M, engine, name):
     row_w = f64(d["tw"])[d["row_src_np"]]
     ref2 = O.grouped_fc2(f64(d["a"]), off, w2_of, row_w)
     assert_close(f64(c2), ref2, 1e-3, f"FC2 {name}/{engine}")
+    c3 = torch.empty((R, H), dtype=torch.bfloat16, device=DEV)
+    M.moe_grouped_gemm(ms, M.GEMM_FC2_BF16, d["a"], d["w2"], d["offsets"], c3,
+                       row_src=d["row_src"], topk_w=d["tw"])
+    assert_close(f64(c3), O.bf16_round(ref2), TOL_BF16, f"FC2 bf16 {name}/{engine}")
+    # bf16 rows are the fp32 rows rounded once (same kernel family, same sums)
+    assert torch.equal(c3, c2.to(torch.bfloat16))
     torch.cuda.synchronize()
     assert M.device_status() == 0
 
