@@ -405,7 +405,7 @@ def main_native(args):
         M.moe_grouped_gemm(shape, M.GEMM_FC2_BF16, actq if fp8 else act, w2, offsets, y,
                            a_scale=acts, w_scale=s2, row_src=row_src, topk_w=tw)
         mark(5)
-        M.moe_combine(y, rop, T, k, out_b)
+        M.moe_combine(y, rop, T, k, out_b, pair_order=True)
         mark(6)
 
     for _ in range(args.warmup):

@@ -72,7 +72,7 @@ typedef enum {
   MOE_GEMM_FC1_RAW = 0,   /* c bf16 [R, 2I] = a W13^T                          */
   MOE_GEMM_FC1_SILU = 1,  /* c bf16 [R, I]  = silu(a W_gate^T) * (a W_up^T)   */
   MOE_GEMM_FC2 = 2,       /* c fp32 [R, H]  = topk_w[row] * (a W2^T)           */
-  MOE_GEMM_FC2_BF16 = 3   /* c bf16 [R, H]  = bf16(topk_w[row] * (a W2^T))     */
+  MOE_GEMM_FC2_BF16 = 3   /* c bf16 [R, H]: row r stored at row row_src[r]      */
 } moe_gemm_mode;
 
 /* Engine used for the grouped GEMMs.  AUTO picks by the host-known average
@@ -246,8 +246,9 @@ moe_status moe_permute(const int32_t* ids, int32_t T, int32_t E, int32_t k, int3
  *   FC1_SILU: c[r, n] = bf16( silu(g) * u ),  g = sum_h a[r,h] w[e,n,h],
  *                                             u = sum_h a[r,h] w[e,I+n,h]  n < I
  *   FC2:      c[r, n] = topk_w[row_src[r]] * sum_i a[r, i] * w[e, n, i]   n < H
- *             (fp32 output; FC2_BF16: the same rounded to bf16;
- *             topk_w/row_src NULL -> weight 1)
+ *             (fp32 output; topk_w/row_src NULL -> weight 1)
+ *   FC2_BF16: the same rounded to bf16 and written to row row_src[r] of c,
+ *             i.e. back in (token, slot) order (row r when row_src is NULL)
  * a: bf16 [R, K] (or e4m3 with a_scale fp32 [R] when shape->wdtype is FP8,
  * then w is e4m3 with w_scale fp32 [E, N]); products accumulate in fp32 and
  * are scaled by a_scale[r] * w_scale[e, n].  R = offsets[E] <= T*top_k. */
@@ -260,12 +261,16 @@ moe_status moe_grouped_gemm(const moe_shape* shape, int32_t mode, const void* a,
  * silu(z) = z / (1 + exp(-z)); h bf16 [R, 2I], a bf16 [R, I]; I % 8 == 0. */
 moe_status moe_silu_and_mul(const void* h, int32_t R, int32_t I, void* a, moe_stream_t stream);
 
-/* Weighted combine: out[t, :] = bf16( sum_{j=0..k-1} y[row_of_pair[t*k+j], :] )
- * summed in fp32 in j order (the routing weight is already in y).
- * y [T*k, H], fp32 (y_bf16 = 0) or bf16 (y_bf16 = 1); out bf16 [T, H];
- * H % 8 == 0.  Rows whose row_of_pair is -1 are skipped. */
-moe_status moe_combine(const void* y, int32_t y_bf16, const int32_t* row_of_pair, int32_t T,
-                       int32_t k, int32_t H, void* out, moe_stream_t stream);
+/* Weighted combine: out[t, :] = bf16( sum_{j=0..k-1} y_{t,j} ) summed in fp32
+ * in j order (the routing weight is already in y), where y_{t,j} is row
+ * row_of_pair[t*k+j] of y (y_pair_order = 0: rows in expert order, as
+ * MOE_GEMM_FC2 writes them) or row t*k+j (y_pair_order = 1: rows in
+ * (token, slot) order, as MOE_GEMM_FC2_BF16 writes them).  Pairs whose
+ * row_of_pair is -1 are skipped.  y [T*k, H], fp32 (y_bf16 = 0) or bf16
+ * (y_bf16 = 1); out bf16 [T, H]; H % 8 == 0. */
+moe_status moe_combine(const void* y, int32_t y_bf16, int32_t y_pair_order,
+                       const int32_t* row_of_pair, int32_t T, int32_t k, int32_t H, void* out,
+                       moe_stream_t stream);
 
 /* Row-wise dynamic E4M3 quantisation ([SM] 3.2, W8A8):
  *   scale[r] = max|x[r, :]| / 448 (1 for a zero row), fp32;

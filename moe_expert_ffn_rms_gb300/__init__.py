@@ -73,7 +73,7 @@ _SIGS = {
     "moe_grouped_gemm": (ctypes.c_int, [ctypes.POINTER(MoeShape), _I32, _P, _P, _P, _P, _P, _P, _P,
                                         _P, _P]),
     "moe_silu_and_mul": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
-    "moe_combine": (ctypes.c_int, [_P, _I32, _P, _I32, _I32, _I32, _P, _P]),
+    "moe_combine": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _I32, _I32, _P, _P]),
     "moe_quantize_fp8_rows": (ctypes.c_int, [_P, ctypes.c_int64, _I32, _P, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -229,10 +229,11 @@ def moe_silu_and_mul(h, a, stream=None):
     return a
 
 
-def moe_combine(y, row_of_pair, T, k, out, stream=None):
+def moe_combine(y, row_of_pair, T, k, out, pair_order=False, stream=None):
     H = y.shape[1]
     y_bf16 = 1 if y.dtype == torch.bfloat16 else 0
-    _check(lib.moe_combine(_ptr(y), y_bf16, _ptr(row_of_pair), T, k, H, _ptr(out), _stream(stream)))
+    _check(lib.moe_combine(_ptr(y), y_bf16, 1 if pair_order else 0, _ptr(row_of_pair), T, k, H,
+                           _ptr(out), _stream(stream)))
     return out
 
 

@@ -112,8 +112,8 @@ moe_status check_shape(const moe_shape* s) {
 }
 
 struct Ws {
-  size_t xhat, xq, xscale, part, ids, tw, offsets, row_src, row_of_pair, perm_cnt, xp, xp_scale,
-      act, actq, act_scale, y, total;
+  size_t xhat, xq, xscale, part, ids, tw, offsets, row_src, row_of_pair, perm_cnt, sched, xp,
+      xp_scale, act, actq, act_scale, y, total;
 };
 
 size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -134,6 +134,7 @@ Ws layout(const moe_shape* s) {
   w.row_src = take(R * 4);
   w.row_of_pair = take(R * 4);
   w.perm_cnt = take(moe::permute_workspace_bytes(s->T, s->E, s->top_k));
+  w.sched = take((E + 1) * 4);  // fused decode FFN: unit counter + per-expert FC1 progress
   w.xp = take(R * H * (f8 ? 1 : 2));
   w.xp_scale = take(f8 ? R * 4 : 0);
   w.act = take(R * I * 2);
@@ -230,6 +231,13 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   float* act_scale = f8 ? at<float>(workspace, L.act_scale) : nullptr;
   bf16* y = at<bf16>(workspace, L.y);
   int32_t* perm_cnt = at<int32_t>(workspace, L.perm_cnt);
+  int32_t* sched = at<int32_t>(workspace, L.sched);
+  // FC1 and FC2 run in one persistent launch on the decode engine (bf16),
+  // unless MOE_FUSE=0 or the SIMT engine is forced.
+  const char* fuse_env = getenv("MOE_FUSE");
+  const char* simt_env = getenv("MOE_FORCE_SIMT");
+  const bool fuse = engine == MOE_ENGINE_DECODE && !f8 && !(fuse_env && fuse_env[0] == '0') &&
+                    !(simt_env && simt_env[0] == '1');
 
   // a1: rms_norm (+ per-token E4M3 quantisation on the FP8 path)
   MOE_CUDA(moe::launch_rmsnorm(x, norm_w, T, H, s->eps, xhat, xq, xscale, st), "rmsnorm launch");
@@ -250,11 +258,21 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   }
   // a4: permute + gather of the (quantised) token rows
   MOE_CUDA(moe::launch_permute_any(ids, T, E, k, offsets, row_src, row_of_pair, perm_cnt,
-                                   dev->status, st),
+                                   dev->status, st, sched, E + 1),
            "permute launch");
   MOE_CUDA(moe::launch_gather_rows(offsets, E, row_src, k, R, f8 ? (const void*)xq : (const void*)xhat,
                                    xp, H * (f8 ? 1 : 2), xscale, xp_scale, st),
            "gather launch");
+  if (fuse) {
+    // a5 + a6 + a7 in one persistent launch (FC2 units wait per expert for FC1)
+    cudaError_t e = moe::launch_decode_ffn_fused(xp, w13, w2, act, y, offsets, row_src, tw, sched,
+                                                 E, H, I, R, T, dev->sms, dev->status, st);
+    if (e == cudaSuccess) {
+      MOE_CUDA(moe::launch_combine(y, true, true, row_of_pair, T, k, H, out, st), "combine launch");
+      return MOE_OK;
+    }
+    if (e != cudaErrorNotSupported) return cuda_fail(e, "fused decode FFN launch");
+  }
   // a5 + a6: FC1 with the silu_and_mul epilogue
   rc = run_gemm(s, MOE_GEMM_FC1_SILU, engine, xp, xp_scale, w13, w13_scale, offsets, row_src,
                 nullptr, act, R, dev->sms, dev->status, st);
@@ -270,7 +288,7 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
                 R, dev->sms, dev->status, st);
   if (rc != MOE_OK) return rc;
   // a8: combine (fp32 sum in slot order, one bf16 rounding)
-  MOE_CUDA(moe::launch_combine(y, true, row_of_pair, T, k, H, out, st), "combine launch");
+  MOE_CUDA(moe::launch_combine(y, true, true, row_of_pair, T, k, H, out, st), "combine launch");
   return MOE_OK;
 }
 
@@ -473,8 +491,9 @@ moe_status moe_silu_and_mul(const void* h, int32_t R, int32_t I, void* a, moe_st
   return MOE_OK;
 }
 
-moe_status moe_combine(const void* y, int32_t y_bf16, const int32_t* row_of_pair, int32_t T,
-                       int32_t k, int32_t H, void* out, moe_stream_t stream) {
+moe_status moe_combine(const void* y, int32_t y_bf16, int32_t y_pair_order,
+                       const int32_t* row_of_pair, int32_t T, int32_t k, int32_t H, void* out,
+                       moe_stream_t stream) {
   MOE_REQ(y && row_of_pair && out, MOE_ERR_INVALID_ARG, "y, row_of_pair and out must be non-NULL");
   MOE_REQ(T >= 0 && k > 0 && k <= kMaxTopK && H > 0 && H % 8 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
           "T=%d k=%d H=%d (H %% 8 == 0)", T, k, H);
@@ -482,7 +501,8 @@ moe_status moe_combine(const void* y, int32_t y_bf16, const int32_t* row_of_pair
   DevInfo* d = nullptr;
   moe_status rc = device_info(&d);
   if (rc != MOE_OK) return rc;
-  MOE_CUDA(moe::launch_combine(y, y_bf16 != 0, row_of_pair, T, k, H, out, (cudaStream_t)stream),
+  MOE_CUDA(moe::launch_combine(y, y_bf16 != 0, y_pair_order != 0, row_of_pair, T, k, H, out,
+                               (cudaStream_t)stream),
            "combine launch");
   return MOE_OK;
 }

@@ -22,4 +22,13 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
                            int I, int N_out, int R_max, int T, int sms, int* status,
                            cudaStream_t st);
 
+// Decode FFN in one persistent launch: FC1 + silu_and_mul (xp -> act) and
+// FC2 + routing weight (act -> y, bf16 rows in (token, slot) order), with a
+// dynamic unit scheduler.  `sched` holds 1 + E ints that must be zero when
+// the kernel starts.  bf16 only; cudaErrorNotSupported when not covered.
+cudaError_t launch_decode_ffn_fused(const void* xp, const void* w13, const void* w2, void* act,
+                                    void* y, const int32_t* offsets, const int32_t* row_src,
+                                    const float* topk_w, int* sched, int E, int H, int I, int R_max,
+                                    int T, int sms, int* status, cudaStream_t st);
+
 }  // namespace moe

@@ -33,7 +33,7 @@ MOE_DEV void load8(const void* base, size_t elem_off, float* f) {
 // MODE 0: FC1 raw (W rows n of [2I]), out bf16 [R, 2I]
 // MODE 1: FC1 silu (gate rows n, up rows I+n), out bf16 [R, I]
 // MODE 2: FC2 (W rows n of [H]), out fp32 [R, H] x topk_w
-// MODE 3: FC2, out bf16 [R, H] x topk_w
+// MODE 3: FC2, out bf16 x topk_w, row r stored at row_src[r] ((token, slot) order)
 template <int MODE, bool FP8>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(
     const void* __restrict__ A, const float* __restrict__ a_scale, const void* __restrict__ W,
@@ -158,8 +158,12 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(
         float v = acc[0][i][c];
         if (FP8) v = v * sa * w_scale[(size_t)e * N_w + n];
         const float tw = topk_w ? topk_w[row_src[r]] : 1.f;
-        if (MODE == 2) reinterpret_cast<float*>(C)[(size_t)r * N_out + n] = tw * v;
-        else reinterpret_cast<bf16*>(C)[(size_t)r * N_out + n] = __float2bfloat16_rn(tw * v);
+        if (MODE == 2) {
+          reinterpret_cast<float*>(C)[(size_t)r * N_out + n] = tw * v;
+        } else {  // bf16 rows go back to (token, slot) order
+          const int orow = row_src ? row_src[r] : r;
+          reinterpret_cast<bf16*>(C)[(size_t)orow * N_out + n] = __float2bfloat16_rn(tw * v);
+        }
       }
     }
   }

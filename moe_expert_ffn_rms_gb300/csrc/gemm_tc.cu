@@ -31,6 +31,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -52,31 +54,47 @@ constexpr int kDecodeMaxN = 128;     // token rows per decode unit
 constexpr int kDecodeBoxRows = 16;   // token rows per TMA box (decode)
 constexpr int kSmemLimit = 227 * 1024;
 
-struct Params {
-  const int32_t* offsets;
-  const int32_t* row_src;
-  const float* topk_w;
+// One grouped GEMM of a launch.
+struct JobP {
   const float* a_scale;  // per token row (E4M3)
   const float* w_scale;  // per weight row (E4M3)
+  const int32_t* row_src;
+  const float* topk_w;
   void* out;
-  int ldo;     // output row stride (elements)
-  int E, I, N_w, n_out;
-  int R_max;   // rows of the activation operand / output
-  int nt;      // N tiles per (expert, token chunk)
+  int ldo;    // output row stride (elements)
+  int N_w;    // weight rows per expert
+  int n_out;  // output columns
+  int nt;     // N tiles per (expert, token chunk)
+  int kst;    // K stages (kw 128-byte K atoms each)
+};
+
+struct Params {
+  const int32_t* offsets;
+  int E, I;
+  int R_max;   // rows of the activation operands / outputs
   int chunk;   // token rows per unit (decode: the B tile height; prefill: 128)
-  int kst;     // K stages (128-byte K slices)
   int stages;
   int stage_bytes;
-  int a_bytes;  // bytes of the A region of a stage (decode FC1: gate+up tiles)
+  int a_bytes;  // bytes of the A region of a stage (kw atoms of a_atom bytes)
+  int kw;       // 128-byte K atoms per stage (wider stages: longer runs per weight row)
+  int a_atom;   // bytes of one A atom (128 rows x 128 B)
+  int b_atom;   // bytes of one B atom
+  int njobs;    // 1, or 2 for FC1 -> FC2 in one launch
+  // Dynamic scheduling (fused launch): sched[0] is the unit counter, sched[1 + e]
+  // counts finished FC1 epilogue warps of expert e.  NULL: static schedule.
+  int* sched;
   int* status;
+  JobP job[2];
 };
 
 struct Unit {
-  int e, nt, row0, rows;
+  int job, e, nt, row0, rows;
 };
 
-// Unit enumeration shared by all roles: expert e has ceil(cnt/chunk) token
-// chunks, each with nt N tiles; s_up[e] is the exclusive prefix of units.
+constexpr int kUnitRing = 4;  // claimed-unit slots between the roles
+
+// Unit u of a job: expert e has ceil(cnt/chunk) token chunks, each with nt N
+// tiles; s_up[e] is the exclusive prefix of units.
 MOE_DEV Unit unit_of(int u, const int* s_off, const int* s_up, int E, int nt, int chunk) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
@@ -86,6 +104,7 @@ MOE_DEV Unit unit_of(int u, const int* s_off, const int* s_up, int E, int nt, in
   const int local = u - s_up[lo];
   const int mt = local / nt;
   Unit un;
+  un.job = 0;
   un.e = lo;
   un.nt = local - mt * nt;
   un.row0 = s_off[lo] + mt * chunk;
@@ -93,31 +112,234 @@ MOE_DEV Unit unit_of(int u, const int* s_off, const int* s_up, int E, int nt, in
   return un;
 }
 
+MOE_DEV int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+MOE_DEV void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// TMA loads of one K slice of a unit into ring slot (a, b).
+template <bool SWAP, int MODE>
+MOE_DEV void issue_stage(uint8_t* a, uint8_t* b, uint64_t* bar, const CUtensorMap* tw,
+                         const CUtensorMap* tx, const Unit& un, int kx, int wrow, int I, int nb,
+                         uint64_t pol_w, uint64_t pol_x) {
+  if (SWAP) {
+    if (MODE == 1) {  // 64 gate rows then 64 up rows of N-slice nt
+      tma_load_2d(a, tw, bar, kx, wrow + un.nt * 64, pol_w);
+      tma_load_2d(a + 64 * kRowBytes, tw, bar, kx, wrow + I + un.nt * 64, pol_w);
+    } else {
+      tma_load_2d(a, tw, bar, kx, wrow + un.nt * 128, pol_w);
+      tma_load_2d(a + 64 * kRowBytes, tw, bar, kx, wrow + un.nt * 128 + 64, pol_w);
+    }
+    for (int bb = 0; bb < nb; ++bb)
+      tma_load_2d(b + bb * kDecodeBoxRows * kRowBytes, tx, bar, kx,
+                  un.row0 + bb * kDecodeBoxRows, pol_x);
+  } else {
+    tma_load_2d(a, tx, bar, kx, un.row0, pol_x);
+    if (MODE == 1) {  // 128 gate rows then 128 up rows of N-slice nt
+      tma_load_2d(b, tw, bar, kx, wrow + un.nt * 128, pol_w);
+      tma_load_2d(b + kTileBytes, tw, bar, kx, wrow + I + un.nt * 128, pol_w);
+    } else {
+      tma_load_2d(b, tw, bar, kx, wrow + un.nt * 256, pol_w);
+      tma_load_2d(b + kTileBytes, tw, bar, kx, wrow + un.nt * 256 + 128, pol_w);
+    }
+  }
+}
+
+// Epilogue of one unit: TMEM -> registers -> fused op -> global memory.
+// Returns false if a bounded wait ran out.
 template <bool SWAP, int MODE, bool FP8>
+MOE_DEV bool epilogue_unit(const Unit& un, const JobP& j, int I, uint32_t tbase, int lrow,
+                           float* s_xch, uint64_t* xch_bar, uint32_t& xph, volatile int* abort) {
+  constexpr bool IS_FC2 = (MODE == 2 || MODE == 3);  // routing-weight epilogue
+  constexpr bool OUT_F32 = (MODE == 2);              // fp32 output (else bf16)
+  const int wrow0 = un.e * j.N_w;
+  if (SWAP) {
+    // lane = weight row of the slice, columns = the unit's token rows
+    const int ncols = ((un.rows + 15) / 16) * 16;
+    if (MODE == 1) {
+      const bool is_gate = lrow < 64;
+      const int n = un.nt * 64 + (lrow & 63);  // output column (intermediate index)
+      const float ws = FP8 ? j.w_scale[wrow0 + (is_gate ? n : I + n)] : 1.f;
+      for (int c = 0; c < ncols; c += 16) {
+        float v[16];
+        tmem_ld16(tbase + c, v);
+        tmem_ld_wait();
+        if (!is_gate) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) s_xch[(lrow - 64) * 17 + t] = v[t] * ws;
+        }
+        // bounded sync of the 128 epilogue threads (up values written)
+        mbar_arrive(xch_bar);
+        if (!mbar_wait(xch_bar, xph, abort)) return false;
+        xph ^= 1;
+        if (is_gate && n < I) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const int r = un.row0 + c + t;
+            if (c + t < un.rows) {
+              const float sa = FP8 ? j.a_scale[r] : 1.f;
+              const float g = v[t] * ws * sa;
+              const float up = s_xch[lrow * 17 + t] * sa;
+              reinterpret_cast<bf16*>(j.out)[(size_t)r * j.ldo + n] =
+                  __float2bfloat16_rn(silu_f(g) * up);
+            }
+          }
+        }
+        // bounded sync (up values consumed before the next chunk)
+        mbar_arrive(xch_bar);
+        if (!mbar_wait(xch_bar, xph, abort)) return false;
+        xph ^= 1;
+      }
+    } else {
+      const int n = un.nt * 128 + lrow;
+      const bool nvalid = n < j.n_out;
+      const float ws = (FP8 && nvalid) ? j.w_scale[wrow0 + n] : 1.f;
+      for (int c = 0; c < ncols; c += 16) {
+        float v[16];
+        tmem_ld16(tbase + c, v);
+        tmem_ld_wait();
+        if (nvalid) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const int r = un.row0 + c + t;
+            if (c + t < un.rows) {
+              float x = v[t] * ws * (FP8 ? j.a_scale[r] : 1.f);
+              if (IS_FC2 && j.topk_w) x *= j.topk_w[j.row_src[r]];
+              if (OUT_F32) {
+                reinterpret_cast<float*>(j.out)[(size_t)r * j.ldo + n] = x;
+              } else {
+                // FC2 bf16 rows go back to (token, slot) order
+                const int orow = (MODE == 3 && j.row_src) ? j.row_src[r] : r;
+                reinterpret_cast<bf16*>(j.out)[(size_t)orow * j.ldo + n] = __float2bfloat16_rn(x);
+              }
+            }
+          }
+        }
+      }
+    }
+  } else {
+    // lane = token row of the tile, columns = weight rows
+    const int r = un.row0 + lrow;
+    const bool rvalid = lrow < un.rows;
+    const float sa = (FP8 && rvalid) ? j.a_scale[r] : 1.f;
+    if (MODE == 1) {
+      for (int c = 0; c < 128; c += 16) {
+        float g[16], up[16];
+        tmem_ld16(tbase + c, g);
+        tmem_ld16(tbase + 128 + c, up);
+        tmem_ld_wait();
+        const int n0 = un.nt * 128 + c;
+        if (rvalid) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int t = 0; t < 16; t += 2) {
+            float o[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int n = min(n0 + t + h, I - 1);
+              const float gs = FP8 ? sa * j.w_scale[wrow0 + n] : 1.f;
+              const float us = FP8 ? sa * j.w_scale[wrow0 + I + n] : 1.f;
+              o[h] = silu_f(g[t + h] * gs) * (up[t + h] * us);
+            }
+            pk[t / 2] = pack2_bf16(o[0], o[1]);
+          }
+          bf16* dst = reinterpret_cast<bf16*>(j.out) + (size_t)r * j.ldo + n0;
+          if (n0 + 16 <= I) {
+            reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          } else {
+            for (int t = 0; t < 16 && n0 + t < I; ++t) {
+              const uint32_t w2 = pk[t / 2];
+              const uint16_t h = (t & 1) ? (uint16_t)(w2 >> 16) : (uint16_t)(w2 & 0xffffu);
+              reinterpret_cast<uint16_t*>(dst)[t] = h;
+            }
+          }
+        }
+      }
+    } else {
+      const float tw = (IS_FC2 && rvalid && j.topk_w) ? j.topk_w[j.row_src[r]] : 1.f;
+      // FC2 bf16 rows go back to (token, slot) order
+      const int orow = (MODE == 3 && rvalid && j.row_src) ? j.row_src[r] : r;
+      for (int c = 0; c < 256; c += 16) {
+        float v[16];
+        tmem_ld16(tbase + c, v);
+        tmem_ld_wait();
+        const int n0 = un.nt * 256 + c;
+        if (rvalid && n0 < j.n_out) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const float ws = FP8 ? j.w_scale[wrow0 + min(n0 + t, j.n_out - 1)] : 1.f;
+            v[t] = v[t] * ws * sa * tw;
+          }
+          if (OUT_F32) {
+            float* dst = reinterpret_cast<float*>(j.out) + (size_t)r * j.ldo + n0;
+            if (n0 + 16 <= j.n_out) {
+#pragma unroll
+              for (int t = 0; t < 16; t += 4)
+                reinterpret_cast<float4*>(dst)[t / 4] = make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]);
+            } else {
+              for (int t = 0; t < 16 && n0 + t < j.n_out; ++t) dst[t] = v[t];
+            }
+          } else {
+            bf16* dst = reinterpret_cast<bf16*>(j.out) + (size_t)orow * j.ldo + n0;
+            if (n0 + 16 <= j.n_out) {
+              uint32_t pk[8];
+#pragma unroll
+              for (int t = 0; t < 16; t += 2) pk[t / 2] = pack2_bf16(v[t], v[t + 1]);
+              reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            } else {
+              for (int t = 0; t < 16 && n0 + t < j.n_out; ++t) dst[t] = __float2bfloat16_rn(v[t]);
+            }
+          }
+        }
+      }
+    }
+  }
+  return true;
+}
+
+// Persistent grouped GEMM.  One launch runs job 0 (mode M0) and, when M1 >= 0,
+// job 1 (mode M1) after it: units of job 0 come first in the unit order.
+// Static schedule (p.sched == NULL): CTA c takes units c, c + grid, ...
+// Dynamic schedule: the producer claims units from p.sched[0]; a unit of job 1
+// for expert e first waits until every job-0 unit of expert e has finished its
+// epilogue (p.sched[1 + e]), so job 1 may read job 0's output with TMA.  Since
+// job-0 units are all claimed before any job-1 unit and a producer issues all
+// loads of a unit before it claims the next, every wait ends.
+template <bool SWAP, bool FP8, int M0, int M1>
 __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
-    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+    const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_x0,
+    const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_x1,
     const Params p) {
+  constexpr int NJ = (M1 >= 0) ? 2 : 1;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ int s_off[kMaxExperts + 1];
-  __shared__ int s_up[kMaxExperts + 1];
+  __shared__ int s_up[NJ][kMaxExperts + 1];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t ufull_bar[kUnitRing];
+  __shared__ __align__(8) uint64_t uempty_bar[kUnitRing];
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ __align__(8) uint64_t xch_bar;
+  __shared__ int s_uring[kUnitRing];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ float s_xch[SWAP && MODE == 1 ? 64 * 17 : 1];  // decode FC1: up values
+  __shared__ float s_xch[SWAP && (M0 == 1 || M1 == 1) ? 64 * 17 : 1];  // decode FC1: up values
 
-  constexpr bool IS_FC2 = (MODE == 2 || MODE == 3);  // routing-weight epilogue
-  constexpr bool OUT_F32 = (MODE == 2);              // fp32 output (else bf16)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~(uintptr_t)1023);
 
   // ---- set-up: barriers and TMEM first (no global memory), then wait for
-  // the previous kernel and build the unit table from the expert offsets
+  // the previous kernel and build the unit tables from the expert offsets
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -127,12 +349,20 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
       mbar_init(&tfull_bar[a], 1);
       mbar_init(&tempty_bar[a], 128);
     }
+    for (int i = 0; i < kUnitRing; ++i) {
+      mbar_init(&ufull_bar[i], 1);
+      mbar_init(&uempty_bar[i], 1 + 4);  // MMA thread + the four epilogue warps
+    }
     mbar_init(&drain_bar, 1);
     mbar_init(&xch_bar, 128);
     s_abort = 0;
     fence_mbar_init();
-    prefetch_tmap(&tm_w);
-    prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_w0);
+    prefetch_tmap(&tm_x0);
+    if (NJ == 2) {
+      prefetch_tmap(&tm_w1);
+      prefetch_tmap(&tm_x1);
+    }
   } else if (warp == 1) {
     tmem_alloc(&s_tmem, 2 * kAccCols);
     tmem_relinquish();
@@ -157,28 +387,46 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
     if (bad && blockIdx.x == 0) flag_status(p.status, MOE_ERR_INVALID_ARG);
   }
   __syncthreads();
-  if (warp == 0) {
+  if (warp < NJ) {  // warp jb builds job jb's unit prefix
+    const int jb = warp;
+    const int nt = p.job[jb].nt;
     int carry = 0;
     for (int base = 0; base < p.E; base += 32) {
       const int e = base + lane;
       const int cnt = (e < p.E) ? s_off[e + 1] - s_off[e] : 0;
-      const int v = ((cnt + p.chunk - 1) / p.chunk) * p.nt;
+      const int v = ((cnt + p.chunk - 1) / p.chunk) * nt;
       int incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += n;
       }
-      if (e < p.E) s_up[e] = carry + incl - v;
+      if (e < p.E) s_up[jb][e] = carry + incl - v;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) s_up[p.E] = carry;
+    if (lane == 0) s_up[jb][p.E] = carry;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const int U = s_up[p.E];
+  const int U0 = s_up[0][p.E];
+  const int U = U0 + (NJ == 2 ? s_up[NJ - 1][p.E] : 0);
+
+  auto decode_unit = [&](int u) -> Unit {
+    if (NJ == 2 && u >= U0) {
+      Unit un = unit_of(u - U0, s_off, s_up[NJ - 1], p.E, p.job[NJ - 1].nt, p.chunk);
+      un.job = 1;
+      return un;
+    }
+    return unit_of(u, s_off, s_up[0], p.E, p.job[0].nt, p.chunk);
+  };
+  // Consumers read claimed units in order from the unit ring.
+  auto next_unit = [&](int i) -> int {
+    const int slot = i % kUnitRing;
+    if (!mbar_wait(&ufull_bar[slot], (uint32_t)((i / kUnitRing) & 1), &s_abort)) return -2;
+    return s_uring[slot];
+  };
 
   if (warp == 0) {
     // ===================================================== TMA producer
@@ -188,38 +436,55 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-        const Unit un = unit_of(u, s_off, s_up, p.E, p.nt, p.chunk);
+      for (int i = 0; ok; ++i) {
+        // claim the next unit and publish it to the other roles
+        const int slot = i % kUnitRing;
+        if (!mbar_wait(&uempty_bar[slot], (uint32_t)(((i / kUnitRing) & 1) ^ 1), &s_abort)) {
+          ok = false;
+          break;
+        }
+        int u = p.sched ? atomicAdd(p.sched, 1) : (int)blockIdx.x + i * (int)gridDim.x;
+        if (u >= U) u = -1;
+        s_uring[slot] = u;
+        mbar_arrive(&ufull_bar[slot]);
+        if (u < 0) break;
+        const Unit un = decode_unit(u);
+        const JobP& j = p.job[un.job];
+        if (NJ == 2 && un.job == 1 && p.sched) {
+          // wait until job 0 (FC1) has written every row of expert e
+          const int cnt = s_off[un.e + 1] - s_off[un.e];
+          const int need = ((cnt + p.chunk - 1) / p.chunk) * p.job[0].nt * 4;
+          const long long t0 = clock64();
+          while (ld_acquire(p.sched + 1 + un.e) < need) {
+            if (s_abort || clock64() - t0 > kSpinLimitCycles) {
+              s_abort = 1;
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          fence_proxy_async_global();
+        }
         const int nb = SWAP ? (un.rows + kDecodeBoxRows - 1) / kDecodeBoxRows : 0;
-        const uint32_t tx = SWAP ? (uint32_t)(p.a_bytes + nb * kDecodeBoxRows * kRowBytes)
-                                 : (uint32_t)(kTileBytes + 2 * kTileBytes);
-        for (int ks = 0; ks < p.kst; ++ks) {
+        const uint32_t tx = (uint32_t)p.kw *
+                            (SWAP ? (uint32_t)(p.a_atom + nb * kDecodeBoxRows * kRowBytes)
+                                  : (uint32_t)(kTileBytes + 2 * kTileBytes));
+        const CUtensorMap* tw = un.job ? &tm_w1 : &tm_w0;
+        const CUtensorMap* tx_map = un.job ? &tm_x1 : &tm_x0;
+        for (int ks = 0; ks < j.kst; ++ks) {
           if (!mbar_wait(&empty_bar[s], ph ^ 1, &s_abort)) { ok = false; break; }
           mbar_arrive_expect_tx(&full_bar[s], tx);
           uint8_t* a = ring + (size_t)s * p.stage_bytes;
           uint8_t* b = a + p.a_bytes;
-          const int kx = ks * (FP8 ? 128 : 64);  // element coordinate along K
-          const int wrow = un.e * p.N_w;
-          if (SWAP) {
-            if (MODE == 1) {  // 64 gate rows then 64 up rows of N-slice nt
-              tma_load_2d(a, &tm_w, &full_bar[s], kx, wrow + un.nt * 64, pol_w);
-              tma_load_2d(a + 64 * kRowBytes, &tm_w, &full_bar[s], kx, wrow + p.I + un.nt * 64, pol_w);
-            } else {
-              tma_load_2d(a, &tm_w, &full_bar[s], kx, wrow + un.nt * 128, pol_w);
-              tma_load_2d(a + 64 * kRowBytes, &tm_w, &full_bar[s], kx, wrow + un.nt * 128 + 64, pol_w);
-            }
-            for (int bb = 0; bb < nb; ++bb)
-              tma_load_2d(b + bb * kDecodeBoxRows * kRowBytes, &tm_x, &full_bar[s], kx,
-                          un.row0 + bb * kDecodeBoxRows, pol_x);
-          } else {
-            tma_load_2d(a, &tm_x, &full_bar[s], kx, un.row0, pol_x);
-            if (MODE == 1) {  // 128 gate rows then 128 up rows of N-slice nt
-              tma_load_2d(b, &tm_w, &full_bar[s], kx, wrow + un.nt * 128, pol_w);
-              tma_load_2d(b + kTileBytes, &tm_w, &full_bar[s], kx, wrow + p.I + un.nt * 128, pol_w);
-            } else {
-              tma_load_2d(b, &tm_w, &full_bar[s], kx, wrow + un.nt * 256, pol_w);
-              tma_load_2d(b + kTileBytes, &tm_w, &full_bar[s], kx, wrow + un.nt * 256 + 128, pol_w);
-            }
+          const int wrow = un.e * j.N_w;
+          for (int w = 0; w < p.kw; ++w) {
+            const int kx = (ks * p.kw + w) * (FP8 ? 128 : 64);  // element coordinate along K
+            if ((un.job == 0 ? M0 : M1) == 1)
+              issue_stage<SWAP, 1>(a + w * p.a_atom, b + w * p.b_atom, &full_bar[s], tw, tx_map, un,
+                                   kx, wrow, p.I, nb, pol_w, pol_x);
+            else
+              issue_stage<SWAP, 0>(a + w * p.a_atom, b + w * p.b_atom, &full_bar[s], tw, tx_map, un,
+                                   kx, wrow, p.I, nb, pol_w, pol_x);
           }
           if (++s == p.stages) { s = 0; ph ^= 1; }
         }
@@ -244,25 +509,33 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
       uint32_t aph = 0;
       bool ok = true;
       bool issued = false;
-      for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-        const Unit un = unit_of(u, s_off, s_up, p.E, p.nt, p.chunk);
+      for (int i = 0; ok; ++i) {
+        const int u = next_unit(i);
+        if (u == -2) { ok = false; break; }
+        mbar_arrive(&uempty_bar[i % kUnitRing]);
+        if (u < 0) break;
+        const Unit un = decode_unit(u);
+        const int kst = p.job[un.job].kst;
         if (!mbar_wait(&tempty_bar[acc], aph ^ 1, &s_abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + acc * kAccCols;
         const int n = SWAP ? ((un.rows + 15) / 16) * 16 : 256;
         const uint32_t idesc = make_idesc(n, FP8 ? 0u : 1u);
-        for (int ks = 0; ks < p.kst; ++ks) {
+        for (int ks = 0; ks < kst; ++ks) {
           if (!mbar_wait(&full_bar[s], ph, &s_abort)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a = smem_u32(ring + (size_t)s * p.stage_bytes);
-          const uint32_t b = a + p.a_bytes;
+          const uint32_t a0 = smem_u32(ring + (size_t)s * p.stage_bytes);
+          const uint32_t b0 = a0 + p.a_bytes;
+          for (int w = 0; w < p.kw; ++w) {
+            const uint32_t a = a0 + w * p.a_atom, b = b0 + w * p.b_atom;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {  // four 32-byte K steps per 128-byte slice
-            const uint64_t ad = sw128_desc(a + kk * 32);
-            const uint64_t bd = sw128_desc(b + kk * 32);
-            const uint32_t accum = (ks | kk) ? 1u : 0u;
-            if (FP8) mma_e4m3(d, ad, bd, idesc, accum);
-            else mma_bf16(d, ad, bd, idesc, accum);
+            for (int kk = 0; kk < 4; ++kk) {  // four 32-byte K steps per 128-byte atom
+              const uint64_t ad = sw128_desc(a + kk * 32);
+              const uint64_t bd = sw128_desc(b + kk * 32);
+              const uint32_t accum = (ks | w | kk) ? 1u : 0u;
+              if (FP8) mma_e4m3(d, ad, bd, idesc, accum);
+              else mma_bf16(d, ad, bd, idesc, accum);
+            }
           }
           issued = true;
           mma_commit(&empty_bar[s]);
@@ -287,162 +560,43 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
     int acc = 0;
     uint32_t aph = 0;
     uint32_t xph = 0;  // phase of xch_bar (decode FC1 exchange)
-    bool ok = true;
-    for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-      const Unit un = unit_of(u, s_off, s_up, p.E, p.nt, p.chunk);
+    for (int i = 0;; ++i) {
+      const int u = next_unit(i);
+      __syncwarp();
+      if (lane == 0 && u != -2) mbar_arrive(&uempty_bar[i % kUnitRing]);
+      if (u == -2) {
+        flag_status(p.status, MOE_ERR_TIMEOUT);
+        break;
+      }
+      if (u < 0) break;
+      const Unit un = decode_unit(u);
       if (!mbar_wait(&tfull_bar[acc], aph, &s_abort)) {
         flag_status(p.status, MOE_ERR_TIMEOUT);
         break;
       }
       tc_fence_after();
       const uint32_t tbase = tmem + acc * kAccCols + ((uint32_t)(q * 32) << 16);
-      const int wrow0 = un.e * p.N_w;
-      if (SWAP) {
-        // lane = weight row of the slice, columns = the unit's token rows
-        const int ncols = ((un.rows + 15) / 16) * 16;
-        if (MODE == 1) {
-          const bool is_gate = lrow < 64;
-          const int n = un.nt * 64 + (lrow & 63);  // output column (intermediate index)
-          const float ws = FP8 ? p.w_scale[wrow0 + (is_gate ? n : p.I + n)] : 1.f;
-          for (int c = 0; c < ncols; c += 16) {
-            float v[16];
-            tmem_ld16(tbase + c, v);
-            tmem_ld_wait();
-            if (!is_gate) {
-#pragma unroll
-              for (int t = 0; t < 16; ++t) s_xch[(lrow - 64) * 17 + t] = v[t] * ws;
-            }
-            // bounded sync of the 128 epilogue threads (up values written)
-            mbar_arrive(&xch_bar);
-            if (!mbar_wait(&xch_bar, xph, &s_abort)) { ok = false; break; }
-            xph ^= 1;
-            if (is_gate && n < p.I) {
-#pragma unroll
-              for (int t = 0; t < 16; ++t) {
-                const int r = un.row0 + c + t;
-                if (c + t < un.rows) {
-                  const float sa = FP8 ? p.a_scale[r] : 1.f;
-                  const float g = v[t] * ws * sa;
-                  const float up = s_xch[lrow * 17 + t] * sa;
-                  reinterpret_cast<bf16*>(p.out)[(size_t)r * p.ldo + n] =
-                      __float2bfloat16_rn(silu_f(g) * up);
-                }
-              }
-            }
-            // bounded sync (up values consumed before the next chunk)
-            mbar_arrive(&xch_bar);
-            if (!mbar_wait(&xch_bar, xph, &s_abort)) { ok = false; break; }
-            xph ^= 1;
-          }
-          if (!ok) {
-            flag_status(p.status, MOE_ERR_TIMEOUT);
-            break;
-          }
-        } else {
-          const int n = un.nt * 128 + lrow;
-          const bool nvalid = n < p.n_out;
-          const float ws = (FP8 && nvalid) ? p.w_scale[wrow0 + n] : 1.f;
-          for (int c = 0; c < ncols; c += 16) {
-            float v[16];
-            tmem_ld16(tbase + c, v);
-            tmem_ld_wait();
-            if (nvalid) {
-#pragma unroll
-              for (int t = 0; t < 16; ++t) {
-                const int r = un.row0 + c + t;
-                if (c + t < un.rows) {
-                  float x = v[t] * ws * (FP8 ? p.a_scale[r] : 1.f);
-                  if (IS_FC2 && p.topk_w) x *= p.topk_w[p.row_src[r]];
-                  if (OUT_F32) {
-                    reinterpret_cast<float*>(p.out)[(size_t)r * p.ldo + n] = x;
-                  } else {
-                    reinterpret_cast<bf16*>(p.out)[(size_t)r * p.ldo + n] = __float2bfloat16_rn(x);
-                  }
-                }
-              }
-            }
-          }
-        }
-      } else {
-        // lane = token row of the tile, columns = weight rows
-        const int r = un.row0 + lrow;
-        const bool rvalid = lrow < un.rows;
-        const float sa = (FP8 && rvalid) ? p.a_scale[r] : 1.f;
-        if (MODE == 1) {
-          for (int c = 0; c < 128; c += 16) {
-            float g[16], up[16];
-            tmem_ld16(tbase + c, g);
-            tmem_ld16(tbase + 128 + c, up);
-            tmem_ld_wait();
-            const int n0 = un.nt * 128 + c;
-            if (rvalid) {
-              uint32_t pk[8];
-#pragma unroll
-              for (int t = 0; t < 16; t += 2) {
-                float o[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const int n = min(n0 + t + h, p.I - 1);
-                  const float gs = FP8 ? sa * p.w_scale[wrow0 + n] : 1.f;
-                  const float us = FP8 ? sa * p.w_scale[wrow0 + p.I + n] : 1.f;
-                  o[h] = silu_f(g[t + h] * gs) * (up[t + h] * us);
-                }
-                pk[t / 2] = pack2_bf16(o[0], o[1]);
-              }
-              bf16* dst = reinterpret_cast<bf16*>(p.out) + (size_t)r * p.ldo + n0;
-              if (n0 + 16 <= p.I) {
-                reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-              } else {
-                for (int t = 0; t < 16 && n0 + t < p.I; ++t) {
-                  const uint32_t w2 = pk[t / 2];
-                  const uint16_t h = (t & 1) ? (uint16_t)(w2 >> 16) : (uint16_t)(w2 & 0xffffu);
-                  reinterpret_cast<uint16_t*>(dst)[t] = h;
-                }
-              }
-            }
-          }
-        } else {
-          const float tw = (IS_FC2 && rvalid && p.topk_w) ? p.topk_w[p.row_src[r]] : 1.f;
-          for (int c = 0; c < 256; c += 16) {
-            float v[16];
-            tmem_ld16(tbase + c, v);
-            tmem_ld_wait();
-            const int n0 = un.nt * 256 + c;
-            if (rvalid && n0 < p.n_out) {
-#pragma unroll
-              for (int t = 0; t < 16; ++t) {
-                const float ws = FP8 ? p.w_scale[wrow0 + min(n0 + t, p.n_out - 1)] : 1.f;
-                v[t] = v[t] * ws * sa * tw;
-              }
-              if (OUT_F32) {
-                float* dst = reinterpret_cast<float*>(p.out) + (size_t)r * p.ldo + n0;
-                if (n0 + 16 <= p.n_out) {
-#pragma unroll
-                  for (int t = 0; t < 16; t += 4)
-                    reinterpret_cast<float4*>(dst)[t / 4] = make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]);
-                } else {
-                  for (int t = 0; t < 16 && n0 + t < p.n_out; ++t) dst[t] = v[t];
-                }
-              } else {
-                bf16* dst = reinterpret_cast<bf16*>(p.out) + (size_t)r * p.ldo + n0;
-                if (n0 + 16 <= p.n_out) {
-                  uint32_t pk[8];
-#pragma unroll
-                  for (int t = 0; t < 16; t += 2) pk[t / 2] = pack2_bf16(v[t], v[t + 1]);
-                  reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                  reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                } else {
-                  for (int t = 0; t < 16 && n0 + t < p.n_out; ++t) dst[t] = __float2bfloat16_rn(v[t]);
-                }
-              }
-            }
-          }
-        }
+      bool ok;
+      if (un.job == 0)
+        ok = epilogue_unit<SWAP, M0, FP8>(un, p.job[0], p.I, tbase, lrow, s_xch, &xch_bar, xph,
+                                          &s_abort);
+      else
+        ok = epilogue_unit<SWAP, (M1 >= 0 ? M1 : M0), FP8>(un, p.job[1], p.I, tbase, lrow, s_xch,
+                                                           &xch_bar, xph, &s_abort);
+      if (!ok) {
+        flag_status(p.status, MOE_ERR_TIMEOUT);
+        break;
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
       if (++acc == 2) { acc = 0; aph ^= 1; }
+      if (NJ == 2 && un.job == 0 && p.sched) {
+        // publish this warp's rows of the FC1 output to later TMA readers
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.sched + 1 + un.e, 1);
+      }
     }
   }
 
@@ -481,22 +635,85 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, int64_t rows, int64_t 
   return r == CUDA_SUCCESS;
 }
 
-template <bool SWAP, int MODE, bool FP8>
-cudaError_t launch_one(const CUtensorMap& tw, const CUtensorMap& tx, const Params& p, int grid,
-                       size_t smem, cudaStream_t st) {
-  auto k = moe_tc_gemm_kernel<SWAP, MODE, FP8>;
+template <bool SWAP, bool FP8, int M0, int M1>
+cudaError_t launch_k(const CUtensorMap* maps, const Params& p, int grid, size_t smem,
+                     cudaStream_t st) {
+  auto k = moe_tc_gemm_kernel<SWAP, FP8, M0, M1>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(k, dim3(grid), dim3(kThreads), smem, st, tw, tx, p);
+  return launch_kernel(k, dim3(grid), dim3(kThreads), smem, st, maps[0], maps[1], maps[2], maps[3],
+                       p);
 }
 
 template <bool SWAP, bool FP8>
-cudaError_t launch_mode(int mode, const CUtensorMap& tw, const CUtensorMap& tx, const Params& p,
-                        int grid, size_t smem, cudaStream_t st) {
-  if (mode == 0) return launch_one<SWAP, 0, FP8>(tw, tx, p, grid, smem, st);
-  if (mode == 1) return launch_one<SWAP, 1, FP8>(tw, tx, p, grid, smem, st);
-  if (mode == 2) return launch_one<SWAP, 2, FP8>(tw, tx, p, grid, smem, st);
-  return launch_one<SWAP, 3, FP8>(tw, tx, p, grid, smem, st);
+cudaError_t launch_mode(int mode, const CUtensorMap* maps, const Params& p, int grid, size_t smem,
+                        cudaStream_t st) {
+  if (mode == 0) return launch_k<SWAP, FP8, 0, -1>(maps, p, grid, smem, st);
+  if (mode == 1) return launch_k<SWAP, FP8, 1, -1>(maps, p, grid, smem, st);
+  if (mode == 2) return launch_k<SWAP, FP8, 2, -1>(maps, p, grid, smem, st);
+  return launch_k<SWAP, FP8, 3, -1>(maps, p, grid, smem, st);
+}
+
+// Token rows per decode unit: an expert normally holds <= T rows (distinct
+// experts per token); larger segments are split into more units, so the B
+// tile of a unit always fits its ring slot.
+int decode_chunk(int T) {
+  int chunk = T < kDecodeMaxN ? T : kDecodeMaxN;
+  return ((chunk < 1 ? 1 : chunk) + kDecodeBoxRows - 1) / kDecodeBoxRows * kDecodeBoxRows;
+}
+
+// Fills one job and its two tensor maps; false if the shape is not covered.
+bool make_job(JobP* j, CUtensorMap* tw, CUtensorMap* tx, int mode, bool fp8, bool decode,
+              const void* a, const float* a_scale, const void* w, const float* w_scale,
+              const int32_t* row_src, const float* topk_w, void* c, int E, int K, int I,
+              int N_out, int R_max) {
+  if (K % 64 != 0) return false;
+  const int elem = fp8 ? 1 : 2;
+  j->a_scale = a_scale;
+  j->w_scale = w_scale;
+  j->row_src = row_src;
+  j->topk_w = topk_w;
+  j->out = c;
+  j->ldo = N_out;
+  j->N_w = (mode >= 2) ? N_out : 2 * I;
+  j->n_out = N_out;
+  j->kst = K * elem;  // bytes of K; set_ring() turns it into stages
+  if (decode) {
+    if (mode == 1 && I % 64 != 0) return false;
+    j->nt = (mode == 1) ? I / 64 : (N_out + 127) / 128;
+  } else {
+    j->nt = (mode == 1) ? (I + 127) / 128 : (N_out + 255) / 256;
+  }
+  return make_map(tw, w, fp8, (int64_t)E * j->N_w, K, decode ? 64 : 128) &&
+         make_map(tx, a, fp8, R_max, K, decode ? kDecodeBoxRows : 128);
+}
+
+// Ring geometry shared by the launches; converts each job's K bytes into
+// stages of kw atoms.
+bool set_ring(Params* p, bool decode, int T, size_t* smem) {
+  const int static_smem = 8 * 1024;
+  p->chunk = decode ? decode_chunk(T) : kTileRows;
+  p->a_atom = kTileBytes;
+  p->b_atom = decode ? p->chunk * kRowBytes : 2 * kTileBytes;
+  int kw = 1;
+  if (decode) {
+    kw = 2;
+    const char* env = getenv("MOE_DECODE_KW");
+    if (env && (env[0] == '1' || env[0] == '2' || env[0] == '4')) kw = env[0] - '0';
+    while (kw > 1 && (kSmemLimit - static_smem - 1024) / (kw * (p->a_atom + p->b_atom)) < 3) kw /= 2;
+  }
+  p->kw = kw;
+  p->a_bytes = kw * p->a_atom;
+  p->stage_bytes = kw * (p->a_atom + p->b_atom);
+  int stages = (kSmemLimit - static_smem - 1024) / p->stage_bytes;
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return false;
+  p->stages = stages;
+  *smem = (size_t)stages * p->stage_bytes + 1024;
+  const int atom_bytes = kw * kRowBytes;
+  for (int jb = 0; jb < p->njobs; ++jb)
+    p->job[jb].kst = (p->job[jb].kst + atom_bytes - 1) / atom_bytes;
+  return true;
 }
 
 }  // namespace
@@ -509,62 +726,61 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
                            int I, int N_out, int R_max, int T, int sms, int* status,
                            cudaStream_t st) {
   std::call_once(g_encode_once, load_encode);
-  if (!g_encode || R_max == 0) return R_max == 0 ? cudaSuccess : cudaErrorNotSupported;
-  if (E > kMaxExperts || K % 64 != 0) return cudaErrorNotSupported;
-  const int elem = fp8 ? 1 : 2;
-  const int N_w = (mode >= 2) ? N_out : 2 * I;  // weight rows per expert
+  if (R_max == 0) return cudaSuccess;
+  if (!g_encode || E > kMaxExperts) return cudaErrorNotSupported;
   Params p{};
   p.offsets = offsets;
-  p.row_src = row_src;
-  p.topk_w = topk_w;
-  p.a_scale = a_scale;
-  p.w_scale = w_scale;
-  p.out = c;
-  p.ldo = N_out;
   p.E = E;
-  p.R_max = R_max;
   p.I = I;
-  p.N_w = N_w;
-  p.n_out = N_out;
-  p.kst = (K * elem + kRowBytes - 1) / kRowBytes;
+  p.R_max = R_max;
+  p.njobs = 1;
+  p.sched = nullptr;
   p.status = status;
-  if (decode) {
-    // Token rows per unit: an expert normally holds <= T rows (distinct
-    // experts per token); larger segments are split into more units, so the
-    // B tile of a unit always fits its ring slot.
-    int chunk = T < kDecodeMaxN ? T : kDecodeMaxN;
-    chunk = ((chunk < 1 ? 1 : chunk) + kDecodeBoxRows - 1) / kDecodeBoxRows * kDecodeBoxRows;
-    if (mode == 1 && I % 64 != 0) return cudaErrorNotSupported;
-    p.chunk = chunk;
-    p.nt = (mode == 1) ? I / 64 : (N_out + 127) / 128;
-    p.a_bytes = kTileBytes;
-    p.stage_bytes = p.a_bytes + chunk * kRowBytes;
-  } else {
-    p.chunk = kTileRows;
-    p.nt = (mode == 1) ? (I + 127) / 128 : (N_out + 255) / 256;
-    p.a_bytes = kTileBytes;
-    p.stage_bytes = 3 * kTileBytes;
-  }
-  const int static_smem = 8 * 1024;
-  int stages = (kSmemLimit - static_smem - 1024) / p.stage_bytes;
-  if (stages > kMaxStages) stages = kMaxStages;
-  if (stages < 2) return cudaErrorNotSupported;
-  p.stages = stages;
-  const size_t smem = (size_t)stages * p.stage_bytes + 1024;
-
-  CUtensorMap tm_w, tm_x;
-  if (!make_map(&tm_w, w, fp8, (int64_t)E * N_w, K, decode ? 64 : 128)) return cudaErrorNotSupported;
-  if (!make_map(&tm_x, a, fp8, R_max, K, decode ? kDecodeBoxRows : 128)) return cudaErrorNotSupported;
+  CUtensorMap maps[4];
+  if (!make_job(&p.job[0], &maps[0], &maps[1], mode, fp8, decode, a, a_scale, w, w_scale, row_src,
+                topk_w, c, E, K, I, N_out, R_max))
+    return cudaErrorNotSupported;
+  maps[2] = maps[0];
+  maps[3] = maps[1];
+  size_t smem = 0;
+  if (!set_ring(&p, decode, T, &smem)) return cudaErrorNotSupported;
+  p.job[1] = p.job[0];
   // upper bound on units: every expert's token chunks times the N tiles
   const int64_t chunks = (int64_t)(R_max + p.chunk - 1) / p.chunk + E;
-  int64_t units = chunks * p.nt;
+  const int64_t units = chunks * p.job[0].nt;
   int grid = (int)(units < sms ? units : sms);
   if (grid < 1) grid = 1;
   if (decode)
-    return fp8 ? launch_mode<true, true>(mode, tm_w, tm_x, p, grid, smem, st)
-               : launch_mode<true, false>(mode, tm_w, tm_x, p, grid, smem, st);
-  return fp8 ? launch_mode<false, true>(mode, tm_w, tm_x, p, grid, smem, st)
-             : launch_mode<false, false>(mode, tm_w, tm_x, p, grid, smem, st);
+    return fp8 ? launch_mode<true, true>(mode, maps, p, grid, smem, st)
+               : launch_mode<true, false>(mode, maps, p, grid, smem, st);
+  return fp8 ? launch_mode<false, true>(mode, maps, p, grid, smem, st)
+             : launch_mode<false, false>(mode, maps, p, grid, smem, st);
+}
+
+cudaError_t launch_decode_ffn_fused(const void* xp, const void* w13, const void* w2, void* act,
+                                    void* y, const int32_t* offsets, const int32_t* row_src,
+                                    const float* topk_w, int* sched, int E, int H, int I, int R_max,
+                                    int T, int sms, int* status, cudaStream_t st) {
+  std::call_once(g_encode_once, load_encode);
+  if (R_max == 0) return cudaSuccess;
+  if (!g_encode || E > kMaxExperts || !sched) return cudaErrorNotSupported;
+  Params p{};
+  p.offsets = offsets;
+  p.E = E;
+  p.I = I;
+  p.R_max = R_max;
+  p.njobs = 2;
+  p.sched = sched;
+  p.status = status;
+  CUtensorMap maps[4];
+  if (!make_job(&p.job[0], &maps[0], &maps[1], 1, false, true, xp, nullptr, w13, nullptr, row_src,
+                nullptr, act, E, H, I, I, R_max) ||
+      !make_job(&p.job[1], &maps[2], &maps[3], 3, false, true, act, nullptr, w2, nullptr, row_src,
+                topk_w, y, E, I, I, H, R_max))
+    return cudaErrorNotSupported;
+  size_t smem = 0;
+  if (!set_ring(&p, true, T, &smem)) return cudaErrorNotSupported;
+  return launch_k<true, false, 1, 3>(maps, p, sms, smem, st);
 }
 
 }  // namespace moe

@@ -16,21 +16,26 @@ cudaError_t launch_router_logits(const void* xhat, const float* wr, int T, int H
                                  float* part, cudaStream_t st);
 cudaError_t launch_topk(const float* part, int ks, const float* bias, int T, int E, int k,
                         int32_t* ids, float* w, float* logits_out, cudaStream_t st);
+// The permute kernels also zero nzero ints at zero_buf (counters of later
+// kernels in the same forward); zero_buf may be NULL with nzero = 0.
 cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* offsets,
-                           int32_t* row_src, int32_t* row_of_pair, int* status, cudaStream_t st);
+                           int32_t* row_src, int32_t* row_of_pair, int* status, cudaStream_t st,
+                           int32_t* zero_buf = nullptr, int nzero = 0);
 // Permute for any batch: the one-CTA kernel for small batches, else the
 // parallel count / scan / scatter kernels, which need
 // permute_workspace_bytes() of device scratch (cnt_ws).
 size_t permute_workspace_bytes(int T, int E, int k);
 cudaError_t launch_permute_any(const int32_t* ids, int T, int E, int k, int32_t* offsets,
                                int32_t* row_src, int32_t* row_of_pair, int32_t* cnt_ws,
-                               int* status, cudaStream_t st);
+                               int* status, cudaStream_t st, int32_t* zero_buf = nullptr,
+                               int nzero = 0);
 cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* row_src, int k,
                                int R_max, const void* src, void* dst, int row_bytes,
                                const float* sscale, float* dscale, cudaStream_t st);
 cudaError_t launch_silu_and_mul(const void* h, int R, int I, void* a, cudaStream_t st);
-cudaError_t launch_combine(const void* y, bool y_bf16, const int32_t* row_of_pair, int T, int k,
-                           int H, void* out, cudaStream_t st);
+cudaError_t launch_combine(const void* y, bool y_bf16, bool pair_order,
+                           const int32_t* row_of_pair, int T, int k, int H, void* out,
+                           cudaStream_t st);
 cudaError_t launch_quant_rows(const void* x, int64_t rows, int cols, void* q, float* scale,
                               const int32_t* nrows_dev, cudaStream_t st);
 

@@ -95,43 +95,60 @@ cudaError_t launch_rmsnorm(const void* x, const void* w, int T, int H, float eps
 // ================================================================ router logits
 // part[z, t, e] = sum over the z-th K chunk of xhat[t, h] * Wr[h, e]  (fp32,
 // h ascending within the chunk).  The chunks are summed in order by the
-// top-k kernel, so the logits are deterministic.  CTA tile: 64 tokens x 64
-// experts, K step 32, 256 threads with a 4 x 4 register tile each (float4
-// shared-memory reads: 2 loads per 16 FMA).
-constexpr int RT_T = 64, RT_E = 64, RT_K = 32;
+// top-k kernel, so the logits are deterministic.  CTA tile: TT tokens x TE
+// experts, K step 32; each thread owns an 8 x 8 register tile (four 16-byte
+// shared-memory reads per 64 FMA).  The next K slice is prefetched into
+// registers while the current one is multiplied out of shared memory.
+constexpr int RT_K = 32;
 
-__global__ void __launch_bounds__(256) router_logits_kernel(const bf16* __restrict__ xhat,
-                                                            const float* __restrict__ wr, int T,
-                                                            int H, int E, int kchunk,
-                                                            float* __restrict__ part) {
+struct RouterTile {
+  int tt, te;
+};
+
+// 128x64 for many tokens, 64x128 for few tokens and many experts, else 64x64.
+RouterTile router_tile(int T, int E) {
+  if (T >= 128) return {128, 64};
+  if (E >= 128) return {64, 128};
+  return {64, 64};
+}
+
+template <int TT, int TE>
+__global__ void __launch_bounds__((TT / 8) * (TE / 8)) router_logits_kernel(
+    const bf16* __restrict__ xhat, const float* __restrict__ wr, int T, int H, int E, int kchunk,
+    float* __restrict__ part) {
+  constexpr int NT = (TT / 8) * (TE / 8);           // threads
+  constexpr int XV = TT * RT_K * 2 / 16 / NT;       // x_hat uint4 loads per thread
+  constexpr int WV = RT_K * TE * 4 / 16 / NT;       // W_r float4 loads per thread
+  constexpr int XPT = RT_K / 8 / (NT / TT);         // uint4 of one token row per thread
+  __shared__ __align__(16) float xs[RT_K][TT + 4];  // [k][token]
+  __shared__ __align__(16) float ws[RT_K][TE];      // [k][expert]
   pdl_trigger();
   pdl_wait();
-  __shared__ __align__(16) float xs[RT_K][RT_T + 4];  // [k][token]
-  __shared__ __align__(16) float ws[RT_K][RT_E];      // [k][expert]
   const int tid = threadIdx.x;
-  const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E;
+  const int t0 = blockIdx.x * TT, e0 = blockIdx.y * TE;
   const int kb0 = blockIdx.z * kchunk;
   const int kb1 = min(H, kb0 + kchunk);
-  const int tx = tid & 15, ty = tid >> 4;  // experts tx*4.., tokens ty*4..
+  const int tx = tid % (TE / 8), ty = tid / (TE / 8);  // experts tx*8.., tokens ty*8..
   const bool e_vec = (E % 4 == 0);
-  float acc[4][4];
+  // x_hat loads: thread -> token xt, uint4 chunks xc .. xc + XV - 1 of its 32-k row
+  const int xt = tid / (NT / TT), xc = (tid % (NT / TT)) * XPT;
+  float acc[8][8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  // Global loads of the next K slice go to registers while the current one
-  // is multiplied out of shared memory (software pipelining).
-  const int xt = tid >> 2, xk = (tid & 3) * 8;  // x_hat: token, first k of 8
-  uint4 xr = make_uint4(0u, 0u, 0u, 0u);
-  float4 wv[2];
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  uint4 xr[XV];
+  float4 wv[WV];
   auto gload = [&](int kb) {
     const int t = t0 + xt;
-    xr = (t < T) ? *reinterpret_cast<const uint4*>(xhat + (size_t)t * H + kb + xk)
-                 : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {  // W_r: 32 k x 64 experts, a float4 per thread per i
-      const int idx = tid + i * 256;
-      const int kk = idx >> 4, e = e0 + (idx & 15) * 4;
+    for (int i = 0; i < XV; ++i)
+      xr[i] = (t < T) ? *reinterpret_cast<const uint4*>(xhat + (size_t)t * H + kb + (xc + i) * 8)
+                      : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int i = 0; i < WV; ++i) {
+      const int idx = tid + i * NT;
+      const int kk = idx / (TE / 4), e = e0 + (idx % (TE / 4)) * 4;
       const float* src = wr + (size_t)(kb + kk) * E + e;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (e_vec && e + 3 < E) {
@@ -147,48 +164,54 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const bf16* __restri
   };
   if (kb0 < kb1) gload(kb0);
   for (int kb = kb0; kb < kb1; kb += RT_K) {
-    {
+#pragma unroll
+    for (int i = 0; i < XV; ++i) {
       float f[8];
-      unpack8_bf16(xr, f);
+      unpack8_bf16(xr[i], f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) xs[xk + i][xt] = f[i];
+      for (int q = 0; q < 8; ++q) xs[(xc + i) * 8 + q][xt] = f[q];
+    }
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int idx = tid + i * 256;
-        *reinterpret_cast<float4*>(&ws[idx >> 4][(idx & 15) * 4]) = wv[i];
-      }
+    for (int i = 0; i < WV; ++i) {
+      const int idx = tid + i * NT;
+      *reinterpret_cast<float4*>(&ws[idx / (TE / 4)][(idx % (TE / 4)) * 4]) = wv[i];
     }
     __syncthreads();
     if (kb + RT_K < kb1) gload(kb + RT_K);
-#pragma unroll 8
+#pragma unroll 4
     for (int kk = 0; kk < RT_K; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
-      const float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      const float4 a0 = *reinterpret_cast<const float4*>(&xs[kk][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&xs[kk][ty * 8 + 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&ws[kk][tx * 8]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&ws[kk][tx * 8 + 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + ty * 8 + i;
     if (t >= T) continue;
+    float* dst = part + ((size_t)blockIdx.z * T + t) * E;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx * 4 + j;
-      if (e < E) part[((size_t)blockIdx.z * T + t) * E + e] = acc[i][j];
+    for (int j = 0; j < 8; ++j) {
+      const int e = e0 + tx * 8 + j;
+      if (e < E) dst[e] = acc[i][j];
     }
   }
 }
 
 int route_splits(int T, int H, int E) {
-  const int tiles = ((T + RT_T - 1) / RT_T) * ((E + RT_E - 1) / RT_E);
+  const RouterTile rt = router_tile(T, E);
+  const int tiles = ((T + rt.tt - 1) / rt.tt) * ((E + rt.te - 1) / rt.te);
   const int steps = H / RT_K;
-  int ks = (2 * 152 + tiles - 1) / tiles;
-  const int min_steps = 8;  // at least 256 K per chunk
+  int ks = (4 * 152 + tiles - 1) / tiles;  // about four CTAs per SM
+  const int min_steps = 8;                 // at least 256 K per chunk
   if (ks > steps / min_steps) ks = steps / min_steps;
   if (ks < 1) ks = 1;
   const int per = (steps + ks - 1) / ks;  // K steps per chunk
@@ -204,9 +227,16 @@ cudaError_t launch_router_logits(const void* xhat, const float* wr, int T, int H
   const int kchunk = per * RT_K;
   const int ks_eff = (H + kchunk - 1) / kchunk;
   if (ks_eff != ks) return cudaErrorInvalidValue;  // route_splits() keeps these equal
-  dim3 grid((T + RT_T - 1) / RT_T, (E + RT_E - 1) / RT_E, ks);
-  return launch_kernel(router_logits_kernel, grid, dim3(256), 0, st, (const bf16*)xhat, wr, T, H, E,
-                       kchunk, part);
+  const RouterTile rt = router_tile(T, E);
+  dim3 grid((T + rt.tt - 1) / rt.tt, (E + rt.te - 1) / rt.te, ks);
+  if (rt.tt == 128)
+    return launch_kernel(router_logits_kernel<128, 64>, grid, dim3(128), 0, st, (const bf16*)xhat,
+                         wr, T, H, E, kchunk, part);
+  if (rt.te == 128)
+    return launch_kernel(router_logits_kernel<64, 128>, grid, dim3(128), 0, st, (const bf16*)xhat,
+                         wr, T, H, E, kchunk, part);
+  return launch_kernel(router_logits_kernel<64, 64>, grid, dim3(64), 0, st, (const bf16*)xhat, wr,
+                       T, H, E, kchunk, part);
 }
 
 // ==================================================== softmax / top-k / renorm
@@ -314,10 +344,12 @@ constexpr int PERM_WARPS = 32;
 
 __global__ void __launch_bounds__(PERM_WARPS * 32) permute_kernel(
     const int32_t* __restrict__ ids, int T, int E, int k, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ row_src, int32_t* __restrict__ row_of_pair, int* status) {
+    int32_t* __restrict__ row_src, int32_t* __restrict__ row_of_pair, int* status,
+    int32_t* __restrict__ zero_buf, int nzero) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ int sm[];
+  for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero_buf[i] = 0;  // later kernels' counters
   int* cnt = sm;                         // [PERM_WARPS][E]
   int* tot = sm + PERM_WARPS * E;        // [E + 1]
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -391,10 +423,11 @@ __global__ void __launch_bounds__(PERM_WARPS * 32) permute_kernel(
 }
 
 cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* offsets,
-                           int32_t* row_src, int32_t* row_of_pair, int* status, cudaStream_t st) {
+                           int32_t* row_src, int32_t* row_of_pair, int* status, cudaStream_t st,
+                           int32_t* zero_buf, int nzero) {
   size_t smem = (size_t)(PERM_WARPS * E + E + 1) * sizeof(int);
   return launch_kernel(permute_kernel, dim3(1), dim3(PERM_WARPS * 32), smem, st, ids, T, E, k,
-                       offsets, row_src, row_of_pair, status);
+                       offsets, row_src, row_of_pair, status, zero_buf, nzero);
 }
 
 // Parallel form of the same stable counting sort, for large batches: chunks
@@ -430,9 +463,12 @@ __global__ void __launch_bounds__(256) permute_count_kernel(const int32_t* __res
 
 __global__ void __launch_bounds__(256) permute_scan_kernel(int nch, int E,
                                                            int32_t* __restrict__ cnt,
-                                                           int32_t* __restrict__ offsets) {
+                                                           int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ zero_buf,
+                                                           int nzero) {
   pdl_trigger();
   pdl_wait();
+  for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero_buf[i] = 0;  // later kernels' counters
   __shared__ int tot[kMaxExperts + 1];
   const int e = threadIdx.x;
   if (e < E) {
@@ -509,14 +545,16 @@ size_t permute_workspace_bytes(int T, int E, int k) {
 
 cudaError_t launch_permute_any(const int32_t* ids, int T, int E, int k, int32_t* offsets,
                                int32_t* row_src, int32_t* row_of_pair, int32_t* cnt_ws,
-                               int* status, cudaStream_t st) {
+                               int* status, cudaStream_t st, int32_t* zero_buf, int nzero) {
   if (!permute_parallel(T, k))
-    return launch_permute(ids, T, E, k, offsets, row_src, row_of_pair, status, st);
+    return launch_permute(ids, T, E, k, offsets, row_src, row_of_pair, status, st, zero_buf,
+                          nzero);
   const int nch = permute_chunks(T);
   cudaError_t e = launch_kernel(permute_count_kernel, dim3(nch), dim3(256), 0, st, ids, T, E, k,
                                 cnt_ws, status);
   if (e != cudaSuccess) return e;
-  e = launch_kernel(permute_scan_kernel, dim3(1), dim3(256), 0, st, nch, E, cnt_ws, offsets);
+  e = launch_kernel(permute_scan_kernel, dim3(1), dim3(256), 0, st, nch, E, cnt_ws, offsets,
+                    zero_buf, nzero);
   if (e != cudaSuccess) return e;
   return launch_kernel(permute_scatter_kernel, dim3(nch), dim3(32), 0, st, ids, T, E, k,
                        (const int32_t*)cnt_ws, row_src, row_of_pair);
@@ -588,9 +626,11 @@ cudaError_t launch_silu_and_mul(const void* h, int R, int I, void* a, cudaStream
 }
 
 // ===================================================================== combine
-// out[t, :] = bf16( sum_j y[row_of_pair[t*k + j], :] ), fp32, j ascending;
-// y is fp32 or bf16.  Each thread handles 8 consecutive columns.
-template <bool YBF16>
+// out[t, :] = bf16( sum_j y_j ), fp32, j ascending, where y_j is row
+// t*k + j of y (PAIR = true: rows in (token, slot) order, row_of_pair only
+// marks skipped pairs with -1) or row row_of_pair[t*k + j] (PAIR = false:
+// rows in expert order).  y is fp32 or bf16.  Each thread handles 8 columns.
+template <bool YBF16, bool PAIR>
 __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y,
                                                       const int32_t* __restrict__ row_of_pair,
                                                       int T, int k, int H, bf16* __restrict__ out) {
@@ -605,13 +645,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
   float v[kMaxTopK][8];
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) {  // all loads first (up to 8 rows in flight)
-    if (j < k && rows[j] >= 0) {
+    // in pair order the row address does not wait for the index load
+    const int64_t row = PAIR ? (int64_t)t * k + j : (int64_t)rows[j];
+    if (j < k && (PAIR || rows[j] >= 0)) {
       if (YBF16) {
         unpack8_bf16(reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(y) +
-                                                    (size_t)rows[j] * H)[h8], v[j]);
+                                                    row * H)[h8], v[j]);
       } else {
         const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(y) +
-                                                            (size_t)rows[j] * H) + 2 * h8;
+                                                            row * H) + 2 * h8;
         const float4 a = src[0], b = src[1];
         v[j][0] = a.x; v[j][1] = a.y; v[j][2] = a.z; v[j][3] = a.w;
         v[j][4] = b.x; v[j][5] = b.y; v[j][6] = b.z; v[j][7] = b.w;
@@ -625,8 +667,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
 #pragma unroll
   for (int i = 0; i < 8; ++i) s[i] = 0.f;
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {  // summed in j order
-    if (j < k) {
+  for (int j = 0; j < kMaxTopK; ++j) {  // summed in j order, skipped pairs excluded
+    if (j < k && rows[j] >= 0) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) s[i] += v[j][i];
     }
@@ -639,16 +681,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
   reinterpret_cast<uint4*>(out + (size_t)t * H)[h8] = o;
 }
 
-cudaError_t launch_combine(const void* y, bool y_bf16, const int32_t* row_of_pair, int T, int k,
-                           int H, void* out, cudaStream_t st) {
+cudaError_t launch_combine(const void* y, bool y_bf16, bool pair_order,
+                           const int32_t* row_of_pair, int T, int k, int H, void* out,
+                           cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   const int h8 = H / 8;
   dim3 grid((h8 + 255) / 256, T);
-  if (y_bf16)
-    return launch_kernel(combine_kernel<true>, grid, dim3(256), 0, st, y, row_of_pair, T, k, H,
-                         (bf16*)out);
-  return launch_kernel(combine_kernel<false>, grid, dim3(256), 0, st, y, row_of_pair, T, k, H,
-                       (bf16*)out);
+#define MOE_COMBINE(B, P) \
+  return launch_kernel(combine_kernel<B, P>, grid, dim3(256), 0, st, y, row_of_pair, T, k, H, (bf16*)out)
+  if (y_bf16) { if (pair_order) MOE_COMBINE(true, true); else MOE_COMBINE(true, false); }
+  else { if (pair_order) MOE_COMBINE(false, true); else MOE_COMBINE(false, false); }
+#undef MOE_COMBINE
 }
 
 // ========================================================== row E4M3 quantiser

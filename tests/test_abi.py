@@ -111,8 +111,8 @@ def test_step_entry_points_reject_bad_arguments_on_host(M):
     assert M.lib.moe_permute(fake, 4096, 64, 8, fake, fake, fake, None, None, 0, None, None, None,
                              0, None) == 4
     assert M.lib.moe_silu_and_mul(fake, 4, 12, fake, None) == 2
-    assert M.lib.moe_combine(fake, 0, fake, 4, 9, 256, fake, None) == 2
-    assert M.lib.moe_combine(fake, 1, fake, 4, 2, 252, fake, None) == 2
+    assert M.lib.moe_combine(fake, 0, 0, fake, 4, 9, 256, fake, None) == 2
+    assert M.lib.moe_combine(fake, 1, 1, fake, 4, 2, 252, fake, None) == 2
     assert M.lib.moe_quantize_fp8_rows(fake, 4, 20, fake, fake, None) == 2
     shape = M.make_shape(4, 256, 8, 512, 2)
     assert M.lib.moe_grouped_gemm(ctypes.byref(shape), 7, fake, None, fake, None, fake, None,

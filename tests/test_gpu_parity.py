@@ -41,13 +41,19 @@ SMALL = {
 }
 
 ENGINES = ["auto", "decode", "prefill", "simt"]
+# decode: FC1 and FC2 fused in one persistent launch; decode_unfused: two launches
+FWD_ENGINES = ENGINES + ["decode_unfused"]
 
 
 def _set_engine(shape_obj, engine, M):
     os.environ.pop("MOE_FORCE_SIMT", None)
+    os.environ.pop("MOE_FUSE", None)
     if engine == "simt":
         os.environ["MOE_FORCE_SIMT"] = "1"
         return M.ENGINE_AUTO
+    if engine == "decode_unfused":
+        os.environ["MOE_FUSE"] = "0"
+        return M.ENGINE_DECODE
     return {"auto": M.ENGINE_AUTO, "decode": M.ENGINE_DECODE, "prefill": M.ENGINE_PREFILL}[engine]
 
 
@@ -55,6 +61,7 @@ def _set_engine(shape_obj, engine, M):
 def _clear_env():
     yield
     os.environ.pop("MOE_FORCE_SIMT", None)
+    os.environ.pop("MOE_FUSE", None)
 
 
 # ----------------------------------------------------------------- steps ---
@@ -214,6 +221,18 @@ def test_combine(M, ydtype):
     got = f64(out)
     ulp = np.ldexp(1.0, np.frexp(np.abs(ref))[1] - 8)
     assert np.all(np.abs(got - ref) <= ulp + 1e-30)
+    # the same rows in (token, slot) order, with one skipped pair
+    y_pair = torch.empty_like(y)
+    y_pair[perm.long().to(DEV)] = y
+    rop2 = rop.clone()
+    rop2[4] = -1
+    out2 = torch.empty_like(out)
+    M.moe_combine(y_pair, rop2.to(DEV), T, k, out2, pair_order=True)
+    keep = np.ones(T * k)
+    keep[4] = 0
+    yp = f64(y_pair) * keep[:, None]
+    ref2 = O.bf16_round(yp.reshape(T, k, H).sum(axis=1))
+    assert np.all(np.abs(f64(out2) - ref2) <= np.ldexp(1.0, np.frexp(np.abs(ref2))[1] - 8) + 1e-30)
 
 
 def _grouped_inputs(shape, seed, fp8=False, hot=False):
@@ -271,9 +290,12 @@ def test_grouped_gemm_modes(M, engine, name):
     c3 = torch.empty((R, H), dtype=torch.bfloat16, device=DEV)
     M.moe_grouped_gemm(ms, M.GEMM_FC2_BF16, d["a"], d["w2"], d["offsets"], c3,
                        row_src=d["row_src"], topk_w=d["tw"])
-    assert_close(f64(c3), O.bf16_round(ref2), TOL_BF16, f"FC2 bf16 {name}/{engine}")
+    # rows come back in (token, slot) order: c3[row_src[r]] holds row r
+    ref3 = np.empty_like(ref2)
+    ref3[d["row_src_np"]] = ref2
+    assert_close(f64(c3), O.bf16_round(ref3), TOL_BF16, f"FC2 bf16 {name}/{engine}")
     # bf16 rows are the fp32 rows rounded once (same kernel family, same sums)
-    assert torch.equal(c3, c2.to(torch.bfloat16))
+    assert torch.equal(c3[d["row_src"].long()], c2.to(torch.bfloat16))
     torch.cuda.synchronize()
     assert M.device_status() == 0
 
@@ -396,7 +418,7 @@ def check_forward(M, inp, sample=None, engine=None, seed=0):
     return m, ndiff
 
 
-@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("engine", FWD_ENGINES)
 @pytest.mark.parametrize("name", list(SMALL))
 def test_forward_small_shapes(M, name, engine):
     for routing in ("learned", "zipf"):
@@ -424,6 +446,13 @@ def test_forward_fp8_small(M):
 def test_forward_reference_workloads(M, cfg, sample):
     inp = workloads.make_inputs(cfg, DEV)
     m, ndiff = check_forward(M, inp, sample=sample)
+    if cfg in ("c2_decode_balanced", "c3_decode_skewed"):
+        # the fused and the two-launch decode paths give identical bits
+        o1, i1, _ = _run_forward(M, inp)
+        os.environ["MOE_FUSE"] = "0"
+        o2, i2, _ = _run_forward(M, inp)
+        os.environ.pop("MOE_FUSE", None)
+        assert torch.equal(i1, i2) and torch.equal(o1, o2)
     print(f"{cfg}: max scaled error {m:.3e}, near-tie routing differences {ndiff}")
     del inp
     torch.cuda.empty_cache()
