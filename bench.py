@@ -381,7 +381,12 @@ def main_native(args):
     y = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
     pws = M.alloc_workspace(max(256, M.moe_permute_workspace_size(T, E, k)), dev)
     out_b = torch.empty_like(out)
-    stages = ["rmsnorm", "route", "permute", "fc1", "fc2", "combine"]
+    # The decode engine with bf16 weights runs FC1 and FC2 in one fused launch:
+    # time that launch (moe_grouped_ffn) as one stage; otherwise FC1 and FC2.
+    fused = (T * k / E <= 96.0) and not fp8 and os.environ.get("MOE_FUSE", "1") != "0"
+    fws = M.alloc_workspace(max(256, M.moe_grouped_ffn_workspace_size(shape)), dev)
+    stages = (["rmsnorm", "route", "permute", "ffn", "combine"] if fused else
+              ["rmsnorm", "route", "permute", "fc1", "fc2", "combine"])
 
     def step_b(evs=None):
         def mark(i):
@@ -397,16 +402,20 @@ def main_native(args):
         M.moe_permute(ids, T, E, k, offsets, row_src, rop, xhat=xq if fp8 else xhat, xp=xp,
                       row_bytes=H * (1 if fp8 else 2), xscale=xs, xp_scale=xps, workspace=pws)
         mark(3)
-        M.moe_grouped_gemm(shape, M.GEMM_FC1_SILU, xp, w13, offsets, act, a_scale=xps, w_scale=s13)
-        if fp8:
-            M.lib.moe_quantize_fp8_rows(act.data_ptr(), R, I, actq.data_ptr(), acts.data_ptr(),
-                                        st.cuda_stream)
-        mark(4)
-        M.moe_grouped_gemm(shape, M.GEMM_FC2_BF16, actq if fp8 else act, w2, offsets, y,
-                           a_scale=acts, w_scale=s2, row_src=row_src, topk_w=tw)
-        mark(5)
+        if fused:
+            M.moe_grouped_ffn(shape, xp, w13, w2, offsets, row_src, tw, act, y, fws)
+        else:
+            M.moe_grouped_gemm(shape, M.GEMM_FC1_SILU, xp, w13, offsets, act, a_scale=xps,
+                               w_scale=s13)
+            if fp8:
+                M.lib.moe_quantize_fp8_rows(act.data_ptr(), R, I, actq.data_ptr(),
+                                            acts.data_ptr(), st.cuda_stream)
+            mark(4)
+            M.moe_grouped_gemm(shape, M.GEMM_FC2_BF16, actq if fp8 else act, w2, offsets, y,
+                               a_scale=acts, w_scale=s2, row_src=row_src, topk_w=tw)
+        mark(len(stages) - 1)
         M.moe_combine(y, rop, T, k, out_b, pair_order=True)
-        mark(6)
+        mark(len(stages))
 
     for _ in range(args.warmup):
         step_b()
@@ -418,7 +427,7 @@ def main_native(args):
     for i in range(args.steps):
         if flush is not None:
             flush.zero_()
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
         step_b(evs)
         evs_all.append(evs)
     torch.cuda.synchronize()
@@ -428,8 +437,16 @@ def main_native(args):
     work = algorithmic_work(dict(inp, fp8=fp8), offsets_np)
     peaks = load_peaks()
     decode = T <= 64
-    if decode:
-        dom = "fc1"
+    if decode and fused:
+        ffn_bytes = work["fc1_bytes"] + work["fc2_bytes"]
+        achieved = ffn_bytes / (stage_ms["ffn"] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": read_traffic("ffn", args.workload),
+                "kernel": "fused decode FFN (FC1 + silu_and_mul + FC2 + routing weight, one launch)",
+                "peak_source": peaks["source"],
+                "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
+                "algorithmic_bytes_per_launch": ffn_bytes}
+    elif decode:
         achieved = work["fc1_bytes"] / (stage_ms["fc1"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": read_traffic("fc1", args.workload),
@@ -483,8 +500,11 @@ def main_native(args):
     h2d = x_h.numel() * 2 + (lg_h.numel() * 4 if lg_h is not None else 0)
     d2h = out_h.numel() * 2
 
-    launches_per_step = (1 + (1 if inp["router_w"] is not None else 0) + 1 + 1 + 1 + 1 +
-                         (1 if fp8 else 0) + 1 + 1)
+    # rmsnorm, [router], top-k, permute (1, or 3 for large batches), gather,
+    # FC1 + FC2 (one fused launch or two), [FP8 quant], combine
+    launches_per_step = (1 + (1 if inp["router_w"] is not None else 0) + 1 +
+                         (3 if T * k > 4096 else 1) + 1 + (1 if fused else 2) +
+                         (1 if fp8 else 0) + 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = args.cpu_tokens or auto_cpu_tokens(args.workload)

@@ -257,6 +257,23 @@ moe_status moe_grouped_gemm(const moe_shape* shape, int32_t mode, const void* a,
                             const int32_t* offsets, const int32_t* row_src, const float* topk_w,
                             void* c, moe_stream_t stream);
 
+/* Device workspace bytes moe_grouped_ffn needs (0 when the shape is invalid). */
+size_t moe_grouped_ffn_workspace_size(const moe_shape* shape);
+
+/* The expert FFN of the grouped rows in one call ([RUBIN] Locality domain:
+ * FC1 then FC2):  act = FC1_SILU(xp), then y = FC2_BF16(act) -- exactly the
+ * two moe_grouped_gemm steps the forward runs (same arguments and layouts:
+ * xp [R, H] (+ xp_scale [R] for FP8), act bf16 [R, I], y bf16 [R, H] in
+ * (token, slot) order, R = T * top_k).  On the decode engine with bf16
+ * weights both GEMMs run in one persistent launch whose FC2 units wait per
+ * expert for that expert's FC1 units.  workspace >=
+ * moe_grouped_ffn_workspace_size(shape) bytes, 256-byte aligned. */
+moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* xp_scale,
+                           const void* w13, const float* w13_scale, const void* w2,
+                           const float* w2_scale, const int32_t* offsets, const int32_t* row_src,
+                           const float* topk_w, void* act, void* y, void* workspace,
+                           size_t workspace_bytes, moe_stream_t stream);
+
 /* silu_and_mul ([V100] "2nd wall"): a[r, i] = bf16( silu(h[r, i]) * h[r, I+i] ),
  * silu(z) = z / (1 + exp(-z)); h bf16 [R, 2I], a bf16 [R, I]; I % 8 == 0. */
 moe_status moe_silu_and_mul(const void* h, int32_t R, int32_t I, void* a, moe_stream_t stream);

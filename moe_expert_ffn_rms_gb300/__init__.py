@@ -72,6 +72,9 @@ _SIGS = {
                                    _P]),
     "moe_grouped_gemm": (ctypes.c_int, [ctypes.POINTER(MoeShape), _I32, _P, _P, _P, _P, _P, _P, _P,
                                         _P, _P]),
+    "moe_grouped_ffn_workspace_size": (_SZ, [ctypes.POINTER(MoeShape)]),
+    "moe_grouped_ffn": (ctypes.c_int, [ctypes.POINTER(MoeShape), _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                       _P, _P, _P, _SZ, _P]),
     "moe_silu_and_mul": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
     "moe_combine": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _I32, _I32, _P, _P]),
     "moe_quantize_fp8_rows": (ctypes.c_int, [_P, ctypes.c_int64, _I32, _P, _P, _P]),
@@ -221,6 +224,19 @@ def moe_grouped_gemm(shape: MoeShape, mode, a, w, offsets, c, a_scale=None, w_sc
                                 _ptr(w_scale), _ptr(offsets), _ptr(row_src), _ptr(topk_w), _ptr(c),
                                 _stream(stream)))
     return c
+
+
+def moe_grouped_ffn_workspace_size(shape: MoeShape) -> int:
+    return lib.moe_grouped_ffn_workspace_size(ctypes.byref(shape))
+
+
+def moe_grouped_ffn(shape: MoeShape, xp, w13, w2, offsets, row_src, topk_w, act, y, workspace,
+                    xp_scale=None, w13_scale=None, w2_scale=None, stream=None):
+    _check(lib.moe_grouped_ffn(ctypes.byref(shape), _ptr(xp), _ptr(xp_scale), _ptr(w13),
+                               _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(offsets),
+                               _ptr(row_src), _ptr(topk_w), _ptr(act), _ptr(y), _ws_ptr(workspace),
+                               _ws_bytes(workspace), _stream(stream)))
+    return y
 
 
 def moe_silu_and_mul(h, a, stream=None):

@@ -184,6 +184,43 @@ moe_status run_gemm(const moe_shape* s, int mode, int engine, const void* a, con
   return MOE_OK;
 }
 
+// FC1 + silu_and_mul then FC2 + routing weight (bf16 rows in (token, slot)
+// order).  `sched` (1 + E ints) must be zero when the fused decode launch is
+// used; actq / act_scale are the FP8 path's scratch.
+moe_status ffn_impl(const moe_shape* s, int engine, bool fuse, const void* xp,
+                    const float* xp_scale, const void* w13, const float* w13_scale, const void* w2,
+                    const float* w2_scale, const int32_t* offsets, const int32_t* row_src,
+                    const float* tw, void* act, void* y, int32_t* sched, uint8_t* actq,
+                    float* act_scale, DevInfo* dev, cudaStream_t st) {
+  const bool f8 = s->wdtype == MOE_W_FP8_E4M3;
+  const int T = s->T, H = s->H, E = s->E, I = s->I, R = s->T * s->top_k;
+  if (fuse) {
+    // one persistent launch (FC2 units wait per expert for FC1)
+    cudaError_t e = moe::launch_decode_ffn_fused(xp, w13, w2, act, y, offsets, row_src, tw, sched,
+                                                 E, H, I, R, T, dev->sms, dev->status, st);
+    if (e == cudaSuccess) return MOE_OK;
+    if (e != cudaErrorNotSupported) return cuda_fail(e, "fused decode FFN launch");
+  }
+  moe_status rc = run_gemm(s, MOE_GEMM_FC1_SILU, engine, xp, xp_scale, w13, w13_scale, offsets,
+                           row_src, nullptr, act, R, dev->sms, dev->status, st);
+  if (rc != MOE_OK) return rc;
+  // FP8: per-row quantisation of the bf16 intermediate before FC2
+  const void* a2 = act;
+  if (f8) {
+    MOE_CUDA(moe::launch_quant_rows(act, R, I, actq, act_scale, offsets + E, st), "quant launch");
+    a2 = actq;
+  }
+  return run_gemm(s, MOE_GEMM_FC2_BF16, engine, a2, act_scale, w2, w2_scale, offsets, row_src, tw,
+                  y, R, dev->sms, dev->status, st);
+}
+
+bool fuse_decode(const moe_shape* s, int engine) {
+  const char* fuse_env = getenv("MOE_FUSE");
+  const char* simt_env = getenv("MOE_FORCE_SIMT");
+  return engine == MOE_ENGINE_DECODE && s->wdtype == MOE_W_BF16 &&
+         !(fuse_env && fuse_env[0] == '0') && !(simt_env && simt_env[0] == '1');
+}
+
 moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, const float* router_w,
                         const float* router_logits, const float* router_bias,
                         const int32_t* ids_in, const float* tw_in, const void* w13, const void* w2,
@@ -234,10 +271,7 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   int32_t* sched = at<int32_t>(workspace, L.sched);
   // FC1 and FC2 run in one persistent launch on the decode engine (bf16),
   // unless MOE_FUSE=0 or the SIMT engine is forced.
-  const char* fuse_env = getenv("MOE_FUSE");
-  const char* simt_env = getenv("MOE_FORCE_SIMT");
-  const bool fuse = engine == MOE_ENGINE_DECODE && !f8 && !(fuse_env && fuse_env[0] == '0') &&
-                    !(simt_env && simt_env[0] == '1');
+  const bool fuse = fuse_decode(s, engine);
 
   // a1: rms_norm (+ per-token E4M3 quantisation on the FP8 path)
   MOE_CUDA(moe::launch_rmsnorm(x, norm_w, T, H, s->eps, xhat, xq, xscale, st), "rmsnorm launch");
@@ -263,29 +297,9 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   MOE_CUDA(moe::launch_gather_rows(offsets, E, row_src, k, R, f8 ? (const void*)xq : (const void*)xhat,
                                    xp, H * (f8 ? 1 : 2), xscale, xp_scale, st),
            "gather launch");
-  if (fuse) {
-    // a5 + a6 + a7 in one persistent launch (FC2 units wait per expert for FC1)
-    cudaError_t e = moe::launch_decode_ffn_fused(xp, w13, w2, act, y, offsets, row_src, tw, sched,
-                                                 E, H, I, R, T, dev->sms, dev->status, st);
-    if (e == cudaSuccess) {
-      MOE_CUDA(moe::launch_combine(y, true, true, row_of_pair, T, k, H, out, st), "combine launch");
-      return MOE_OK;
-    }
-    if (e != cudaErrorNotSupported) return cuda_fail(e, "fused decode FFN launch");
-  }
-  // a5 + a6: FC1 with the silu_and_mul epilogue
-  rc = run_gemm(s, MOE_GEMM_FC1_SILU, engine, xp, xp_scale, w13, w13_scale, offsets, row_src,
-                nullptr, act, R, dev->sms, dev->status, st);
-  if (rc != MOE_OK) return rc;
-  // FP8: per-row quantisation of the bf16 intermediate before FC2
-  const void* a2 = act;
-  if (f8) {
-    MOE_CUDA(moe::launch_quant_rows(act, R, I, actq, act_scale, offsets + E, st), "quant launch");
-    a2 = actq;
-  }
-  // a7: FC2 with the routing-weight epilogue (bf16 output rows)
-  rc = run_gemm(s, MOE_GEMM_FC2_BF16, engine, a2, act_scale, w2, w2_scale, offsets, row_src, tw, y,
-                R, dev->sms, dev->status, st);
+  // a5 + a6 + a7: FC1 + silu_and_mul, FC2 + routing weight
+  rc = ffn_impl(s, engine, fuse, xp, xp_scale, w13, w13_scale, w2, w2_scale, offsets, row_src, tw,
+                act, y, sched, actq, act_scale, dev, st);
   if (rc != MOE_OK) return rc;
   // a8: combine (fp32 sum in slot order, one bf16 rounding)
   MOE_CUDA(moe::launch_combine(y, true, true, row_of_pair, T, k, H, out, st), "combine launch");
@@ -478,6 +492,49 @@ moe_status moe_grouped_gemm(const moe_shape* shape, int32_t mode, const void* a,
   return run_gemm(shape, mode, pick_engine(shape), a, a_scale, w, w_scale, offsets, row_src,
                   mode >= MOE_GEMM_FC2 ? topk_w : nullptr, c, R_max, d->sms, d->status,
                   (cudaStream_t)stream);
+}
+
+size_t moe_grouped_ffn_workspace_size(const moe_shape* shape) {
+  if (check_shape(shape) != MOE_OK) return 0;
+  const size_t R = (size_t)shape->T * shape->top_k;
+  size_t n = up256((size_t)(shape->E + 1) * 4);
+  if (shape->wdtype == MOE_W_FP8_E4M3) n += up256(R * shape->I) + up256(R * 4);
+  return n;
+}
+
+moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* xp_scale,
+                           const void* w13, const float* w13_scale, const void* w2,
+                           const float* w2_scale, const int32_t* offsets, const int32_t* row_src,
+                           const float* topk_w, void* act, void* y, void* workspace,
+                           size_t workspace_bytes, moe_stream_t stream) {
+  moe_status rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  const bool f8 = shape->wdtype == MOE_W_FP8_E4M3;
+  MOE_REQ(xp && w13 && w2 && offsets && row_src && topk_w && act && y && workspace,
+          MOE_ERR_INVALID_ARG, "xp, w13, w2, offsets, row_src, topk_w, act, y and workspace must be non-NULL");
+  MOE_REQ(!f8 || (xp_scale && w13_scale && w2_scale), MOE_ERR_INVALID_ARG,
+          "FP8 needs xp_scale, w13_scale and w2_scale");
+  MOE_REQ(aligned16(xp) && aligned16(w13) && aligned16(w2) && aligned16(act) && aligned16(y),
+          MOE_ERR_INVALID_ARG, "misaligned pointer");
+  MOE_REQ(((uintptr_t)workspace & 255u) == 0, MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const size_t need = moe_grouped_ffn_workspace_size(shape);
+  MOE_REQ(workspace_bytes >= need, MOE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes",
+          workspace_bytes, need);
+  DevInfo* dev = nullptr;
+  if ((rc = device_info(&dev)) != MOE_OK) return rc;
+  if (shape->T == 0) return MOE_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t R = (size_t)shape->T * shape->top_k;
+  int32_t* sched = at<int32_t>(workspace, 0);
+  uint8_t* actq = f8 ? at<uint8_t>(workspace, up256((size_t)(shape->E + 1) * 4)) : nullptr;
+  float* act_scale =
+      f8 ? at<float>(workspace, up256((size_t)(shape->E + 1) * 4) + up256(R * shape->I)) : nullptr;
+  const int engine = pick_engine(shape);
+  const bool fuse = fuse_decode(shape, engine);
+  if (fuse)
+    MOE_CUDA(cudaMemsetAsync(sched, 0, (size_t)(shape->E + 1) * 4, st), "scheduler reset");
+  return ffn_impl(shape, engine, fuse, xp, xp_scale, w13, w13_scale, w2, w2_scale, offsets,
+                  row_src, topk_w, act, y, sched, actq, act_scale, dev, st);
 }
 
 moe_status moe_silu_and_mul(const void* h, int32_t R, int32_t I, void* a, moe_stream_t stream) {

@@ -117,6 +117,10 @@ def test_step_entry_points_reject_bad_arguments_on_host(M):
     shape = M.make_shape(4, 256, 8, 512, 2)
     assert M.lib.moe_grouped_gemm(ctypes.byref(shape), 7, fake, None, fake, None, fake, None,
                                   None, fake, None) == 1
+    assert M.lib.moe_grouped_ffn(ctypes.byref(shape), fake, None, fake, None, fake, None, fake,
+                                 fake, fake, fake, fake, fake, 16, None) == 4
+    assert M.lib.moe_grouped_ffn(ctypes.byref(shape), None, None, fake, None, fake, None, fake,
+                                 fake, fake, fake, fake, fake, 1 << 20, None) == 1
     assert M.lib.moe_route_workspace_size(4, 256, 8) > 0
     assert M.lib.moe_route_workspace_size(4, 250, 8) == 0
 

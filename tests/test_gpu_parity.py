@@ -336,6 +336,59 @@ def test_grouped_gemm_fp8(M, engine):
     assert_close(f64(c2), ref2, 1e-3, f"FP8 FC2 {engine}")
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("engine", ["decode", "prefill"])
+@pytest.mark.parametrize("name", ["ragged_a", "prefill_like", "hot"])
+def test_grouped_ffn_matches_steps(M, engine, name, fp8):
+    """moe_grouped_ffn (fused on the decode engine for bf16) gives the same bits
+    as FC1_SILU then FC2_BF16 through moe_grouped_gemm, and matches the oracle."""
+    shape = SMALL.get(name, workloads.Shape(T=150, H=256, E=5, k=2, I=192))
+    d = _grouped_inputs(shape, 41, hot=(name == "hot"))
+    T, H, E, k, I = shape.T, shape.H, shape.E, shape.k, shape.I
+    R = T * k
+    eng = _set_engine(shape, engine, M)
+    ms = M.make_shape(T, H, E, I, k, fp8=fp8, engine=eng)
+    xp, w13, w2, s13, s2, xs = d["xp"], d["w13"], d["w2"], None, None, None
+    if fp8:
+        w13 = torch.empty((E, 2 * I, H), dtype=torch.uint8, device=DEV)
+        s13 = torch.empty((E, 2 * I), dtype=torch.float32, device=DEV)
+        w2 = torch.empty((E, H, I), dtype=torch.uint8, device=DEV)
+        s2 = torch.empty((E, H), dtype=torch.float32, device=DEV)
+        M.moe_quantize_fp8_rows(d["w13"], w13, s13)
+        M.moe_quantize_fp8_rows(d["w2"], w2, s2)
+        xp = torch.empty((R, H), dtype=torch.uint8, device=DEV)
+        xs = torch.empty((R,), dtype=torch.float32, device=DEV)
+        M.moe_quantize_fp8_rows(d["xp"], xp, xs)
+    act = torch.empty((R, I), dtype=torch.bfloat16, device=DEV)
+    y = torch.empty((R, H), dtype=torch.bfloat16, device=DEV)
+    ws = M.alloc_workspace(M.moe_grouped_ffn_workspace_size(ms), DEV)
+    for _ in range(2):  # twice: the scheduler counters are reset per call
+        M.moe_grouped_ffn(ms, xp, w13, w2, d["offsets"], d["row_src"], d["tw"], act, y, ws,
+                          xp_scale=xs, w13_scale=s13, w2_scale=s2)
+    act2 = torch.empty_like(act)
+    y2 = torch.empty_like(y)
+    M.moe_grouped_gemm(ms, M.GEMM_FC1_SILU, xp, w13, d["offsets"], act2, a_scale=xs, w_scale=s13)
+    a2, as2 = act2, None
+    if fp8:
+        a2 = torch.empty((R, I), dtype=torch.uint8, device=DEV)
+        as2 = torch.empty((R,), dtype=torch.float32, device=DEV)
+        M.moe_quantize_fp8_rows(act2, a2, as2)
+    M.moe_grouped_gemm(ms, M.GEMM_FC2_BF16, a2, w2, d["offsets"], y2, a_scale=as2, w_scale=s2,
+                       row_src=d["row_src"], topk_w=d["tw"])
+    torch.cuda.synchronize()
+    assert torch.equal(act, act2) and torch.equal(y, y2)
+    if not fp8:
+        off = d["offsets_np"]
+        ref_a = O.grouped_fc1(f64(d["xp"]), off, lambda e: f64(d["w13"][e]), I)
+        assert_close(f64(act), ref_a, TOL_BF16, f"ffn act {name}/{engine}")
+        row_w = f64(d["tw"])[d["row_src_np"]]
+        ref_y = O.grouped_fc2(ref_a, off, lambda e: f64(d["w2"][e]), row_w)
+        ref_pair = np.empty_like(ref_y)
+        ref_pair[d["row_src_np"]] = ref_y
+        assert_close(f64(y), ref_pair, TOL_BF16, f"ffn y {name}/{engine}")
+    assert M.device_status() == 0
+
+
 # ------------------------------------------------------------ end to end ---
 
 def _run_forward(M, inp, engine=None, fp8_weights=None, out=None, ws=None):
