@@ -111,6 +111,8 @@ moe_status check_shape(const moe_shape* s) {
   return MOE_OK;
 }
 
+size_t router_ws_bytes(int T, int H, int E);
+
 struct Ws {
   size_t xhat, xq, xscale, part, ids, tw, offsets, row_src, row_of_pair, perm_cnt, sched, xp,
       xp_scale, act, actq, act_scale, y, total;
@@ -127,7 +129,7 @@ Ws layout(const moe_shape* s) {
   w.xhat = take(T * H * 2);
   w.xq = take(f8 ? T * H : 0);
   w.xscale = take(f8 ? T * 4 : 0);
-  w.part = take((size_t)moe::route_splits(s->T > 0 ? s->T : 1, s->H, s->E) * (T > 0 ? T : 1) * E * 4);
+  w.part = take(router_ws_bytes(s->T, s->H, s->E));
   w.ids = take(R * 4);
   w.tw = take(R * 4);
   w.offsets = take((E + 1) * 4);
@@ -149,6 +151,62 @@ template <typename T>
 T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(reinterpret_cast<char*>(base) + off);
 }
+
+// ---------------------------------------------------------------- router --
+// Large batches compute the router logits on the tensor cores (W_r split into
+// three bf16 pieces, one grouped GEMM with fp32 rows [T, 3E]); small ones use
+// the fp32 SIMT router with split-K partial sums.
+bool router_on_tensor_cores(int T) {
+  const char* env = getenv("MOE_ROUTER_TC");
+  if (env && env[0] == '0') return false;
+  return T >= 256;
+}
+
+size_t router_tc_bytes(int T, int H, int E) {
+  return up256((size_t)3 * E * H * 2) + up256(2 * 4) + up256((size_t)T * 3 * E * 4);
+}
+
+size_t router_ws_bytes(int T, int H, int E) {
+  const int Tc = T > 0 ? T : 1;
+  size_t n = (size_t)moe::route_splits(Tc, H, E) * Tc * E * 4;
+  if (router_on_tensor_cores(T)) {
+    const size_t tc = router_tc_bytes(T, H, E);
+    if (tc > n) n = tc;
+  }
+  return up256(n);
+}
+
+// Enqueues the router logits of xhat into `ws` and returns how top-k reads
+// them: logit(t, e) = sum_z part[z*zstride + t*tstride + e].
+moe_status compute_router_logits(const void* xhat, const float* router_w, int T, int H, int E, void* ws,
+                         DevInfo* dev, cudaStream_t st, const float** part, int* ks,
+                         size_t* zstride, size_t* tstride) {
+  if (router_on_tensor_cores(T)) {
+    void* wt = ws;
+    int32_t* seg = at<int32_t>(ws, up256((size_t)3 * E * H * 2));
+    float* d = at<float>(ws, up256((size_t)3 * E * H * 2) + up256(2 * 4));
+    MOE_CUDA(moe::launch_router_split(router_w, H, E, T, wt, seg, st), "router split launch");
+    cudaError_t e = moe::launch_gemm_tc(MOE_GEMM_FC2, false, false, xhat, nullptr, wt, nullptr,
+                                        seg, nullptr, nullptr, d, 1, H, H, 3 * E, T, T, dev->sms,
+                                        dev->status, st);
+    if (e == cudaSuccess) {
+      *part = d;
+      *ks = 3;
+      *zstride = (size_t)E;
+      *tstride = (size_t)3 * E;
+      return MOE_OK;
+    }
+    if (e != cudaErrorNotSupported) return cuda_fail(e, "router GEMM launch");
+  }
+  *ks = moe::route_splits(T, H, E);
+  MOE_CUDA(moe::launch_router_logits(xhat, router_w, T, H, E, *ks, (float*)ws, st),
+           "router launch");
+  *part = (const float*)ws;
+  *zstride = (size_t)T * E;
+  *tstride = (size_t)E;
+  return MOE_OK;
+}
+
 
 int pick_engine(const moe_shape* s) {
   if (s->engine != MOE_ENGINE_AUTO) return s->engine;
@@ -282,13 +340,14 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   } else {
     const float* part = router_logits;
     int ks = 1;
+    size_t zs = 0, ts = 0;
     if (router_w) {
-      ks = moe::route_splits(T, H, E);
-      float* pbuf = at<float>(workspace, L.part);
-      MOE_CUDA(moe::launch_router_logits(xhat, router_w, T, H, E, ks, pbuf, st), "router launch");
-      part = pbuf;
+      rc = compute_router_logits(xhat, router_w, T, H, E, at<void>(workspace, L.part), dev, st, &part, &ks,
+                         &zs, &ts);
+      if (rc != MOE_OK) return rc;
     }
-    MOE_CUDA(moe::launch_topk(part, ks, router_bias, T, E, k, ids, tw, nullptr, st), "top-k launch");
+    MOE_CUDA(moe::launch_topk(part, ks, router_bias, T, E, k, ids, tw, nullptr, st, zs, ts),
+             "top-k launch");
   }
   // a4: permute + gather of the (quantised) token rows
   MOE_CUDA(moe::launch_permute_any(ids, T, E, k, offsets, row_src, row_of_pair, perm_cnt,
@@ -398,7 +457,7 @@ moe_status moe_rmsnorm(const void* x, const void* w, int32_t T, int32_t H, float
 
 size_t moe_route_workspace_size(int32_t T, int32_t H, int32_t E) {
   if (T < 0 || H <= 0 || H % 64 || E <= 0 || E > kMaxExperts) return 0;
-  return up256((size_t)moe::route_splits(T > 0 ? T : 1, H, E) * (T > 0 ? T : 1) * E * 4);
+  return router_ws_bytes(T, H, E);
 }
 
 moe_status moe_route_topk(const void* xhat, const float* router_w, const float* router_bias,
@@ -422,13 +481,14 @@ moe_status moe_route_topk(const void* xhat, const float* router_w, const float* 
   cudaStream_t st = (cudaStream_t)stream;
   const float* part = logits_in;
   int ks = 1;
+  size_t zs = 0, ts = 0;
   if (!logits_in) {
-    ks = moe::route_splits(T, H, E);
-    MOE_CUDA(moe::launch_router_logits(xhat, router_w, T, H, E, ks, (float*)workspace, st),
-             "router launch");
-    part = (const float*)workspace;
+    MOE_REQ(((uintptr_t)workspace & 255u) == 0, MOE_ERR_INVALID_ARG,
+            "workspace must be 256-byte aligned");
+    rc = compute_router_logits(xhat, router_w, T, H, E, workspace, d, st, &part, &ks, &zs, &ts);
+    if (rc != MOE_OK) return rc;
   }
-  MOE_CUDA(moe::launch_topk(part, ks, router_bias, T, E, k, ids, weights, logits_out, st),
+  MOE_CUDA(moe::launch_topk(part, ks, router_bias, T, E, k, ids, weights, logits_out, st, zs, ts),
            "top-k launch");
   return MOE_OK;
 }

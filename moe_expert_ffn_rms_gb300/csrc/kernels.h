@@ -14,8 +14,15 @@ cudaError_t launch_rmsnorm(const void* x, const void* w, int T, int H, float eps
                            void* yq, float* yscale, cudaStream_t st);
 cudaError_t launch_router_logits(const void* xhat, const float* wr, int T, int H, int E, int ks,
                                  float* part, cudaStream_t st);
+// Logit of (t, e) = sum over z < ks of part[z*zstride + t*tstride + e]
+// (+ bias[e]); zstride / tstride 0 mean T*E / E.
 cudaError_t launch_topk(const float* part, int ks, const float* bias, int T, int E, int k,
-                        int32_t* ids, float* w, float* logits_out, cudaStream_t st);
+                        int32_t* ids, float* w, float* logits_out, cudaStream_t st,
+                        size_t zstride = 0, size_t tstride = 0);
+// Tensor-core router: split W_r into three transposed bf16 pieces [3E, H]
+// and write the one-segment offsets {0, T}.
+cudaError_t launch_router_split(const float* wr, int H, int E, int T, void* wt, int32_t* seg,
+                                cudaStream_t st);
 // The permute kernels also zero nzero ints at zero_buf (counters of later
 // kernels in the same forward); zero_buf may be NULL with nzero = 0.
 cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* offsets,

@@ -245,6 +245,7 @@ cudaError_t launch_router_logits(const void* xhat, const float* wr, int T, int H
 // a warp arg-max (larger logit first, lower index on ties); the weights are
 // the softmax over the selected logits (= full softmax renormalised).
 __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ part, int ks,
+                                                   size_t zstride, size_t tstride,
                                                    const float* __restrict__ bias, int T, int E,
                                                    int k, int32_t* __restrict__ ids,
                                                    float* __restrict__ wout,
@@ -260,8 +261,7 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
   for (int i = 0; i < PER; ++i) v[i] = 0.f;
   // Partial sums: chunk z outer, experts inner, so a lane has up to PER loads
   // in flight; each logit is still summed in z order.
-  const size_t zstride = (size_t)T * E;
-  const float* pt = part + (size_t)t * E;
+  const float* pt = part + (size_t)t * tstride;
   for (int z = 0; z < ks; ++z) {
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
@@ -328,10 +328,58 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
 }
 
 cudaError_t launch_topk(const float* part, int ks, const float* bias, int T, int E, int k,
-                        int32_t* ids, float* w, float* logits_out, cudaStream_t st) {
+                        int32_t* ids, float* w, float* logits_out, cudaStream_t st,
+                        size_t zstride, size_t tstride) {
   if (T == 0) return cudaSuccess;
-  return launch_kernel(topk_kernel, dim3((T + 3) / 4), dim3(128), 0, st, part, ks, bias, T, E, k,
-                       ids, w, logits_out);
+  if (zstride == 0) zstride = (size_t)T * E;  // default: part[z][t][e]
+  if (tstride == 0) tstride = (size_t)E;
+  return launch_kernel(topk_kernel, dim3((T + 3) / 4), dim3(128), 0, st, part, ks, zstride, tstride,
+                       bias, T, E, k, ids, w, logits_out);
+}
+
+// Router weights for the tensor-core router: W_r fp32 [H, E] -> three bf16
+// pieces, transposed to K-major rows wt[p*E + e][h] (p = 0 hi, 1 mid, 2 lo):
+// hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid); the differences
+// are exact in fp32, so hi + mid + lo equals w to 2^-24 relative and each
+// product with a bf16 x_hat is exact.  Also writes the one-segment offsets
+// {0, T} the grouped GEMM reads.
+__global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ wr, int H,
+                                                           int E, int T, bf16* __restrict__ wt,
+                                                           int32_t* __restrict__ seg) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float tile[32][33];
+  const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int i = ty; i < 32; i += 8) {
+    const int h = h0 + i, e = e0 + tx;
+    tile[i][tx] = (h < H && e < E) ? wr[(size_t)h * E + e] : 0.f;
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int e = e0 + i, h = h0 + tx;
+    if (e < E && h < H) {
+      const float w = tile[tx][i];
+      const bf16 hi = __float2bfloat16_rn(w);
+      const float r1 = w - __bfloat162float(hi);
+      const bf16 mid = __float2bfloat16_rn(r1);
+      const float r2 = r1 - __bfloat162float(mid);
+      const bf16 lo = __float2bfloat16_rn(r2);
+      wt[(size_t)e * H + h] = hi;
+      wt[((size_t)E + e) * H + h] = mid;
+      wt[((size_t)2 * E + e) * H + h] = lo;
+    }
+  }
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    seg[0] = 0;
+    seg[1] = T;
+  }
+}
+
+cudaError_t launch_router_split(const float* wr, int H, int E, int T, void* wt, int32_t* seg,
+                                cudaStream_t st) {
+  dim3 grid((H + 31) / 32, (E + 31) / 32);
+  return launch_kernel(router_split_kernel, grid, dim3(256), 0, st, wr, H, E, T, (bf16*)wt, seg);
 }
 
 // ====================================================================== permute

@@ -60,8 +60,8 @@ def _set_engine(shape_obj, engine, M):
 @pytest.fixture(autouse=True)
 def _clear_env():
     yield
-    os.environ.pop("MOE_FORCE_SIMT", None)
-    os.environ.pop("MOE_FUSE", None)
+    for v in ("MOE_FORCE_SIMT", "MOE_FUSE", "MOE_ROUTER_TC"):
+        os.environ.pop(v, None)
 
 
 # ----------------------------------------------------------------- steps ---
@@ -131,9 +131,17 @@ def test_route_topk_given_logits_bit_exact(M, T, E, k):
         np.testing.assert_allclose(w.cpu().double().numpy(), w_ref, rtol=2e-6, atol=1e-7)
 
 
-@pytest.mark.parametrize("cfg", ["c1_tiny", "c3_decode_skewed", "c5_prefill"])
-def test_route_topk_router(M, cfg):
-    inp = workloads.make_inputs(cfg, DEV)
+@pytest.mark.parametrize("tc", ["1", "0"])
+@pytest.mark.parametrize("cfg", ["c1_tiny", "c3_decode_skewed", "c5_prefill", "wide_prefill"])
+def test_route_topk_router(M, cfg, tc):
+    """Router logits from x_hat and W_r (tensor-core bf16x3 split for >= 256
+    tokens unless MOE_ROUTER_TC=0, else fp32 SIMT) against the fp64 oracle."""
+    os.environ["MOE_ROUTER_TC"] = tc
+    if cfg == "wide_prefill":   # E = 256 -> three N tiles of the split router GEMM
+        inp = workloads.make_inputs("c3_decode_skewed", DEV,
+                                    shape=workloads.Shape(T=600, H=1024, E=256, k=8, I=256))
+    else:
+        inp = workloads.make_inputs(cfg, DEV)
     T, H, E, k = inp["T"], inp["H"], inp["E"], inp["k"]
     xhat = torch.empty_like(inp["x"])
     M.moe_rmsnorm(inp["x"], inp["norm_w"], inp["eps"], xhat)
@@ -148,7 +156,9 @@ def test_route_topk_router(M, cfg):
                           None if inp["router_bias"] is None else f64(inp["router_bias"]))
     np.testing.assert_allclose(lo.cpu().double().numpy(), l64, rtol=1e-4, atol=1e-4)
     _, _, ndiff = check_routing(ids.cpu().numpy(), w.cpu().double().numpy(), l64, k)
-    print(f"{cfg}: {ndiff} near-tie tokens routed differently")
+    err = np.abs(lo.cpu().double().numpy() - l64).max()
+    print(f"{cfg} tc={tc}: max |logit error| {err:.2e}, {ndiff} near-tie tokens routed differently")
+    os.environ.pop("MOE_ROUTER_TC", None)
 
 
 @pytest.mark.parametrize("T,E,k", [(1, 4, 1), (37, 6, 2), (64, 256, 8), (4096, 64, 8), (333, 7, 7),
