@@ -383,7 +383,7 @@ def main_native(args):
     out_b = torch.empty_like(out)
     # The decode engine with bf16 weights runs FC1 and FC2 in one fused launch:
     # time that launch (moe_grouped_ffn) as one stage; otherwise FC1 and FC2.
-    fused = (T * k / E <= 96.0) and not fp8 and os.environ.get("MOE_FUSE", "1") != "0"
+    fused = (T * k / E <= 96.0) and os.environ.get("MOE_FUSE", "1") != "0"
     fws = M.alloc_workspace(max(256, M.moe_grouped_ffn_workspace_size(shape)), dev)
     stages = (["rmsnorm", "route", "permute", "ffn", "combine"] if fused else
               ["rmsnorm", "route", "permute", "fc1", "fc2", "combine"])
@@ -403,7 +403,8 @@ def main_native(args):
                       row_bytes=H * (1 if fp8 else 2), xscale=xs, xp_scale=xps, workspace=pws)
         mark(3)
         if fused:
-            M.moe_grouped_ffn(shape, xp, w13, w2, offsets, row_src, tw, act, y, fws)
+            M.moe_grouped_ffn(shape, xp, w13, w2, offsets, row_src, tw, act, y, fws, xp_scale=xps,
+                              w13_scale=s13, w2_scale=s2)
         else:
             M.moe_grouped_gemm(shape, M.GEMM_FC1_SILU, xp, w13, offsets, act, a_scale=xps,
                                w_scale=s13)

@@ -136,7 +136,7 @@ Ws layout(const moe_shape* s) {
   w.row_src = take(R * 4);
   w.row_of_pair = take(R * 4);
   w.perm_cnt = take(moe::permute_workspace_bytes(s->T, s->E, s->top_k));
-  w.sched = take((E + 1) * 4);  // fused decode FFN: unit counter + per-expert FC1 progress
+  w.sched = take((2 * E + 1) * 4);  // fused decode FFN: unit counter + per-expert progress
   w.xp = take(R * H * (f8 ? 1 : 2));
   w.xp_scale = take(f8 ? R * 4 : 0);
   w.act = take(R * I * 2);
@@ -254,8 +254,9 @@ moe_status ffn_impl(const moe_shape* s, int engine, bool fuse, const void* xp,
   const int T = s->T, H = s->H, E = s->E, I = s->I, R = s->T * s->top_k;
   if (fuse) {
     // one persistent launch (FC2 units wait per expert for FC1)
-    cudaError_t e = moe::launch_decode_ffn_fused(xp, w13, w2, act, y, offsets, row_src, tw, sched,
-                                                 E, H, I, R, T, dev->sms, dev->status, st);
+    cudaError_t e = moe::launch_decode_ffn_fused(f8, xp, xp_scale, w13, w13_scale, w2, w2_scale,
+                                                 act, actq, act_scale, y, offsets, row_src, tw,
+                                                 sched, E, H, I, R, T, dev->sms, dev->status, st);
     if (e == cudaSuccess) return MOE_OK;
     if (e != cudaErrorNotSupported) return cuda_fail(e, "fused decode FFN launch");
   }
@@ -275,8 +276,8 @@ moe_status ffn_impl(const moe_shape* s, int engine, bool fuse, const void* xp,
 bool fuse_decode(const moe_shape* s, int engine) {
   const char* fuse_env = getenv("MOE_FUSE");
   const char* simt_env = getenv("MOE_FORCE_SIMT");
-  return engine == MOE_ENGINE_DECODE && s->wdtype == MOE_W_BF16 &&
-         !(fuse_env && fuse_env[0] == '0') && !(simt_env && simt_env[0] == '1');
+  return engine == MOE_ENGINE_DECODE && !(fuse_env && fuse_env[0] == '0') &&
+         !(simt_env && simt_env[0] == '1');
 }
 
 moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, const float* router_w,
@@ -351,7 +352,7 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   }
   // a4: permute + gather of the (quantised) token rows
   MOE_CUDA(moe::launch_permute_any(ids, T, E, k, offsets, row_src, row_of_pair, perm_cnt,
-                                   dev->status, st, sched, E + 1),
+                                   dev->status, st, sched, 2 * E + 1),
            "permute launch");
   MOE_CUDA(moe::launch_gather_rows(offsets, E, row_src, k, R, f8 ? (const void*)xq : (const void*)xhat,
                                    xp, H * (f8 ? 1 : 2), xscale, xp_scale, st),
@@ -557,7 +558,7 @@ moe_status moe_grouped_gemm(const moe_shape* shape, int32_t mode, const void* a,
 size_t moe_grouped_ffn_workspace_size(const moe_shape* shape) {
   if (check_shape(shape) != MOE_OK) return 0;
   const size_t R = (size_t)shape->T * shape->top_k;
-  size_t n = up256((size_t)(shape->E + 1) * 4);
+  size_t n = up256((size_t)(2 * shape->E + 1) * 4);
   if (shape->wdtype == MOE_W_FP8_E4M3) n += up256(R * shape->I) + up256(R * 4);
   return n;
 }
@@ -585,14 +586,13 @@ moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* 
   if (shape->T == 0) return MOE_OK;
   cudaStream_t st = (cudaStream_t)stream;
   const size_t R = (size_t)shape->T * shape->top_k;
+  const size_t sched_bytes = (size_t)(2 * shape->E + 1) * 4;
   int32_t* sched = at<int32_t>(workspace, 0);
-  uint8_t* actq = f8 ? at<uint8_t>(workspace, up256((size_t)(shape->E + 1) * 4)) : nullptr;
-  float* act_scale =
-      f8 ? at<float>(workspace, up256((size_t)(shape->E + 1) * 4) + up256(R * shape->I)) : nullptr;
+  uint8_t* actq = f8 ? at<uint8_t>(workspace, up256(sched_bytes)) : nullptr;
+  float* act_scale = f8 ? at<float>(workspace, up256(sched_bytes) + up256(R * shape->I)) : nullptr;
   const int engine = pick_engine(shape);
   const bool fuse = fuse_decode(shape, engine);
-  if (fuse)
-    MOE_CUDA(cudaMemsetAsync(sched, 0, (size_t)(shape->E + 1) * 4, st), "scheduler reset");
+  if (fuse) MOE_CUDA(cudaMemsetAsync(sched, 0, sched_bytes, st), "scheduler reset");
   return ffn_impl(shape, engine, fuse, xp, xp_scale, w13, w13_scale, w2, w2_scale, offsets,
                   row_src, topk_w, act, y, sched, actq, act_scale, dev, st);
 }

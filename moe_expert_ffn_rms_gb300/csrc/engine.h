@@ -24,11 +24,16 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
 
 // Decode FFN in one persistent launch: FC1 + silu_and_mul (xp -> act) and
 // FC2 + routing weight (act -> y, bf16 rows in (token, slot) order), with a
-// dynamic unit scheduler.  `sched` holds 1 + E ints that must be zero when
-// the kernel starts.  bf16 only; cudaErrorNotSupported when not covered.
-cudaError_t launch_decode_ffn_fused(const void* xp, const void* w13, const void* w2, void* act,
-                                    void* y, const int32_t* offsets, const int32_t* row_src,
-                                    const float* topk_w, int* sched, int E, int H, int I, int R_max,
-                                    int T, int sms, int* status, cudaStream_t st);
+// dynamic unit scheduler.  `sched` holds 1 + 2E ints that must be zero when
+// the kernel starts.  With fp8, xp / w13 / w2 are E4M3 codes with scales and
+// the FC1 rows are quantised per row into actq / act_scale inside the launch.
+// cudaErrorNotSupported when not covered.
+cudaError_t launch_decode_ffn_fused(bool fp8, const void* xp, const float* xp_scale,
+                                    const void* w13, const float* w13_scale, const void* w2,
+                                    const float* w2_scale, void* act, uint8_t* actq,
+                                    float* act_scale, void* y, const int32_t* offsets,
+                                    const int32_t* row_src, const float* topk_w, int* sched, int E,
+                                    int H, int I, int R_max, int T, int sms, int* status,
+                                    cudaStream_t st);
 
 }  // namespace moe

@@ -81,8 +81,14 @@ struct Params {
   int b_atom;   // bytes of one B atom
   int njobs;    // 1, or 2 for FC1 -> FC2 in one launch
   // Dynamic scheduling (fused launch): sched[0] is the unit counter, sched[1 + e]
-  // counts finished FC1 epilogue warps of expert e.  NULL: static schedule.
+  // counts finished FC1 epilogue warps (bf16) or units (E4M3) of expert e, and
+  // sched[1 + E + e] is set once expert e's FC1 rows are quantised (E4M3).
+  // NULL: static schedule.
   int* sched;
+  // E4M3 fused launch: the bf16 FC1 rows are quantised per row into these
+  // (the FC2 job's A operand and its scales).
+  uint8_t* actq;
+  float* act_scale;
   int* status;
   JobP job[2];
 };
@@ -330,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ __align__(8) uint64_t xch_bar;
   __shared__ int s_uring[kUnitRing];
+  __shared__ int s_last;  // E4M3 fused: this warpgroup finished an expert's FC1
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ float s_xch[SWAP && (M0 == 1 || M1 == 1) ? 64 * 17 : 1];  // decode FC1: up values
@@ -453,9 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
         if (NJ == 2 && un.job == 1 && p.sched) {
           // wait until job 0 (FC1) has written every row of expert e
           const int cnt = s_off[un.e + 1] - s_off[un.e];
-          const int need = ((cnt + p.chunk - 1) / p.chunk) * p.job[0].nt * 4;
+          // bf16: every FC1 epilogue warp of e has published its rows;
+          // E4M3: e's rows are quantised
+          const int need = FP8 ? 1 : ((cnt + p.chunk - 1) / p.chunk) * p.job[0].nt * 4;
+          const int* flag = FP8 ? p.sched + 1 + p.E + un.e : p.sched + 1 + un.e;
           const long long t0 = clock64();
-          while (ld_acquire(p.sched + 1 + un.e) < need) {
+          while (ld_acquire(flag) < need) {
             if (s_abort || clock64() - t0 > kSpinLimitCycles) {
               s_abort = 1;
               ok = false;
@@ -590,12 +600,62 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
       if (++acc == 2) { acc = 0; aph ^= 1; }
-      if (NJ == 2 && un.job == 0 && p.sched) {
+      if (NJ == 2 && un.job == 0 && p.sched && !FP8) {
         // publish this warp's rows of the FC1 output to later TMA readers
         fence_proxy_async_global();
         __threadfence();
         __syncwarp();
         if (lane == 0) atomicAdd(p.sched + 1 + un.e, 1);
+      }
+      if (NJ == 2 && un.job == 0 && p.sched && FP8) {
+        // count this unit; the warpgroup that completes expert e's last FC1
+        // unit quantises e's rows (per row: s = absmax / 448, q = e4m3(a / s))
+        __threadfence();
+        mbar_arrive(&xch_bar);
+        if (!mbar_wait(&xch_bar, xph, &s_abort)) { flag_status(p.status, MOE_ERR_TIMEOUT); break; }
+        xph ^= 1;
+        const int r0 = s_off[un.e], r1 = s_off[un.e + 1];
+        if (lrow == 0) {
+          const int units_e = ((r1 - r0 + p.chunk - 1) / p.chunk) * p.job[0].nt;
+          s_last = (atomicAdd(p.sched + 1 + un.e, 1) + 1 == units_e) ? 1 : 0;
+        }
+        mbar_arrive(&xch_bar);
+        if (!mbar_wait(&xch_bar, xph, &s_abort)) { flag_status(p.status, MOE_ERR_TIMEOUT); break; }
+        xph ^= 1;
+        if (s_last) {
+          __threadfence();  // every CTA's rows of expert e are visible
+          const bf16* act = reinterpret_cast<const bf16*>(p.job[0].out);
+          for (int r = r0 + q; r < r1; r += 4) {  // warp q: rows q, q+4, ...
+            const uint4* row = reinterpret_cast<const uint4*>(act + (size_t)r * p.I);
+            float amax = 0.f;
+            for (int v = lane; v < p.I / 8; v += 32) {
+              float f[8];
+              unpack8_bf16(__ldcg(row + v), f);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+            }
+            amax = warp_max(amax);
+            const float sc = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+            uint2* qrow = reinterpret_cast<uint2*>(p.actq + (size_t)r * p.I);
+            for (int v = lane; v < p.I / 8; v += 32) {
+              float f[8];
+              unpack8_bf16(__ldcg(row + v), f);
+              uint32_t lo = 0, hi = 0;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) lo |= (uint32_t)f_to_e4m3(__fdiv_rn(f[i], sc)) << (8 * i);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) hi |= (uint32_t)f_to_e4m3(__fdiv_rn(f[4 + i], sc)) << (8 * i);
+              qrow[v] = make_uint2(lo, hi);
+            }
+            if (lane == 0) p.act_scale[r] = sc;
+          }
+          fence_proxy_async_global();
+          __threadfence();
+          mbar_arrive(&xch_bar);
+          if (!mbar_wait(&xch_bar, xph, &s_abort)) { flag_status(p.status, MOE_ERR_TIMEOUT); break; }
+          xph ^= 1;
+          if (lrow == 0) atomicExch(p.sched + 1 + p.E + un.e, 1);
+        }
       }
     }
   }
@@ -1037,13 +1097,17 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
              : launch_mode<false, false>(mode, maps, p, grid, smem, st);
 }
 
-cudaError_t launch_decode_ffn_fused(const void* xp, const void* w13, const void* w2, void* act,
-                                    void* y, const int32_t* offsets, const int32_t* row_src,
-                                    const float* topk_w, int* sched, int E, int H, int I, int R_max,
-                                    int T, int sms, int* status, cudaStream_t st) {
+cudaError_t launch_decode_ffn_fused(bool fp8, const void* xp, const float* xp_scale,
+                                    const void* w13, const float* w13_scale, const void* w2,
+                                    const float* w2_scale, void* act, uint8_t* actq,
+                                    float* act_scale, void* y, const int32_t* offsets,
+                                    const int32_t* row_src, const float* topk_w, int* sched, int E,
+                                    int H, int I, int R_max, int T, int sms, int* status,
+                                    cudaStream_t st) {
   std::call_once(g_encode_once, load_encode);
   if (R_max == 0) return cudaSuccess;
-  if (!g_encode || E > kMaxExperts || !sched) return cudaErrorNotSupported;
+  if (!g_encode || E > kMaxExperts || !sched || I % 8 != 0) return cudaErrorNotSupported;
+  if (fp8 && (!actq || !act_scale || ((uintptr_t)actq & 15u))) return cudaErrorNotSupported;
   Params p{};
   p.offsets = offsets;
   p.E = E;
@@ -1052,15 +1116,20 @@ cudaError_t launch_decode_ffn_fused(const void* xp, const void* w13, const void*
   p.njobs = 2;
   p.sched = sched;
   p.status = status;
+  p.actq = actq;
+  p.act_scale = act_scale;
   CUtensorMap maps[4];
-  if (!make_job(&p.job[0], &maps[0], &maps[1], 1, false, true, xp, nullptr, w13, nullptr, row_src,
-                nullptr, act, E, H, I, I, R_max) ||
-      !make_job(&p.job[1], &maps[2], &maps[3], 3, false, true, act, nullptr, w2, nullptr, row_src,
-                topk_w, y, E, I, I, H, R_max))
+  // FC1 reads x rows (E4M3 with per-row scales on the FP8 path) and writes bf16
+  // rows; FC2 reads those rows (E4M3 copies and scales on the FP8 path)
+  if (!make_job(&p.job[0], &maps[0], &maps[1], 1, fp8, true, xp, xp_scale, w13, w13_scale,
+                row_src, nullptr, act, E, H, I, I, R_max) ||
+      !make_job(&p.job[1], &maps[2], &maps[3], 3, fp8, true, fp8 ? (const void*)actq : act,
+                act_scale, w2, w2_scale, row_src, topk_w, y, E, I, I, H, R_max))
     return cudaErrorNotSupported;
   size_t smem = 0;
   if (!set_ring(&p, true, T, &smem)) return cudaErrorNotSupported;
-  return launch_k<true, false, 1, 3>(maps, p, sms, smem, st);
+  return fp8 ? launch_k<true, true, 1, 3>(maps, p, sms, smem, st)
+             : launch_k<true, false, 1, 3>(maps, p, sms, smem, st);
 }
 
 }  // namespace moe

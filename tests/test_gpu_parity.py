@@ -509,11 +509,12 @@ def test_forward_fp8_small(M):
 def test_forward_reference_workloads(M, cfg, sample):
     inp = workloads.make_inputs(cfg, DEV)
     m, ndiff = check_forward(M, inp, sample=sample)
-    if cfg in ("c2_decode_balanced", "c3_decode_skewed"):
-        # the fused and the two-launch decode paths give identical bits
-        o1, i1, _ = _run_forward(M, inp)
+    if cfg in ("c2_decode_balanced", "c3_decode_skewed", "c4_decode_fp8"):
+        # the fused and the separate-launch decode paths give identical bits
+        fp8w = quantize_weights_gpu(M, inp) if inp["fp8"] else None
+        o1, i1, _ = _run_forward(M, inp, fp8_weights=fp8w)
         os.environ["MOE_FUSE"] = "0"
-        o2, i2, _ = _run_forward(M, inp)
+        o2, i2, _ = _run_forward(M, inp, fp8_weights=fp8w)
         os.environ.pop("MOE_FUSE", None)
         assert torch.equal(i1, i2) and torch.equal(o1, o2)
     print(f"{cfg}: max scaled error {m:.3e}, near-tie routing differences {ndiff}")
