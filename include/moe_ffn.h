@@ -112,6 +112,13 @@ moe_status moe_check_device(void);
  * `status_out` is a HOST pointer.  Synchronises the device. */
 moe_status moe_device_status(int32_t* status_out, int32_t clear);
 
+/* Self-test of the library's bounded device waits (failure detection; not a
+ * step of the method).  Enqueues one kernel that waits on an mbarrier no
+ * thread arrives on, gives up after limit_cycles SM cycles (0 < limit <=
+ * 2^32), records MOE_ERR_TIMEOUT in the device status word and returns, so
+ * the CUDA context stays usable.  Read the result with moe_device_status(). */
+moe_status moe_selftest_wait_timeout(int64_t limit_cycles, moe_stream_t stream);
+
 /* ------------------------------------------------------- whole forward -- */
 
 /* Device workspace bytes moe_ffn_forward / moe_ffn_forward_routed need for

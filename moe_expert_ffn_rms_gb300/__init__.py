@@ -56,6 +56,7 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_check_device": (ctypes.c_int, []),
     "moe_device_status": (ctypes.c_int, [ctypes.POINTER(_I32), _I32]),
+    "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, _P]),
     "moe_ffn_workspace_size": (_SZ, [ctypes.POINTER(MoeShape)]),
     "moe_ffn_forward": (ctypes.c_int, [ctypes.POINTER(MoeShape), _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                        _P, _P, _P, _P, _SZ, _P]),
@@ -130,6 +131,10 @@ def device_status(clear: bool = True) -> int:
     v = _I32(0)
     _check(lib.moe_device_status(ctypes.byref(v), 1 if clear else 0))
     return v.value
+
+
+def moe_selftest_wait_timeout(limit_cycles: int, stream=None):
+    _check(lib.moe_selftest_wait_timeout(limit_cycles, _stream(stream)))
 
 
 def moe_ffn_workspace_size(shape: MoeShape) -> int:

@@ -413,6 +413,17 @@ moe_status moe_device_status(int32_t* status_out, int32_t clear) {
   return MOE_OK;
 }
 
+moe_status moe_selftest_wait_timeout(int64_t limit_cycles, moe_stream_t stream) {
+  MOE_REQ(limit_cycles > 0 && limit_cycles <= (int64_t)1 << 32, MOE_ERR_INVALID_ARG,
+          "limit_cycles must be in (0, 2^32]");
+  DevInfo* d = nullptr;
+  moe_status rc = device_info(&d);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(moe::launch_wait_selftest(limit_cycles, d->status, (cudaStream_t)stream),
+           "self-test launch");
+  return MOE_OK;
+}
+
 size_t moe_ffn_workspace_size(const moe_shape* shape) {
   if (check_shape(shape) != MOE_OK) return 0;
   return layout(shape).total;

@@ -36,4 +36,8 @@ cudaError_t launch_decode_ffn_fused(bool fp8, const void* xp, const float* xp_sc
                                     int H, int I, int R_max, int T, int sms, int* status,
                                     cudaStream_t st);
 
+// Bounded-wait self-test: a kernel that waits on an mbarrier nothing arrives
+// on for at most limit_cycles SM cycles and records MOE_ERR_TIMEOUT.
+cudaError_t launch_wait_selftest(long long limit_cycles, int* status, cudaStream_t st);
+
 }  // namespace moe

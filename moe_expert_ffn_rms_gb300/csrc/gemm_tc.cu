@@ -310,6 +310,47 @@ MOE_DEV bool epilogue_unit(const Unit& un, const JobP& j, int I, uint32_t tbase,
   return true;
 }
 
+// ------------------------------------------------------ pipeline tails --
+// tcgen05.commit arrives on its mbarriers asynchronously, and with a CTA pair
+// the even CTA's commits also arrive on the odd CTA's barriers.  A CTA must
+// not exit while such an arrival is still on its way to its shared memory
+// (the next CTA on the SM reuses it), so before teardown each role waits for
+// the arrivals it has not consumed yet.
+
+// Producer tail: waits until the MMAs have released the last use of every
+// ring slot.  (s, ph) is the producer's position after its last slot; a slot
+// never used passes at once.
+MOE_DEV bool producer_tail(uint64_t* empty_bar, int stages, int s, uint32_t ph,
+                           volatile int* abort) {
+  for (int i = 0; i < stages; ++i) {
+    if (!mbar_wait(&empty_bar[s], ph ^ 1, abort)) return false;
+    if (++s == stages) { s = 0; ph ^= 1; }
+  }
+  return true;
+}
+
+// MMA tail: waits until the epilogues have released both accumulators.
+MOE_DEV bool accumulator_tail(uint64_t* tempty_bar, int acc, uint32_t aph, volatile int* abort) {
+  for (int i = 0; i < 2; ++i) {
+    if (!mbar_wait(&tempty_bar[acc], aph ^ 1, abort)) return false;
+    if (++acc == 2) { acc = 0; aph ^= 1; }
+  }
+  return true;
+}
+
+// After an abort: waits, bounded, for the copies of the last arming of every
+// slot (bit i of `armed`; its phase parity in bit i of `armed_ph`), whether or
+// not the MMAs consumed them.
+MOE_DEV void drain_armed(uint64_t* full_bar, int stages, uint32_t armed, uint32_t armed_ph) {
+  for (int i = 0; i < stages; ++i) {
+    if (!((armed >> i) & 1u)) continue;
+    const uint32_t par = (armed_ph >> i) & 1u;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(&full_bar[i], par) && clock64() - t0 < kSpinLimitCycles) {
+    }
+  }
+}
+
 // Persistent grouped GEMM.  One launch runs job 0 (mode M0) and, when M1 >= 0,
 // job 1 (mode M1) after it: units of job 0 come first in the unit order.
 // Static schedule (p.sched == NULL): CTA c takes units c, c + grid, ...
@@ -442,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
       const uint64_t pol_x = l2_policy_evict_last();
       int s = 0;
       uint32_t ph = 0;
+      uint32_t armed = 0, armed_ph = 0;
       bool ok = true;
       for (int i = 0; ok; ++i) {
         // claim the next unit and publish it to the other roles
@@ -496,18 +538,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
               issue_stage<SWAP, 0>(a + w * p.a_atom, b + w * p.b_atom, &full_bar[s], tw, tx_map, un,
                                    kx, wrow, p.I, nb, pol_w, pol_x);
           }
+          armed |= 1u << s;
+          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
           if (++s == p.stages) { s = 0; ph ^= 1; }
         }
       }
+      if (ok) ok = producer_tail(empty_bar, p.stages, s, ph, &s_abort);
       if (!ok) {
-        // Drain: every slot armed last and not consumed completes its copies.
         flag_status(p.status, MOE_ERR_TIMEOUT);
-        for (int i = 0; i < p.stages; ++i) {
-          const long long t0 = clock64();
-          while (!mbar_try_wait(&full_bar[i], 0) && !mbar_try_wait(&full_bar[i], 1) &&
-                 clock64() - t0 < kSpinLimitCycles) {
-          }
-        }
+        drain_armed(full_bar, p.stages, armed, armed_ph);
       }
     }
   } else if (warp == 1) {
@@ -555,6 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
         mma_commit(&tfull_bar[acc]);
         if (++acc == 2) { acc = 0; aph ^= 1; }
       }
+      if (ok) ok = accumulator_tail(tempty_bar, acc, aph, &s_abort);
       if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
       if (issued) {  // all issued MMAs complete before TMEM can be released
         mma_commit(&drain_bar);
@@ -770,6 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_pair_kernel(
       const uint64_t pol_x = l2_policy_evict_last();
       int s = 0;
       uint32_t ph = 0;
+      uint32_t armed = 0, armed_ph = 0;
       bool ok = true;
       const uint32_t bytes_pair = 2u * (uint32_t)(p.a_atom + p.b_atom);
       for (int u = pair; u < U && ok; u += npairs) {
@@ -787,19 +828,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_pair_kernel(
           const int kx = ks * (FP8 ? 128 : 64);
           tma_load_2d_pair(a, &tm_x, fb, kx, arow, pol_x);
           tma_load_2d_pair(b, &tm_w, fb, kx, brow, pol_w);
+          armed |= 1u << s;
+          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
           if (++s == p.stages) { s = 0; ph ^= 1; }
         }
       }
+      // both CTAs: the even CTA's commits arrive on this CTA's empty barriers
+      if (ok) ok = producer_tail(empty_bar, p.stages, s, ph, &s_abort);
       if (!ok) {
         flag_status(p.status, MOE_ERR_TIMEOUT);
-        if (leader) {  // the even CTA's full barriers count both CTAs' copies
-          for (int i = 0; i < p.stages; ++i) {
-            const long long t0 = clock64();
-            while (!mbar_try_wait(&full_bar[i], 0) && !mbar_try_wait(&full_bar[i], 1) &&
-                   clock64() - t0 < kSpinLimitCycles) {
-            }
-          }
-        }
+        // the even CTA's full barriers count both CTAs' copies
+        if (leader) drain_armed(full_bar, p.stages, armed, armed_ph);
       }
     }
   } else if (warp == 1) {
@@ -837,6 +876,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_pair_kernel(
         mma_commit_pair(&tfull_bar[acc], 0x3);
         if (++acc == 2) { acc = 0; aph ^= 1; }
       }
+      // both CTAs' epilogues (remote arrivals from the odd CTA) have released
+      // the accumulators before teardown
+      if (ok) ok = accumulator_tail(tempty_bar, acc, aph, &s_abort);
       if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
       if (issued) {
         mma_commit_pair(&drain_bar, 0x1);
@@ -1052,7 +1094,25 @@ cudaError_t launch_prefill_pair(int mode, bool fp8, const Params& base, const Jo
              : launch_pair<3, false>(tw, tx, p, 2 * npairs, smem, st);
 }
 
+// Self-test of the bounded waits: one thread waits on an mbarrier that no
+// thread arrives on, for at most `limit` cycles, and records the timeout.
+__global__ void wait_selftest_kernel(long long limit, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    if (!mbar_wait_limit(&bar, 0, &abort_flag, limit)) flag_status(status, MOE_ERR_TIMEOUT);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(long long limit_cycles, int* status, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(limit_cycles, status);
+  return cudaGetLastError();
+}
 
 void engine_init_device() { std::call_once(g_encode_once, load_encode); }
 

@@ -625,7 +625,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restr
     const int t = row_src[r] / k;
     const uint4* s = src + (size_t)t * row_vec;
     uint4* d = dst + (size_t)r * row_vec;
-    for (int v = lane; v < row_vec; v += 32) d[v] = s[v];
+    int v = lane;
+    for (; v + 96 < row_vec; v += 128) {  // four 16-byte loads in flight per lane
+      const uint4 a = s[v], b = s[v + 32], c = s[v + 64], e4 = s[v + 96];
+      d[v] = a;
+      d[v + 32] = b;
+      d[v + 64] = c;
+      d[v + 96] = e4;
+    }
+    for (; v < row_vec; v += 32) d[v] = s[v];
     if (dscale && lane == 0) dscale[r] = sscale[t];
   }
 }
@@ -729,10 +737,72 @@ __global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y
   reinterpret_cast<uint4*>(out + (size_t)t * H)[h8] = o;
 }
 
+// Persistent form for (token, slot)-ordered bf16 rows: each thread takes two
+// (token, 8-column group) items per pass with all of their row loads in
+// flight before any sum, and the grid strides over the items.
+__global__ void __launch_bounds__(256) combine_pair_bf16_kernel(const bf16* __restrict__ y,
+                                                                const int32_t* __restrict__ rop,
+                                                                int T, int k, int H,
+                                                                bf16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int g8 = H >> 3;
+  const int64_t total = (int64_t)T * g8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 2 * stride) {
+    uint4 raw[2][kMaxTopK];
+    int valid[2][kMaxTopK];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t it = i0 + u * stride;
+      const bool in = it < total;
+      const int64_t t = in ? it / g8 : 0;
+      const int64_t g = in ? it % g8 : 0;
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) {
+        const bool use = in && j < k;
+        valid[u][j] = use ? rop[t * k + j] : -1;
+        raw[u][j] = use ? reinterpret_cast<const uint4*>(y + (t * k + j) * H)[g]
+                        : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t it = i0 + u * stride;
+      if (it >= total) break;
+      float s[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) {  // summed in j order, skipped pairs excluded
+        if (j < k && valid[u][j] >= 0) {
+          float f[8];
+          unpack8_bf16(raw[u][j], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) s[i] += f[i];
+        }
+      }
+      uint4 o;
+      o.x = pack2_bf16(s[0], s[1]);
+      o.y = pack2_bf16(s[2], s[3]);
+      o.z = pack2_bf16(s[4], s[5]);
+      o.w = pack2_bf16(s[6], s[7]);
+      reinterpret_cast<uint4*>(out)[it] = o;
+    }
+  }
+}
+
 cudaError_t launch_combine(const void* y, bool y_bf16, bool pair_order,
                            const int32_t* row_of_pair, int T, int k, int H, void* out,
                            cudaStream_t st) {
   if (T == 0) return cudaSuccess;
+  if (y_bf16 && pair_order) {
+    const int64_t items = (int64_t)T * (H / 8);
+    int64_t blocks = (items + 511) / 512;
+    if (blocks > 152 * 4) blocks = 152 * 4;
+    return launch_kernel(combine_pair_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, st,
+                         (const bf16*)y, row_of_pair, T, k, H, (bf16*)out);
+  }
   const int h8 = H / 8;
   dim3 grid((h8 + 255) / 256, T);
 #define MOE_COMBINE(B, P) \

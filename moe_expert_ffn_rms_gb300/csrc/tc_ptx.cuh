@@ -47,17 +47,22 @@ MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits for the phase of `bar` with the given parity to complete.  Returns
 // false (and raises *abort) when the wait runs past kSpinLimitCycles or when
 // another role already raised *abort.
-MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+MOE_DEV bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort,
+                             long long limit_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kSpinLimitCycles) {
+    if (clock64() - t0 > limit_cycles) {
       *abort = 1;
       return false;
     }
   }
+}
+
+MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return mbar_wait_limit(bar, parity, abort, kSpinLimitCycles);
 }
 
 // ------------------------------------------------------------------ TMA --

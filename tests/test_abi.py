@@ -121,6 +121,7 @@ def test_step_entry_points_reject_bad_arguments_on_host(M):
                                  fake, fake, fake, fake, fake, 16, None) == 4
     assert M.lib.moe_grouped_ffn(ctypes.byref(shape), None, None, fake, None, fake, None, fake,
                                  fake, fake, fake, fake, fake, 1 << 20, None) == 1
+    assert M.lib.moe_selftest_wait_timeout(0, None) == 1
     assert M.lib.moe_route_workspace_size(4, 256, 8) > 0
     assert M.lib.moe_route_workspace_size(4, 250, 8) == 0
 

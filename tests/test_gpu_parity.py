@@ -587,3 +587,20 @@ def test_identity_experts_on_gpu(M):
     expect = O.bf16_round(O.bf16_round(xh * xh * scipy.special.expit(xh)))
     err = scaled_err(f64(out), expect)
     assert err.max() <= 1e-2
+
+
+def test_bounded_wait_times_out_and_context_survives(M):
+    """A device wait that nothing completes gives up after its limit, records
+    MOE_ERR_TIMEOUT in the status word, and the context keeps working."""
+    import time
+    M.device_status(clear=True)
+    t0 = time.perf_counter()
+    M.moe_selftest_wait_timeout(20_000_000)        # ~10 ms of SM cycles
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 5.0
+    assert M.device_status(clear=True) == 6        # MOE_ERR_TIMEOUT
+    inp = workloads.make_inputs("c1_tiny", DEV)
+    out, ids, _ = _run_forward(M, inp)
+    assert torch.isfinite(out.float()).all()
+    assert M.device_status() == 0
+
