@@ -311,6 +311,10 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   cudaStream_t st = (cudaStream_t)stream;
   const int T = s->T, H = s->H, E = s->E, I = s->I, k = s->top_k, R = T * k;
   const int engine = pick_engine(s);
+  // The prefill forward runs without programmatic dependent launch: each
+  // kernel starts after its predecessor has completed (the launch overlap is
+  // worth ~1% there; decode, where it matters, keeps it).
+  PdlOff no_pdl(engine == MOE_ENGINE_PREFILL);
 
   bf16* xhat = at<bf16>(workspace, L.xhat);
   uint8_t* xq = f8 ? at<uint8_t>(workspace, L.xq) : nullptr;
@@ -602,6 +606,7 @@ moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* 
   uint8_t* actq = f8 ? at<uint8_t>(workspace, up256(sched_bytes)) : nullptr;
   float* act_scale = f8 ? at<float>(workspace, up256(sched_bytes) + up256(R * shape->I)) : nullptr;
   const int engine = pick_engine(shape);
+  PdlOff no_pdl(engine == MOE_ENGINE_PREFILL);  // as in the forward
   const bool fuse = fuse_decode(shape, engine);
   if (fuse) MOE_CUDA(cudaMemsetAsync(sched, 0, sched_bytes, st), "scheduler reset");
   return ffn_impl(shape, engine, fuse, xp, xp_scale, w13, w13_scale, w2, w2_scale, offsets,

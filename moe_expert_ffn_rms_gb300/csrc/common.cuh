@@ -63,9 +63,23 @@ MOE_DEV uint8_t f_to_e4m3(float v) {
 // silu(z) = z / (1 + exp(-z)), fp32.
 MOE_DEV float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-// Host: launch `kern` on `st`, with programmatic stream serialisation unless
-// the environment sets MOE_PDL=0.
+// Host: programmatic dependent launch is used unless the environment sets
+// MOE_PDL=0 or the calling thread is inside a PdlOff scope with off = true.
 bool pdl_enabled();
+
+class PdlOff {
+ public:
+  explicit PdlOff(bool off = true);
+  ~PdlOff();
+  PdlOff(const PdlOff&) = delete;
+  PdlOff& operator=(const PdlOff&) = delete;
+
+ private:
+  bool prev_;
+};
+
+// Host: launch `kern` on `st`, with programmatic stream serialisation when
+// pdl_enabled().
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,

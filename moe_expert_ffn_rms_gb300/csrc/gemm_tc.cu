@@ -1058,12 +1058,15 @@ cudaError_t launch_pair(const CUtensorMap& tw, const CUtensorMap& tx, const Para
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Prefill on CTA pairs; cudaErrorNotSupported when not covered.
+// Prefill on CTA pairs; cudaErrorNotSupported when not covered or not
+// enabled.  Off unless MOE_PREFILL_PAIR=1: prefill runs with this kernel
+// stalled intermittently on GB300 and the cause has not been found, so the
+// single-CTA tiles are the default.
 cudaError_t launch_prefill_pair(int mode, bool fp8, const Params& base, const JobP& job,
                                 const CUtensorMap& tw, const CUtensorMap& tx, int sms,
                                 cudaStream_t st) {
   const char* env = getenv("MOE_PREFILL_PAIR");
-  if (env && env[0] == '0') return cudaErrorNotSupported;
+  if (!(env && env[0] == '1')) return cudaErrorNotSupported;
   Params p = base;
   p.job[0] = job;
   p.njobs = 1;
@@ -1124,6 +1127,8 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
   std::call_once(g_encode_once, load_encode);
   if (R_max == 0) return cudaSuccess;
   if (!g_encode || E > kMaxExperts) return cudaErrorNotSupported;
+  // prefill tiles start only after their predecessor has completed
+  PdlOff no_pdl(!decode);
   Params p{};
   p.offsets = offsets;
   p.E = E;

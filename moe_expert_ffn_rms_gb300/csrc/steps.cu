@@ -8,13 +8,23 @@
 #include <float.h>
 #include <stdlib.h>
 
+namespace {
+thread_local bool t_pdl_off = false;
+}  // namespace
+
 bool pdl_enabled() {
   static const bool on = [] {
     const char* e = getenv("MOE_PDL");
     return !(e && e[0] == '0');
   }();
-  return on;
+  return on && !t_pdl_off;
 }
+
+PdlOff::PdlOff(bool off) : prev_(t_pdl_off) {
+  if (off) t_pdl_off = true;
+}
+
+PdlOff::~PdlOff() { t_pdl_off = prev_; }
 
 namespace moe {
 
