@@ -207,6 +207,26 @@ moe_status compute_router_logits(const void* xhat, const float* router_w, int T,
   return MOE_OK;
 }
 
+// Router (when router_w is given) + softmax / top-k / renorm into ids, w.
+moe_status route_topk_impl(const void* xhat, const float* router_w, const float* logits_in,
+                           const float* bias, int T, int H, int E, int k, int32_t* ids, float* w,
+                           float* logits_out, void* ws, DevInfo* dev, cudaStream_t st) {
+  if (!logits_in && !router_on_tensor_cores(T) && moe::route_small(H, E)) {
+    MOE_CUDA(moe::launch_route_small(xhat, router_w, bias, T, H, E, k, ids, w, logits_out, st),
+             "router launch");
+    return MOE_OK;
+  }
+  const float* part = logits_in;
+  int ks = 1;
+  size_t zs = 0, ts = 0;
+  if (!logits_in) {
+    moe_status rc = compute_router_logits(xhat, router_w, T, H, E, ws, dev, st, &part, &ks, &zs, &ts);
+    if (rc != MOE_OK) return rc;
+  }
+  MOE_CUDA(moe::launch_topk(part, ks, bias, T, E, k, ids, w, logits_out, st, zs, ts),
+           "top-k launch");
+  return MOE_OK;
+}
 
 int pick_engine(const moe_shape* s) {
   if (s->engine != MOE_ENGINE_AUTO) return s->engine;
@@ -343,16 +363,9 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
     ids = const_cast<int32_t*>(ids_in);
     tw = const_cast<float*>(tw_in);
   } else {
-    const float* part = router_logits;
-    int ks = 1;
-    size_t zs = 0, ts = 0;
-    if (router_w) {
-      rc = compute_router_logits(xhat, router_w, T, H, E, at<void>(workspace, L.part), dev, st, &part, &ks,
-                         &zs, &ts);
-      if (rc != MOE_OK) return rc;
-    }
-    MOE_CUDA(moe::launch_topk(part, ks, router_bias, T, E, k, ids, tw, nullptr, st, zs, ts),
-             "top-k launch");
+    rc = route_topk_impl(xhat, router_w, router_logits, router_bias, T, H, E, k, ids, tw, nullptr,
+                         at<void>(workspace, L.part), dev, st);
+    if (rc != MOE_OK) return rc;
   }
   // a4: permute + gather of the (quantised) token rows
   MOE_CUDA(moe::launch_permute_any(ids, T, E, k, offsets, row_src, row_of_pair, perm_cnt,
@@ -495,18 +508,11 @@ moe_status moe_route_topk(const void* xhat, const float* router_w, const float* 
   moe_status rc = device_info(&d);
   if (rc != MOE_OK) return rc;
   cudaStream_t st = (cudaStream_t)stream;
-  const float* part = logits_in;
-  int ks = 1;
-  size_t zs = 0, ts = 0;
-  if (!logits_in) {
+  if (!logits_in)
     MOE_REQ(((uintptr_t)workspace & 255u) == 0, MOE_ERR_INVALID_ARG,
             "workspace must be 256-byte aligned");
-    rc = compute_router_logits(xhat, router_w, T, H, E, workspace, d, st, &part, &ks, &zs, &ts);
-    if (rc != MOE_OK) return rc;
-  }
-  MOE_CUDA(moe::launch_topk(part, ks, router_bias, T, E, k, ids, weights, logits_out, st, zs, ts),
-           "top-k launch");
-  return MOE_OK;
+  return route_topk_impl(xhat, router_w, logits_in, router_bias, T, H, E, k, ids, weights,
+                         logits_out, workspace, d, st);
 }
 
 size_t moe_permute_workspace_size(int32_t T, int32_t E, int32_t k) {

@@ -19,6 +19,12 @@ cudaError_t launch_router_logits(const void* xhat, const float* wr, int T, int H
 cudaError_t launch_topk(const float* part, int ks, const float* bias, int T, int E, int k,
                         int32_t* ids, float* w, float* logits_out, cudaStream_t st,
                         size_t zstride = 0, size_t tstride = 0);
+// Router + top-k in one launch for small routers (one CTA per token); used
+// when route_small(H, E).
+bool route_small(int H, int E);
+cudaError_t launch_route_small(const void* xhat, const float* wr, const float* bias, int T,
+                               int H, int E, int k, int32_t* ids, float* w, float* logits_out,
+                               cudaStream_t st);
 // Tensor-core router: split W_r into three transposed bf16 pieces [3E, H]
 // and write the one-segment offsets {0, T}.
 cudaError_t launch_router_split(const float* wr, int H, int E, int T, void* wt, int32_t* seg,

@@ -250,45 +250,15 @@ cudaError_t launch_router_logits(const void* xhat, const float* wr, int T, int H
 }
 
 // ==================================================== softmax / top-k / renorm
-// One warp per token.  Logit of expert e = sum_z part[z, t, e] (+ bias[e]);
-// lane l holds experts l, l+32, ...  The k winners are taken one at a time by
-// a warp arg-max (larger logit first, lower index on ties); the weights are
-// the softmax over the selected logits (= full softmax renormalised).
-__global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ part, int ks,
-                                                   size_t zstride, size_t tstride,
-                                                   const float* __restrict__ bias, int T, int E,
-                                                   int k, int32_t* __restrict__ ids,
-                                                   float* __restrict__ wout,
-                                                   float* __restrict__ logits_out) {
-  pdl_trigger();
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  constexpr int PER = kMaxExperts / 32;
-  float v[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) v[i] = 0.f;
-  // Partial sums: chunk z outer, experts inner, so a lane has up to PER loads
-  // in flight; each logit is still summed in z order.
-  const float* pt = part + (size_t)t * tstride;
-  for (int z = 0; z < ks; ++z) {
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) v[i] += pt[z * zstride + e];
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
-      if (bias) v[i] += bias[e];
-      if (logits_out) logits_out[(size_t)t * E + e] = v[i];
-    } else {
-      v[i] = -FLT_MAX;
-    }
-  }
+// Top-k of one token by one warp: lane l holds the logits of experts l, l+32,
+// ... in v (-FLT_MAX past E).  The k winners are taken one at a time by a warp
+// arg-max (larger logit first, lower index on ties); the weights are the
+// softmax over the selected logits (= full softmax renormalised).  Lane 0
+// writes ids[0..k) and w[0..k).
+constexpr int kTopkPer = kMaxExperts / 32;
+
+MOE_DEV void warp_topk(const float (&v)[kTopkPer], int E, int k, int lane, int32_t* ids,
+                       float* w) {
   unsigned taken = 0;
   float sel_v[kMaxTopK];
   int sel_e[kMaxTopK];
@@ -298,7 +268,7 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
     float bv = -INFINITY;
     int be = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
+    for (int i = 0; i < kTopkPer; ++i) {
       const int e = lane + 32 * i;
       if (e < E && !(taken & (1u << i)) && (v[i] > bv || (v[i] == bv && e < be))) {
         bv = v[i];
@@ -331,10 +301,118 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
       if (j >= k) break;
-      ids[(size_t)t * k + j] = sel_e[j];
-      wout[(size_t)t * k + j] = p[j] / s;
+      ids[j] = sel_e[j];
+      w[j] = p[j] / s;
     }
   }
+}
+
+// One warp per token.  Logit of expert e = sum_z part[z, t, e] (+ bias[e]).
+__global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ part, int ks,
+                                                   size_t zstride, size_t tstride,
+                                                   const float* __restrict__ bias, int T, int E,
+                                                   int k, int32_t* __restrict__ ids,
+                                                   float* __restrict__ wout,
+                                                   float* __restrict__ logits_out) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float v[kTopkPer];
+#pragma unroll
+  for (int i = 0; i < kTopkPer; ++i) v[i] = 0.f;
+  // Partial sums: chunk z outer, experts inner, so a lane has up to
+  // kTopkPer loads in flight; each logit is still summed in z order.
+  const float* pt = part + (size_t)t * tstride;
+  for (int z = 0; z < ks; ++z) {
+#pragma unroll
+    for (int i = 0; i < kTopkPer; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) v[i] += pt[z * zstride + e];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kTopkPer; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      if (bias) v[i] += bias[e];
+      if (logits_out) logits_out[(size_t)t * E + e] = v[i];
+    } else {
+      v[i] = -FLT_MAX;
+    }
+  }
+  warp_topk(v, E, k, lane, ids + (size_t)t * k, wout + (size_t)t * k);
+}
+
+// Router + top-k for small routers (H * E <= kRouteSmallMaxHE, H <= 8192): one
+// CTA per token.  The token's x_hat row is staged in shared memory as fp32;
+// thread (g, e), g < G = 256 / E, sums x_hat[h] * W_r[h, e] over the rows
+// h = g, g + G, ... (a row of W_r is read by consecutive threads), the G
+// partial sums of expert e are added in g order, and warp 0 selects the top k.
+constexpr int kRouteSmallMaxHE = 65536;
+constexpr int kRouteSmallMaxH = 8192;
+
+__global__ void __launch_bounds__(256) route_small_kernel(const bf16* __restrict__ xhat,
+                                                          const float* __restrict__ wr,
+                                                          const float* __restrict__ bias, int T,
+                                                          int H, int E, int k,
+                                                          int32_t* __restrict__ ids,
+                                                          float* __restrict__ wout,
+                                                          float* __restrict__ logits_out) {
+  __shared__ float xs[kRouteSmallMaxH];
+  __shared__ float ps[256];
+  __shared__ float lg[kMaxExperts];
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(xhat + (size_t)t * H);
+  for (int v = tid; v < H / 8; v += blockDim.x) {
+    float f[8];
+    unpack8_bf16(xr[v], f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) xs[v * 8 + q] = f[q];
+  }
+  __syncthreads();
+  const int G = blockDim.x / E;  // row groups (>= 1: E <= 256)
+  const int g = tid / E, e = tid % E;
+  float acc = 0.f;
+  if (g < G) {
+    for (int h = g; h < H; h += G) acc = fmaf(xs[h], wr[(size_t)h * E + e], acc);
+  }
+  ps[tid] = acc;
+  __syncthreads();
+  for (int ee = tid; ee < E; ee += blockDim.x) {
+    float s = 0.f;
+    for (int gg = 0; gg < G; ++gg) s += ps[gg * E + ee];
+    if (bias) s += bias[ee];
+    lg[ee] = s;
+    if (logits_out) logits_out[(size_t)t * E + ee] = s;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    float v[kTopkPer];
+#pragma unroll
+    for (int i = 0; i < kTopkPer; ++i) {
+      const int ex = tid + 32 * i;
+      v[i] = ex < E ? lg[ex] : -FLT_MAX;
+    }
+    warp_topk(v, E, k, tid, ids + (size_t)t * k, wout + (size_t)t * k);
+  }
+}
+
+bool route_small(int H, int E) {
+  return H <= kRouteSmallMaxH && (int64_t)H * E <= kRouteSmallMaxHE;
+}
+
+cudaError_t launch_route_small(const void* xhat, const float* wr, const float* bias, int T,
+                               int H, int E, int k, int32_t* ids, float* w, float* logits_out,
+                               cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  if (!route_small(H, E)) return cudaErrorInvalidValue;
+  return launch_kernel(route_small_kernel, dim3(T), dim3(256), 0, st, (const bf16*)xhat, wr, bias,
+                       T, H, E, k, ids, w, logits_out);
 }
 
 cudaError_t launch_topk(const float* part, int ks, const float* bias, int T, int E, int k,

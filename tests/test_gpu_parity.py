@@ -132,14 +132,22 @@ def test_route_topk_given_logits_bit_exact(M, T, E, k):
 
 
 @pytest.mark.parametrize("tc", ["1", "0"])
-@pytest.mark.parametrize("cfg", ["c1_tiny", "c3_decode_skewed", "c5_prefill", "wide_prefill"])
+@pytest.mark.parametrize("cfg", ["c1_tiny", "c3_decode_skewed", "c5_prefill", "wide_prefill",
+                                 "small_uneven", "small_bias"])
 def test_route_topk_router(M, cfg, tc):
     """Router logits from x_hat and W_r (tensor-core bf16x3 split for >= 256
-    tokens unless MOE_ROUTER_TC=0, else fp32 SIMT) against the fp64 oracle."""
+    tokens unless MOE_ROUTER_TC=0; a one-CTA-per-token router fused with top-k
+    when H * E is small; else fp32 SIMT split-K) against the fp64 oracle."""
     os.environ["MOE_ROUTER_TC"] = tc
     if cfg == "wide_prefill":   # E = 256 -> three N tiles of the split router GEMM
         inp = workloads.make_inputs("c3_decode_skewed", DEV,
                                     shape=workloads.Shape(T=600, H=1024, E=256, k=8, I=256))
+    elif cfg == "small_uneven":  # E does not divide the 256 threads of the small router
+        inp = workloads.make_inputs("c1_tiny", DEV,
+                                    shape=workloads.Shape(T=5, H=512, E=24, k=3, I=256))
+    elif cfg == "small_bias":    # Zipf bias on a small router, H * E at the size limit
+        inp = workloads.make_inputs("c3_decode_skewed", DEV,
+                                    shape=workloads.Shape(T=9, H=256, E=256, k=8, I=256))
     else:
         inp = workloads.make_inputs(cfg, DEV)
     T, H, E, k = inp["T"], inp["H"], inp["E"], inp["k"]
