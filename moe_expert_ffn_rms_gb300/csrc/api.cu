@@ -136,7 +136,9 @@ Ws layout(const moe_shape* s) {
   w.row_src = take(R * 4);
   w.row_of_pair = take(R * 4);
   w.perm_cnt = take(moe::permute_workspace_bytes(s->T, s->E, s->top_k));
-  w.sched = take((2 * E + 1) * 4);  // fused decode FFN: unit counter + per-expert progress
+  // fused decode FFN: unit counter + per-expert progress; then the two grid
+  // barrier words of the one-launch decode forward
+  w.sched = take((2 * E + 3) * 4);
   w.xp = take(R * H * (f8 ? 1 : 2));
   w.xp_scale = take(f8 ? R * 4 : 0);
   w.act = take(R * I * 2);
@@ -356,6 +358,38 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   // unless MOE_FUSE=0 or the SIMT engine is forced.
   const bool fuse = fuse_decode(s, engine);
 
+  // Small decode batches, opt-in: a1..a8 in one cooperative launch
+  if (fuse && moe::decode_forward_mega_covers(T, H, E, k, router_logits != nullptr, routed)) {
+    moe::DecodeForward f{};
+    f.x = x;
+    f.norm_w = norm_w;
+    f.eps = s->eps;
+    f.T = T;
+    f.H = H;
+    f.k = k;
+    f.logits = routed ? nullptr : router_logits;
+    f.router_w = routed ? nullptr : router_w;
+    f.bias = routed ? nullptr : router_bias;
+    f.ids_in = routed ? ids_in : nullptr;
+    f.tw_in = routed ? tw_in : nullptr;
+    f.xhat = xhat;
+    f.xq = xq;
+    f.xscale = xscale;
+    f.ids = ids;
+    f.tw = tw;
+    f.offsets = offsets;
+    f.row_src = row_src;
+    f.row_of_pair = row_of_pair;
+    f.xp = xp;
+    f.xp_scale = xp_scale;
+    f.y = y;
+    f.out = out;
+    f.bar = sched + 2 * E + 1;
+    cudaError_t e = moe::launch_decode_forward_mega(f8, f, w13, w13_scale, w2, w2_scale, act, actq,
+                                                    act_scale, sched, E, I, dev->sms, dev->status, st);
+    if (e == cudaSuccess) return MOE_OK;
+    if (e != cudaErrorNotSupported) return cuda_fail(e, "decode forward launch");
+  }
   // a1: rms_norm (+ per-token E4M3 quantisation on the FP8 path)
   MOE_CUDA(moe::launch_rmsnorm(x, norm_w, T, H, s->eps, xhat, xq, xscale, st), "rmsnorm launch");
   // a2 + a3: router logits, softmax, top-k, renorm

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
+#include <float.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "../../include/moe_ffn.h"
@@ -62,6 +64,64 @@ MOE_DEV uint8_t f_to_e4m3(float v) {
 
 // silu(z) = z / (1 + exp(-z)), fp32.
 MOE_DEV float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// ------------------------------------------------------------- top-k --
+// Top-k of one token by one warp: lane l holds the logits of experts l, l+32,
+// ... in v (-FLT_MAX past E).  The k winners are taken one at a time by a warp
+// arg-max (larger logit first, lower index on ties); the weights are the
+// softmax over the selected logits (= full softmax renormalised).  Lane 0
+// writes ids[0..k) and w[0..k).
+constexpr int kTopkPer = kMaxExperts / 32;
+
+MOE_DEV void warp_topk(const float (&v)[kTopkPer], int E, int k, int lane, int32_t* ids,
+                       float* w) {
+  unsigned taken = 0;
+  float sel_v[kMaxTopK];
+  int sel_e[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j >= k) break;
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kTopkPer; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !(taken & (1u << i)) && (v[i] > bv || (v[i] == bv && e < be))) {
+        bv = v[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    sel_v[j] = bv;
+    sel_e[j] = be;
+  }
+  if (lane == 0) {
+    const float m = sel_v[0];
+    float p[kMaxTopK];
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j >= k) break;
+      p[j] = expf(sel_v[j] - m);
+      s += p[j];
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j >= k) break;
+      ids[j] = sel_e[j];
+      w[j] = p[j] / s;
+    }
+  }
+}
 
 // Host: programmatic dependent launch is used unless the environment sets
 // MOE_PDL=0 or the calling thread is inside a PdlOff scope with off = true.

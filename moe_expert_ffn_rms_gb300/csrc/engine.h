@@ -36,6 +36,44 @@ cudaError_t launch_decode_ffn_fused(bool fp8, const void* xp, const float* xp_sc
                                     int H, int I, int R_max, int T, int sms, int* status,
                                     cudaStream_t st);
 
+// The whole decode forward in one cooperative launch (one CTA per SM):
+// rms_norm, routing, permute and row gather, the fused FC1 + FC2, the combine,
+// separated by grid barriers.  bf16 tensors are passed as void pointers.
+struct DecodeForward {
+  const void* x;          // bf16 [T, H]
+  const void* norm_w;     // bf16 [H]
+  float eps;
+  int T, H, k;
+  const float* logits;    // router logits [T, E], or NULL
+  const float* router_w;  // [H, E], or NULL (used when logits is NULL)
+  const float* bias;      // [E] or NULL
+  const int32_t* ids_in;  // caller routing [T, k] and weights, or NULL
+  const float* tw_in;
+  void* xhat;             // bf16 [T, H]
+  uint8_t* xq;            // E4M3 path: quantised x_hat [T, H] and scales [T]
+  float* xscale;
+  int32_t* ids;           // routing outputs (used when ids_in is NULL)
+  float* tw;
+  int32_t* offsets;       // [E + 1]
+  int32_t* row_src;       // [T k]
+  int32_t* row_of_pair;   // [T k]
+  void* xp;               // gathered rows [T k, H] (bf16, or E4M3 with xp_scale)
+  float* xp_scale;
+  void* y;                // FC2 rows bf16 [T k, H], (token, slot) order
+  void* out;              // bf16 [T, H]
+  int* bar;               // grid barrier words (2 ints), zeroed by the launcher
+};
+
+// Whether the one-launch forward is enabled (MOE_MEGA=1) and covers the
+// batch and router (host check).
+bool decode_forward_mega_covers(int T, int H, int E, int k, bool logits, bool routed);
+
+cudaError_t launch_decode_forward_mega(bool fp8, const DecodeForward& f, const void* w13,
+                                       const float* w13_scale, const void* w2,
+                                       const float* w2_scale, void* act, uint8_t* actq,
+                                       float* act_scale, int* sched, int E, int I, int sms,
+                                       int* status, cudaStream_t st);
+
 // Bounded-wait self-test: a kernel that waits on an mbarrier nothing arrives
 // on for at most limit_cycles SM cycles and records MOE_ERR_TIMEOUT.
 cudaError_t launch_wait_selftest(long long limit_cycles, int* status, cudaStream_t st);

@@ -97,6 +97,9 @@ struct Unit {
   int job, e, nt, row0, rows;
 };
 
+// The whole decode forward in one launch: the arguments (engine.h).
+using MegaP = DecodeForward;
+
 constexpr int kUnitRing = 4;  // claimed-unit slots between the roles
 
 // Unit u of a job: expert e has ceil(cnt/chunk) token chunks, each with nt N
@@ -351,6 +354,265 @@ MOE_DEV void drain_armed(uint64_t* full_bar, int stages, uint32_t armed, uint32_
   }
 }
 
+// ------------------------------------------ whole decode forward phases --
+// Grid-wide barrier of a cooperative launch.  bar[0] counts arrivals, bar[1]
+// is the generation; `gen` (thread 0) is the generation this CTA waits past.
+// The CTA's writes before the barrier are visible to every CTA after it.
+// Bounded: a wait that runs out records MOE_ERR_TIMEOUT and returns false.
+MOE_DEV bool grid_sync(int* bar, unsigned& gen, int* status, volatile int* s_ok) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool ok = true;
+    __threadfence();
+    const int g = (int)gen;
+    if (atomicAdd(&bar[0], 1) == (int)gridDim.x - 1) {
+      atomicExch(&bar[0], 0);
+      __threadfence();
+      atomicExch(&bar[1], g + 1);
+    } else {
+      const long long t0 = clock64();
+      while (ld_acquire(&bar[1]) == g) {
+        if (clock64() - t0 > kSpinLimitCycles) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    if (!ok) flag_status(status, MOE_ERR_TIMEOUT);
+    gen = (unsigned)(g + 1);
+    *s_ok = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
+// rms_norm, one CTA per token row (the arithmetic of rmsnorm_kernel); on the
+// E4M3 path also the per-token quantisation s = absmax / 448, q = e4m3(y / s).
+template <bool FP8>
+MOE_DEV void mega_rmsnorm(const MegaP& mp, float* red) {
+  const int H = mp.H, nv = H >> 3;
+  const uint4* wr = reinterpret_cast<const uint4*>(mp.norm_w);
+  for (int t = blockIdx.x; t < mp.T; t += gridDim.x) {
+    const uint4* xr = reinterpret_cast<const uint4*>(static_cast<const bf16*>(mp.x) + (size_t)t * H);
+    uint4* yr = reinterpret_cast<uint4*>(static_cast<bf16*>(mp.xhat) + (size_t)t * H);
+    float ss = 0.f;
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      float f[8];
+      unpack8_bf16(xr[v], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+    }
+    ss = block_sum(ss, red);
+    const float r = 1.0f / sqrtf(ss / (float)H + mp.eps);
+    float amax = 0.f;
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      float f[8], g[8];
+      unpack8_bf16(xr[v], f);
+      unpack8_bf16(wr[v], g);
+      uint4 o;
+      o.x = pack2_bf16((f[0] * r) * g[0], (f[1] * r) * g[1]);
+      o.y = pack2_bf16((f[2] * r) * g[2], (f[3] * r) * g[3]);
+      o.z = pack2_bf16((f[4] * r) * g[4], (f[5] * r) * g[5]);
+      o.w = pack2_bf16((f[6] * r) * g[6], (f[7] * r) * g[7]);
+      yr[v] = o;
+      if (FP8) {
+        float h[8];
+        unpack8_bf16(o, h);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
+      }
+    }
+    if (FP8) {
+      amax = block_max(amax, red);
+      const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      uint2* qr = reinterpret_cast<uint2*>(mp.xq + (size_t)t * H);
+      for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+        float h[8];
+        unpack8_bf16(yr[v], h);  // this thread wrote yr[v] above
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lo |= (uint32_t)f_to_e4m3(__fdiv_rn(h[i], s)) << (8 * i);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hi |= (uint32_t)f_to_e4m3(__fdiv_rn(h[4 + i], s)) << (8 * i);
+        qr[v] = make_uint2(lo, hi);
+      }
+      if (threadIdx.x == 0) mp.xscale[t] = s;
+    }
+  }
+}
+
+// Routing: from given logits, one warp per token; or a small router (E <=
+// blockDim), one CTA per token: thread (g, e) sums the rows h = g, g + G, ...
+// of W_r (G = blockDim / E), the G partial sums are added in g order.  Then
+// the shared warp top-k.  `scratch` holds H + blockDim + E floats.
+MOE_DEV void mega_route(const MegaP& mp, int E, float* scratch) {
+  if (mp.ids_in) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int T = mp.T, k = mp.k;
+  if (mp.logits) {
+    for (int t = blockIdx.x * nw + warp; t < T; t += gridDim.x * nw) {
+      float v[kTopkPer];
+#pragma unroll
+      for (int i = 0; i < kTopkPer; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) {
+          float x = 0.f;
+          x += mp.logits[(size_t)t * E + e];
+          if (mp.bias) x += mp.bias[e];
+          v[i] = x;
+        } else {
+          v[i] = -FLT_MAX;
+        }
+      }
+      warp_topk(v, E, k, lane, mp.ids + (size_t)t * k, mp.tw + (size_t)t * k);
+    }
+    return;
+  }
+  const int H = mp.H, tid = threadIdx.x;
+  float* xs = scratch;
+  float* ps = scratch + H;
+  float* lg = ps + blockDim.x;
+  const int G = blockDim.x / E, g = tid / E, e = tid % E;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const uint4* xr = reinterpret_cast<const uint4*>(static_cast<const bf16*>(mp.xhat) + (size_t)t * H);
+    for (int v = tid; v < H / 8; v += blockDim.x) {
+      float f[8];
+      unpack8_bf16(xr[v], f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) xs[v * 8 + q] = f[q];
+    }
+    __syncthreads();
+    float acc = 0.f;
+    if (g < G)
+      for (int h = g; h < H; h += G) acc = fmaf(xs[h], mp.router_w[(size_t)h * E + e], acc);
+    ps[tid] = acc;
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += blockDim.x) {
+      float s = 0.f;
+      for (int gg = 0; gg < G; ++gg) s += ps[gg * E + ee];
+      if (mp.bias) s += mp.bias[ee];
+      lg[ee] = s;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float v[kTopkPer];
+#pragma unroll
+      for (int i = 0; i < kTopkPer; ++i) {
+        const int ex = lane + 32 * i;
+        v[i] = ex < E ? lg[ex] : -FLT_MAX;
+      }
+      warp_topk(v, E, k, lane, mp.ids + (size_t)t * k, mp.tw + (size_t)t * k);
+    }
+    __syncthreads();
+  }
+}
+
+// Stable counting sort of the T k pairs by expert, in CTA 0: counts with
+// shared atomics, an exclusive scan, then warp 0 walks the pairs in order in
+// batches of 32 and ranks equal experts inside a batch with __match_any_sync.
+// `cnt` holds E + 1 ints.  Pairs with an expert outside [0, E) are dropped
+// (row_of_pair = -1) and flagged as MOE_ERR_INVALID_ARG.
+MOE_DEV void mega_permute(const MegaP& mp, int E, int* cnt, int* status) {
+  if (blockIdx.x != 0) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = mp.T * mp.k;
+  const int32_t* ids = mp.ids_in ? mp.ids_in : mp.ids;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int q = threadIdx.x; q < R; q += blockDim.x) {
+    const int e = ids[q];
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    else bad = true;
+  }
+  if (bad) flag_status(status, MOE_ERR_INVALID_ARG);
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int v = (e < E) ? cnt[e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e < E) {
+        cnt[e] = carry + incl - v;
+        mp.offsets[e] = carry + incl - v;
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) mp.offsets[E] = carry;
+    __syncwarp();
+    const unsigned below = (1u << lane) - 1u;
+    for (int pb = 0; pb < R; pb += 32) {
+      const int q = pb + lane;
+      const bool valid = q < R;
+      const int e = valid ? ids[q] : -1;
+      const bool ok = valid && e >= 0 && e < E;
+      const unsigned grp = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
+      if (ok) {
+        const int r = cnt[e] + __popc(grp & below);
+        mp.row_src[r] = q;
+        mp.row_of_pair[q] = r;
+      } else if (valid) {
+        mp.row_of_pair[q] = -1;
+      }
+      __syncwarp();
+      if (ok && (grp & below) == 0) cnt[e] += __popc(grp);
+      __syncwarp();
+    }
+  }
+}
+
+// Row gather xp[r] = x_hat[row_src[r] / k] (E4M3 rows and scales on the FP8
+// path), one warp per row, then an async-proxy fence for the TMA readers.
+template <bool FP8>
+MOE_DEV void mega_gather(const MegaP& mp, int E) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int R = min(mp.offsets[E], mp.T * mp.k);
+  const int row_vec = mp.H * (FP8 ? 1 : 2) / 16;
+  const uint4* src = reinterpret_cast<const uint4*>(FP8 ? (const void*)mp.xq : (const void*)mp.xhat);
+  uint4* dst = reinterpret_cast<uint4*>(mp.xp);
+  for (int r = blockIdx.x * nw + warp; r < R; r += gridDim.x * nw) {
+    const int t = mp.row_src[r] / mp.k;
+    const uint4* s = src + (size_t)t * row_vec;
+    uint4* d = dst + (size_t)r * row_vec;
+    for (int v = lane; v < row_vec; v += 32) d[v] = s[v];
+    if (FP8 && lane == 0) mp.xp_scale[r] = mp.xscale[t];
+  }
+  fence_proxy_async_global();
+}
+
+// out[t, :] = bf16(sum_j y[t k + j, :]) over the pairs kept, fp32 in j order
+// (the arithmetic of the combine kernel for (token, slot)-ordered rows).
+MOE_DEV void mega_combine(const MegaP& mp) {
+  const int H = mp.H, k = mp.k, g8 = H >> 3;
+  const int64_t total = (int64_t)mp.T * g8;
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = it / g8, g = it % g8;
+    float s[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      if (mp.row_of_pair[t * k + j] < 0) continue;
+      float f[8];
+      unpack8_bf16(reinterpret_cast<const uint4*>(static_cast<const bf16*>(mp.y) + (t * k + j) * H)[g], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s[i] += f[i];
+    }
+    uint4 o;
+    o.x = pack2_bf16(s[0], s[1]);
+    o.y = pack2_bf16(s[2], s[3]);
+    o.z = pack2_bf16(s[4], s[5]);
+    o.w = pack2_bf16(s[6], s[7]);
+    reinterpret_cast<uint4*>(mp.out)[it] = o;
+  }
+}
+
 // Persistent grouped GEMM.  One launch runs job 0 (mode M0) and, when M1 >= 0,
 // job 1 (mode M1) after it: units of job 0 come first in the unit order.
 // Static schedule (p.sched == NULL): CTA c takes units c, c + grid, ...
@@ -359,11 +621,14 @@ MOE_DEV void drain_armed(uint64_t* full_bar, int stages, uint32_t armed, uint32_
 // epilogue (p.sched[1 + e]), so job 1 may read job 0's output with TMA.  Since
 // job-0 units are all claimed before any job-1 unit and a producer issues all
 // loads of a unit before it claims the next, every wait ends.
-template <bool SWAP, bool FP8, int M0, int M1>
+// MEGA: the whole decode forward in this launch (cooperative, one CTA per SM):
+// rms_norm, routing, permute and row gather before the FFN, the combine after
+// it, each phase separated by a grid barrier (MegaP).
+template <bool SWAP, bool FP8, int M0, int M1, bool MEGA = false>
 __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
     const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_x0,
     const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_x1,
-    const Params p) {
+    const Params p, const MegaP mp) {
   constexpr int NJ = (M1 >= 0) ? 2 : 1;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ int s_off[kMaxExperts + 1];
@@ -381,6 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ float s_xch[SWAP && (M0 == 1 || M1 == 1) ? 64 * 17 : 1];  // decode FC1: up values
+  __shared__ volatile int s_gok;  // MEGA: grid barrier result
+  unsigned mega_gen = 0;          // MEGA: grid barrier generation (thread 0)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = reinterpret_cast<uint8_t*>(
@@ -417,6 +684,18 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
   }
   pdl_trigger();
   pdl_wait();
+  if constexpr (MEGA) {
+    // the forward's steps before the FFN; s_up and the ring are scratch here
+    mega_rmsnorm<FP8>(mp, reinterpret_cast<float*>(&s_up[0][0]));
+    grid_sync(mp.bar, mega_gen, p.status, &s_gok);
+    mega_route(mp, p.E, reinterpret_cast<float*>(ring));
+    grid_sync(mp.bar, mega_gen, p.status, &s_gok);
+    mega_permute(mp, p.E, s_off, p.status);
+    grid_sync(mp.bar, mega_gen, p.status, &s_gok);
+    mega_gather<FP8>(mp, p.E);
+    grid_sync(mp.bar, mega_gen, p.status, &s_gok);
+    fence_proxy_async_global();  // gathered rows are read by TMA below
+  }
   for (int e = threadIdx.x; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
   __syncthreads();
   if (threadIdx.x == 0) {  // offsets must be monotone within [0, R_max]
@@ -700,6 +979,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
     }
   }
 
+  if constexpr (MEGA) {
+    grid_sync(mp.bar, mega_gen, p.status, &s_gok);  // every FC2 row is written
+    mega_combine(mp);
+  }
+
   // ---- teardown: every role is done; release TMEM
   tc_fence_before();
   __syncthreads();
@@ -960,7 +1244,7 @@ cudaError_t launch_k(const CUtensorMap* maps, const Params& p, int grid, size_t 
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(k, dim3(grid), dim3(kThreads), smem, st, maps[0], maps[1], maps[2], maps[3],
-                       p);
+                       p, MegaP{});
 }
 
 template <bool SWAP, bool FP8>
@@ -1195,6 +1479,80 @@ cudaError_t launch_decode_ffn_fused(bool fp8, const void* xp, const float* xp_sc
   if (!set_ring(&p, true, T, &smem)) return cudaErrorNotSupported;
   return fp8 ? launch_k<true, true, 1, 3>(maps, p, sms, smem, st)
              : launch_k<true, false, 1, 3>(maps, p, sms, smem, st);
+}
+
+// Opt-in (MOE_MEGA=1): on GB300 the separate launches with programmatic
+// dependent launch are faster for the decode workloads measured (a grid
+// barrier costs about as much as a programmatic launch boundary, and the
+// cooperative launch cannot overlap the previous kernel's tail).
+bool decode_forward_mega_covers(int T, int H, int E, int k, bool logits, bool routed) {
+  const char* env = getenv("MOE_MEGA");
+  if (!(env && env[0] == '1')) return false;
+  if (T < 1 || T > 64 || T * k > 512 || E > kMaxExperts) return false;
+  if (logits || routed) return true;
+  // small router: one CTA per token, W_r rows read by consecutive threads
+  return H <= 8192 && (int64_t)H * E <= 65536 && E <= kThreads;
+}
+
+cudaError_t launch_decode_forward_mega(bool fp8, const DecodeForward& f, const void* w13,
+                                       const float* w13_scale, const void* w2,
+                                       const float* w2_scale, void* act, uint8_t* actq,
+                                       float* act_scale, int* sched, int E, int I, int sms,
+                                       int* status, cudaStream_t st) {
+  std::call_once(g_encode_once, load_encode);
+  const int T = f.T, H = f.H, R_max = T * f.k;
+  if (!g_encode || !sched || !f.bar || I % 8 != 0 || R_max == 0 ||
+      !decode_forward_mega_covers(T, H, E, f.k, f.logits != nullptr, f.ids_in != nullptr))
+    return cudaErrorNotSupported;
+  if (fp8 && (!actq || !act_scale || ((uintptr_t)actq & 15u))) return cudaErrorNotSupported;
+  Params p{};
+  p.offsets = f.offsets;
+  p.E = E;
+  p.I = I;
+  p.R_max = R_max;
+  p.njobs = 2;
+  p.sched = sched;
+  p.status = status;
+  p.actq = actq;
+  p.act_scale = act_scale;
+  const float* topk_w = f.ids_in ? f.tw_in : f.tw;
+  CUtensorMap maps[4];
+  if (!make_job(&p.job[0], &maps[0], &maps[1], 1, fp8, true, f.xp, f.xp_scale, w13, w13_scale,
+                f.row_src, nullptr, act, E, H, I, I, R_max) ||
+      !make_job(&p.job[1], &maps[2], &maps[3], 3, fp8, true, fp8 ? (const void*)actq : act,
+                act_scale, w2, w2_scale, f.row_src, topk_w, f.y, E, I, I, H, R_max))
+    return cudaErrorNotSupported;
+  size_t smem = 0;
+  if (!set_ring(&p, true, T, &smem)) return cudaErrorNotSupported;
+  auto k = fp8 ? moe_tc_gemm_kernel<true, true, 1, 3, true>
+               : moe_tc_gemm_kernel<true, false, 1, 3, true>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  // every CTA must be resident (grid barriers): one per SM
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorNotSupported;
+  // scheduler counters and grid barrier words start at zero
+  if (f.bar == sched + 2 * E + 1) {
+    e = cudaMemsetAsync(sched, 0, (size_t)(2 * E + 3) * sizeof(int), st);
+  } else {
+    e = cudaMemsetAsync(sched, 0, (size_t)(2 * E + 1) * sizeof(int), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(f.bar, 0, 2 * sizeof(int), st);
+  }
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], p, f);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace moe

@@ -41,16 +41,22 @@ SMALL = {
 }
 
 ENGINES = ["auto", "decode", "prefill", "simt"]
-# decode: FC1 and FC2 fused in one persistent launch; decode_unfused: two launches
-FWD_ENGINES = ENGINES + ["decode_unfused"]
+# decode: FC1 and FC2 fused in one persistent launch; decode_mega: the whole
+# forward in one cooperative launch where it is covered (MOE_MEGA=1);
+# decode_unfused: FC1 and FC2 in two launches
+FWD_ENGINES = ENGINES + ["decode_mega", "decode_unfused"]
+ENV_SWITCHES = ("MOE_FORCE_SIMT", "MOE_FUSE", "MOE_ROUTER_TC", "MOE_MEGA")
 
 
 def _set_engine(shape_obj, engine, M):
-    os.environ.pop("MOE_FORCE_SIMT", None)
-    os.environ.pop("MOE_FUSE", None)
+    for v in ENV_SWITCHES:
+        os.environ.pop(v, None)
     if engine == "simt":
         os.environ["MOE_FORCE_SIMT"] = "1"
         return M.ENGINE_AUTO
+    if engine == "decode_mega":
+        os.environ["MOE_MEGA"] = "1"
+        return M.ENGINE_DECODE
     if engine == "decode_unfused":
         os.environ["MOE_FUSE"] = "0"
         return M.ENGINE_DECODE
@@ -60,7 +66,7 @@ def _set_engine(shape_obj, engine, M):
 @pytest.fixture(autouse=True)
 def _clear_env():
     yield
-    for v in ("MOE_FORCE_SIMT", "MOE_FUSE", "MOE_ROUTER_TC"):
+    for v in ENV_SWITCHES:
         os.environ.pop(v, None)
 
 
@@ -517,14 +523,29 @@ def test_forward_fp8_small(M):
 def test_forward_reference_workloads(M, cfg, sample):
     inp = workloads.make_inputs(cfg, DEV)
     m, ndiff = check_forward(M, inp, sample=sample)
+    if cfg in ("c1_tiny", "c2_decode_balanced", "c4_decode_fp8"):
+        # the same workload in one cooperative launch
+        os.environ["MOE_MEGA"] = "1"
+        check_forward(M, inp, sample=sample)
+        os.environ.pop("MOE_MEGA", None)
     if cfg in ("c2_decode_balanced", "c3_decode_skewed", "c4_decode_fp8"):
-        # the fused and the separate-launch decode paths give identical bits
+        # the fused and the two-launch FFN give identical bits
         fp8w = quantize_weights_gpu(M, inp) if inp["fp8"] else None
         o1, i1, _ = _run_forward(M, inp, fp8_weights=fp8w)
         os.environ["MOE_FUSE"] = "0"
         o2, i2, _ = _run_forward(M, inp, fp8_weights=fp8w)
         os.environ.pop("MOE_FUSE", None)
         assert torch.equal(i1, i2) and torch.equal(o1, o2)
+        if cfg != "c3_decode_skewed":
+            # one-launch forward: the routing (given logits) is the same, the
+            # outputs agree to a few bf16 ulps (x_hat's sum of squares is
+            # reduced in another order)
+            os.environ["MOE_MEGA"] = "1"
+            o3, i3, _ = _run_forward(M, inp, fp8_weights=fp8w)
+            os.environ.pop("MOE_MEGA", None)
+            assert torch.equal(i1, i3)
+            d = (o3.float() - o1.float()).abs() / o1.float().abs().clamp(min=1.0)
+            assert d.max().item() <= (6e-2 if inp["fp8"] else 2e-2)
     print(f"{cfg}: max scaled error {m:.3e}, near-tie routing differences {ndiff}")
     del inp
     torch.cuda.empty_cache()
@@ -563,6 +584,36 @@ def test_forward_all_tokens_one_expert_and_empty_experts(M):
     ref = O.ffn_token_outputs(xhat, ids.cpu().numpy(), np.ones((T, k)), lambda e: f64(inp["w13"][e]),
                               lambda e: f64(inp["w2"][e]), I)
     assert_close(f64(out), ref, TOL_BF16, "one expert")
+
+
+def test_forward_routed_invalid_ids_dropped(M):
+    """Caller routing with an expert id outside [0, E): the pair is dropped
+    and MOE_ERR_INVALID_ARG recorded, in the one-launch forward and in the
+    separate launches alike."""
+    T, H, E, k, I = 6, 256, 8, 2, 128
+    inp = workloads.make_inputs("c1_tiny", DEV, shape=workloads.Shape(T, H, E, k, I), seed=11)
+    ids = torch.tensor([[0, 1], [2, 9], [3, 4], [-1, 5], [6, 7], [1, 2]], dtype=torch.int32, device=DEV)
+    tw = torch.full((T, k), 0.5, dtype=torch.float32, device=DEV)
+    shape = M.make_shape(T, H, E, I, k)
+    ws = M.alloc_workspace(M.moe_ffn_workspace_size(shape), DEV)
+    outs = []
+    for mega in ("1", "0"):
+        os.environ["MOE_MEGA"] = mega
+        M.device_status(clear=True)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+        M.moe_ffn_forward_routed(shape, inp["x"], inp["norm_w"], ids, tw, inp["w13"], inp["w2"], out, ws)
+        torch.cuda.synchronize()
+        assert M.device_status(clear=True) == 1      # MOE_ERR_INVALID_ARG
+        outs.append(f64(out))
+    os.environ.pop("MOE_MEGA", None)
+    xhat = O.rms_norm(f64(inp["x"]), f64(inp["norm_w"]), 1e-6)
+    idn = ids.cpu().numpy()
+    wn = np.where((idn >= 0) & (idn < E), 0.5, 0.0)
+    ids_ok = np.where((idn >= 0) & (idn < E), idn, 0)
+    ref = O.ffn_token_outputs(xhat, ids_ok, wn, lambda e: f64(inp["w13"][e]),
+                              lambda e: f64(inp["w2"][e]), I)
+    for o in outs:
+        assert_close(o, ref, TOL_BF16, "invalid ids dropped")
 
 
 def test_forward_zero_tokens(M):
