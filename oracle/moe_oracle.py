@@ -26,8 +26,10 @@ FFN formula or the FP8 scale recipe; where they are silent the plain standard
 reading is used and named at each function.
 
 Parity status: every function below is pinned by tests in
-tests/test_oracle_pins.py (closed forms, invariants, brute force, library
-special cases).
+tests/test_oracle_pins.py and tests/test_golden.py (closed forms, invariants,
+brute force, library special cases, hand-derived format tables).  NVFP4
+(E2M1 elements, E4M3 block scales) follows the public format definition; the
+pages name the format without defining it.
 """
 from __future__ import annotations
 
@@ -41,6 +43,8 @@ F64 = np.float64
 
 BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
 E4M3_MAX = 448.0
+E2M1_MAX = 6.0
+NVFP4_BLOCK = 16
 
 
 def bf16_round(a) -> np.ndarray:
@@ -81,6 +85,32 @@ def e4m3_decode(code: int) -> float:
     return s * (1.0 + m / 8.0) * 2.0 ** (ex - 7)
 
 
+def e2m1_round(a) -> np.ndarray:
+    """Round float64 values to FP4 E2M1, nearest-even, saturating to +-6.
+
+    E2M1: 2 exponent bits (bias 1), 1 mantissa bit, no infinity or NaN:
+    magnitudes 0, 0.5 (subnormal), 1, 1.5, 2, 3, 4, 6.  With a = m*2^e,
+    0.5 <= |m| < 1, a normal value (e >= 1) has quantum 2^(e-2); below 1 the
+    subnormal quantum is 0.5.  Ties go to the even mantissa (np.rint), and
+    values beyond +-6 saturate to +-6."""
+    a = np.asarray(a, dtype=F64)
+    _, e = np.frexp(a)
+    q = np.where(e >= 1, e - 2, -1)
+    r = np.ldexp(np.rint(np.ldexp(a, -q)), q)
+    return np.clip(r, -E2M1_MAX, E2M1_MAX)
+
+
+def e2m1_decode(code: int) -> float:
+    """Value of one E2M1 nibble, from the format layout (sign, 2-bit exponent
+    with bias 1, 1-bit mantissa; exponent 0 is subnormal)."""
+    s = -1.0 if code & 0x8 else 1.0
+    ex = (code >> 1) & 0x3
+    m = code & 0x1
+    if ex == 0:
+        return s * m * 0.5
+    return s * (1.0 + m / 2.0) * 2.0 ** (ex - 1)
+
+
 def f32(a) -> np.ndarray:
     """Round to IEEE fp32 (used only where fp32 decides an integer code)."""
     return np.asarray(a, dtype=np.float32)
@@ -99,6 +129,43 @@ def quantize_rows_e4m3(v: np.ndarray):
     ratio = (f32(v) / s[..., None]).astype(F64)          # correctly rounded fp32 divide
     q = e4m3_round(ratio)
     return q, s.astype(F64)
+
+
+def quantize_nvfp4(w: np.ndarray):
+    """NVFP4 quantisation of a weight matrix [N, K] along K.
+
+    [SM] 4.4 and the support table name NVFP4 expert weights for Blackwell
+    MoE but do not define the format.  Reading: the public NVFP4 layout,
+    E2M1 elements in blocks of 16 consecutive K elements, one E4M3 scale per
+    block and one fp32 scale per matrix:
+        s_g = amax|W| / (448 * 6)                (1 for an all-zero matrix)
+        s_b = e4m3( amax_block / (6 * s_g) )
+        q   = e2m1( w / (s_b * s_g) )            (0 where s_b = 0)
+    so that w ~ q * s_b * s_g.  The codes are decided in fp32, the precision
+    the GPU decides them in: s_g, 6 * s_g, each block ratio, each product
+    s_b * s_g and each element quotient are rounded to fp32.
+    Returns (q float64 holding E2M1 values [N, K], s_b float64 holding E4M3
+    values [N, K/16], s_g a float holding an fp32 value)."""
+    w = np.asarray(w, dtype=F64)
+    n, kdim = w.shape
+    assert kdim % NVFP4_BLOCK == 0
+    amax = f32(np.max(np.abs(w))) if w.size else np.float32(0.0)
+    sg = np.float32(amax / np.float32(E4M3_MAX * E2M1_MAX)) if amax > 0 else np.float32(1.0)
+    six_sg = np.float32(np.float32(E2M1_MAX) * sg)
+    wb = f32(w).reshape(n, kdim // NVFP4_BLOCK, NVFP4_BLOCK)
+    amax_b = np.max(np.abs(wb), axis=-1)
+    sb = e4m3_round((amax_b / six_sg).astype(np.float32).astype(F64))
+    scale = (sb.astype(np.float32) * sg).astype(np.float32)          # fp32 product
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = (wb / scale[..., None]).astype(np.float32).astype(F64)
+    q = np.where(scale[..., None] > 0, e2m1_round(ratio), 0.0)
+    return q.reshape(n, kdim), sb, float(sg)
+
+
+def dequantize_nvfp4(q, sb, sg) -> np.ndarray:
+    """w = q * s_b * s_g (exact in fp64: at most 5 significant bits times an fp32)."""
+    q = np.asarray(q, dtype=F64)
+    return q * np.repeat(np.asarray(sb, dtype=F64), NVFP4_BLOCK, axis=-1) * float(sg)
 
 
 # ---------------------------------------------------------------------------
@@ -339,7 +406,9 @@ def ffn_token_outputs(xhat_rows, ids, topk_w, w13_of, w2_of, I, cols=None, fp8=F
     Used for sampled checks at full size: it needs only the experts the
     sampled tokens use.  Work is grouped by expert so each expert's weights
     are converted once.  For fp8=True, ``wq13_of``/``wq2_of`` return
-    (codes, scales) of the quantised expert weights."""
+    (codes, scales) of the quantised expert weights.  NVFP4 weights with bf16
+    activations are the bf16 path on the dequantised weights: pass
+    ``w13_of``/``w2_of`` returning dequantize_nvfp4(...)."""
     xhat_rows = np.asarray(xhat_rows, dtype=F64)
     ids = np.asarray(ids)
     topk_w = np.asarray(topk_w, dtype=F64)

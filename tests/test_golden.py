@@ -25,6 +25,15 @@ def test_e4m3_codes_golden():
             assert O.e4m3_round(float(val)) == float(val)
 
 
+def test_e2m1_codes_and_rounding_golden():
+    for kind, a, b in [r[:3] for r in _rows("e2m1_cases.txt")]:
+        if kind == "code":
+            got = O.e2m1_decode(int(a, 16))
+            assert got == float(b) and math.copysign(1, got) == math.copysign(1, float(b)), (a, b)
+        else:
+            assert O.e2m1_round(float(a)) == float(b), (a, b)
+
+
 def test_bf16_cases_golden():
     for inp, out in _rows("bf16_rne_cases.txt"):
         assert O.bf16_round(float(inp)) == float(out), (inp, out)

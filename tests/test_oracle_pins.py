@@ -105,6 +105,94 @@ def test_quantize_rows_matches_torch_recipe_and_zero_row():
     assert np.all(np.abs(q[np.arange(37) != 5]).max(axis=1) == 448.0)
 
 
+E2M1_GRID = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _e2m1_brute(x):
+    """Nearest of the 15 E2M1 values by exhaustive search; on an exact tie
+    the value whose code has mantissa bit 0 (1.0, 2.0, 4.0 or 0); beyond 6
+    the largest magnitude."""
+    mags = E2M1_GRID
+    a = abs(x)
+    if a >= 6.0:
+        return math.copysign(6.0, x)
+    best = min(mags, key=lambda m: (abs(a - m), 0 if mags.index(m) % 2 == 0 else 1))
+    return math.copysign(best, x) if best != 0 else 0.0
+
+
+def test_e2m1_rounding_brute_force():
+    rng = np.random.default_rng(21)
+    xs = np.concatenate([rng.uniform(-8, 8, 4000),
+                         [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -5.0, 6.0, -6.0]])
+    got = O.e2m1_round(xs)
+    for x, g in zip(xs, got):
+        assert g == _e2m1_brute(x) or (g == 0 and _e2m1_brute(x) == 0), (x, g)
+    # every code value round-trips
+    vals = np.array([O.e2m1_decode(c) for c in range(16)])
+    np.testing.assert_array_equal(O.e2m1_round(vals), vals)
+
+
+def test_nvfp4_constructed_weights_round_trip():
+    """Weights built as q * s_b * s_g with a +-6 in every block are recovered
+    exactly: the block ratio amax_b / (6 s_g) is s_b itself and every element
+    quotient is its code."""
+    rng = np.random.default_rng(22)
+    n, kdim = 12, 64
+    sg = 2.0 ** -12
+    grid = np.array(E2M1_GRID[1:] + [-v for v in E2M1_GRID[1:]])
+    q = rng.choice(grid, (n, kdim))
+    q = q.reshape(n, kdim // 16, 16)
+    q[:, :, 3] = 6.0                                  # the block maximum
+    e4m3_vals = np.array([O.e4m3_decode(c) for c in range(0x08, 0x7F)])  # positive normals
+    sb = rng.choice(e4m3_vals, (n, kdim // 16))
+    sb[0, 0] = 448.0                                  # the matrix maximum: 6 * 448 * s_g
+    w = (q * sb[..., None] * sg).reshape(n, kdim)
+    q2, sb2, sg2 = O.quantize_nvfp4(w)
+    assert sg2 == sg
+    np.testing.assert_array_equal(sb2, sb)
+    np.testing.assert_array_equal(q2, q.reshape(n, kdim))
+    np.testing.assert_array_equal(O.dequantize_nvfp4(q2, sb2, sg2), w)
+
+
+def test_nvfp4_recipe_closed_forms_and_nearest_codes():
+    rng = np.random.default_rng(23)
+    w = (rng.standard_normal((9, 96)) * 0.02).astype(np.float32).astype(np.float64)
+    w[4, 16:32] = 0.0                                 # an all-zero block
+    q, sb, sg = O.quantize_nvfp4(w)
+    amax = np.abs(w).max()
+    assert sg == float(np.float32(np.float32(amax) / np.float32(2688.0)))
+    i, j = np.unravel_index(np.argmax(np.abs(w)), w.shape)
+    assert sb[i, j // 16] == 448.0 and abs(q[i, j]) == 6.0   # amax maps to 6 * 448 * s_g
+    assert np.all(sb[4, 1] == 0) and np.all(q[4, 16:32] == 0)
+    # each code is the E2M1 value nearest the fp32 quotient w / (s_b s_g)
+    scale = np.repeat((sb.astype(np.float32) * np.float32(sg)).astype(np.float32), 16, axis=1)
+    ok = scale > 0
+    quot = (w.astype(np.float32) / np.where(ok, scale, 1)).astype(np.float32).astype(np.float64)
+    for x, g in zip(quot[ok], q[ok]):
+        assert g == _e2m1_brute(x) or (g == 0 and _e2m1_brute(x) == 0)
+    # block scales: e4m3 of amax_block / (6 s_g), decided in fp32
+    ab = np.abs(w).reshape(9, 6, 16).max(axis=-1).astype(np.float32)
+    six_sg = np.float32(np.float32(6.0) * np.float32(sg))
+    np.testing.assert_array_equal(sb, O.e4m3_round((ab / six_sg).astype(np.float32).astype(np.float64)))
+    # zero matrix
+    qz, sbz, sgz = O.quantize_nvfp4(np.zeros((2, 32)))
+    assert sgz == 1.0 and np.all(sbz == 0) and np.all(qz == 0)
+
+
+def test_nvfp4_dequantised_error_bound():
+    """|w - w_hat| <= half an E2M1 spacing at |w|'s magnitude times the block
+    scale, for blocks whose rounded scale does not clip the block maximum."""
+    rng = np.random.default_rng(24)
+    w = (rng.standard_normal((16, 128)) * 0.05).astype(np.float32).astype(np.float64)
+    q, sb, sg = O.quantize_nvfp4(w)
+    wh = O.dequantize_nvfp4(q, sb, sg)
+    scale = np.repeat(sb * sg, 16, axis=1)
+    r = np.abs(w) / scale
+    spacing = np.where(r < 2, 0.5, np.where(r < 4, 1.0, 2.0))
+    bound = np.where(r <= 6, 0.5 * spacing * scale, np.abs(w) - 6 * scale) * (1 + 1e-6)
+    assert np.all(np.abs(w - wh) <= bound + 1e-30)
+
+
 def test_fp8_gemm_equals_bf16_gemm_on_representable_inputs():
     """With E4M3-representable values and power-of-two scales the W8A8 FC1
     equals the plain FC1 exactly (pins where each scale is applied)."""
