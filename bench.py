@@ -62,9 +62,14 @@ def algorithmic_work(inp, offsets_np):
     E, H, I = inp["E"], inp["H"], inp["I"]
     counts = np.diff(offsets_np)
     active = int((counts > 0).sum())
-    elem = 1 if inp["fp8"] else 2
-    fc1_bytes = active * 2 * I * H * elem + (active * 2 * I * 4 if inp["fp8"] else 0)
-    fc2_bytes = active * H * I * elem + (active * H * 4 if inp["fp8"] else 0)
+    if inp.get("nvfp4"):
+        # E2M1 codes (1/2 B), one E4M3 block scale per 16 (1/16 B), an fp32 matrix scale
+        fc1_bytes = active * (2 * I * H // 2 + 2 * I * H // 16 + 4)
+        fc2_bytes = active * (H * I // 2 + H * I // 16 + 4)
+    else:
+        elem = 1 if inp["fp8"] else 2
+        fc1_bytes = active * 2 * I * H * elem + (active * 2 * I * 4 if inp["fp8"] else 0)
+        fc2_bytes = active * H * I * elem + (active * H * 4 if inp["fp8"] else 0)
     rows = int(counts.sum())
     fc1_flops = 2.0 * rows * H * 2 * I
     fc2_flops = 2.0 * rows * I * H
@@ -137,7 +142,8 @@ def _save_sample(inp, toks, path):
     import torch
     k = inp["k"]
     d = dict(x=inp["x"][toks].float().cpu().numpy(), norm_w=inp["norm_w"].float().cpu().numpy(),
-             eps=np.array(inp["eps"]), k=np.array(k), fp8=np.array(inp["fp8"]))
+             eps=np.array(inp["eps"]), k=np.array(k), fp8=np.array(inp["fp8"]),
+             nvfp4=np.array(bool(inp.get("nvfp4"))))
     if inp["router_logits"] is not None:
         d["logits"] = inp["router_logits"][toks].cpu().numpy()
         l = inp["router_logits"][toks].cpu().numpy()
@@ -181,6 +187,10 @@ if "logits" in d: kw["logits"] = d["logits"].astype(np.float64)
 else:
     kw["router_w"] = d["router_w"].astype(np.float64)
     if "router_bias" in d: kw["router_bias"] = d["router_bias"].astype(np.float64)
+if "nvfp4" in d and bool(d["nvfp4"]):
+    # NVFP4 weights: quantised once, like the GPU path's offline quantisation
+    W13 = {e: O.dequantize_nvfp4(*O.quantize_nvfp4(w)) for e, w in W13.items()}
+    W2 = {e: O.dequantize_nvfp4(*O.quantize_nvfp4(w)) for e, w in W2.items()}
 reps = int(sys.argv[3])
 min_seconds = float(sys.argv[4])
 t0 = time.perf_counter()
@@ -307,8 +317,9 @@ def main_native(args):
     M.check_device()
     inp = workloads.make_inputs(args.workload, dev)
     T, H, E, k, I, fp8 = inp["T"], inp["H"], inp["E"], inp["k"], inp["I"], inp["fp8"]
+    nvfp4 = bool(inp.get("nvfp4"))
     R = T * k
-    shape = M.make_shape(T, H, E, I, k, inp["eps"], fp8=fp8)
+    shape = M.make_shape(T, H, E, I, k, inp["eps"], fp8=fp8, nvfp4=nvfp4)
     ws = M.alloc_workspace(M.moe_ffn_workspace_size(shape), dev)
     w13, w2, s13, s2 = inp["w13"], inp["w2"], None, None
     if fp8:
@@ -318,18 +329,40 @@ def main_native(args):
         s2 = torch.empty((E, H), dtype=torch.float32, device=dev)
         M.moe_quantize_fp8_rows(inp["w13"], w13, s13)
         M.moe_quantize_fp8_rows(inp["w2"], w2, s2)
+    nv = None
+    if nvfp4:
+        # NVFP4 codes [E, N, K/2], E4M3 block scales [E, N, K/16], fp32 matrix scales [E]
+        nv = []
+        for w in (inp["w13"], inp["w2"]):
+            n_, k_ = w.shape[1], w.shape[2]
+            q = torch.empty((E, n_, k_ // 2), dtype=torch.uint8, device=dev)
+            sbq = torch.empty((E, n_, k_ // 16), dtype=torch.uint8, device=dev)
+            sgq = torch.empty((E,), dtype=torch.float32, device=dev)
+            M.moe_quantize_nvfp4(w, q, sbq, sgq)
+            nv.append((q, sbq, sgq))
+        torch.cuda.synchronize()
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     ids = torch.empty((T, k), dtype=torch.int32, device=dev)
     tw = torch.empty((T, k), dtype=torch.float32, device=dev)
     st = torch.cuda.current_stream()
-    small = (3 * H * I * (1 if fp8 else 2) * E) < 256 * 2 ** 20
+    wbytes = 3 * H * I * E * (0.5625 if nvfp4 else (1 if fp8 else 2))
+    small = wbytes < 256 * 2 ** 20
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if small else None
 
-    def fwd(x=None, out_=None):
-        M.moe_ffn_forward(shape, inp["x"] if x is None else x, inp["norm_w"], w13, w2,
-                          out if out_ is None else out_, ws, router_w=inp["router_w"],
-                          router_logits=inp["router_logits"], router_bias=inp["router_bias"],
-                          w13_scale=s13, w2_scale=s2, topk_ids_out=ids, topk_w_out=tw)
+    def fwd(x=None, out_=None, logits=None):
+        xi = inp["x"] if x is None else x
+        lg = inp["router_logits"] if logits is None else logits
+        o = out if out_ is None else out_
+        if nvfp4:
+            (q13, sb13, sg13), (q2, sb2, sg2) = nv
+            M.moe_ffn_forward_nvfp4(shape, xi, inp["norm_w"], q13, sb13, sg13, q2, sb2, sg2, o, ws,
+                                    router_w=inp["router_w"], router_logits=lg,
+                                    router_bias=inp["router_bias"], topk_ids_out=ids,
+                                    topk_w_out=tw)
+        else:
+            M.moe_ffn_forward(shape, xi, inp["norm_w"], w13, w2, o, ws, router_w=inp["router_w"],
+                              router_logits=lg, router_bias=inp["router_bias"],
+                              w13_scale=s13, w2_scale=s2, topk_ids_out=ids, topk_w_out=tw)
 
     # ---- region A: the product call, device-resident inputs
     for _ in range(args.warmup):
@@ -383,7 +416,9 @@ def main_native(args):
     out_b = torch.empty_like(out)
     # The decode engine with bf16 weights runs FC1 and FC2 in one fused launch:
     # time that launch (moe_grouped_ffn) as one stage; otherwise FC1 and FC2.
-    fused = (T * k / E <= 96.0) and os.environ.get("MOE_FUSE", "1") != "0"
+    fused = nvfp4 or ((T * k / E <= 96.0) and os.environ.get("MOE_FUSE", "1") != "0")
+    xp16 = torch.empty((R, H), dtype=torch.float16, device=dev) if nvfp4 else None
+    act16 = torch.empty((R, I), dtype=torch.float16, device=dev) if nvfp4 else None
     fws = M.alloc_workspace(max(256, M.moe_grouped_ffn_workspace_size(shape)), dev)
     stages = (["rmsnorm", "route", "permute", "ffn", "combine"] if fused else
               ["rmsnorm", "route", "permute", "fc1", "fc2", "combine"])
@@ -401,8 +436,14 @@ def main_native(args):
         mark(2)
         M.moe_permute(ids, T, E, k, offsets, row_src, rop, xhat=xq if fp8 else xhat, xp=xp,
                       row_bytes=H * (1 if fp8 else 2), xscale=xs, xp_scale=xps, workspace=pws)
+        if nvfp4:
+            xp16.copy_(xp)   # fp16 rows for the NVFP4 FFN step (counted in the permute stage)
         mark(3)
-        if fused:
+        if nvfp4:
+            (q13, sb13, sg13), (q2, sb2, sg2) = nv
+            M.moe_grouped_ffn_nvfp4(shape, xp16, q13, sb13, sg13, q2, sb2, sg2, offsets, row_src,
+                                    tw, act16, y, fws)
+        elif fused:
             M.moe_grouped_ffn(shape, xp, w13, w2, offsets, row_src, tw, act, y, fws, xp_scale=xps,
                               w13_scale=s13, w2_scale=s2)
         else:
@@ -435,7 +476,7 @@ def main_native(args):
     stage_ms = {s: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs_all)
                 for i, s in enumerate(stages)}
     offsets_np = offsets.cpu().numpy()
-    work = algorithmic_work(dict(inp, fp8=fp8), offsets_np)
+    work = algorithmic_work(dict(inp, fp8=fp8, nvfp4=nvfp4), offsets_np)
     peaks = load_peaks()
     decode = T <= 64
     if decode and fused:
@@ -482,9 +523,7 @@ def main_native(args):
         x_d.copy_(x_h, non_blocking=True)
         if lg_h is not None:
             lg_d.copy_(lg_h, non_blocking=True)
-        M.moe_ffn_forward(shape, x_d, inp["norm_w"], w13, w2, out, ws, router_w=inp["router_w"],
-                          router_logits=lg_d, router_bias=inp["router_bias"], w13_scale=s13,
-                          w2_scale=s2)
+        fwd(x=x_d, logits=lg_d)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -518,14 +557,16 @@ def main_native(args):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "fp8-e4m3 x fp8-e4m3 -> f32" if fp8 else "bf16 x bf16 -> f32",
+            "dtype": ("fp16 x fp16 -> f32 (NVFP4 weights dequantised exactly, bf16 activations)"
+                      if nvfp4 else "fp8-e4m3 x fp8-e4m3 -> f32" if fp8 else "bf16 x bf16 -> f32"),
             "data": "synthetic (seeded torch generator; random-init weights)",
             "config": {"workload": args.workload, "T": T, "H": H, "E": E, "top_k": k, "I": I,
-                       "fp8": fp8, "routing": inp["routing"],
+                       "fp8": fp8, "weights": "nvfp4" if nvfp4 else ("e4m3" if fp8 else "bf16"),
+                       "routing": inp["routing"],
                        "active_experts": work["active_experts"],
                        "l2": ("flushed between steps (512 MB write)" if flush is not None else
                               f"inputs larger than L2: expert weights "
-                              f"{3 * H * I * E * (1 if fp8 else 2) / 1e9:.2f} GB"),
+                              f"{wbytes / 1e9:.2f} GB"),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roof,
             "stages_ms": stage_ms,

@@ -65,7 +65,10 @@ typedef enum {
   MOE_ERR_TIMEOUT = 6              /* a bounded device-side wait ran out */
 } moe_status;
 
-typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1 } moe_wdtype;
+/* Expert weight format.  MOE_W_NVFP4 weights go through moe_ffn_forward_nvfp4
+ * (packed codes plus two scale arrays); the other entry points take BF16 or
+ * FP8_E4M3. */
+typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1, MOE_W_NVFP4 = 2 } moe_wdtype;
 
 /* Which step of the grouped GEMM moe_grouped_gemm runs. */
 typedef enum {
@@ -192,6 +195,31 @@ moe_status moe_ffn_forward_static_ws(const moe_shape* shape, const void* x, cons
                                      int32_t* topk_ids_out, float* topk_w_out,
                                      moe_stream_t stream);
 
+/* The forward with NVFP4 expert weights and bf16 activations (W4A16).
+ * [SM] section 4.4 and its support table list NVFP4 MoE expert weights for
+ * Blackwell without defining the format; the library uses the public NVFP4
+ * layout: per expert matrix W [N, K] (w13: N = 2I, K = H; w2: N = H, K = I),
+ *   codes  uint8 [E, N, K/2]  E2M1 (1 sign, 2 exponent bits with bias 1,
+ *                             1 mantissa bit), element 2i in the low nibble
+ *   sb     uint8 [E, N, K/16] E4M3 scale of each block of 16 K elements
+ *   sg     fp32  [E]          scale of each expert matrix
+ *   w[n, k] = e2m1(code) * e4m3(sb[n, k/16]) * sg,
+ * as written by moe_quantize_nvfp4.  Everything else (routing, outputs,
+ * workspace from moe_ffn_workspace_size with shape->wdtype = MOE_W_NVFP4) is
+ * as moe_ffn_forward.  Each code times its block scale is exact in fp16 and
+ * bf16 activations are exact in fp16, so the GEMMs are those of the bf16
+ * forward on the dequantised weights, accumulated in fp32; the intermediate
+ * is rounded to bf16 as in the bf16 forward.
+ * Errors: as moe_ffn_forward; UNSUPPORTED_SHAPE unless H and I are
+ * multiples of 256. */
+moe_status moe_ffn_forward_nvfp4(const moe_shape* shape, const void* x, const void* norm_w,
+                                 const float* router_w, const float* router_logits,
+                                 const float* router_bias, const uint8_t* w13, const uint8_t* w13_sb,
+                                 const float* w13_sg, const uint8_t* w2, const uint8_t* w2_sb,
+                                 const float* w2_sg, void* out, int32_t* topk_ids_out,
+                                 float* topk_w_out, void* workspace, size_t workspace_bytes,
+                                 moe_stream_t stream);
+
 /* ------------------------------------------------------------ the steps -- */
 
 /* rms_norm ([V100] "rewrite on torch::stable::Tensor"):
@@ -281,6 +309,20 @@ moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* 
                            const float* topk_w, void* act, void* y, void* workspace,
                            size_t workspace_bytes, moe_stream_t stream);
 
+/* The NVFP4 expert FFN of the grouped rows (the FFN step of
+ * moe_ffn_forward_nvfp4): act = FC1_SILU(xp), y = FC2_BF16(act) with NVFP4
+ * weights (codes, block and matrix scales as moe_ffn_forward_nvfp4 takes
+ * them), in one persistent launch.  xp fp16 [R, H] (the gathered x_hat rows;
+ * bf16 values are exact in fp16), act fp16 [R, I] (bf16-rounded values),
+ * y bf16 [R, H] in (token, slot) order.  shape->wdtype = MOE_W_NVFP4;
+ * workspace >= moe_grouped_ffn_workspace_size(shape) bytes, 256-byte aligned.
+ * UNSUPPORTED_SHAPE unless H and I are multiples of 256. */
+moe_status moe_grouped_ffn_nvfp4(const moe_shape* shape, const void* xp, const uint8_t* w13,
+                                 const uint8_t* w13_sb, const float* w13_sg, const uint8_t* w2,
+                                 const uint8_t* w2_sb, const float* w2_sg, const int32_t* offsets,
+                                 const int32_t* row_src, const float* topk_w, void* act, void* y,
+                                 void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* silu_and_mul ([V100] "2nd wall"): a[r, i] = bf16( silu(h[r, i]) * h[r, I+i] ),
  * silu(z) = z / (1 + exp(-z)); h bf16 [R, 2I], a bf16 [R, I]; I % 8 == 0. */
 moe_status moe_silu_and_mul(const void* h, int32_t R, int32_t I, void* a, moe_stream_t stream);
@@ -303,6 +345,16 @@ moe_status moe_combine(const void* y, int32_t y_bf16, int32_t y_pair_order,
  * activations.  x bf16 [rows, cols], q e4m3 [rows, cols], cols % 16 == 0. */
 moe_status moe_quantize_fp8_rows(const void* x, int64_t rows, int32_t cols, void* q,
                                  float* scale, moe_stream_t stream);
+
+/* NVFP4 quantisation of M matrices w bf16 [M, N, K] along K (the layout
+ * described at moe_ffn_forward_nvfp4), each step rounded to fp32:
+ *   sg[m] = max|w[m]| / (448 * 6)   (1 for an all-zero matrix)
+ *   sb    = e4m3_satfinite_rne( max|block of 16| / (6 * sg) )
+ *   code  = e2m1_satfinite_rne( w / (e4m3(sb) * sg) )   (0 where sb is 0)
+ * q uint8 [M, N, K/2], sb uint8 [M, N, K/16], sg fp32 [M]; K % 16 == 0;
+ * w, q 16-byte aligned; sb, sg 4-byte aligned. */
+moe_status moe_quantize_nvfp4(const void* w, int32_t M, int32_t N, int32_t K, uint8_t* q,
+                              uint8_t* sb, float* sg, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -28,7 +28,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
                 3: "MOE_ERR_UNSUPPORTED_DEVICE", 4: "MOE_ERR_WORKSPACE_TOO_SMALL",
                 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT"}
-W_BF16, W_FP8_E4M3 = 0, 1
+W_BF16, W_FP8_E4M3, W_NVFP4 = 0, 1, 2
 GEMM_FC1_RAW, GEMM_FC1_SILU, GEMM_FC2, GEMM_FC2_BF16 = 0, 1, 2, 3
 ENGINE_AUTO, ENGINE_DECODE, ENGINE_PREFILL = 0, 1, 2
 
@@ -79,6 +79,11 @@ _SIGS = {
     "moe_silu_and_mul": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
     "moe_combine": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _I32, _I32, _P, _P]),
     "moe_quantize_fp8_rows": (ctypes.c_int, [_P, ctypes.c_int64, _I32, _P, _P, _P]),
+    "moe_ffn_forward_nvfp4": (ctypes.c_int, [ctypes.POINTER(MoeShape), _P, _P, _P, _P, _P, _P, _P, _P,
+                                             _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_quantize_nvfp4": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P]),
+    "moe_grouped_ffn_nvfp4": (ctypes.c_int, [ctypes.POINTER(MoeShape), _P, _P, _P, _P, _P, _P, _P, _P,
+                                             _P, _P, _P, _P, _P, _SZ, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -115,8 +120,9 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def make_shape(T, H, E, I, top_k, eps=1e-6, fp8=False, engine=ENGINE_AUTO) -> MoeShape:
-    return MoeShape(T, H, E, I, top_k, eps, W_FP8_E4M3 if fp8 else W_BF16, engine)
+def make_shape(T, H, E, I, top_k, eps=1e-6, fp8=False, engine=ENGINE_AUTO, nvfp4=False) -> MoeShape:
+    wd = W_NVFP4 if nvfp4 else (W_FP8_E4M3 if fp8 else W_BF16)
+    return MoeShape(T, H, E, I, top_k, eps, wd, engine)
 
 
 def abi_version() -> int:
@@ -256,6 +262,37 @@ def moe_combine(y, row_of_pair, T, k, out, pair_order=False, stream=None):
     _check(lib.moe_combine(_ptr(y), y_bf16, 1 if pair_order else 0, _ptr(row_of_pair), T, k, H,
                            _ptr(out), _stream(stream)))
     return out
+
+
+def moe_ffn_forward_nvfp4(shape: MoeShape, x, norm_w, w13, w13_sb, w13_sg, w2, w2_sb, w2_sg, out,
+                          workspace, router_w=None, router_logits=None, router_bias=None,
+                          topk_ids_out=None, topk_w_out=None, stream=None):
+    """The forward with NVFP4 expert weights (codes, E4M3 block scales, fp32
+    matrix scales from moe_quantize_nvfp4) and bf16 activations."""
+    _check(lib.moe_ffn_forward_nvfp4(ctypes.byref(shape), _ptr(x), _ptr(norm_w), _ptr(router_w),
+                                     _ptr(router_logits), _ptr(router_bias), _ptr(w13), _ptr(w13_sb),
+                                     _ptr(w13_sg), _ptr(w2), _ptr(w2_sb), _ptr(w2_sg), _ptr(out),
+                                     _ptr(topk_ids_out), _ptr(topk_w_out), _ws_ptr(workspace),
+                                     _ws_bytes(workspace), _stream(stream)))
+    return out
+
+
+def moe_grouped_ffn_nvfp4(shape: MoeShape, xp, w13, w13_sb, w13_sg, w2, w2_sb, w2_sg, offsets,
+                          row_src, topk_w, act, y, workspace, stream=None):
+    """The NVFP4 FFN step: xp fp16 [R, H] -> act fp16 [R, I] -> y bf16 [R, H]."""
+    _check(lib.moe_grouped_ffn_nvfp4(ctypes.byref(shape), _ptr(xp), _ptr(w13), _ptr(w13_sb),
+                                     _ptr(w13_sg), _ptr(w2), _ptr(w2_sb), _ptr(w2_sg), _ptr(offsets),
+                                     _ptr(row_src), _ptr(topk_w), _ptr(act), _ptr(y),
+                                     _ws_ptr(workspace), _ws_bytes(workspace), _stream(stream)))
+
+
+def moe_quantize_nvfp4(w, q, sb, sg, stream=None):
+    """NVFP4 quantisation of w bf16 [M, N, K] (or [N, K]) into q uint8
+    [.., N, K/2], sb uint8 [.., N, K/16], sg fp32 [M]."""
+    K = w.shape[-1]
+    N = w.shape[-2]
+    M = w.numel() // (N * K) if w.numel() else 0
+    _check(lib.moe_quantize_nvfp4(_ptr(w), M, N, K, _ptr(q), _ptr(sb), _ptr(sg), _stream(stream)))
 
 
 def moe_quantize_fp8_rows(x, q, scale, stream=None):

@@ -102,8 +102,11 @@ moe_status check_shape(const moe_shape* s) {
   MOE_REQ(s->E <= kMaxExperts, MOE_ERR_UNSUPPORTED_SHAPE, "E=%d > %d", s->E, kMaxExperts);
   MOE_REQ(s->top_k <= kMaxTopK && s->top_k <= s->E, MOE_ERR_UNSUPPORTED_SHAPE,
           "top_k=%d must be <= min(E=%d, %d)", s->top_k, s->E, kMaxTopK);
-  MOE_REQ(s->wdtype == MOE_W_BF16 || s->wdtype == MOE_W_FP8_E4M3, MOE_ERR_INVALID_ARG,
-          "wdtype=%d", s->wdtype);
+  MOE_REQ(s->wdtype == MOE_W_BF16 || s->wdtype == MOE_W_FP8_E4M3 || s->wdtype == MOE_W_NVFP4,
+          MOE_ERR_INVALID_ARG, "wdtype=%d", s->wdtype);
+  MOE_REQ(s->wdtype != MOE_W_NVFP4 || (s->H % 256 == 0 && s->I % 256 == 0),
+          MOE_ERR_UNSUPPORTED_SHAPE, "NVFP4 weights need H=%d and I=%d to be multiples of 256", s->H,
+          s->I);
   MOE_REQ(s->engine >= MOE_ENGINE_AUTO && s->engine <= MOE_ENGINE_PREFILL, MOE_ERR_INVALID_ARG,
           "engine=%d", s->engine);
   MOE_REQ((int64_t)s->T * s->top_k <= (1 << 24), MOE_ERR_UNSUPPORTED_SHAPE, "T*top_k too large");
@@ -302,15 +305,29 @@ bool fuse_decode(const moe_shape* s, int engine) {
          !(simt_env && simt_env[0] == '1');
 }
 
+// Block and matrix scales of NVFP4 expert weights (moe_ffn_forward_nvfp4).
+struct Nvfp4Scales {
+  const uint8_t* w13_sb;
+  const float* w13_sg;
+  const uint8_t* w2_sb;
+  const float* w2_sg;
+};
+
 moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, const float* router_w,
                         const float* router_logits, const float* router_bias,
                         const int32_t* ids_in, const float* tw_in, const void* w13, const void* w2,
                         const float* w13_scale, const float* w2_scale, void* out,
                         int32_t* ids_out, float* tw_out, void* workspace, size_t ws_bytes,
-                        moe_stream_t stream) {
+                        moe_stream_t stream, const Nvfp4Scales* nv = nullptr) {
   moe_status rc = check_shape(s);
   if (rc != MOE_OK) return rc;
   const bool f8 = s->wdtype == MOE_W_FP8_E4M3;
+  MOE_REQ((nv != nullptr) == (s->wdtype == MOE_W_NVFP4), MOE_ERR_INVALID_ARG,
+          "NVFP4 weights (wdtype=2) go through moe_ffn_forward_nvfp4, other formats do not");
+  MOE_REQ(!nv || (nv->w13_sb && nv->w13_sg && nv->w2_sb && nv->w2_sg), MOE_ERR_INVALID_ARG,
+          "NVFP4 block and matrix scales must be non-NULL");
+  MOE_REQ(!nv || (aligned16(nv->w13_sb) && aligned16(nv->w2_sb)), MOE_ERR_INVALID_ARG,
+          "NVFP4 block scales must be 16-byte aligned");
   const bool routed = ids_in != nullptr;
   MOE_REQ(x && norm_w && w13 && w2 && out && workspace, MOE_ERR_INVALID_ARG,
           "x, norm_w, w13, w2, out and workspace must be non-NULL");
@@ -359,7 +376,7 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   const bool fuse = fuse_decode(s, engine);
 
   // Small decode batches, opt-in: a1..a8 in one cooperative launch
-  if (fuse && moe::decode_forward_mega_covers(T, H, E, k, router_logits != nullptr, routed)) {
+  if (!nv && fuse && moe::decode_forward_mega_covers(T, H, E, k, router_logits != nullptr, routed)) {
     moe::DecodeForward f{};
     f.x = x;
     f.norm_w = norm_w;
@@ -405,13 +422,24 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   MOE_CUDA(moe::launch_permute_any(ids, T, E, k, offsets, row_src, row_of_pair, perm_cnt,
                                    dev->status, st, sched, 2 * E + 1),
            "permute launch");
-  MOE_CUDA(moe::launch_gather_rows(offsets, E, row_src, k, R, f8 ? (const void*)xq : (const void*)xhat,
-                                   xp, H * (f8 ? 1 : 2), xscale, xp_scale, st),
-           "gather launch");
-  // a5 + a6 + a7: FC1 + silu_and_mul, FC2 + routing weight
-  rc = ffn_impl(s, engine, fuse, xp, xp_scale, w13, w13_scale, w2, w2_scale, offsets, row_src, tw,
-                act, y, sched, actq, act_scale, dev, st);
-  if (rc != MOE_OK) return rc;
+  if (nv) {
+    // NVFP4 weights: fp16 rows for the fp16 tensor-core GEMMs, one fused launch
+    MOE_CUDA(moe::launch_gather_rows_f16(offsets, E, row_src, k, R, H, xhat, xp, st),
+             "gather launch");
+    MOE_CUDA(moe::launch_decode_ffn_nvfp4(xp, static_cast<const uint8_t*>(w13), nv->w13_sb, nv->w13_sg,
+                                          static_cast<const uint8_t*>(w2), nv->w2_sb, nv->w2_sg, act,
+                                          y, offsets, row_src, tw, sched, E, H, I, R, T, dev->sms,
+                                          dev->status, st),
+             "NVFP4 FFN launch");
+  } else {
+    MOE_CUDA(moe::launch_gather_rows(offsets, E, row_src, k, R, f8 ? (const void*)xq : (const void*)xhat,
+                                     xp, H * (f8 ? 1 : 2), xscale, xp_scale, st),
+             "gather launch");
+    // a5 + a6 + a7: FC1 + silu_and_mul, FC2 + routing weight
+    rc = ffn_impl(s, engine, fuse, xp, xp_scale, w13, w13_scale, w2, w2_scale, offsets, row_src, tw,
+                  act, y, sched, actq, act_scale, dev, st);
+    if (rc != MOE_OK) return rc;
+  }
   // a8: combine (fp32 sum in slot order, one bf16 rounding)
   MOE_CUDA(moe::launch_combine(y, true, true, row_of_pair, T, k, H, out, st), "combine launch");
   return MOE_OK;
@@ -500,6 +528,35 @@ moe_status moe_ffn_forward_routed(const moe_shape* shape, const void* x, const v
   return forward_impl(shape, x, norm_w, nullptr, nullptr, nullptr, topk_ids, topk_w, w13, w2,
                       w13_scale, w2_scale, out, nullptr, nullptr, workspace, workspace_bytes,
                       stream);
+}
+
+moe_status moe_ffn_forward_nvfp4(const moe_shape* shape, const void* x, const void* norm_w,
+                                 const float* router_w, const float* router_logits,
+                                 const float* router_bias, const uint8_t* w13, const uint8_t* w13_sb,
+                                 const float* w13_sg, const uint8_t* w2, const uint8_t* w2_sb,
+                                 const float* w2_sg, void* out, int32_t* topk_ids_out,
+                                 float* topk_w_out, void* workspace, size_t workspace_bytes,
+                                 moe_stream_t stream) {
+  MOE_REQ(shape != nullptr && shape->wdtype == MOE_W_NVFP4, MOE_ERR_INVALID_ARG,
+          "shape->wdtype must be MOE_W_NVFP4");
+  const Nvfp4Scales nv{w13_sb, w13_sg, w2_sb, w2_sg};
+  return forward_impl(shape, x, norm_w, router_w, router_logits, router_bias, nullptr, nullptr, w13,
+                      w2, nullptr, nullptr, out, topk_ids_out, topk_w_out, workspace,
+                      workspace_bytes, stream, &nv);
+}
+
+moe_status moe_quantize_nvfp4(const void* w, int32_t M, int32_t N, int32_t K, uint8_t* q,
+                              uint8_t* sb, float* sg, moe_stream_t stream) {
+  MOE_REQ(w && q && sb && sg, MOE_ERR_INVALID_ARG, "w, q, sb and sg must be non-NULL");
+  MOE_REQ(M >= 0 && N >= 0 && K > 0 && K % 16 == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+          "M=%d N=%d K=%d (K %% 16 == 0)", M, N, K);
+  MOE_REQ(aligned16(w) && aligned16(q) && ((uintptr_t)sb & 3u) == 0 && ((uintptr_t)sg & 3u) == 0,
+          MOE_ERR_INVALID_ARG, "misaligned pointer");
+  DevInfo* d = nullptr;
+  moe_status rc = device_info(&d);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(moe::launch_quantize_nvfp4(w, M, N, K, q, sb, sg, (cudaStream_t)stream), "NVFP4 quantise");
+  return MOE_OK;
 }
 
 moe_status moe_rmsnorm(const void* x, const void* w, int32_t T, int32_t H, float eps, void* y,
@@ -597,6 +654,8 @@ moe_status moe_grouped_gemm(const moe_shape* shape, int32_t mode, const void* a,
   moe_status rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   MOE_REQ(mode >= MOE_GEMM_FC1_RAW && mode <= MOE_GEMM_FC2_BF16, MOE_ERR_INVALID_ARG, "mode=%d", mode);
+  MOE_REQ(shape->wdtype != MOE_W_NVFP4, MOE_ERR_INVALID_ARG,
+          "NVFP4 weights run through moe_ffn_forward_nvfp4");
   MOE_REQ(a && w && offsets && c, MOE_ERR_INVALID_ARG, "a, w, offsets and c must be non-NULL");
   MOE_REQ(aligned16(a) && aligned16(w) && aligned16(c), MOE_ERR_INVALID_ARG, "misaligned pointer");
   const bool f8 = shape->wdtype == MOE_W_FP8_E4M3;
@@ -626,6 +685,8 @@ moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* 
   moe_status rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
   const bool f8 = shape->wdtype == MOE_W_FP8_E4M3;
+  MOE_REQ(shape->wdtype != MOE_W_NVFP4, MOE_ERR_INVALID_ARG,
+          "NVFP4 weights run through moe_ffn_forward_nvfp4");
   MOE_REQ(xp && w13 && w2 && offsets && row_src && topk_w && act && y && workspace,
           MOE_ERR_INVALID_ARG, "xp, w13, w2, offsets, row_src, topk_w, act, y and workspace must be non-NULL");
   MOE_REQ(!f8 || (xp_scale && w13_scale && w2_scale), MOE_ERR_INVALID_ARG,
@@ -651,6 +712,38 @@ moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* 
   if (fuse) MOE_CUDA(cudaMemsetAsync(sched, 0, sched_bytes, st), "scheduler reset");
   return ffn_impl(shape, engine, fuse, xp, xp_scale, w13, w13_scale, w2, w2_scale, offsets,
                   row_src, topk_w, act, y, sched, actq, act_scale, dev, st);
+}
+
+moe_status moe_grouped_ffn_nvfp4(const moe_shape* shape, const void* xp, const uint8_t* w13,
+                                 const uint8_t* w13_sb, const float* w13_sg, const uint8_t* w2,
+                                 const uint8_t* w2_sb, const float* w2_sg, const int32_t* offsets,
+                                 const int32_t* row_src, const float* topk_w, void* act, void* y,
+                                 void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  moe_status rc = check_shape(shape);
+  if (rc != MOE_OK) return rc;
+  MOE_REQ(shape->wdtype == MOE_W_NVFP4, MOE_ERR_INVALID_ARG, "shape->wdtype must be MOE_W_NVFP4");
+  MOE_REQ(xp && w13 && w13_sb && w13_sg && w2 && w2_sb && w2_sg && offsets && row_src && topk_w &&
+              act && y && workspace,
+          MOE_ERR_INVALID_ARG, "every pointer must be non-NULL");
+  MOE_REQ(aligned16(xp) && aligned16(w13) && aligned16(w2) && aligned16(act) && aligned16(y) &&
+              aligned16(w13_sb) && aligned16(w2_sb),
+          MOE_ERR_INVALID_ARG, "misaligned pointer");
+  MOE_REQ(((uintptr_t)workspace & 255u) == 0, MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const size_t need = moe_grouped_ffn_workspace_size(shape);
+  MOE_REQ(workspace_bytes >= need, MOE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes",
+          workspace_bytes, need);
+  DevInfo* dev = nullptr;
+  if ((rc = device_info(&dev)) != MOE_OK) return rc;
+  if (shape->T == 0) return MOE_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t* sched = at<int32_t>(workspace, 0);
+  const int R = shape->T * shape->top_k;
+  MOE_CUDA(cudaMemsetAsync(sched, 0, (size_t)(2 * shape->E + 1) * 4, st), "scheduler reset");
+  MOE_CUDA(moe::launch_decode_ffn_nvfp4(xp, w13, w13_sb, w13_sg, w2, w2_sb, w2_sg, act, y, offsets,
+                                        row_src, topk_w, sched, shape->E, shape->H, shape->I, R,
+                                        shape->T, dev->sms, dev->status, st),
+           "NVFP4 FFN launch");
+  return MOE_OK;
 }
 
 moe_status moe_silu_and_mul(const void* h, int32_t R, int32_t I, void* a, moe_stream_t stream) {

@@ -74,6 +74,22 @@ cudaError_t launch_decode_forward_mega(bool fp8, const DecodeForward& f, const v
                                        float* act_scale, int* sched, int E, int I, int sms,
                                        int* status, cudaStream_t st);
 
+// NVFP4 weights (gemm_nvfp4.cu): quantiser, fp16 row gather, and the
+// decode FFN (FC1 + silu_and_mul -> fp16 act, FC2 + routing weight -> bf16 y
+// rows at row_src) in one persistent launch; `sched` as for
+// launch_decode_ffn_fused.  cudaErrorNotSupported when not covered.
+cudaError_t launch_quantize_nvfp4(const void* w, int M, int N, int K, uint8_t* q, uint8_t* sb,
+                                  float* sg, cudaStream_t st);
+cudaError_t launch_gather_rows_f16(const int32_t* offsets, int E, const int32_t* row_src, int k,
+                                   int R_max, int H, const void* src, void* dst, cudaStream_t st);
+bool nvfp4_decode_covers(int H, int I, int E);
+cudaError_t launch_decode_ffn_nvfp4(const void* xp, const uint8_t* w13_q, const uint8_t* w13_sb,
+                                    const float* w13_sg, const uint8_t* w2_q, const uint8_t* w2_sb,
+                                    const float* w2_sg, void* act, void* y, const int32_t* offsets,
+                                    const int32_t* row_src, const float* topk_w, int* sched, int E,
+                                    int H, int I, int R_max, int T, int sms, int* status,
+                                    cudaStream_t st);
+
 // Bounded-wait self-test: a kernel that waits on an mbarrier nothing arrives
 // on for at most limit_cycles SM cycles and records MOE_ERR_TIMEOUT.
 cudaError_t launch_wait_selftest(long long limit_cycles, int* status, cudaStream_t st);

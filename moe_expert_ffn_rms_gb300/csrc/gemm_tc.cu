@@ -37,12 +37,14 @@
 
 #include "common.cuh"
 #include "engine.h"
+#include "tc_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
 
 using namespace ptx;
+using namespace tc;
 
 constexpr int kThreads = 192;
 constexpr int kRowBytes = 128;       // one swizzle row: K slice of a stage
@@ -93,43 +95,14 @@ struct Params {
   JobP job[2];
 };
 
-struct Unit {
-  int job, e, nt, row0, rows;
-};
 
 // The whole decode forward in one launch: the arguments (engine.h).
 using MegaP = DecodeForward;
 
 constexpr int kUnitRing = 4;  // claimed-unit slots between the roles
 
-// Unit u of a job: expert e has ceil(cnt/chunk) token chunks, each with nt N
-// tiles; s_up[e] is the exclusive prefix of units.
-MOE_DEV Unit unit_of(int u, const int* s_off, const int* s_up, int E, int nt, int chunk) {
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_up[mid] <= u) lo = mid; else hi = mid - 1;
-  }
-  const int local = u - s_up[lo];
-  const int mt = local / nt;
-  Unit un;
-  un.job = 0;
-  un.e = lo;
-  un.nt = local - mt * nt;
-  un.row0 = s_off[lo] + mt * chunk;
-  un.rows = min(chunk, s_off[lo + 1] - un.row0);
-  return un;
-}
 
-MOE_DEV int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
-MOE_DEV void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
 
 // TMA loads of one K slice of a unit into ring slot (a, b).
 template <bool SWAP, int MODE>
@@ -313,46 +286,6 @@ MOE_DEV bool epilogue_unit(const Unit& un, const JobP& j, int I, uint32_t tbase,
   return true;
 }
 
-// ------------------------------------------------------ pipeline tails --
-// tcgen05.commit arrives on its mbarriers asynchronously, and with a CTA pair
-// the even CTA's commits also arrive on the odd CTA's barriers.  A CTA must
-// not exit while such an arrival is still on its way to its shared memory
-// (the next CTA on the SM reuses it), so before teardown each role waits for
-// the arrivals it has not consumed yet.
-
-// Producer tail: waits until the MMAs have released the last use of every
-// ring slot.  (s, ph) is the producer's position after its last slot; a slot
-// never used passes at once.
-MOE_DEV bool producer_tail(uint64_t* empty_bar, int stages, int s, uint32_t ph,
-                           volatile int* abort) {
-  for (int i = 0; i < stages; ++i) {
-    if (!mbar_wait(&empty_bar[s], ph ^ 1, abort)) return false;
-    if (++s == stages) { s = 0; ph ^= 1; }
-  }
-  return true;
-}
-
-// MMA tail: waits until the epilogues have released both accumulators.
-MOE_DEV bool accumulator_tail(uint64_t* tempty_bar, int acc, uint32_t aph, volatile int* abort) {
-  for (int i = 0; i < 2; ++i) {
-    if (!mbar_wait(&tempty_bar[acc], aph ^ 1, abort)) return false;
-    if (++acc == 2) { acc = 0; aph ^= 1; }
-  }
-  return true;
-}
-
-// After an abort: waits, bounded, for the copies of the last arming of every
-// slot (bit i of `armed`; its phase parity in bit i of `armed_ph`), whether or
-// not the MMAs consumed them.
-MOE_DEV void drain_armed(uint64_t* full_bar, int stages, uint32_t armed, uint32_t armed_ph) {
-  for (int i = 0; i < stages; ++i) {
-    if (!((armed >> i) & 1u)) continue;
-    const uint32_t par = (armed_ph >> i) & 1u;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(&full_bar[i], par) && clock64() - t0 < kSpinLimitCycles) {
-    }
-  }
-}
 
 // ------------------------------------------ whole decode forward phases --
 // Grid-wide barrier of a cooperative launch.  bar[0] counts arrivals, bar[1]
@@ -1222,19 +1155,29 @@ void load_encode() {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 }
 
+}  // namespace
+
+bool tc::encode_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,
+                    int64_t rows, int64_t cols, int box_cols, int box_rows, CUtensorMapSwizzle sw) {
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * elem_bytes)};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
 bool make_map(CUtensorMap* m, const void* base, bool fp8, int64_t rows, int64_t cols,
               int box_rows) {
-  if (!g_encode) return false;
   const int elem = fp8 ? 1 : 2;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(cols * elem)};
-  cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / elem), (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                        2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return tc::encode_map(m, base, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        elem, rows, cols, kRowBytes / elem, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <bool SWAP, bool FP8, int M0, int M1>

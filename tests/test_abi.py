@@ -122,6 +122,22 @@ def test_step_entry_points_reject_bad_arguments_on_host(M):
     assert M.lib.moe_grouped_ffn(ctypes.byref(shape), None, None, fake, None, fake, None, fake,
                                  fake, fake, fake, fake, fake, 1 << 20, None) == 1
     assert M.lib.moe_selftest_wait_timeout(0, None) == 1
+    # NVFP4: H and I multiples of 256, only through the NVFP4 entry points
+    nv_bad = M.make_shape(4, 320, 8, 256, 2, nvfp4=True)
+    assert M.lib.moe_ffn_workspace_size(ctypes.byref(nv_bad)) == 0
+    nv = M.make_shape(4, 256, 8, 256, 2, nvfp4=True)
+    assert M.lib.moe_ffn_workspace_size(ctypes.byref(nv)) > 0
+    assert M.lib.moe_ffn_forward(ctypes.byref(nv), fake, fake, fake, None, None, fake, fake, None,
+                                 None, fake, None, None, fake, 1 << 40, None) == 1
+    assert M.lib.moe_ffn_forward_nvfp4(ctypes.byref(shape), fake, fake, fake, None, None, fake, fake,
+                                       fake, fake, fake, fake, fake, None, None, fake, 1 << 40,
+                                       None) == 1          # shape not NVFP4
+    assert M.lib.moe_ffn_forward_nvfp4(ctypes.byref(nv), fake, fake, fake, None, None, fake, None,
+                                       fake, fake, fake, fake, fake, None, None, fake, 1 << 40,
+                                       None) == 1          # block scales missing
+    assert M.lib.moe_quantize_nvfp4(fake, 2, 4, 24, fake, fake, fake, None) == 2   # K % 16
+    assert M.lib.moe_grouped_gemm(ctypes.byref(nv), 1, fake, None, fake, None, fake, None, None,
+                                  fake, None) == 1
     assert M.lib.moe_route_workspace_size(4, 256, 8) > 0
     assert M.lib.moe_route_workspace_size(4, 250, 8) == 0
 

@@ -53,6 +53,7 @@ class Config:
     seed: int
     eps: float = 1e-6
     description: str = ""
+    nvfp4: bool = False   # NVFP4 expert weights (quantised from the drawn bf16 weights)
 
 
 CONFIGS = {
@@ -71,6 +72,10 @@ CONFIGS = {
     "c5_prefill": Config(
         "c5_prefill", Shape(T=4096, H=4096, E=64, k=8, I=1536), "learned", False, 4,
         description="prefill, learned router with natural imbalance"),
+    "c6_decode_nvfp4": Config(
+        "c6_decode_nvfp4", Shape(T=16, H=4096, E=64, k=8, I=1536), "balanced", False, 5,
+        description="decode with NVFP4 expert weights (E2M1 codes, E4M3 block scales of 16, "
+                    "fp32 matrix scales) and bf16 activations", nvfp4=True),
 }
 
 CONFIG_ORDER = ["c1_tiny", "c2_decode_balanced", "c3_decode_skewed", "c4_decode_fp8", "c5_prefill"]
@@ -132,7 +137,8 @@ def make_inputs(cfg: Config | str, device="cpu", shape: Optional[Shape] = None,
         ids = (k * t_idx + j_idx) % E
         router_logits.scatter_(1, ids, vals)
     return dict(
-        name=cfg.name, T=T, H=H, E=E, k=k, I=I, eps=cfg.eps, fp8=cfg.fp8, routing=routing,
+        name=cfg.name, T=T, H=H, E=E, k=k, I=I, eps=cfg.eps, fp8=cfg.fp8, nvfp4=cfg.nvfp4,
+        routing=routing,
         seed=seed, x=x, norm_w=norm_w, router_w=router_w, router_bias=router_bias,
         router_logits=router_logits, w13=w13, w2=w2,
     )
