@@ -336,6 +336,90 @@ def grouped_fc2_fp8(a, offsets, w2q_of, s2_of, row_weight):
 
 
 # ---------------------------------------------------------------------------
+# Block-wise FP8 pieces
+# ---------------------------------------------------------------------------
+
+FP8_BLOCK = 128
+
+
+def quantize_blocks_e4m3(v: np.ndarray, block_rows: int, block_cols: int = FP8_BLOCK):
+    """Block-wise dynamic E4M3 quantisation of a matrix [N, K]: one fp32
+    scale per block_rows x block_cols tile, s = absmax(tile)/448, and
+    q = e4m3(v/s) for every element of the tile.
+
+    [SM] support table ("FP8 block-wise" MoE GEMMs) and the Hopper data-flow
+    figure ("block-wise FP8 dequant inside GEMM loop") name the scheme
+    without defining it.  Reading: 128 x 128 weight tiles (block_rows = 128)
+    and per-token groups of 128 consecutive K elements for activations
+    (block_rows = 1); the scale and the division are taken in fp32, as in
+    quantize_rows_e4m3, and an all-zero tile gets s = 1, q = 0.
+    Returns (q float64 holding E4M3 values [N, K], s float64 holding fp32
+    values [N / block_rows, K / block_cols])."""
+    v = np.asarray(v, dtype=F64)
+    n, kdim = v.shape
+    assert n % block_rows == 0 and kdim % block_cols == 0
+    tiles = f32(v).reshape(n // block_rows, block_rows, kdim // block_cols, block_cols)
+    amax = np.max(np.abs(tiles), axis=(1, 3))
+    s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    ratio = (tiles / s[:, None, :, None]).astype(F64)     # correctly rounded fp32 divide
+    q = e4m3_round(ratio)
+    return q.reshape(n, kdim), s.astype(F64)
+
+
+def block_scaled_matmul(aq, sa, wq, sw, block_cols: int = FP8_BLOCK):
+    """y[r, n] = sum over K groups g of  s_a[r, g] * s_w[n / 128, g] *
+    (sum over k in g of aq[r, k] * wq[n, k]).
+
+    The products of each 128-wide K group are summed exactly (fp64 over E4M3
+    values) and scaled once; the scaled group sums are added in K order (the
+    "dequantise inside the GEMM loop" of the block-wise scheme).  aq [R, K]
+    with sa [R, K/128]; wq [N, K] with sw [N/128, K/128]."""
+    aq = np.asarray(aq, dtype=F64)
+    wq = np.asarray(wq, dtype=F64)
+    sa = np.asarray(sa, dtype=F64)
+    sw = np.asarray(sw, dtype=F64)
+    rows_per_wblock = wq.shape[0] // sw.shape[0]
+    y = np.zeros((aq.shape[0], wq.shape[0]), dtype=F64)
+    for g in range(aq.shape[1] // block_cols):
+        ks = slice(g * block_cols, (g + 1) * block_cols)
+        part = aq[:, ks] @ wq[:, ks].T
+        y += part * sa[:, g, None] * np.repeat(sw[:, g], rows_per_wblock)[None, :]
+    return y
+
+
+def grouped_fc1_fp8_block(xq, sx_rows, offsets, w13q_of, s13_of, I):
+    """FC1 with block-wise FP8: h = block_scaled_matmul(x_q, s_x, W13_q, s_w)
+    per expert segment (s_x [R, H/128] per row and K group, s_w
+    [2I/128, H/128]), then a = silu_and_mul(h) in bf16."""
+    out = np.zeros((xq.shape[0], I), dtype=F64)
+    for e in range(len(offsets) - 1):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 == r0:
+            continue
+        h = block_scaled_matmul(xq[r0:r1], sx_rows[r0:r1], w13q_of(e), s13_of(e))
+        out[r0:r1] = silu_and_mul(h, I)
+    return out
+
+
+def grouped_fc2_fp8_block(a, offsets, w2q_of, s2_of, row_weight):
+    """FC2 with block-wise FP8: the bf16 row a[r] is quantised in groups of
+    128 (quantize_blocks_e4m3 with block_rows = 1), y = block_scaled_matmul
+    (a_q, s_a, W2_q, s_w) with s_w [H/128, I/128]; Y = w_r * y."""
+    aq, sa = quantize_blocks_e4m3(a, 1)
+    Y = None
+    for e in range(len(offsets) - 1):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 == r0:
+            continue
+        w2q = np.asarray(w2q_of(e), dtype=F64)
+        if Y is None:
+            Y = np.zeros((a.shape[0], w2q.shape[0]), dtype=F64)
+        y = block_scaled_matmul(aq[r0:r1], sa[r0:r1], w2q, s2_of(e))
+        Y[r0:r1] = y * np.asarray(row_weight[r0:r1], dtype=F64)[:, None]
+    return Y
+
+
+# ---------------------------------------------------------------------------
 # Whole forward
 # ---------------------------------------------------------------------------
 
@@ -355,8 +439,9 @@ def moe_ffn_forward(x, norm_w, eps, k, w13, w2, router_w=None, router_bias=None,
     ``w13``/``w2`` are [E,2I,H] / [E,H,I] arrays (or callables e -> expert
     matrix).  Routing is computed from ``router_w`` or ``logits`` unless
     ``ids``/``topk_w`` are given.  With fp8=True the weights are quantised
-    per output channel and the activations per row, as quantize_rows_e4m3.
-    Returns a dict with every intermediate."""
+    per output channel and the activations per row, as quantize_rows_e4m3;
+    with fp8="block" in 128 x 128 weight tiles and 1 x 128 activation groups,
+    as quantize_blocks_e4m3.  Returns a dict with every intermediate."""
     x = np.asarray(x, dtype=F64)
     T, H = x.shape
     w13_of = w13 if callable(w13) else (lambda e, _w=w13: _w[e])
@@ -377,6 +462,22 @@ def moe_ffn_forward(x, norm_w, eps, k, w13, w2, router_w=None, router_bias=None,
         xp = xhat[tok]
         A = grouped_fc1(xp, offsets, w13_of, I)
         Y = grouped_fc2(A, offsets, w2_of, row_w)
+    elif fp8 == "block":
+        xq, sx = quantize_blocks_e4m3(xhat, 1)
+        cache13, cache2 = {}, {}
+
+        def b13(e):
+            if e not in cache13:
+                cache13[e] = quantize_blocks_e4m3(w13_of(e), FP8_BLOCK)
+            return cache13[e]
+
+        def b2(e):
+            if e not in cache2:
+                cache2[e] = quantize_blocks_e4m3(w2_of(e), FP8_BLOCK)
+            return cache2[e]
+        A = grouped_fc1_fp8_block(xq[tok], sx[tok], offsets, lambda e: b13(e)[0],
+                                  lambda e: b13(e)[1], I)
+        Y = grouped_fc2_fp8_block(A, offsets, lambda e: b2(e)[0], lambda e: b2(e)[1], row_w)
     else:
         xq, sx = quantize_rows_e4m3(xhat)
         cache13, cache2 = {}, {}
@@ -405,8 +506,9 @@ def ffn_token_outputs(xhat_rows, ids, topk_w, w13_of, w2_of, I, cols=None, fp8=F
 
     Used for sampled checks at full size: it needs only the experts the
     sampled tokens use.  Work is grouped by expert so each expert's weights
-    are converted once.  For fp8=True, ``wq13_of``/``wq2_of`` return
-    (codes, scales) of the quantised expert weights.  NVFP4 weights with bf16
+    are converted once.  For fp8=True (or "block"), ``wq13_of``/``wq2_of``
+    return (codes, scales) of the quantised expert weights (per-channel, or
+    per 128 x 128 tile).  NVFP4 weights with bf16
     activations are the bf16 path on the dequantised weights: pass
     ``w13_of``/``w2_of`` returning dequantize_nvfp4(...)."""
     xhat_rows = np.asarray(xhat_rows, dtype=F64)
@@ -415,7 +517,9 @@ def ffn_token_outputs(xhat_rows, ids, topk_w, w13_of, w2_of, I, cols=None, fp8=F
     n, k = ids.shape
     nc = len(cols) if cols is not None else None
     acc = None
-    if fp8:
+    if fp8 == "block":
+        xq, sx = quantize_blocks_e4m3(xhat_rows, 1)
+    elif fp8:
         xq, sx = quantize_rows_e4m3(xhat_rows)
     for e in np.unique(ids):
         tj = np.argwhere(ids == e)                      # (token-in-subset, slot) pairs
@@ -427,6 +531,19 @@ def ffn_token_outputs(xhat_rows, ids, topk_w, w13_of, w2_of, I, cols=None, fp8=F
             if cols is not None:
                 w2 = w2[cols]
             y = a @ w2.T
+        elif fp8 == "block":
+            q13, s13 = wq13_of(int(e))
+            h = block_scaled_matmul(xq[rows], sx[rows], q13, s13)
+            a = silu_and_mul(h, I)
+            aq, sa = quantize_blocks_e4m3(a, 1)
+            q2, s2 = wq2_of(int(e))
+            q2 = np.asarray(q2, dtype=F64)
+            s2 = np.asarray(s2, dtype=F64)
+            if cols is not None:
+                # the weight scale of output column n is s2[n / 128]
+                s2 = np.repeat(s2, q2.shape[0] // s2.shape[0], axis=0)[cols]
+                q2 = q2[cols]
+            y = block_scaled_matmul(aq, sa, q2, s2)
         else:
             q13, s13 = wq13_of(int(e))
             h = (xq[rows] @ np.asarray(q13, dtype=F64).T) * sx[rows, None] * np.asarray(s13)[None, :]

@@ -227,6 +227,153 @@ def test_fp8_gemm_equals_bf16_gemm_on_representable_inputs():
 
 
 # ---------------------------------------------------------------------------
+# block-wise FP8 (128 x 128 weight tiles, 1 x 128 activation groups)
+# ---------------------------------------------------------------------------
+
+E4M3_NORMALS = np.array(sorted(set(O.e4m3_decode(c) for c in range(0x08, 0x7F))))
+
+
+def _tiled(rng, n, kdim, bn, scales, bk=128):
+    """A matrix whose (bn x bk) tile (i, g) is scales[i, g] times E4M3 normals
+    with one element of magnitude 448 (so the tile's scale is scales[i, g])."""
+    q = rng.choice(E4M3_NORMALS, (n, kdim)) * rng.choice([-1.0, 1.0], (n, kdim))
+    for i in range(n // bn):
+        for g in range(kdim // bk):
+            r, c = rng.integers(bn), rng.integers(bk)
+            q[i * bn + r, g * bk + c] = 448.0 * rng.choice([-1.0, 1.0])
+    return q, q * np.repeat(np.repeat(scales, bn, axis=0), bk, axis=1)
+
+
+def test_fp8_block_quantise_constructed_round_trip():
+    """Tiles built as (E4M3 codes) x (scale with few significant bits) come
+    back exactly, each scale at its own (row block, K group): pins the tile
+    indexing and the absmax/448 scale."""
+    rng = np.random.default_rng(40)
+    sw = np.array([[1.5, 0.75, 2.0 ** -9], [1.25 * 2.0 ** -6, 3.0, 1.0]]) * 2.0 ** -8
+    q, w = _tiled(rng, 256, 384, 128, sw)
+    q2, s2 = O.quantize_blocks_e4m3(w, 128)
+    np.testing.assert_array_equal(q2, q)
+    np.testing.assert_array_equal(s2, sw)
+    # activation groups: one scale per (row, 128 K elements)
+    sa = rng.choice([0.5, 1.0, 1.5, 0.125, 1.75], (5, 3)) * 2.0 ** -5
+    qa, a = _tiled(rng, 5, 384, 1, sa)
+    qa2, sa2 = O.quantize_blocks_e4m3(a, 1)
+    np.testing.assert_array_equal(qa2, qa)
+    np.testing.assert_array_equal(sa2, sa)
+
+
+def test_fp8_block_quantise_special_cases():
+    rng = np.random.default_rng(41)
+    w = torch.from_numpy((rng.standard_normal((256, 256)) * 0.02).astype(np.float32)).to(torch.bfloat16)
+    w64 = w.to(torch.float64).numpy()
+    # one K group and one row per block: the per-row recipe (pinned against torch)
+    q1, s1 = O.quantize_blocks_e4m3(w64[:, :128], 1)
+    qr, sr = O.quantize_rows_e4m3(w64[:, :128])
+    np.testing.assert_array_equal(q1, qr)
+    np.testing.assert_array_equal(s1[:, 0], sr)
+    # torch's float8_e4m3fn on each tile, tile by tile
+    q, s = O.quantize_blocks_e4m3(w64, 128)
+    for i in range(2):
+        for g in range(2):
+            t = w[i * 128:(i + 1) * 128, g * 128:(g + 1) * 128].float()
+            ts = t.abs().max() / 448.0
+            assert s[i, g] == ts.item()
+            tq = (t / ts).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+            np.testing.assert_array_equal(q[i * 128:(i + 1) * 128, g * 128:(g + 1) * 128], tq)
+    # an all-zero tile: scale 1, codes 0; the other tiles are untouched
+    w0 = w64.copy()
+    w0[128:, :128] = 0
+    qz, sz = O.quantize_blocks_e4m3(w0, 128)
+    assert sz[1, 0] == 1.0 and np.all(qz[128:, :128] == 0)
+    np.testing.assert_array_equal(sz[0], s[0])
+
+
+def test_block_scaled_matmul_exact_on_representable_inputs():
+    """With tiles that quantise exactly, the block-scaled product equals the
+    plain fp64 product x @ w^T exactly (all partial sums are exact in fp64):
+    a swapped scale index or a dropped scale fails it."""
+    rng = np.random.default_rng(42)
+    sw = rng.choice([1.0, 2.0, 0.5, 4.0, 0.25], (2, 3)) * 2.0 ** -10
+    sa = rng.choice([1.0, 2.0, 0.5, 0.125], (6, 3)) * 2.0 ** -4
+    qw, w = _tiled(rng, 256, 384, 128, sw)
+    qa, a = _tiled(rng, 6, 384, 1, sa)
+    y = O.block_scaled_matmul(qa, sa, qw, sw)
+    np.testing.assert_array_equal(y, a @ w.T)
+    # the same through the quantiser
+    aq, as_ = O.quantize_blocks_e4m3(a, 1)
+    wq, ws = O.quantize_blocks_e4m3(w, 128)
+    np.testing.assert_array_equal(O.block_scaled_matmul(aq, as_, wq, ws), a @ w.T)
+
+
+def test_block_scaled_matmul_error_bound():
+    """E4M3 round to nearest: |v - v~| <= 2^-4 |v| + 2^-10 s per element (half
+    a normal quantum relative, half the subnormal quantum 2^-9 s absolute), so
+    |y - x w^T| <= sum_k |dx| |w~| + |x| |dw|."""
+    rng = np.random.default_rng(43)
+    x = rng.standard_normal((7, 256)) * np.repeat(rng.choice([0.1, 1.0, 10.0], (7, 2)), 128, axis=1)
+    w = rng.standard_normal((256, 256)) * 0.02
+    x = x.astype(np.float32).astype(np.float64)
+    w = w.astype(np.float32).astype(np.float64)
+    xq, sx = O.quantize_blocks_e4m3(x, 1)
+    wq, sw = O.quantize_blocks_e4m3(w, 128)
+    y = O.block_scaled_matmul(xq, sx, wq, sw)
+    xt = xq * np.repeat(sx, 128, axis=1)
+    wt = wq * np.repeat(np.repeat(sw, 128, axis=0), 128, axis=1)
+    dx = 2.0 ** -4 * np.abs(x) + 2.0 ** -10 * np.repeat(sx, 128, axis=1)
+    dw = 2.0 ** -4 * np.abs(w) + 2.0 ** -10 * np.repeat(np.repeat(sw, 128, axis=0), 128, axis=1)
+    assert np.all(np.abs(xt - x) <= dx) and np.all(np.abs(wt - w) <= dw)
+    bound = dx @ np.abs(wt).T + np.abs(x) @ dw.T
+    assert np.all(np.abs(y - x @ w.T) <= bound * (1 + 1e-12))
+    # and the bound is not vacuous: the error is well below the plain magnitude
+    assert np.max(np.abs(y - x @ w.T)) < 0.2 * np.max(np.abs(x @ w.T))
+
+
+def test_fp8_block_ffn_equals_bf16_ffn_on_representable_inputs():
+    """FC1 and FC2 with block-wise FP8 equal the plain FC1/FC2 when the
+    activations and weights quantise exactly (FC2 compared on the re-quantised
+    FC1 output, the input the block-wise FC2 sees)."""
+    rng = np.random.default_rng(44)
+    H, I, rows = 256, 256, 5
+    s13 = rng.choice([1.0, 2.0, 0.5], (4, 2)) * 2.0 ** -12
+    q13, w13 = _tiled(rng, 2 * I, H, 128, s13)
+    sx = rng.choice([1.0, 0.5, 2.0], (rows, 2)) * 2.0 ** -6
+    qx, x = _tiled(rng, rows, H, 1, sx)
+    offsets = np.array([0, rows])
+    a8 = O.grouped_fc1_fp8_block(qx, sx, offsets, lambda e: q13, lambda e: s13, I)
+    a16 = O.grouped_fc1(x, offsets, lambda e: w13, I)
+    np.testing.assert_array_equal(a8, a16)
+    s2 = rng.choice([1.0, 2.0, 0.25], (2, 2)) * 2.0 ** -11
+    q2, w2 = _tiled(rng, H, I, 128, s2)
+    rw = rng.random(rows)
+    aq, sa = O.quantize_blocks_e4m3(a16, 1)
+    y8 = O.grouped_fc2_fp8_block(a16, offsets, lambda e: q2, lambda e: s2, rw)
+    y16 = O.grouped_fc2(aq * np.repeat(sa, 128, axis=1), offsets, lambda e: w2, rw)
+    np.testing.assert_allclose(y8, y16, rtol=1e-13, atol=0)
+
+
+def test_fp8_block_forward_token_definition_matches_grouped_form():
+    inp = workloads.make_inputs("c1_tiny", "cpu")
+    x = inp["x"].double().numpy()
+    nw = inp["norm_w"].double().numpy()
+    Wr = inp["router_w"].double().numpy()
+    w13 = inp["w13"].double().numpy()
+    w2 = inp["w2"].double().numpy()
+    res = O.moe_ffn_forward(x, nw, 1e-6, 2, w13, w2, router_w=Wr, fp8="block")
+    b13 = {e: O.quantize_blocks_e4m3(w13[e], 128) for e in range(8)}
+    b2 = {e: O.quantize_blocks_e4m3(w2[e], 128) for e in range(8)}
+    direct = O.ffn_token_outputs(res["xhat"], res["ids"], res["topk_w"], None, None, 512,
+                                 fp8="block", wq13_of=b13.get, wq2_of=b2.get)
+    np.testing.assert_array_equal(direct, res["out"])
+    cols = np.array([0, 127, 128, 200])
+    direct_c = O.ffn_token_outputs(res["xhat"], res["ids"], res["topk_w"], None, None, 512,
+                                   cols=cols, fp8="block", wq13_of=b13.get, wq2_of=b2.get)
+    np.testing.assert_array_equal(direct_c, res["out"][:, cols])
+    # block-wise FP8 stays close to the bf16 forward (E4M3 carries 3 mantissa bits)
+    ref = O.moe_ffn_forward(x, nw, 1e-6, 2, w13, w2, router_w=Wr)["out"]
+    assert np.max(np.abs(res["out"] - ref)) < 6e-2 * max(1.0, np.max(np.abs(ref)))
+
+
+# ---------------------------------------------------------------------------
 # silu / rms_norm
 # ---------------------------------------------------------------------------
 
