@@ -66,6 +66,10 @@ def algorithmic_work(inp, offsets_np):
         # E2M1 codes (1/2 B), one E4M3 block scale per 16 (1/16 B), an fp32 matrix scale
         fc1_bytes = active * (2 * I * H // 2 + 2 * I * H // 16 + 4)
         fc2_bytes = active * (H * I // 2 + H * I // 16 + 4)
+    elif inp["fp8"] == "block":
+        # E4M3 codes (1 B) and one fp32 scale per 128 x 128 tile
+        fc1_bytes = active * (2 * I * H + (2 * I // 128) * (H // 128) * 4)
+        fc2_bytes = active * (H * I + (H // 128) * (I // 128) * 4)
     else:
         elem = 1 if inp["fp8"] else 2
         fc1_bytes = active * 2 * I * H * elem + (active * 2 * I * 4 if inp["fp8"] else 0)
@@ -142,7 +146,7 @@ def _save_sample(inp, toks, path):
     import torch
     k = inp["k"]
     d = dict(x=inp["x"][toks].float().cpu().numpy(), norm_w=inp["norm_w"].float().cpu().numpy(),
-             eps=np.array(inp["eps"]), k=np.array(k), fp8=np.array(inp["fp8"]),
+             eps=np.array(inp["eps"]), k=np.array(k), fp8=np.array(str(inp["fp8"])),
              nvfp4=np.array(bool(inp.get("nvfp4"))))
     if inp["router_logits"] is not None:
         d["logits"] = inp["router_logits"][toks].cpu().numpy()
@@ -191,6 +195,8 @@ if "nvfp4" in d and bool(d["nvfp4"]):
     # NVFP4 weights: quantised once, like the GPU path's offline quantisation
     W13 = {e: O.dequantize_nvfp4(*O.quantize_nvfp4(w)) for e, w in W13.items()}
     W2 = {e: O.dequantize_nvfp4(*O.quantize_nvfp4(w)) for e, w in W2.items()}
+fp8 = str(d["fp8"])
+fp8 = "block" if fp8 == "block" else fp8 == "True"
 reps = int(sys.argv[3])
 min_seconds = float(sys.argv[4])
 t0 = time.perf_counter()
@@ -198,7 +204,7 @@ done = 0
 while done < reps or time.perf_counter() - t0 < min_seconds:
     res = O.moe_ffn_forward(d["x"].astype(np.float64), d["norm_w"].astype(np.float64),
                             float(d["eps"]), int(d["k"]), lambda e: W13[e], lambda e: W2[e],
-                            fp8=bool(d["fp8"]), **kw)
+                            fp8=fp8, **kw)
     assert set(res["ids"].reshape(-1).tolist()) <= set(W13), "sample needs more experts"
     done += 1
 dt = time.perf_counter() - t0
@@ -275,7 +281,8 @@ def barrier(world: int):
 
 def auto_cpu_tokens(workload):
     return {"c1_tiny": 4, "c2_decode_balanced": 2, "c3_decode_skewed": 1,
-            "c4_decode_fp8": 2, "c5_prefill": 2}.get(workload, 1)
+            "c4_decode_fp8": 2, "c5_prefill": 2, "c6_decode_nvfp4": 2,
+            "c7_decode_fp8_block": 2}.get(workload, 1)
 
 
 def main_reference(args):
@@ -318,11 +325,20 @@ def main_native(args):
     inp = workloads.make_inputs(args.workload, dev)
     T, H, E, k, I, fp8 = inp["T"], inp["H"], inp["E"], inp["k"], inp["I"], inp["fp8"]
     nvfp4 = bool(inp.get("nvfp4"))
+    fb = fp8 == "block"
     R = T * k
     shape = M.make_shape(T, H, E, I, k, inp["eps"], fp8=fp8, nvfp4=nvfp4)
     ws = M.alloc_workspace(M.moe_ffn_workspace_size(shape), dev)
     w13, w2, s13, s2 = inp["w13"], inp["w2"], None, None
-    if fp8:
+    if fb:
+        # E4M3 codes with one fp32 scale per 128 x 128 tile
+        w13 = torch.empty((E, 2 * I, H), dtype=torch.uint8, device=dev)
+        s13 = torch.empty((E, 2 * I // 128, H // 128), dtype=torch.float32, device=dev)
+        w2 = torch.empty((E, H, I), dtype=torch.uint8, device=dev)
+        s2 = torch.empty((E, H // 128, I // 128), dtype=torch.float32, device=dev)
+        M.moe_quantize_fp8_blocks(inp["w13"], w13, s13, 128)
+        M.moe_quantize_fp8_blocks(inp["w2"], w2, s2, 128)
+    elif fp8:
         w13 = torch.empty((E, 2 * I, H), dtype=torch.uint8, device=dev)
         s13 = torch.empty((E, 2 * I), dtype=torch.float32, device=dev)
         w2 = torch.empty((E, H, I), dtype=torch.uint8, device=dev)
@@ -345,7 +361,7 @@ def main_native(args):
     ids = torch.empty((T, k), dtype=torch.int32, device=dev)
     tw = torch.empty((T, k), dtype=torch.float32, device=dev)
     st = torch.cuda.current_stream()
-    wbytes = 3 * H * I * E * (0.5625 if nvfp4 else (1 if fp8 else 2))
+    wbytes = 3 * H * I * E * (0.5625 if nvfp4 else (1 if fp8 else 2))  # fp8: True or "block"
     small = wbytes < 256 * 2 ** 20
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if small else None
 
@@ -401,22 +417,28 @@ def main_native(args):
     # events around each stage (per-kernel durations for the roofline)
     xhat = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     xq = torch.empty((T, H), dtype=torch.uint8, device=dev) if fp8 else None
-    xs = torch.empty((T,), dtype=torch.float32, device=dev) if fp8 else None
+    hs = H // 128 if fb else 1  # activation scales per row
+    xs = torch.empty((T, hs), dtype=torch.float32, device=dev).squeeze(1) if fp8 else None
     rws = M.alloc_workspace(max(256, M.moe_route_workspace_size(T, H, E)), dev)
     offsets = torch.empty((E + 1,), dtype=torch.int32, device=dev)
     row_src = torch.empty((R,), dtype=torch.int32, device=dev)
     rop = torch.empty((R,), dtype=torch.int32, device=dev)
     xp = torch.empty((R, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
-    xps = torch.empty((R,), dtype=torch.float32, device=dev) if fp8 else None
+    xps = torch.empty((R, hs), dtype=torch.float32, device=dev).squeeze(1) if fp8 else None
     act = torch.empty((R, I), dtype=torch.bfloat16, device=dev)
     actq = torch.empty((R, I), dtype=torch.uint8, device=dev) if fp8 else None
+    if fb:
+        # the scale rows are gathered like the code rows (a second permute
+        # call moves them as rows of H/128 fp32 values)
+        assert (hs * 4) % 16 == 0, "block-wise FP8 stage path needs H % 512 == 0"
+        pxs = torch.empty((R,), dtype=torch.int32, device=dev)
     acts = torch.empty((R,), dtype=torch.float32, device=dev) if fp8 else None
     y = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
     pws = M.alloc_workspace(max(256, M.moe_permute_workspace_size(T, E, k)), dev)
     out_b = torch.empty_like(out)
     # The decode engine with bf16 weights runs FC1 and FC2 in one fused launch:
     # time that launch (moe_grouped_ffn) as one stage; otherwise FC1 and FC2.
-    fused = nvfp4 or ((T * k / E <= 96.0) and os.environ.get("MOE_FUSE", "1") != "0")
+    fused = nvfp4 or fb or ((T * k / E <= 96.0) and os.environ.get("MOE_FUSE", "1") != "0")
     xp16 = torch.empty((R, H), dtype=torch.float16, device=dev) if nvfp4 else None
     act16 = torch.empty((R, I), dtype=torch.float16, device=dev) if nvfp4 else None
     fws = M.alloc_workspace(max(256, M.moe_grouped_ffn_workspace_size(shape)), dev)
@@ -428,14 +450,24 @@ def main_native(args):
             if evs is not None:
                 evs[i].record(st)
         mark(0)
-        M.moe_rmsnorm(inp["x"], inp["norm_w"], inp["eps"], xhat, xq, xs)
+        if fb:
+            M.moe_rmsnorm(inp["x"], inp["norm_w"], inp["eps"], xhat)
+            M.moe_quantize_fp8_blocks(xhat, xq, xs, 1)
+        else:
+            M.moe_rmsnorm(inp["x"], inp["norm_w"], inp["eps"], xhat, xq, xs)
         mark(1)
         M.moe_route_topk(T, H, E, k, ids, tw, xhat=xhat, router_w=inp["router_w"],
                          router_bias=inp["router_bias"], logits_in=inp["router_logits"],
                          workspace=rws)
         mark(2)
-        M.moe_permute(ids, T, E, k, offsets, row_src, rop, xhat=xq if fp8 else xhat, xp=xp,
-                      row_bytes=H * (1 if fp8 else 2), xscale=xs, xp_scale=xps, workspace=pws)
+        if fb:
+            M.moe_permute(ids, T, E, k, offsets, row_src, rop, xhat=xq, xp=xp, row_bytes=H,
+                          workspace=pws)
+            M.moe_permute(ids, T, E, k, offsets, row_src, pxs, xhat=xs, xp=xps,
+                          row_bytes=hs * 4, workspace=pws)
+        else:
+            M.moe_permute(ids, T, E, k, offsets, row_src, rop, xhat=xq if fp8 else xhat, xp=xp,
+                          row_bytes=H * (1 if fp8 else 2), xscale=xs, xp_scale=xps, workspace=pws)
         if nvfp4:
             xp16.copy_(xp)   # fp16 rows for the NVFP4 FFN step (counted in the permute stage)
         mark(3)
@@ -444,8 +476,8 @@ def main_native(args):
             M.moe_grouped_ffn_nvfp4(shape, xp16, q13, sb13, sg13, q2, sb2, sg2, offsets, row_src,
                                     tw, act16, y, fws)
         elif fused:
-            M.moe_grouped_ffn(shape, xp, w13, w2, offsets, row_src, tw, act, y, fws, xp_scale=xps,
-                              w13_scale=s13, w2_scale=s2)
+            M.moe_grouped_ffn(shape, xp, w13, w2, offsets, row_src, tw, actq if fb else act, y, fws,
+                              xp_scale=xps, w13_scale=s13, w2_scale=s2)
         else:
             M.moe_grouped_gemm(shape, M.GEMM_FC1_SILU, xp, w13, offsets, act, a_scale=xps,
                                w_scale=s13)
@@ -544,7 +576,7 @@ def main_native(args):
     # FC1 + FC2 (one fused launch or two), [FP8 quant], combine
     launches_per_step = (1 + (1 if inp["router_w"] is not None else 0) + 1 +
                          (3 if T * k > 4096 else 1) + 1 + (1 if fused else 2) +
-                         (1 if fp8 else 0) + 1)
+                         (1 if fp8 and not fb else 0) + 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = args.cpu_tokens or auto_cpu_tokens(args.workload)
@@ -558,10 +590,14 @@ def main_native(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ("fp16 x fp16 -> f32 (NVFP4 weights dequantised exactly, bf16 activations)"
-                      if nvfp4 else "fp8-e4m3 x fp8-e4m3 -> f32" if fp8 else "bf16 x bf16 -> f32"),
+                      if nvfp4 else
+                      "fp8-e4m3 x fp8-e4m3 -> f32 per 128-wide K group, scaled and summed in f32"
+                      if fb else "fp8-e4m3 x fp8-e4m3 -> f32" if fp8 else "bf16 x bf16 -> f32"),
             "data": "synthetic (seeded torch generator; random-init weights)",
             "config": {"workload": args.workload, "T": T, "H": H, "E": E, "top_k": k, "I": I,
-                       "fp8": fp8, "weights": "nvfp4" if nvfp4 else ("e4m3" if fp8 else "bf16"),
+                       "fp8": fp8,
+                       "weights": ("nvfp4" if nvfp4 else "e4m3, 128x128 tile scales" if fb else
+                                   ("e4m3" if fp8 else "bf16")),
                        "routing": inp["routing"],
                        "active_experts": work["active_experts"],
                        "l2": ("flushed between steps (512 MB write)" if flush is not None else

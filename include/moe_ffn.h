@@ -66,9 +66,19 @@ typedef enum {
 } moe_status;
 
 /* Expert weight format.  MOE_W_NVFP4 weights go through moe_ffn_forward_nvfp4
- * (packed codes plus two scale arrays); the other entry points take BF16 or
- * FP8_E4M3. */
-typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1, MOE_W_NVFP4 = 2 } moe_wdtype;
+ * (packed codes plus two scale arrays); the other entry points take BF16,
+ * FP8_E4M3 (per-output-channel weight scales, per-token activation scales)
+ * or FP8_BLOCK (block-wise FP8: one weight scale per 128 x 128 tile, one
+ * activation scale per token and 128-element group; [SM] support table,
+ * "FP8 block-wise" MoE GEMMs, and the Hopper data-flow figure, "block-wise
+ * FP8 dequant inside GEMM loop").  FP8_BLOCK needs H % 256 == 0,
+ * I % 128 == 0 and H, I <= 8192. */
+typedef enum {
+  MOE_W_BF16 = 0,
+  MOE_W_FP8_E4M3 = 1,
+  MOE_W_NVFP4 = 2,
+  MOE_W_FP8_BLOCK = 3
+} moe_wdtype;
 
 /* Which step of the grouped GEMM moe_grouped_gemm runs. */
 typedef enum {
@@ -142,16 +152,26 @@ size_t moe_ffn_workspace_size(const moe_shape* shape);
  *   w13         [E, 2I, H]           bf16, or e4m3 codes when wdtype is
  *                                    FP8 (rows 0..I-1 gate, I..2I-1 up).
  *   w2          [E, H, I]            bf16 or e4m3 codes.
- *   w13_scale   fp32 [E, 2I] / NULL  per-output-channel dequant scale (FP8).
- *   w2_scale    fp32 [E, H]  / NULL  ditto for w2.
+ *   w13_scale   fp32 [E, 2I] / NULL  per-output-channel dequant scale (FP8);
+ *                                    fp32 [E, 2I/128, H/128] tile scales
+ *                                    (FP8_BLOCK).
+ *   w2_scale    fp32 [E, H]  / NULL  ditto for w2 (FP8_BLOCK: [E, H/128, I/128]).
  *   out         bf16 [T, H]          result.
  *   topk_ids_out int32 [T, top_k] / NULL  the routing decision, descending
  *   topk_w_out  fp32 [T, top_k]  / NULL   weight, ties to the lower index.
  *   workspace   >= moe_ffn_workspace_size(shape) bytes, 256-byte aligned;
  *               must not be used by other work while this call runs.
+ * FP8 (per channel): x_hat is quantised per token, the bf16 intermediate per
+ * row; FC1/FC2 are E4M3 x E4M3 products accumulated in fp32 and scaled by
+ * s_x[r] * s_w[e, n].  FP8_BLOCK: x_hat and the bf16 intermediate are
+ * quantised per row and 128-element group; each 128-wide K group of a
+ * product is accumulated on its own and scaled by s_a[r, g] * s_w[e, n/128, g]
+ * before the groups are added in K order (one persistent launch for FC1 and
+ * FC2 on every batch size).
  * Errors: INVALID_ARG (null/misaligned/both or neither router input),
  * UNSUPPORTED_SHAPE (H or I not a multiple of 64, top_k > 8 or > E,
- * E > 256), WORKSPACE_TOO_SMALL, UNSUPPORTED_DEVICE, CUDA. */
+ * E > 256, the FP8_BLOCK limits above), WORKSPACE_TOO_SMALL,
+ * UNSUPPORTED_DEVICE, CUDA. */
 moe_status moe_ffn_forward(const moe_shape* shape, const void* x, const void* norm_w,
                            const float* router_w, const float* router_logits,
                            const float* router_bias, const void* w13, const void* w2,
@@ -301,8 +321,12 @@ size_t moe_grouped_ffn_workspace_size(const moe_shape* shape);
  * xp [R, H] (+ xp_scale [R] for FP8), act bf16 [R, I], y bf16 [R, H] in
  * (token, slot) order, R = T * top_k).  On the decode engine with bf16
  * weights both GEMMs run in one persistent launch whose FC2 units wait per
- * expert for that expert's FC1 units.  workspace >=
- * moe_grouped_ffn_workspace_size(shape) bytes, 256-byte aligned. */
+ * expert for that expert's FC1 units.  FP8_BLOCK (always one launch): xp
+ * e4m3 [R, H] with xp_scale fp32 [R, H/128] (one scale per row and group,
+ * as moe_quantize_fp8_blocks with block_rows = 1 writes them), act e4m3
+ * [R, I] receives the quantised intermediate (its group scales stay in the
+ * workspace).  workspace >= moe_grouped_ffn_workspace_size(shape) bytes,
+ * 256-byte aligned. */
 moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* xp_scale,
                            const void* w13, const float* w13_scale, const void* w2,
                            const float* w2_scale, const int32_t* offsets, const int32_t* row_src,
@@ -355,6 +379,17 @@ moe_status moe_quantize_fp8_rows(const void* x, int64_t rows, int32_t cols, void
  * w, q 16-byte aligned; sb, sg 4-byte aligned. */
 moe_status moe_quantize_nvfp4(const void* w, int32_t M, int32_t N, int32_t K, uint8_t* q,
                               uint8_t* sb, float* sg, moe_stream_t stream);
+
+/* Block-wise E4M3 quantisation (the FP8_BLOCK format) of x bf16 [N, K]:
+ * tiles of block_rows x 128 elements (block_rows = 128 for weights: pass
+ * N = E * rows per expert, whose row counts are multiples of 128; 1 for
+ * activation rows), each with
+ *   scale[N / block_rows, K / 128] = max|tile| / 448 (1 for a zero tile), fp32;
+ *   q[n, k] = e4m3_satfinite_rne( x[n, k] / scale of its tile ) (IEEE fp32 divide).
+ * q e4m3 [N, K]; K % 128 == 0, N % block_rows == 0; x, q 16-byte aligned,
+ * scale 4-byte aligned. */
+moe_status moe_quantize_fp8_blocks(const void* x, int32_t N, int32_t K, int32_t block_rows,
+                                   uint8_t* q, float* scale, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

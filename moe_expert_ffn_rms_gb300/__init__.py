@@ -28,7 +28,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
                 3: "MOE_ERR_UNSUPPORTED_DEVICE", 4: "MOE_ERR_WORKSPACE_TOO_SMALL",
                 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT"}
-W_BF16, W_FP8_E4M3, W_NVFP4 = 0, 1, 2
+W_BF16, W_FP8_E4M3, W_NVFP4, W_FP8_BLOCK = 0, 1, 2, 3
 GEMM_FC1_RAW, GEMM_FC1_SILU, GEMM_FC2, GEMM_FC2_BF16 = 0, 1, 2, 3
 ENGINE_AUTO, ENGINE_DECODE, ENGINE_PREFILL = 0, 1, 2
 
@@ -84,6 +84,7 @@ _SIGS = {
     "moe_quantize_nvfp4": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P]),
     "moe_grouped_ffn_nvfp4": (ctypes.c_int, [ctypes.POINTER(MoeShape), _P, _P, _P, _P, _P, _P, _P, _P,
                                              _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_quantize_fp8_blocks": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -121,7 +122,8 @@ def _stream(stream):
 
 
 def make_shape(T, H, E, I, top_k, eps=1e-6, fp8=False, engine=ENGINE_AUTO, nvfp4=False) -> MoeShape:
-    wd = W_NVFP4 if nvfp4 else (W_FP8_E4M3 if fp8 else W_BF16)
+    """fp8: False (bf16), True (per-channel E4M3) or "block" (block-wise E4M3)."""
+    wd = W_NVFP4 if nvfp4 else (W_FP8_BLOCK if fp8 == "block" else (W_FP8_E4M3 if fp8 else W_BF16))
     return MoeShape(T, H, E, I, top_k, eps, wd, engine)
 
 
@@ -299,4 +301,14 @@ def moe_quantize_fp8_rows(x, q, scale, stream=None):
     cols = x.shape[-1]
     rows = x.numel() // cols
     _check(lib.moe_quantize_fp8_rows(_ptr(x), rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+    return q, scale
+
+
+def moe_quantize_fp8_blocks(x, q, scale, block_rows, stream=None):
+    """Block-wise E4M3 quantisation of x bf16 [..., K] viewed as [N, K]:
+    q uint8 [N, K], scale fp32 [N / block_rows, K / 128] (block_rows 1 or 128)."""
+    K = x.shape[-1]
+    N = x.numel() // K if x.numel() else 0
+    _check(lib.moe_quantize_fp8_blocks(_ptr(x), N, K, block_rows, _ptr(q), _ptr(scale),
+                                       _stream(stream)))
     return q, scale

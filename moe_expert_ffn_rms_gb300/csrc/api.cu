@@ -102,8 +102,14 @@ moe_status check_shape(const moe_shape* s) {
   MOE_REQ(s->E <= kMaxExperts, MOE_ERR_UNSUPPORTED_SHAPE, "E=%d > %d", s->E, kMaxExperts);
   MOE_REQ(s->top_k <= kMaxTopK && s->top_k <= s->E, MOE_ERR_UNSUPPORTED_SHAPE,
           "top_k=%d must be <= min(E=%d, %d)", s->top_k, s->E, kMaxTopK);
-  MOE_REQ(s->wdtype == MOE_W_BF16 || s->wdtype == MOE_W_FP8_E4M3 || s->wdtype == MOE_W_NVFP4,
+  MOE_REQ(s->wdtype == MOE_W_BF16 || s->wdtype == MOE_W_FP8_E4M3 || s->wdtype == MOE_W_NVFP4 ||
+              s->wdtype == MOE_W_FP8_BLOCK,
           MOE_ERR_INVALID_ARG, "wdtype=%d", s->wdtype);
+  MOE_REQ(s->wdtype != MOE_W_FP8_BLOCK ||
+              (s->H % 256 == 0 && s->I % 128 == 0 && s->H <= 8192 && s->I <= 8192),
+          MOE_ERR_UNSUPPORTED_SHAPE,
+          "block-wise FP8 weights need H=%d a multiple of 256, I=%d a multiple of 128, both <= 8192",
+          s->H, s->I);
   MOE_REQ(s->wdtype != MOE_W_NVFP4 || (s->H % 256 == 0 && s->I % 256 == 0),
           MOE_ERR_UNSUPPORTED_SHAPE, "NVFP4 weights need H=%d and I=%d to be multiples of 256", s->H,
           s->I);
@@ -125,13 +131,16 @@ size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 Ws layout(const moe_shape* s) {
   const size_t T = s->T, H = s->H, E = s->E, I = s->I, k = s->top_k, R = T * k;
-  const bool f8 = s->wdtype == MOE_W_FP8_E4M3;
+  const bool fb = s->wdtype == MOE_W_FP8_BLOCK;
+  const bool f8 = s->wdtype == MOE_W_FP8_E4M3 || fb;
+  // scales per row: one (per-token FP8) or one per 128-element group (block-wise)
+  const size_t hs = fb ? H / 128 : 1, is = fb ? I / 128 : 1;
   Ws w{};
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o += up256(bytes); return at; };
   w.xhat = take(T * H * 2);
   w.xq = take(f8 ? T * H : 0);
-  w.xscale = take(f8 ? T * 4 : 0);
+  w.xscale = take(f8 ? T * hs * 4 : 0);
   w.part = take(router_ws_bytes(s->T, s->H, s->E));
   w.ids = take(R * 4);
   w.tw = take(R * 4);
@@ -143,10 +152,10 @@ Ws layout(const moe_shape* s) {
   // barrier words of the one-launch decode forward
   w.sched = take((2 * E + 3) * 4);
   w.xp = take(R * H * (f8 ? 1 : 2));
-  w.xp_scale = take(f8 ? R * 4 : 0);
+  w.xp_scale = take(f8 ? R * hs * 4 : 0);
   w.act = take(R * I * 2);
   w.actq = take(f8 ? R * I : 0);
-  w.act_scale = take(f8 ? R * 4 : 0);
+  w.act_scale = take(f8 ? R * is * 4 : 0);
   w.y = take(R * H * 2);  // FC2 output in bf16
   w.total = o;
   return w;
@@ -277,6 +286,17 @@ moe_status ffn_impl(const moe_shape* s, int engine, bool fuse, const void* xp,
                     float* act_scale, DevInfo* dev, cudaStream_t st) {
   const bool f8 = s->wdtype == MOE_W_FP8_E4M3;
   const int T = s->T, H = s->H, E = s->E, I = s->I, R = s->T * s->top_k;
+  if (s->wdtype == MOE_W_FP8_BLOCK) {
+    // block-wise FP8: one persistent launch on every batch size; the
+    // intermediate is E4M3 codes (actq) with one scale per 128 columns
+    MOE_CUDA(moe::launch_decode_ffn_fp8b(static_cast<const uint8_t*>(xp), xp_scale,
+                                         static_cast<const uint8_t*>(w13), w13_scale,
+                                         static_cast<const uint8_t*>(w2), w2_scale, actq, act_scale,
+                                         y, offsets, row_src, tw, sched, E, H, I, R, T, dev->sms,
+                                         dev->status, st),
+             "block-wise FP8 FFN launch");
+    return MOE_OK;
+  }
   if (fuse) {
     // one persistent launch (FC2 units wait per expert for FC1)
     cudaError_t e = moe::launch_decode_ffn_fused(f8, xp, xp_scale, w13, w13_scale, w2, w2_scale,
@@ -321,7 +341,8 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
                         moe_stream_t stream, const Nvfp4Scales* nv = nullptr) {
   moe_status rc = check_shape(s);
   if (rc != MOE_OK) return rc;
-  const bool f8 = s->wdtype == MOE_W_FP8_E4M3;
+  const bool fb = s->wdtype == MOE_W_FP8_BLOCK;
+  const bool f8 = s->wdtype == MOE_W_FP8_E4M3 || fb;  // E4M3 activations
   MOE_REQ((nv != nullptr) == (s->wdtype == MOE_W_NVFP4), MOE_ERR_INVALID_ARG,
           "NVFP4 weights (wdtype=2) go through moe_ffn_forward_nvfp4, other formats do not");
   MOE_REQ(!nv || (nv->w13_sb && nv->w13_sg && nv->w2_sb && nv->w2_sg), MOE_ERR_INVALID_ARG,
@@ -376,7 +397,8 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   const bool fuse = fuse_decode(s, engine);
 
   // Small decode batches, opt-in: a1..a8 in one cooperative launch
-  if (!nv && fuse && moe::decode_forward_mega_covers(T, H, E, k, router_logits != nullptr, routed)) {
+  if (!nv && !fb && fuse &&
+      moe::decode_forward_mega_covers(T, H, E, k, router_logits != nullptr, routed)) {
     moe::DecodeForward f{};
     f.x = x;
     f.norm_w = norm_w;
@@ -407,8 +429,13 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
     if (e == cudaSuccess) return MOE_OK;
     if (e != cudaErrorNotSupported) return cuda_fail(e, "decode forward launch");
   }
-  // a1: rms_norm (+ per-token E4M3 quantisation on the FP8 path)
-  MOE_CUDA(moe::launch_rmsnorm(x, norm_w, T, H, s->eps, xhat, xq, xscale, st), "rmsnorm launch");
+  // a1: rms_norm (+ E4M3 quantisation of x_hat: per token on the FP8 path,
+  // per 128-element group on the block-wise FP8 path)
+  if (fb)
+    MOE_CUDA(moe::launch_rmsnorm_q128(x, norm_w, T, H, s->eps, xhat, xq, xscale, st),
+             "rmsnorm launch");
+  else
+    MOE_CUDA(moe::launch_rmsnorm(x, norm_w, T, H, s->eps, xhat, xq, xscale, st), "rmsnorm launch");
   // a2 + a3: router logits, softmax, top-k, renorm
   if (routed) {
     ids = const_cast<int32_t*>(ids_in);
@@ -433,7 +460,7 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
              "NVFP4 FFN launch");
   } else {
     MOE_CUDA(moe::launch_gather_rows(offsets, E, row_src, k, R, f8 ? (const void*)xq : (const void*)xhat,
-                                     xp, H * (f8 ? 1 : 2), xscale, xp_scale, st),
+                                     xp, H * (f8 ? 1 : 2), xscale, xp_scale, st, fb ? H / 128 : 1),
              "gather launch");
     // a5 + a6 + a7: FC1 + silu_and_mul, FC2 + routing weight
     rc = ffn_impl(s, engine, fuse, xp, xp_scale, w13, w13_scale, w2, w2_scale, offsets, row_src, tw,
@@ -559,6 +586,23 @@ moe_status moe_quantize_nvfp4(const void* w, int32_t M, int32_t N, int32_t K, ui
   return MOE_OK;
 }
 
+moe_status moe_quantize_fp8_blocks(const void* x, int32_t N, int32_t K, int32_t block_rows,
+                                   uint8_t* q, float* scale, moe_stream_t stream) {
+  MOE_REQ(x && q && scale, MOE_ERR_INVALID_ARG, "x, q and scale must be non-NULL");
+  MOE_REQ(block_rows == 1 || block_rows == 128, MOE_ERR_INVALID_ARG, "block_rows=%d (1 or 128)",
+          block_rows);
+  MOE_REQ(N >= 0 && K > 0 && K % 128 == 0 && N % block_rows == 0, MOE_ERR_UNSUPPORTED_SHAPE,
+          "N=%d K=%d block_rows=%d (K %% 128 == 0, N %% block_rows == 0)", N, K, block_rows);
+  MOE_REQ(aligned16(x) && aligned16(q) && ((uintptr_t)scale & 3u) == 0, MOE_ERR_INVALID_ARG,
+          "misaligned pointer");
+  DevInfo* d = nullptr;
+  moe_status rc = device_info(&d);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(moe::launch_quantize_fp8_blocks(x, N, K, block_rows, q, scale, (cudaStream_t)stream),
+           "block-wise FP8 quantise");
+  return MOE_OK;
+}
+
 moe_status moe_rmsnorm(const void* x, const void* w, int32_t T, int32_t H, float eps, void* y,
                        void* yq, float* yscale, moe_stream_t stream) {
   MOE_REQ(x && w && y, MOE_ERR_INVALID_ARG, "x, w and y must be non-NULL");
@@ -656,6 +700,8 @@ moe_status moe_grouped_gemm(const moe_shape* shape, int32_t mode, const void* a,
   MOE_REQ(mode >= MOE_GEMM_FC1_RAW && mode <= MOE_GEMM_FC2_BF16, MOE_ERR_INVALID_ARG, "mode=%d", mode);
   MOE_REQ(shape->wdtype != MOE_W_NVFP4, MOE_ERR_INVALID_ARG,
           "NVFP4 weights run through moe_ffn_forward_nvfp4");
+  MOE_REQ(shape->wdtype != MOE_W_FP8_BLOCK, MOE_ERR_INVALID_ARG,
+          "block-wise FP8 weights run through moe_grouped_ffn or the forward");
   MOE_REQ(a && w && offsets && c, MOE_ERR_INVALID_ARG, "a, w, offsets and c must be non-NULL");
   MOE_REQ(aligned16(a) && aligned16(w) && aligned16(c), MOE_ERR_INVALID_ARG, "misaligned pointer");
   const bool f8 = shape->wdtype == MOE_W_FP8_E4M3;
@@ -674,6 +720,7 @@ size_t moe_grouped_ffn_workspace_size(const moe_shape* shape) {
   const size_t R = (size_t)shape->T * shape->top_k;
   size_t n = up256((size_t)(2 * shape->E + 1) * 4);
   if (shape->wdtype == MOE_W_FP8_E4M3) n += up256(R * shape->I) + up256(R * 4);
+  if (shape->wdtype == MOE_W_FP8_BLOCK) n += up256(R * (shape->I / 128) * 4);
   return n;
 }
 
@@ -684,7 +731,8 @@ moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* 
                            size_t workspace_bytes, moe_stream_t stream) {
   moe_status rc = check_shape(shape);
   if (rc != MOE_OK) return rc;
-  const bool f8 = shape->wdtype == MOE_W_FP8_E4M3;
+  const bool fb = shape->wdtype == MOE_W_FP8_BLOCK;
+  const bool f8 = shape->wdtype == MOE_W_FP8_E4M3 || fb;
   MOE_REQ(shape->wdtype != MOE_W_NVFP4, MOE_ERR_INVALID_ARG,
           "NVFP4 weights run through moe_ffn_forward_nvfp4");
   MOE_REQ(xp && w13 && w2 && offsets && row_src && topk_w && act && y && workspace,
@@ -706,6 +754,11 @@ moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* 
   int32_t* sched = at<int32_t>(workspace, 0);
   uint8_t* actq = f8 ? at<uint8_t>(workspace, up256(sched_bytes)) : nullptr;
   float* act_scale = f8 ? at<float>(workspace, up256(sched_bytes) + up256(R * shape->I)) : nullptr;
+  if (fb) {  // the E4M3 intermediate goes to the caller's act, its scales to the workspace
+    actq = static_cast<uint8_t*>(act);
+    act_scale = at<float>(workspace, up256(sched_bytes));
+    MOE_CUDA(cudaMemsetAsync(sched, 0, sched_bytes, st), "scheduler reset");
+  }
   const int engine = pick_engine(shape);
   PdlOff no_pdl(engine == MOE_ENGINE_PREFILL);  // as in the forward
   const bool fuse = fuse_decode(shape, engine);

@@ -90,6 +90,24 @@ cudaError_t launch_decode_ffn_nvfp4(const void* xp, const uint8_t* w13_q, const 
                                     int H, int I, int R_max, int T, int sms, int* status,
                                     cudaStream_t st);
 
+// Block-wise FP8 weights (gemm_fp8b.cu): E4M3 codes with one fp32 scale per
+// 128 x 128 weight tile and per 1 x 128 activation group.  Quantiser
+// (block_rows 1 or 128), rms_norm with group quantisation of x_hat, and the
+// decode FFN (FC1 + silu_and_mul -> E4M3 act with group scales, FC2 + routing
+// weight -> bf16 y rows at row_src) in one persistent launch; `sched` as for
+// launch_decode_ffn_fused.  cudaErrorNotSupported when not covered.
+cudaError_t launch_quantize_fp8_blocks(const void* x, int N, int K, int block_rows, uint8_t* q,
+                                       float* scale, cudaStream_t st);
+cudaError_t launch_rmsnorm_q128(const void* x, const void* w, int T, int H, float eps, void* y,
+                                uint8_t* yq, float* yscale, cudaStream_t st);
+bool fp8b_decode_covers(int H, int I, int E);
+cudaError_t launch_decode_ffn_fp8b(const uint8_t* xp, const float* xp_scale, const uint8_t* w13,
+                                   const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                                   uint8_t* actq, float* act_scale, void* y, const int32_t* offsets,
+                                   const int32_t* row_src, const float* topk_w, int* sched, int E,
+                                   int H, int I, int R_max, int T, int sms, int* status,
+                                   cudaStream_t st);
+
 // Bounded-wait self-test: a kernel that waits on an mbarrier nothing arrives
 // on for at most limit_cycles SM cycles and records MOE_ERR_TIMEOUT.
 cudaError_t launch_wait_selftest(long long limit_cycles, int* status, cudaStream_t st);

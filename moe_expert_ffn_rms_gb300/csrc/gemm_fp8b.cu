@@ -1,0 +1,706 @@
+// Block-wise FP8 expert weights with per-group activation scales (W8A8).
+//
+// Format: E4M3 codes; each 128 x 128 tile of an expert matrix W [N, K] has
+// one fp32 scale s_w (absmax / 448), and each group of 128 consecutive K
+// elements of an activation row has one fp32 scale s_a.  The product is
+//   y[r, n] = sum over K groups g of  s_a[r, g] * s_w[n / 128, g] * (q_a[r, g] . q_w[n, g]),
+// i.e. the scales change every 128 K elements, so they cannot be applied
+// once after the whole dot product as with per-channel scales.
+//
+// Design.  The tensor cores compute each 128-wide K group on its own: the MMA
+// thread writes the group's E4M3 x E4M3 product (fp32, four K = 32 steps of
+// tcgen05 kind::f8f6f4) into a fresh TMEM slot of a four-slot ring, and eight
+// epilogue warps fold each slot into fp32 registers with the group's two
+// scales (one per weight tile, one per token column), then hand the slot
+// back.  The MMA never waits for the fold unless all four slots are full, and
+// the TMA ring behind it keeps streaming weights.
+//
+// A unit is 256 weight rows x up to 64 token rows of one expert: FC1 takes
+// the 128 gate rows and the matching 128 up rows of one 128-column slice of
+// the intermediate (one TMEM lane holds g and u of the same column), FC2 two
+// consecutive 128-row slices of W2.  FC1's epilogue forms a = bf16(silu(g) u)
+// for 128 consecutive intermediate columns, which is exactly one K group of
+// FC2, so it quantises them in place: group absmax over the 128 lanes, one
+// scale per token row, E4M3 codes.  FC2's epilogue multiplies by the routing
+// weight and writes bf16 rows in (token, slot) order.  FC1 and FC2 share one
+// persistent launch with a dynamic unit scheduler; an FC2 unit waits until
+// every FC1 unit of its expert has published its rows.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "engine.h"
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace ptx;
+using namespace tc;
+
+constexpr int kGroup = 128;  // K elements per scale group; rows per weight tile
+
+// ------------------------------------------------------------ quantiser --
+// absmax over 16 lanes (one 128-element group as 16 vectors of 8); every
+// lane of the warp takes part, each half-warp reduces its own group.
+MOE_DEV float half_warp_max(float v) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+MOE_DEV uint2 quant8(const float (&f)[8], float s) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) lo |= (uint32_t)f_to_e4m3(__fdiv_rn(f[i], s)) << (8 * i);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) hi |= (uint32_t)f_to_e4m3(__fdiv_rn(f[4 + i], s)) << (8 * i);
+  return make_uint2(lo, hi);
+}
+
+// block_rows = 1: sixteen (row, group) tiles per CTA, sixteen threads a tile.
+__global__ void __launch_bounds__(256) quant_groups_kernel(const bf16* __restrict__ x, int64_t tiles,
+                                                           int K, uint8_t* __restrict__ q,
+                                                           float* __restrict__ scale) {
+  pdl_trigger();
+  pdl_wait();
+  const int KG = K / kGroup;
+  const int64_t tile = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4);
+  const int sub = threadIdx.x & 15;
+  const bool valid = tile < tiles;
+  const int64_t r = valid ? tile / KG : 0;
+  const int g = valid ? (int)(tile % KG) : 0;
+  const size_t off = (size_t)r * K + (size_t)g * kGroup + sub * 8;
+  float f[8];
+  float amax = 0.f;
+  if (valid) {
+    unpack8_bf16(*reinterpret_cast<const uint4*>(x + off), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  }
+  amax = half_warp_max(amax);
+  const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  if (valid) {
+    *reinterpret_cast<uint2*>(q + off) = quant8(f, s);
+    if (sub == 0) scale[tile] = s;
+  }
+}
+
+// block_rows = 128: one 128 x 128 tile per CTA (64 elements a thread).
+__global__ void __launch_bounds__(256) quant_tiles_kernel(const bf16* __restrict__ x, int K,
+                                                          uint8_t* __restrict__ q,
+                                                          float* __restrict__ scale) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[32];
+  const int g = blockIdx.x, rb = blockIdx.y, KG = K / kGroup;
+  const bf16* base = x + (size_t)rb * kGroup * K + (size_t)g * kGroup;
+  float amax = 0.f;
+  for (int v = threadIdx.x; v < kGroup * 16; v += blockDim.x) {
+    float f[8];
+    unpack8_bf16(*reinterpret_cast<const uint4*>(base + (size_t)(v >> 4) * K + (v & 15) * 8), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  }
+  amax = block_max(amax, red);
+  const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  uint8_t* qb = q + (size_t)rb * kGroup * K + (size_t)g * kGroup;
+  for (int v = threadIdx.x; v < kGroup * 16; v += blockDim.x) {
+    float f[8];
+    unpack8_bf16(*reinterpret_cast<const uint4*>(base + (size_t)(v >> 4) * K + (v & 15) * 8), f);
+    *reinterpret_cast<uint2*>(qb + (size_t)(v >> 4) * K + (v & 15) * 8) = quant8(f, s);
+  }
+  if (threadIdx.x == 0) scale[(size_t)rb * KG + g] = s;
+}
+
+// rms_norm of one token per CTA (the arithmetic of the bf16 path's rms_norm),
+// then E4M3 codes of x_hat with one scale per 128-element group.
+__global__ void __launch_bounds__(512) rmsnorm_q128_kernel(const bf16* __restrict__ x,
+                                                           const bf16* __restrict__ w, int H,
+                                                           float eps, bf16* __restrict__ y,
+                                                           uint8_t* __restrict__ yq,
+                                                           float* __restrict__ ys) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[32];
+  const int t = blockIdx.x;
+  const int nv = H >> 3;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  uint4* yr = reinterpret_cast<uint4*>(y + (size_t)t * H);
+  float ss = 0.f;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float f[8];
+    unpack8_bf16(xr[v], f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+  }
+  ss = block_sum(ss, red);
+  const float r = 1.0f / sqrtf(ss / (float)H + eps);
+  // blockDim.x is a multiple of 16 and nv of 16, so each run of 16 threads
+  // holds one group in every pass
+  for (int v0 = 0; v0 < nv; v0 += blockDim.x) {
+    const int v = v0 + threadIdx.x;
+    const bool valid = v < nv;
+    float h[8];
+    float amax = 0.f;
+    if (valid) {
+      float f[8], g[8];
+      unpack8_bf16(xr[v], f);
+      unpack8_bf16(wr[v], g);
+      uint4 o;
+      o.x = pack2_bf16((f[0] * r) * g[0], (f[1] * r) * g[1]);
+      o.y = pack2_bf16((f[2] * r) * g[2], (f[3] * r) * g[3]);
+      o.z = pack2_bf16((f[4] * r) * g[4], (f[5] * r) * g[5]);
+      o.w = pack2_bf16((f[6] * r) * g[6], (f[7] * r) * g[7]);
+      yr[v] = o;
+      unpack8_bf16(o, h);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
+    }
+    amax = half_warp_max(amax);
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    if (valid) {
+      *reinterpret_cast<uint2*>(yq + (size_t)t * H + (size_t)v * 8) = quant8(h, s);
+      if ((v & 15) == 0) ys[(size_t)t * (H / kGroup) + (v >> 4)] = s;
+    }
+  }
+}
+
+// ------------------------------------------------------- fused FFN kernel --
+constexpr int kThreadsB = 320;      // warp 0 TMA, 1 MMA (+ TMEM owner), 2-9 epilogue
+constexpr int kEpiWarpsB = 8;       // warps 2-5: rows 0-127 of the unit, 6-9: rows 128-255
+constexpr int kHalfBytes = 128 * 128;  // one 128-row x 128-byte E4M3 weight tile
+constexpr int kMaxStagesB = 8;
+constexpr int kBoxRowsB = 16;       // token rows per TMA box
+constexpr int kRingB = 4;           // claimed-unit slots
+constexpr int kMaxChunkB = 64;      // token rows per unit (MMA N)
+constexpr int kSlotsB = 4;          // K-group accumulator slots
+constexpr int kSlotCols = 2 * kMaxChunkB;  // two 128-row halves x up to 64 columns
+constexpr int kTmemColsB = kSlotsB * kSlotCols;
+constexpr int kMaxKG = 64;          // K groups per unit (K <= 8192)
+constexpr int kSmemLimitB = 227 * 1024;
+static_assert(kTmemColsB == 512, "TMEM budget");
+
+struct BJob {
+  const float* w_scale;     // [E, N_w / 128, kg] weight tile scales
+  const float* a_scale;     // [R, kg] activation group scales of the job's input rows
+  const int32_t* row_src;
+  const float* topk_w;      // FC2: routing weight of pair row_src[r]
+  void* out;                // FC1: E4M3 codes [R, I]; FC2: bf16 [R, H], row r at row_src[r]
+  float* out_scale;         // FC1: [R, I / 128] group scales of `out`
+  int N_w;                  // weight rows per expert
+  int n_out;                // output columns
+  int nt;                   // units per (expert, token chunk)
+  int kg;                   // K groups
+};
+
+// Token-row (B) tensor maps per job with box heights 2, 4, 8 and 16 rows.
+struct BMaps {
+  CUtensorMap m[2][4];
+};
+
+struct BParams {
+  const int32_t* offsets;
+  int E, I, R_max;
+  int chunk;                // token rows per unit (a multiple of 16, <= 64)
+  int stages, stage_bytes;  // ring: [W rows 0-127][W rows 128-255][B: chunk rows x 128 B]
+  int* sched;               // [0] unit counter, [1 + e] finished FC1 gate warps of e
+  int* status;
+  BJob job[2];
+};
+
+__global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
+    const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+    const __grid_constant__ BMaps bx, const BParams p) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_up[2][kMaxExperts + 1];
+  __shared__ __align__(8) uint64_t sfull[kMaxStagesB];
+  __shared__ __align__(8) uint64_t sempty[kMaxStagesB];
+  __shared__ __align__(8) uint64_t kfull[kSlotsB];
+  __shared__ __align__(8) uint64_t kempty[kSlotsB];
+  __shared__ __align__(8) uint64_t ufull[kRingB];
+  __shared__ __align__(8) uint64_t uempty[kRingB];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t epi_bar;   // the 256 epilogue threads
+  __shared__ __align__(8) uint64_t gate_bar;  // the 128 threads of rows 0-127
+  __shared__ int s_uring[kRingB];
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  __shared__ __align__(16) float s_as[kMaxKG * kMaxChunkB];  // unit's activation scales [g][col]
+  __shared__ float s_ws[2][kMaxKG];                          // unit's weight scales [half][g]
+  __shared__ int s_rs[kMaxChunkB];                           // FC2: row_src of the unit's rows
+  __shared__ float s_tw[kMaxChunkB];                         // FC2: their routing weights
+  __shared__ float s_xch[128 * 17];                          // FC1: u values, 16 columns a pass
+  __shared__ float s_red[4][16];                             // FC1: per-warp column maxima
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~(uintptr_t)1023);
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sempty[s], 1);  // the MMA commit
+    }
+    for (int q = 0; q < kSlotsB; ++q) {
+      mbar_init(&kfull[q], 1);             // the MMA commit
+      mbar_init(&kempty[q], kEpiWarpsB);   // lane 0 of each epilogue warp
+    }
+    for (int i = 0; i < kRingB; ++i) {
+      mbar_init(&ufull[i], 1);
+      mbar_init(&uempty[i], 1 + kEpiWarpsB);  // MMA thread and epilogue warps
+    }
+    mbar_init(&drain_bar, 1);
+    mbar_init(&epi_bar, 32 * kEpiWarpsB);
+    mbar_init(&gate_bar, 128);
+    s_abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_w0);
+    prefetch_tmap(&tm_w1);
+    for (int jb = 0; jb < 2; ++jb)
+      for (int bi = 0; bi < 4; ++bi) prefetch_tmap(&bx.m[jb][bi]);
+  } else if (warp == 1) {
+    tmem_alloc(&s_tmem, kTmemColsB);
+    tmem_relinquish();
+  }
+  pdl_trigger();
+  pdl_wait();
+  for (int e = threadIdx.x; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
+  __syncthreads();
+  if (threadIdx.x == 0) {  // offsets must be monotone within [0, R_max]
+    int prev = 0;
+    bool bad = false;
+    for (int e = 0; e <= p.E; ++e) {
+      int v = s_off[e];
+      if (v < prev || v > p.R_max || (e == 0 && v != 0)) {
+        bad = true;
+        v = v < prev ? prev : (v > p.R_max ? p.R_max : v);
+        if (e == 0) v = 0;
+      }
+      s_off[e] = v;
+      prev = v;
+    }
+    if (bad && blockIdx.x == 0) flag_status(p.status, MOE_ERR_INVALID_ARG);
+  }
+  __syncthreads();
+  if (warp < 2) {  // warp jb builds job jb's unit prefix
+    const int nt = p.job[warp].nt;
+    int carry = 0;
+    for (int base = 0; base < p.E; base += 32) {
+      const int e = base + lane;
+      const int cnt = (e < p.E) ? s_off[e + 1] - s_off[e] : 0;
+      const int v = ((cnt + p.chunk - 1) / p.chunk) * nt;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e < p.E) s_up[warp][e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_up[warp][p.E] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int U0 = s_up[0][p.E];
+  const int U = U0 + s_up[1][p.E];
+
+  auto decode_unit = [&](int u) -> Unit {
+    if (u >= U0) {
+      Unit un = unit_of(u - U0, s_off, s_up[1], p.E, p.job[1].nt, p.chunk);
+      un.job = 1;
+      return un;
+    }
+    return unit_of(u, s_off, s_up[0], p.E, p.job[0].nt, p.chunk);
+  };
+  auto next_unit = [&](int i) -> int {
+    const int slot = i % kRingB;
+    if (!mbar_wait(&ufull[slot], (uint32_t)((i / kRingB) & 1), &s_abort)) return -2;
+    return s_uring[slot];
+  };
+
+  if (warp == 0) {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
+      const uint64_t pol_x = l2_policy_evict_last();
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t armed = 0, armed_ph = 0;
+      bool ok = true;
+      for (int i = 0; ok; ++i) {
+        const int slot = i % kRingB;
+        if (!mbar_wait(&uempty[slot], (uint32_t)(((i / kRingB) & 1) ^ 1), &s_abort)) {
+          ok = false;
+          break;
+        }
+        int u = atomicAdd(p.sched, 1);
+        if (u >= U) u = -1;
+        s_uring[slot] = u;
+        mbar_arrive(&ufull[slot]);
+        if (u < 0) break;
+        const Unit un = decode_unit(u);
+        const BJob& j = p.job[un.job];
+        if (un.job == 1) {
+          // FC2 of expert e reads its FC1 rows: wait until every FC1 gate
+          // warp of e has published them (FC1 units are all claimed first)
+          const int cnt = s_off[un.e + 1] - s_off[un.e];
+          const int need = ((cnt + p.chunk - 1) / p.chunk) * p.job[0].nt * 4;
+          const int* flag = p.sched + 1 + un.e;
+          const long long t0 = clock64();
+          while (ld_acquire(flag) < need) {
+            if (s_abort || clock64() - t0 > kSpinLimitCycles) {
+              s_abort = 1;
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          fence_proxy_async_global();
+        }
+        // B boxes: the smallest height of 2, 4, 8, 16 rows covering the unit
+        const int bi = un.rows > 8 ? 3 : (un.rows > 4 ? 2 : (un.rows > 2 ? 1 : 0));
+        const int brows = 2 << bi;
+        const int nb = bi == 3 ? (un.rows + kBoxRowsB - 1) / kBoxRowsB : 1;
+        const uint32_t tx = (uint32_t)(2 * kHalfBytes + nb * brows * 128);
+        const CUtensorMap* tw = un.job ? &tm_w1 : &tm_w0;
+        const CUtensorMap* tx_map = &bx.m[un.job][bi];
+        const int wrow = un.e * j.N_w;
+        // FC1: 128 gate rows and the matching 128 up rows; FC2: 256 rows
+        const int r0 = un.job == 0 ? wrow + un.nt * 128 : wrow + un.nt * 256;
+        const int r1 = un.job == 0 ? wrow + p.I + un.nt * 128 : r0 + 128;
+        for (int g = 0; g < j.kg; ++g) {
+          if (!mbar_wait_spin(&sempty[s], ph ^ 1, &s_abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sfull[s], tx);
+          uint8_t* st = ring + (size_t)s * p.stage_bytes;
+          tma_load_2d(st, tw, &sfull[s], g * kGroup, r0, pol_w);
+          tma_load_2d(st + kHalfBytes, tw, &sfull[s], g * kGroup, r1, pol_w);
+          for (int bb = 0; bb < nb; ++bb)
+            tma_load_2d(st + 2 * kHalfBytes + bb * kBoxRowsB * 128, tx_map, &sfull[s], g * kGroup,
+                        un.row0 + bb * kBoxRowsB, pol_x);
+          armed |= 1u << s;
+          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+          if (++s == p.stages) { s = 0; ph ^= 1; }
+        }
+      }
+      if (ok) ok = producer_tail(sempty, p.stages, s, ph, &s_abort);
+      if (!ok) {
+        flag_status(p.status, MOE_ERR_TIMEOUT);
+        drain_armed(sfull, p.stages, armed, armed_ph);
+      }
+    }
+  } else if (warp == 1) {
+    // ====================================================== MMA issuer
+    if (lane == 0) {
+      int s = 0, q = 0;
+      uint32_t ph = 0, qph = 0;
+      bool ok = true, issued = false;
+      for (int i = 0; ok; ++i) {
+        const int u = next_unit(i);
+        if (u == -2) { ok = false; break; }
+        mbar_arrive(&uempty[i % kRingB]);
+        if (u < 0) break;
+        const Unit un = decode_unit(u);
+        const int kg = p.job[un.job].kg;
+        const uint32_t idesc = make_idesc(((un.rows + 15) / 16) * 16, 0u);  // E4M3 A and B
+        for (int g = 0; g < kg; ++g) {
+          if (!mbar_wait_spin(&sfull[s], ph, &s_abort) ||
+              !mbar_wait_spin(&kempty[q], qph ^ 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(ring + (size_t)s * p.stage_bytes);
+          const uint32_t b0 = a0 + 2 * kHalfBytes;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t d = tmem + q * kSlotCols + h * kMaxChunkB;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // four 32-byte K steps: each group starts a fresh sum
+              mma_e4m3(d, sw128_desc(a0 + h * kHalfBytes + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                       kk ? 1u : 0u);
+          }
+          issued = true;
+          mma_commit(&sempty[s]);
+          mma_commit(&kfull[q]);
+          if (++s == p.stages) { s = 0; ph ^= 1; }
+          if (++q == kSlotsB) { q = 0; qph ^= 1; }
+        }
+      }
+      // tail: the epilogues have handed back every slot
+      for (int i = 0; ok && i < kSlotsB; ++i) {
+        ok = mbar_wait(&kempty[q], qph ^ 1, &s_abort);
+        if (++q == kSlotsB) { q = 0; qph ^= 1; }
+      }
+      if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
+      if (issued) {  // all issued MMAs complete before TMEM is released
+        mma_commit(&drain_bar);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&drain_bar, 0) && clock64() - t0 < kSpinLimitCycles) {
+        }
+      }
+    }
+  } else {
+    // ======================================================== epilogue
+    // Warp w (2..9) owns rows l = 32 (w % 4) + lane (its TMEM lane quarter)
+    // of half h = (w - 2) / 4 of the unit's 256 weight rows.
+    const int h = (warp - 2) >> 2;
+    const int qtr = warp & 3;
+    const int l = qtr * 32 + lane;
+    const int et = threadIdx.x - 64;  // 0..255
+    const uint32_t tlane = (uint32_t)(qtr * 32) << 16;
+    int q = 0;
+    uint32_t qph = 0, eph = 0, gph = 0;
+    bool ok = true;
+    auto sync_on = [&](uint64_t* bar, uint32_t& par) -> bool {
+      mbar_arrive(bar);
+      const bool r = mbar_wait(bar, par, &s_abort);
+      par ^= 1;
+      return r;
+    };
+    for (int i = 0; ok; ++i) {
+      const int u = next_unit(i);
+      __syncwarp();
+      if (lane == 0 && u != -2) mbar_arrive(&uempty[i % kRingB]);
+      if (u == -2) { ok = false; break; }
+      if (u < 0) break;
+      const Unit un = decode_unit(u);
+      const BJob& j = p.job[un.job];
+      const int ncols = ((un.rows + 15) / 16) * 16;
+      // stage the unit's scales (and FC2's row_src / routing weights) once
+      // every epilogue thread is done with the previous unit's
+      if (!sync_on(&epi_bar, eph)) { ok = false; break; }
+      if (un.job == 1) {
+        // FC2's activation scales are FC1 output: every thread acquires the
+        // expert's FC1 count itself before reading them (the unit is handed
+        // out before the producer's own wait on that count)
+        const int cnt = s_off[un.e + 1] - s_off[un.e];
+        const int need = ((cnt + p.chunk - 1) / p.chunk) * p.job[0].nt * 4;
+        const int* flag = p.sched + 1 + un.e;
+        const long long t0 = clock64();
+        while (ld_acquire(flag) < need) {
+          if (s_abort || clock64() - t0 > kSpinLimitCycles) {
+            s_abort = 1;
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+      }
+      for (int idx = et; idx < j.kg * ncols; idx += 32 * kEpiWarpsB) {
+        const int g = idx / ncols, c = idx - g * ncols;
+        s_as[g * kMaxChunkB + c] = c < un.rows ? j.a_scale[(size_t)(un.row0 + c) * j.kg + g] : 0.f;
+      }
+      for (int idx = et; idx < 2 * j.kg; idx += 32 * kEpiWarpsB) {
+        const int hh = idx / j.kg, g = idx - hh * j.kg;
+        const int rb = un.job == 0 ? (hh ? p.I / kGroup + un.nt : un.nt) : 2 * un.nt + hh;
+        s_ws[hh][g] = j.w_scale[((size_t)un.e * (j.N_w / kGroup) + rb) * j.kg + g];
+      }
+      if (un.job == 1 && et < un.rows) {
+        const int orow = j.row_src[un.row0 + et];
+        s_rs[et] = orow;
+        s_tw[et] = j.topk_w[orow];
+      }
+      if (!sync_on(&epi_bar, eph)) { ok = false; break; }
+
+      float acc[kMaxChunkB];
+#pragma unroll
+      for (int c = 0; c < kMaxChunkB; ++c) acc[c] = 0.f;
+      for (int g = 0; g < j.kg; ++g) {
+        int wok = 1;
+        if (lane == 0) wok = mbar_wait_spin(&kfull[q], qph, &s_abort);
+        wok = __shfl_sync(0xffffffffu, wok, 0);
+        if (!wok) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t ta = tmem + tlane + q * kSlotCols + h * kMaxChunkB;
+        const float sw = s_ws[h][g];
+        const float4* sa = reinterpret_cast<const float4*>(s_as + g * kMaxChunkB);
+        // two passes of up to 32 columns (bounds the registers held in flight)
+#pragma unroll
+        for (int c32 = 0; c32 < kMaxChunkB; c32 += 32) {
+          if (c32 < ncols) {
+            float v[32];
+            tmem_ld16(ta + c32, &v[0]);
+            if (c32 + 16 < ncols) tmem_ld16(ta + c32 + 16, &v[16]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              if (c32 + c4 * 4 < ncols) {
+                const float4 a = sa[c32 / 4 + c4];
+                float* ac = &acc[c32 + 4 * c4];
+                ac[0] = fmaf(v[4 * c4 + 0], sw * a.x, ac[0]);
+                ac[1] = fmaf(v[4 * c4 + 1], sw * a.y, ac[1]);
+                ac[2] = fmaf(v[4 * c4 + 2], sw * a.z, ac[2]);
+                ac[3] = fmaf(v[4 * c4 + 3], sw * a.w, ac[3]);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&kempty[q]);
+        if (++q == kSlotsB) { q = 0; qph ^= 1; }
+      }
+      if (!ok) break;
+
+      if (un.job == 1) {
+        // FC2: bf16(routing weight x y) at row row_src[r] of the output
+        const int n = un.nt * 256 + h * 128 + l;
+        bf16* out = reinterpret_cast<bf16*>(j.out);
+        if (n < j.n_out) {
+#pragma unroll
+          for (int c = 0; c < kMaxChunkB; ++c)
+            if (c < un.rows)
+              out[(size_t)s_rs[c] * j.n_out + n] = __float2bfloat16_rn(acc[c] * s_tw[c]);
+        }
+      } else {
+        // FC1: half 1 hands u to half 0 through shared memory, 16 columns a
+        // pass; half 0 forms a = bf16(silu(g) u), the absmax of each column
+        // over its 128 lanes (one K group of FC2), and the E4M3 codes.
+        const int n = un.nt * 128 + l;  // intermediate column of this lane
+        uint8_t* outq = reinterpret_cast<uint8_t*>(j.out);
+        const int kg_out = j.n_out / kGroup;
+#pragma unroll
+        for (int c0 = 0; c0 < kMaxChunkB; c0 += 16) {
+          if (c0 < ncols) {
+            if (h == 1) {
+#pragma unroll
+              for (int t = 0; t < 16; ++t) s_xch[l * 17 + t] = acc[c0 + t];
+            }
+            if (!sync_on(&epi_bar, eph)) { ok = false; break; }
+            if (h == 0) {
+              float a[16];
+#pragma unroll
+              for (int t = 0; t < 16; ++t) {
+                a[t] = bf16_round_f(silu_f(acc[c0 + t]) * s_xch[l * 17 + t]);
+                const float m = warp_max(fabsf(a[t]));
+                if (lane == 0) s_red[qtr][t] = m;
+              }
+              if (!sync_on(&gate_bar, gph)) { ok = false; break; }
+#pragma unroll
+              for (int t = 0; t < 16; ++t) {
+                const int c = c0 + t;
+                const float amax =
+                    fmaxf(fmaxf(s_red[0][t], s_red[1][t]), fmaxf(s_red[2][t], s_red[3][t]));
+                const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+                if (c < un.rows) {
+                  const size_t r = (size_t)(un.row0 + c);
+                  outq[r * j.n_out + n] = f_to_e4m3(__fdiv_rn(a[t], s));
+                  if (l == 0) j.out_scale[r * kg_out + un.nt] = s;
+                }
+              }
+            }
+            // s_xch and s_red are free again once every thread is here
+            if (!sync_on(&epi_bar, eph)) { ok = false; break; }
+          }
+        }
+        if (!ok) break;
+        if (h == 0) {
+          // publish this warp's FC1 rows to the TMA readers of FC2
+          fence_proxy_async_global();
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) atomicAdd(p.sched + 1 + un.e, 1);
+        }
+      }
+    }
+    if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemColsB);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host --
+cudaError_t launch_quantize_fp8_blocks(const void* x, int N, int K, int block_rows, uint8_t* q,
+                                       float* scale, cudaStream_t st) {
+  if (N == 0) return cudaSuccess;
+  if (K % kGroup != 0 || (block_rows != 1 && block_rows != kGroup) || N % block_rows != 0)
+    return cudaErrorInvalidValue;
+  if (block_rows == 1) {
+    const int64_t tiles = (int64_t)N * (K / kGroup);
+    return launch_kernel(quant_groups_kernel, dim3((unsigned)((tiles + 15) / 16)), dim3(256), 0, st,
+                         (const bf16*)x, tiles, K, q, scale);
+  }
+  return launch_kernel(quant_tiles_kernel, dim3(K / kGroup, N / kGroup), dim3(256), 0, st,
+                       (const bf16*)x, K, q, scale);
+}
+
+cudaError_t launch_rmsnorm_q128(const void* x, const void* w, int T, int H, float eps, void* y,
+                                uint8_t* yq, float* yscale, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  if (H % kGroup != 0) return cudaErrorInvalidValue;
+  const int nv = H / 8;
+  const int threads = nv >= 512 ? 512 : nv;  // nv is a multiple of 16
+  return launch_kernel(rmsnorm_q128_kernel, dim3(T), dim3(((threads + 31) / 32) * 32), 0, st,
+                       (const bf16*)x, (const bf16*)w, H, eps, (bf16*)y, yq, yscale);
+}
+
+bool fp8b_decode_covers(int H, int I, int E) {
+  return H % 256 == 0 && I % kGroup == 0 && H / kGroup <= kMaxKG && I / kGroup <= kMaxKG &&
+         E <= kMaxExperts;
+}
+
+cudaError_t launch_decode_ffn_fp8b(const uint8_t* xp, const float* xp_scale, const uint8_t* w13,
+                                   const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                                   uint8_t* actq, float* act_scale, void* y, const int32_t* offsets,
+                                   const int32_t* row_src, const float* topk_w, int* sched, int E,
+                                   int H, int I, int R_max, int T, int sms, int* status,
+                                   cudaStream_t st) {
+  if (R_max == 0) return cudaSuccess;
+  if (!fp8b_decode_covers(H, I, E) || !sched) return cudaErrorNotSupported;
+  BParams p{};
+  p.offsets = offsets;
+  p.E = E;
+  p.I = I;
+  p.R_max = R_max;
+  int chunk = T < kMaxChunkB ? T : kMaxChunkB;
+  chunk = ((chunk < 1 ? 1 : chunk) + kBoxRowsB - 1) / kBoxRowsB * kBoxRowsB;
+  p.chunk = chunk;
+  p.sched = sched;
+  p.status = status;
+  p.stage_bytes = 2 * kHalfBytes + chunk * 128;
+  cudaFuncAttributes fa{};
+  cudaError_t e = cudaFuncGetAttributes(&fa, moe_tc_fp8b_kernel);
+  if (e != cudaSuccess) return e;
+  int stages = (int)((kSmemLimitB - (int)fa.sharedSizeBytes - 1024) / p.stage_bytes);
+  if (stages > kMaxStagesB) stages = kMaxStagesB;
+  if (stages < 2) return cudaErrorNotSupported;
+  p.stages = stages;
+  const size_t smem = 1024 + (size_t)stages * p.stage_bytes;
+  // job 0: FC1 + silu_and_mul -> E4M3 act [R, I] + group scales [R, I/128];
+  // job 1: FC2 + routing weight -> bf16 rows at row_src
+  p.job[0] = BJob{w13_scale, xp_scale, row_src, nullptr, actq, act_scale, 2 * I, I, I / kGroup,
+                  H / kGroup};
+  p.job[1] = BJob{w2_scale, act_scale, row_src, topk_w, y, nullptr, H, H, H / 256, I / kGroup};
+  CUtensorMap m[2];
+  BMaps bx;
+  for (int bi = 0; bi < 4; ++bi)
+    if (!tc::encode_map(&bx.m[0][bi], xp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, R_max, H, kGroup, 2 << bi,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tc::encode_map(&bx.m[1][bi], actq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, R_max, I, kGroup,
+                        2 << bi, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorNotSupported;
+  if (!tc::encode_map(&m[0], w13, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (int64_t)E * 2 * I, H, kGroup,
+                      kGroup, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::encode_map(&m[1], w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (int64_t)E * H, I, kGroup, kGroup,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorNotSupported;
+  e = cudaFuncSetAttribute(moe_tc_fp8b_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(moe_tc_fp8b_kernel, dim3(sms), dim3(kThreadsB), smem, st, m[0], m[1], bx, p);
+}
+
+}  // namespace moe

@@ -44,7 +44,8 @@ cudaError_t launch_permute_any(const int32_t* ids, int T, int E, int k, int32_t*
                                int nzero = 0);
 cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* row_src, int k,
                                int R_max, const void* src, void* dst, int row_bytes,
-                               const float* sscale, float* dscale, cudaStream_t st);
+                               const float* sscale, float* dscale, cudaStream_t st,
+                               int scols = 1);  // fp32 scales per row gathered with it
 cudaError_t launch_silu_and_mul(const void* h, int R, int I, void* a, cudaStream_t st);
 cudaError_t launch_combine(const void* y, bool y_bf16, bool pair_order,
                            const int32_t* row_of_pair, int T, int k, int H, void* out,

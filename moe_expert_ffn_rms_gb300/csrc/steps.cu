@@ -647,7 +647,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restr
                                                           const uint4* __restrict__ src,
                                                           uint4* __restrict__ dst, int row_vec,
                                                           const float* __restrict__ sscale,
-                                                          float* __restrict__ dscale) {
+                                                          float* __restrict__ dscale, int scols) {
   pdl_trigger();
   pdl_wait();
   const int R = min(offsets[E], R_max);
@@ -665,18 +665,19 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restr
       d[v + 96] = e4;
     }
     for (; v < row_vec; v += 32) d[v] = s[v];
-    if (dscale && lane == 0) dscale[r] = sscale[t];
+    if (dscale)
+      for (int c = lane; c < scols; c += 32) dscale[(size_t)r * scols + c] = sscale[(size_t)t * scols + c];
   }
 }
 
 cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* row_src, int k,
                                int R_max, const void* src, void* dst, int row_bytes,
-                               const float* sscale, float* dscale, cudaStream_t st) {
+                               const float* sscale, float* dscale, cudaStream_t st, int scols) {
   if (R_max == 0) return cudaSuccess;
   int blocks = (R_max + 7) / 8;
   if (blocks > 152 * 8) blocks = 152 * 8;
   return launch_kernel(gather_rows_kernel, dim3(blocks), dim3(256), 0, st, offsets, E, row_src, k,
-                       R_max, (const uint4*)src, (uint4*)dst, row_bytes / 16, sscale, dscale);
+                       R_max, (const uint4*)src, (uint4*)dst, row_bytes / 16, sscale, dscale, scols);
 }
 
 // ================================================================ silu_and_mul

@@ -138,6 +138,24 @@ def test_step_entry_points_reject_bad_arguments_on_host(M):
     assert M.lib.moe_quantize_nvfp4(fake, 2, 4, 24, fake, fake, fake, None) == 2   # K % 16
     assert M.lib.moe_grouped_gemm(ctypes.byref(nv), 1, fake, None, fake, None, fake, None, None,
                                   fake, None) == 1
+    # block-wise FP8: H % 256, I % 128, tiles of 1 or 128 rows by 128 columns
+    fb_bad = M.make_shape(4, 384, 8, 256, 2, fp8="block")
+    assert M.lib.moe_ffn_workspace_size(ctypes.byref(fb_bad)) == 0
+    fb_bad_i = M.make_shape(4, 256, 8, 192, 2, fp8="block")
+    assert M.lib.moe_ffn_workspace_size(ctypes.byref(fb_bad_i)) == 0
+    fb = M.make_shape(4, 512, 8, 384, 2, fp8="block")
+    assert fb.wdtype == M.W_FP8_BLOCK == 3
+    n_fb = M.moe_ffn_workspace_size(fb)
+    assert n_fb >= 4 * 512 * 2 + 4 * 512 + 4 * 4 * 4 + 8 * 512 + 8 * 4 * 4 + 8 * 384 + 8 * 3 * 4
+    assert M.lib.moe_ffn_forward(ctypes.byref(fb), fake, fake, fake, None, None, fake, fake, None,
+                                 None, fake, None, None, fake, 1 << 40, None) == 1  # scales missing
+    assert M.lib.moe_grouped_gemm(ctypes.byref(fb), 1, fake, fake, fake, fake, fake, None, None,
+                                  fake, None) == 1
+    assert M.lib.moe_grouped_ffn_workspace_size(ctypes.byref(fb)) >= 8 * 3 * 4
+    assert M.lib.moe_quantize_fp8_blocks(fake, 256, 200, 128, fake, fake, None) == 2  # K % 128
+    assert M.lib.moe_quantize_fp8_blocks(fake, 200, 256, 128, fake, fake, None) == 2  # N % 128
+    assert M.lib.moe_quantize_fp8_blocks(fake, 4, 256, 64, fake, fake, None) == 1   # block_rows
+    assert M.lib.moe_quantize_fp8_blocks(None, 4, 256, 1, fake, fake, None) == 1
     assert M.lib.moe_route_workspace_size(4, 256, 8) > 0
     assert M.lib.moe_route_workspace_size(4, 250, 8) == 0
 

@@ -49,7 +49,7 @@ class Config:
     name: str
     shape: Shape
     routing: str          # "learned" | "balanced" | "zipf"
-    fp8: bool
+    fp8: bool | str       # False, True (per-channel E4M3) or "block" (128 x 128 tiles)
     seed: int
     eps: float = 1e-6
     description: str = ""
@@ -76,6 +76,10 @@ CONFIGS = {
         "c6_decode_nvfp4", Shape(T=16, H=4096, E=64, k=8, I=1536), "balanced", False, 5,
         description="decode with NVFP4 expert weights (E2M1 codes, E4M3 block scales of 16, "
                     "fp32 matrix scales) and bf16 activations", nvfp4=True),
+    "c7_decode_fp8_block": Config(
+        "c7_decode_fp8_block", Shape(T=16, H=4096, E=64, k=8, I=1536), "balanced", "block", 6,
+        description="decode with block-wise FP8 (E4M3, one scale per 128 x 128 weight tile and "
+                    "per 1 x 128 activation group)"),
 }
 
 CONFIG_ORDER = ["c1_tiny", "c2_decode_balanced", "c3_decode_skewed", "c4_decode_fp8", "c5_prefill"]
