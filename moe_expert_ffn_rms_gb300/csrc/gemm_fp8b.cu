@@ -9,16 +9,16 @@
 //
 // Design.  The tensor cores compute each 128-wide K group on its own: the MMA
 // thread writes the group's E4M3 x E4M3 product (fp32, four K = 32 steps of
-// tcgen05 kind::f8f6f4) into a fresh TMEM slot of a four-slot ring, and eight
+// tcgen05 kind::f8f6f4) into a fresh TMEM slot of a ring of up to 16, and four
 // epilogue warps fold each slot into fp32 registers with the group's two
 // scales (one per weight tile, one per token column), then hand the slot
-// back.  The MMA never waits for the fold unless all four slots are full, and
-// the TMA ring behind it keeps streaming weights.
+// back.  The MMA never waits for the fold unless every slot is full, and the
+// TMA ring behind it keeps streaming weights.
 //
 // A unit is 256 weight rows x up to 64 token rows of one expert: FC1 takes
 // the 128 gate rows and the matching 128 up rows of one 128-column slice of
-// the intermediate (one TMEM lane holds g and u of the same column), FC2 two
-// consecutive 128-row slices of W2.  FC1's epilogue forms a = bf16(silu(g) u)
+// the intermediate (one TMEM lane, and so one epilogue thread, holds g and u
+// of the same column), FC2 two consecutive 128-row slices of W2.  FC1's epilogue forms a = bf16(silu(g) u)
 // for 128 consecutive intermediate columns, which is exactly one K group of
 // FC2, so it quantises them in place: group absmax over the 128 lanes, one
 // scale per token row, E4M3 codes.  FC2's epilogue multiplies by the routing
@@ -170,19 +170,21 @@ __global__ void __launch_bounds__(512) rmsnorm_q128_kernel(const bf16* __restric
 }
 
 // ------------------------------------------------------- fused FFN kernel --
-constexpr int kThreadsB = 320;      // warp 0 TMA, 1 MMA (+ TMEM owner), 2-9 epilogue
-constexpr int kEpiWarpsB = 8;       // warps 2-5: rows 0-127 of the unit, 6-9: rows 128-255
+constexpr int kThreadsB = 224;      // warp 0 TMA, 1 MMA (+ TMEM owner), 2-5 epilogue, 6 publisher
+constexpr int kEpiWarpsB = 4;       // one per TMEM lane quarter, both 128-row halves
 constexpr int kHalfBytes = 128 * 128;  // one 128-row x 128-byte E4M3 weight tile
 constexpr int kMaxStagesB = 8;
 constexpr int kBoxRowsB = 16;       // token rows per TMA box
 constexpr int kRingB = 4;           // claimed-unit slots
 constexpr int kMaxChunkB = 64;      // token rows per unit (MMA N)
-constexpr int kSlotsB = 4;          // K-group accumulator slots
-constexpr int kSlotCols = 2 * kMaxChunkB;  // two 128-row halves x up to 64 columns
-constexpr int kTmemColsB = kSlotsB * kSlotCols;
+// K-group accumulator slots: 2 x chunk TMEM columns each (two 128-row
+// halves), as many as fit in 512 columns, at most 16: 16 slots at chunk 16,
+// 4 at chunk 64.  The slots are the slack that lets the MMA (and behind it
+// the TMA ring) run on while the epilogue finishes a unit.
+constexpr int kMaxSlotsB = 16;
+constexpr int kTmemColsB = 512;
 constexpr int kMaxKG = 64;          // K groups per unit (K <= 8192)
 constexpr int kSmemLimitB = 227 * 1024;
-static_assert(kTmemColsB == 512, "TMEM budget");
 
 struct BJob {
   const float* w_scale;     // [E, N_w / 128, kg] weight tile scales
@@ -207,7 +209,9 @@ struct BParams {
   int E, I, R_max;
   int chunk;                // token rows per unit (a multiple of 16, <= 64)
   int stages, stage_bytes;  // ring: [W rows 0-127][W rows 128-255][B: chunk rows x 128 B]
-  int* sched;               // [0] unit counter, [1 + e] finished FC1 gate warps of e
+  int slots, slot_cols;     // accumulator ring in TMEM
+  // after the ring: the unit's activation scales [kg][chunk]
+  int* sched;               // [0] unit counter, [1 + e] finished FC1 units of e
   int* status;
   BJob job[2];
 };
@@ -220,43 +224,44 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
   __shared__ int s_up[2][kMaxExperts + 1];
   __shared__ __align__(8) uint64_t sfull[kMaxStagesB];
   __shared__ __align__(8) uint64_t sempty[kMaxStagesB];
-  __shared__ __align__(8) uint64_t kfull[kSlotsB];
-  __shared__ __align__(8) uint64_t kempty[kSlotsB];
+  __shared__ __align__(8) uint64_t kfull[kMaxSlotsB];
+  __shared__ __align__(8) uint64_t kempty[kMaxSlotsB];
   __shared__ __align__(8) uint64_t ufull[kRingB];
   __shared__ __align__(8) uint64_t uempty[kRingB];
   __shared__ __align__(8) uint64_t drain_bar;
-  __shared__ __align__(8) uint64_t epi_bar;   // the 256 epilogue threads
-  __shared__ __align__(8) uint64_t gate_bar;  // the 128 threads of rows 0-127
+  __shared__ __align__(8) uint64_t epi_bar;   // the 128 epilogue threads
+  __shared__ __align__(8) uint64_t pub_bar;   // FC1 unit written (128 epilogue threads)
+  __shared__ __align__(8) uint64_t pub_free;  // the publisher is done with the previous one
   __shared__ int s_uring[kRingB];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ __align__(16) float s_as[kMaxKG * kMaxChunkB];  // unit's activation scales [g][col]
   __shared__ float s_ws[2][kMaxKG];                          // unit's weight scales [half][g]
   __shared__ int s_rs[kMaxChunkB];                           // FC2: row_src of the unit's rows
   __shared__ float s_tw[kMaxChunkB];                         // FC2: their routing weights
-  __shared__ float s_xch[128 * 17];                          // FC1: u values, 16 columns a pass
-  __shared__ float s_red[4][16];                             // FC1: per-warp column maxima
+  __shared__ float s_red[2][4][16];                          // FC1: per-warp token maxima
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~(uintptr_t)1023);
+  float* s_as = reinterpret_cast<float*>(ring + (size_t)p.stages * p.stage_bytes);
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&sfull[s], 1);
       mbar_init(&sempty[s], 1);  // the MMA commit
     }
-    for (int q = 0; q < kSlotsB; ++q) {
+    for (int q = 0; q < p.slots; ++q) {
       mbar_init(&kfull[q], 1);             // the MMA commit
       mbar_init(&kempty[q], kEpiWarpsB);   // lane 0 of each epilogue warp
     }
     for (int i = 0; i < kRingB; ++i) {
       mbar_init(&ufull[i], 1);
-      mbar_init(&uempty[i], 1 + kEpiWarpsB);  // MMA thread and epilogue warps
+      mbar_init(&uempty[i], 2 + kEpiWarpsB);  // MMA thread, epilogue warps, publisher
     }
     mbar_init(&drain_bar, 1);
     mbar_init(&epi_bar, 32 * kEpiWarpsB);
-    mbar_init(&gate_bar, 128);
+    mbar_init(&pub_bar, 32 * kEpiWarpsB);
+    mbar_init(&pub_free, 1);
     s_abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_w0);
@@ -349,10 +354,10 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
         const Unit un = decode_unit(u);
         const BJob& j = p.job[un.job];
         if (un.job == 1) {
-          // FC2 of expert e reads its FC1 rows: wait until every FC1 gate
-          // warp of e has published them (FC1 units are all claimed first)
+          // FC2 of expert e reads its FC1 rows: wait until every FC1 unit of
+          // e has been published (FC1 units are all claimed first)
           const int cnt = s_off[un.e + 1] - s_off[un.e];
-          const int need = ((cnt + p.chunk - 1) / p.chunk) * p.job[0].nt * 4;
+          const int need = ((cnt + p.chunk - 1) / p.chunk) * p.job[0].nt;
           const int* flag = p.sched + 1 + un.e;
           const long long t0 = clock64();
           while (ld_acquire(flag) < need) {
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
           const uint32_t b0 = a0 + 2 * kHalfBytes;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint32_t d = tmem + q * kSlotCols + h * kMaxChunkB;
+            const uint32_t d = tmem + q * p.slot_cols + h * p.chunk;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)  // four 32-byte K steps: each group starts a fresh sum
               mma_e4m3(d, sw128_desc(a0 + h * kHalfBytes + kk * 32), sw128_desc(b0 + kk * 32), idesc,
@@ -431,13 +436,13 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
           mma_commit(&sempty[s]);
           mma_commit(&kfull[q]);
           if (++s == p.stages) { s = 0; ph ^= 1; }
-          if (++q == kSlotsB) { q = 0; qph ^= 1; }
+          if (++q == p.slots) { q = 0; qph ^= 1; }
         }
       }
       // tail: the epilogues have handed back every slot
-      for (int i = 0; ok && i < kSlotsB; ++i) {
+      for (int i = 0; ok && i < p.slots; ++i) {
         ok = mbar_wait(&kempty[q], qph ^ 1, &s_abort);
-        if (++q == kSlotsB) { q = 0; qph ^= 1; }
+        if (++q == p.slots) { q = 0; qph ^= 1; }
       }
       if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
       if (issued) {  // all issued MMAs complete before TMEM is released
@@ -447,22 +452,23 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
         }
       }
     }
-  } else {
+  } else if (warp < 2 + kEpiWarpsB) {
     // ======================================================== epilogue
-    // Warp w (2..9) owns rows l = 32 (w % 4) + lane (its TMEM lane quarter)
-    // of half h = (w - 2) / 4 of the unit's 256 weight rows.
-    const int h = (warp - 2) >> 2;
+    // Warp w (2..5) owns rows l = 32 (w % 4) + lane (its TMEM lane quarter)
+    // of both 128-row halves of the unit: FC1 gate and up row of one
+    // intermediate column, or two W2 rows 128 apart.
     const int qtr = warp & 3;
     const int l = qtr * 32 + lane;
-    const int et = threadIdx.x - 64;  // 0..255
+    const int et = threadIdx.x - 64;  // 0..127
     const uint32_t tlane = (uint32_t)(qtr * 32) << 16;
     int q = 0;
-    uint32_t qph = 0, eph = 0, gph = 0;
+    uint32_t qph = 0, eph = 0;
+    uint32_t nf = 0;  // FC1 units handed to the publisher
     bool ok = true;
-    auto sync_on = [&](uint64_t* bar, uint32_t& par) -> bool {
-      mbar_arrive(bar);
-      const bool r = mbar_wait(bar, par, &s_abort);
-      par ^= 1;
+    auto epi_sync = [&]() -> bool {
+      mbar_arrive(&epi_bar);
+      const bool r = mbar_wait(&epi_bar, eph, &s_abort);
+      eph ^= 1;
       return r;
     };
     for (int i = 0; ok; ++i) {
@@ -476,13 +482,13 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
       const int ncols = ((un.rows + 15) / 16) * 16;
       // stage the unit's scales (and FC2's row_src / routing weights) once
       // every epilogue thread is done with the previous unit's
-      if (!sync_on(&epi_bar, eph)) { ok = false; break; }
+      if (!epi_sync()) { ok = false; break; }
       if (un.job == 1) {
         // FC2's activation scales are FC1 output: every thread acquires the
         // expert's FC1 count itself before reading them (the unit is handed
         // out before the producer's own wait on that count)
         const int cnt = s_off[un.e + 1] - s_off[un.e];
-        const int need = ((cnt + p.chunk - 1) / p.chunk) * p.job[0].nt * 4;
+        const int need = ((cnt + p.chunk - 1) / p.chunk) * p.job[0].nt;
         const int* flag = p.sched + 1 + un.e;
         const long long t0 = clock64();
         while (ld_acquire(flag) < need) {
@@ -496,7 +502,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
       }
       for (int idx = et; idx < j.kg * ncols; idx += 32 * kEpiWarpsB) {
         const int g = idx / ncols, c = idx - g * ncols;
-        s_as[g * kMaxChunkB + c] = c < un.rows ? j.a_scale[(size_t)(un.row0 + c) * j.kg + g] : 0.f;
+        s_as[g * p.chunk + c] = c < un.rows ? j.a_scale[(size_t)(un.row0 + c) * j.kg + g] : 0.f;
       }
       for (int idx = et; idx < 2 * j.kg; idx += 32 * kEpiWarpsB) {
         const int hh = idx / j.kg, g = idx - hh * j.kg;
@@ -508,37 +514,43 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
         s_rs[et] = orow;
         s_tw[et] = j.topk_w[orow];
       }
-      if (!sync_on(&epi_bar, eph)) { ok = false; break; }
+      if (!epi_sync()) { ok = false; break; }
 
-      float acc[kMaxChunkB];
+      float acc0[kMaxChunkB], acc1[kMaxChunkB];  // rows l and 128 + l of the unit
 #pragma unroll
-      for (int c = 0; c < kMaxChunkB; ++c) acc[c] = 0.f;
+      for (int c = 0; c < kMaxChunkB; ++c) {
+        acc0[c] = 0.f;
+        acc1[c] = 0.f;
+      }
       for (int g = 0; g < j.kg; ++g) {
+        // a suspending wait: the epilogue has slack (the slot ring), while a
+        // polling loop here would take issue slots from the TMA and MMA
+        // threads that share the SM's sub-partitions
         int wok = 1;
-        if (lane == 0) wok = mbar_wait_spin(&kfull[q], qph, &s_abort);
+        if (lane == 0) wok = mbar_wait(&kfull[q], qph, &s_abort);
         wok = __shfl_sync(0xffffffffu, wok, 0);
         if (!wok) { ok = false; break; }
         tc_fence_after();
-        const uint32_t ta = tmem + tlane + q * kSlotCols + h * kMaxChunkB;
-        const float sw = s_ws[h][g];
-        const float4* sa = reinterpret_cast<const float4*>(s_as + g * kMaxChunkB);
-        // two passes of up to 32 columns (bounds the registers held in flight)
+        const uint32_t ta = tmem + tlane + q * p.slot_cols;
+        const float sw0 = s_ws[0][g], sw1 = s_ws[1][g];
+        const float4* sa = reinterpret_cast<const float4*>(s_as + g * p.chunk);
+        // passes of up to 16 columns of both halves
 #pragma unroll
-        for (int c32 = 0; c32 < kMaxChunkB; c32 += 32) {
-          if (c32 < ncols) {
-            float v[32];
-            tmem_ld16(ta + c32, &v[0]);
-            if (c32 + 16 < ncols) tmem_ld16(ta + c32 + 16, &v[16]);
+        for (int c16 = 0; c16 < kMaxChunkB; c16 += 16) {
+          if (c16 < ncols) {
+            float v0[16], v1[16];
+            tmem_ld16(ta + c16, v0);
+            tmem_ld16(ta + p.chunk + c16, v1);
             tmem_ld_wait();
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              if (c32 + c4 * 4 < ncols) {
-                const float4 a = sa[c32 / 4 + c4];
-                float* ac = &acc[c32 + 4 * c4];
-                ac[0] = fmaf(v[4 * c4 + 0], sw * a.x, ac[0]);
-                ac[1] = fmaf(v[4 * c4 + 1], sw * a.y, ac[1]);
-                ac[2] = fmaf(v[4 * c4 + 2], sw * a.z, ac[2]);
-                ac[3] = fmaf(v[4 * c4 + 3], sw * a.w, ac[3]);
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const float4 a = sa[c16 / 4 + c4];
+              const float as[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int c = c16 + 4 * c4 + t;
+                acc0[c] = fmaf(v0[4 * c4 + t], sw0 * as[t], acc0[c]);
+                acc1[c] = fmaf(v1[4 * c4 + t], sw1 * as[t], acc1[c]);
               }
             }
           }
@@ -546,72 +558,96 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&kempty[q]);
-        if (++q == kSlotsB) { q = 0; qph ^= 1; }
+        if (++q == p.slots) { q = 0; qph ^= 1; }
       }
       if (!ok) break;
 
       if (un.job == 1) {
         // FC2: bf16(routing weight x y) at row row_src[r] of the output
-        const int n = un.nt * 256 + h * 128 + l;
+        const int n = un.nt * 256 + l;
         bf16* out = reinterpret_cast<bf16*>(j.out);
-        if (n < j.n_out) {
 #pragma unroll
-          for (int c = 0; c < kMaxChunkB; ++c)
-            if (c < un.rows)
-              out[(size_t)s_rs[c] * j.n_out + n] = __float2bfloat16_rn(acc[c] * s_tw[c]);
-        }
+        for (int c = 0; c < kMaxChunkB; ++c)
+          if (c < un.rows) {
+            bf16* o = out + (size_t)s_rs[c] * j.n_out + n;
+            o[0] = __float2bfloat16_rn(acc0[c] * s_tw[c]);
+            o[128] = __float2bfloat16_rn(acc1[c] * s_tw[c]);
+          }
       } else {
-        // FC1: half 1 hands u to half 0 through shared memory, 16 columns a
-        // pass; half 0 forms a = bf16(silu(g) u), the absmax of each column
-        // over its 128 lanes (one K group of FC2), and the E4M3 codes.
-        const int n = un.nt * 128 + l;  // intermediate column of this lane
+        // FC1: a = bf16(silu(g) u) of intermediate column n for each token,
+        // 16 tokens a pass; each token's absmax over the unit's 128 columns
+        // (one K group of FC2) from a warp reduction and four per-warp
+        // maxima (double-buffered, so one barrier a pass); then the E4M3
+        // codes and the group scale.
+        const int n = un.nt * 128 + l;
         uint8_t* outq = reinterpret_cast<uint8_t*>(j.out);
         const int kg_out = j.n_out / kGroup;
 #pragma unroll
         for (int c0 = 0; c0 < kMaxChunkB; c0 += 16) {
           if (c0 < ncols) {
-            if (h == 1) {
+            float (*red)[16] = s_red[(c0 / 16) & 1];
+            float a[16];
 #pragma unroll
-              for (int t = 0; t < 16; ++t) s_xch[l * 17 + t] = acc[c0 + t];
+            for (int t = 0; t < 16; ++t) {
+              const float gt = acc0[c0 + t];
+              a[t] = bf16_round_f(__fdividef(gt, 1.0f + __expf(-gt)) * acc1[c0 + t]);
+              // |a| >= 0 orders like its bit pattern
+              const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(a[t])));
+              if (lane == 0) red[qtr][t] = __uint_as_float(m);
             }
-            if (!sync_on(&epi_bar, eph)) { ok = false; break; }
-            if (h == 0) {
-              float a[16];
+            if (!epi_sync()) { ok = false; break; }
 #pragma unroll
-              for (int t = 0; t < 16; ++t) {
-                a[t] = bf16_round_f(silu_f(acc[c0 + t]) * s_xch[l * 17 + t]);
-                const float m = warp_max(fabsf(a[t]));
-                if (lane == 0) s_red[qtr][t] = m;
-              }
-              if (!sync_on(&gate_bar, gph)) { ok = false; break; }
-#pragma unroll
-              for (int t = 0; t < 16; ++t) {
-                const int c = c0 + t;
-                const float amax =
-                    fmaxf(fmaxf(s_red[0][t], s_red[1][t]), fmaxf(s_red[2][t], s_red[3][t]));
-                const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-                if (c < un.rows) {
-                  const size_t r = (size_t)(un.row0 + c);
-                  outq[r * j.n_out + n] = f_to_e4m3(__fdiv_rn(a[t], s));
-                  if (l == 0) j.out_scale[r * kg_out + un.nt] = s;
-                }
+            for (int t = 0; t < 16; ++t) {
+              const int c = c0 + t;
+              const float amax = fmaxf(fmaxf(red[0][t], red[1][t]), fmaxf(red[2][t], red[3][t]));
+              const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+              if (c < un.rows) {
+                const size_t r = (size_t)(un.row0 + c);
+                outq[r * j.n_out + n] = f_to_e4m3(a[t] * __frcp_rn(s));
+                if (l == 0) j.out_scale[r * kg_out + un.nt] = s;
               }
             }
-            // s_xch and s_red are free again once every thread is here
-            if (!sync_on(&epi_bar, eph)) { ok = false; break; }
           }
         }
         if (!ok) break;
-        if (h == 0) {
-          // publish this warp's FC1 rows to the TMA readers of FC2
-          fence_proxy_async_global();
-          __threadfence();
-          __syncwarp();
-          if (lane == 0) atomicAdd(p.sched + 1 + un.e, 1);
-        }
+        // make this thread's rows visible to the async proxy (FC2's TMA
+        // loads) and hand the unit to the publisher, once it has taken the
+        // previous one (so that pub_bar never runs two phases ahead)
+        fence_proxy_async_global();
+        if (nf > 0 && !mbar_wait(&pub_free, (nf - 1) & 1, &s_abort)) { ok = false; break; }
+        mbar_arrive(&pub_bar);
+        ++nf;
       }
     }
     if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
+  } else if (warp == 6) {
+    // ====================================================== publisher
+    // Per FC1 unit: once its 128 epilogue threads have arrived, a gpu-scope
+    // fence (cumulative over the writes ordered before the arrivals) and the
+    // count FC2's readers acquire.  Off the epilogue's path, which goes on
+    // with the next unit.
+    uint32_t pph = 0;
+    bool ok = true;
+    for (int i = 0; ok; ++i) {
+      const int u = next_unit(i);
+      __syncwarp();
+      if (lane == 0 && u != -2) mbar_arrive(&uempty[i % kRingB]);
+      if (u == -2) { ok = false; break; }
+      if (u < 0) break;
+      const Unit un = decode_unit(u);
+      if (un.job != 0) continue;
+      if (lane == 0) {
+        ok = mbar_wait(&pub_bar, pph, &s_abort);
+        if (ok) {
+          __threadfence();
+          atomicAdd(p.sched + 1 + un.e, 1);
+          mbar_arrive(&pub_free);
+        }
+      }
+      pph ^= 1;
+      ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+    }
+    if (!ok && lane == 0) flag_status(p.status, MOE_ERR_TIMEOUT);
   }
 
   // ---- teardown
@@ -672,14 +708,18 @@ cudaError_t launch_decode_ffn_fp8b(const uint8_t* xp, const float* xp_scale, con
   p.sched = sched;
   p.status = status;
   p.stage_bytes = 2 * kHalfBytes + chunk * 128;
+  p.slot_cols = 2 * chunk;
+  p.slots = kTmemColsB / p.slot_cols < kMaxSlotsB ? kTmemColsB / p.slot_cols : kMaxSlotsB;
+  const int kg_max = (H > I ? H : I) / kGroup;
+  const int scratch = kg_max * chunk * 4;
   cudaFuncAttributes fa{};
   cudaError_t e = cudaFuncGetAttributes(&fa, moe_tc_fp8b_kernel);
   if (e != cudaSuccess) return e;
-  int stages = (int)((kSmemLimitB - (int)fa.sharedSizeBytes - 1024) / p.stage_bytes);
+  int stages = (int)((kSmemLimitB - (int)fa.sharedSizeBytes - 1024 - scratch) / p.stage_bytes);
   if (stages > kMaxStagesB) stages = kMaxStagesB;
   if (stages < 2) return cudaErrorNotSupported;
   p.stages = stages;
-  const size_t smem = 1024 + (size_t)stages * p.stage_bytes;
+  const size_t smem = 1024 + (size_t)stages * p.stage_bytes + scratch;
   // job 0: FC1 + silu_and_mul -> E4M3 act [R, I] + group scales [R, I/128];
   // job 1: FC2 + routing weight -> bf16 rows at row_src
   p.job[0] = BJob{w13_scale, xp_scale, row_src, nullptr, actq, act_scale, 2 * I, I, I / kGroup,
