@@ -620,19 +620,28 @@ def main_native(args):
         dist.destroy_process_group()
 
 
+def kernel_source_sha(workload):
+    """sha256 (12 hex digits) of the source that defines the workload's GEMM
+    kernel: its .cu file and the device headers it includes."""
+    import hashlib
+    import workloads
+    cfg = workloads.CONFIGS[workload]
+    src = os.path.join(ROOT, "moe_expert_ffn_rms_gb300", "csrc")
+    main = ("gemm_nvfp4.cu" if cfg.nvfp4 else "gemm_fp8b.cu" if cfg.fp8 == "block" else
+            "gemm_tc.cu")
+    h = hashlib.sha256()
+    for fn in [main] + sorted(f for f in os.listdir(src) if f.endswith(".cuh")):
+        h.update(open(os.path.join(src, fn), "rb").read())
+    return h.hexdigest()[:12]
+
+
 def read_traffic(kernel, workload):
     """DRAM traffic per launch from a committed ncu summary, if it was taken on
     the current kernel source; else None."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
-    import hashlib
-    src = os.path.join(ROOT, "moe_expert_ffn_rms_gb300", "csrc")
-    h = hashlib.sha256()
-    for fn in sorted(os.listdir(src)):
-        if fn.startswith("gemm_") or fn.endswith(".cuh"):
-            h.update(open(os.path.join(src, fn), "rb").read())
-    sha = h.hexdigest()[:12]
+    sha = kernel_source_sha(workload)
     with open(p) as f:
         for ln in f:
             parts = ln.split()
@@ -643,6 +652,9 @@ def read_traffic(kernel, workload):
 
 
 if __name__ == "__main__":
+    if len(sys.argv) == 3 and sys.argv[1] == "--kernel-sha":
+        print(kernel_source_sha(sys.argv[2]))
+        sys.exit(0)
     a = parse()
     if a.impl == "reference":
         main_reference(a)
