@@ -210,11 +210,19 @@ MOE_DEV bool epilogue_unit(const Unit& un, const JobP& j, int I, uint32_t tbase,
     const bool rvalid = lrow < un.rows;
     const float sa = (FP8 && rvalid) ? j.a_scale[r] : 1.f;
     if (MODE == 1) {
-      for (int c = 0; c < 128; c += 16) {
-        float g[16], up[16];
-        tmem_ld16(tbase + c, g);
-        tmem_ld16(tbase + 128 + c, up);
+      for (int c2 = 0; c2 < 128; c2 += 32) {
+        // two 16-column chunks of gate and up per TMEM round trip
+        float gg[32], uu[32];
+        tmem_ld16(tbase + c2, gg);
+        tmem_ld16(tbase + c2 + 16, gg + 16);
+        tmem_ld16(tbase + 128 + c2, uu);
+        tmem_ld16(tbase + 128 + c2 + 16, uu + 16);
         tmem_ld_wait();
+#pragma unroll
+        for (int cc = 0; cc < 32; cc += 16) {
+        const float* g = gg + cc;
+        const float* up = uu + cc;
+        const int c = c2 + cc;
         const int n0 = un.nt * 128 + c;
         if (rvalid) {
           uint32_t pk[8];
@@ -235,22 +243,32 @@ MOE_DEV bool epilogue_unit(const Unit& un, const JobP& j, int I, uint32_t tbase,
             reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           } else {
-            for (int t = 0; t < 16 && n0 + t < I; ++t) {
-              const uint32_t w2 = pk[t / 2];
-              const uint16_t h = (t & 1) ? (uint16_t)(w2 >> 16) : (uint16_t)(w2 & 0xffffu);
-              reinterpret_cast<uint16_t*>(dst)[t] = h;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+              if (n0 + t < I) {
+                const uint32_t w2 = pk[t / 2];
+                const uint16_t h = (t & 1) ? (uint16_t)(w2 >> 16) : (uint16_t)(w2 & 0xffffu);
+                reinterpret_cast<uint16_t*>(dst)[t] = h;
+              }
             }
           }
+        }
         }
       }
     } else {
       const float tw = (IS_FC2 && rvalid && j.topk_w) ? j.topk_w[j.row_src[r]] : 1.f;
       // FC2 bf16 rows go back to (token, slot) order
       const int orow = (MODE == 3 && rvalid && j.row_src) ? j.row_src[r] : r;
-      for (int c = 0; c < 256; c += 16) {
-        float v[16];
-        tmem_ld16(tbase + c, v);
+      for (int c4 = 0; c4 < 256; c4 += 64) {
+        // four 16-column chunks per TMEM round trip
+        float vv[64];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld16(tbase + c4 + 16 * q, vv + 16 * q);
         tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+        float* v = vv + 16 * q;
+        const int c = c4 + 16 * q;
         const int n0 = un.nt * 256 + c;
         if (rvalid && n0 < j.n_out) {
 #pragma unroll
@@ -279,6 +297,7 @@ MOE_DEV bool epilogue_unit(const Unit& un, const JobP& j, int I, uint32_t tbase,
               for (int t = 0; t < 16 && n0 + t < j.n_out; ++t) dst[t] = __float2bfloat16_rn(v[t]);
             }
           }
+        }
         }
       }
     }

@@ -139,6 +139,32 @@ def test_forward_fp8_block_full_decode_workload(M):
     print(f"c7_decode_fp8_block: max scaled error {m:.3e}")
 
 
+def test_forward_fp8_block_prefill_workload(M):
+    """Block-wise FP8 at the prefill size (T=4096, H=4096, E=64, k=8, I=1536):
+    token chunks of 64 rows; 8 sampled tokens recomputed by the oracle."""
+    inp = workloads.make_inputs("c9_prefill_fp8_block", DEV)
+    inp["name"] = "c9_prefill_fp8_block"
+    _, m, _ = check_fp8_block(M, inp, sample=8)
+    print(f"c9_prefill_fp8_block: max scaled error {m:.3e}")
+    del inp
+    torch.cuda.empty_cache()
+
+
+def test_forward_fp8_block_zero_tokens(M):
+    shape = M.make_shape(0, 256, 8, 128, 2, fp8="block")
+    ws = M.alloc_workspace(max(256, M.moe_ffn_workspace_size(shape)), DEV)
+    w = torch.ones((256,), dtype=torch.bfloat16, device=DEV)
+    q13 = torch.zeros((8, 256, 256), dtype=torch.uint8, device=DEV)
+    q2 = torch.zeros((8, 256, 128), dtype=torch.uint8, device=DEV)
+    s13 = torch.ones((8, 2, 2), dtype=torch.float32, device=DEV)
+    s2 = torch.ones((8, 2, 1), dtype=torch.float32, device=DEV)
+    rw = torch.zeros((256, 8), dtype=torch.float32, device=DEV)
+    out = torch.empty((1, 256), dtype=torch.bfloat16, device=DEV)
+    M.moe_ffn_forward(shape, w, w, q13, q2, out, ws, router_w=rw, w13_scale=s13, w2_scale=s2)
+    torch.cuda.synchronize()
+    assert M.device_status() == 0
+
+
 def test_routed_forward_fp8_block_matches_routed_oracle(M):
     inp = workloads.make_inputs("c1_tiny", DEV, shape=SHAPES["rows_64"][1], seed=23)
     inp["name"] = "routed"

@@ -519,7 +519,7 @@ def test_forward_fp8_small(M):
 
 @pytest.mark.parametrize("cfg,sample", [("c1_tiny", None), ("c2_decode_balanced", None),
                                         ("c3_decode_skewed", 16), ("c4_decode_fp8", None),
-                                        ("c5_prefill", 48)])
+                                        ("c5_prefill", 48), ("c8_prefill_fp8", 24)])
 def test_forward_reference_workloads(M, cfg, sample):
     inp = workloads.make_inputs(cfg, DEV)
     m, ndiff = check_forward(M, inp, sample=sample)

@@ -80,6 +80,14 @@ CONFIGS = {
         "c7_decode_fp8_block", Shape(T=16, H=4096, E=64, k=8, I=1536), "balanced", "block", 6,
         description="decode with block-wise FP8 (E4M3, one scale per 128 x 128 weight tile and "
                     "per 1 x 128 activation group)"),
+    "c8_prefill_fp8": Config(
+        "c8_prefill_fp8", Shape(T=4096, H=4096, E=64, k=8, I=1536), "learned", True, 7,
+        description="prefill with FP8 W8A8 (E4M3, per-channel weight / per-token activation "
+                    "scales)"),
+    "c9_prefill_fp8_block": Config(
+        "c9_prefill_fp8_block", Shape(T=4096, H=4096, E=64, k=8, I=1536), "learned", "block", 8,
+        description="prefill with block-wise FP8 (E4M3, 128 x 128 weight tiles, 1 x 128 "
+                    "activation groups)"),
 }
 
 CONFIG_ORDER = ["c1_tiny", "c2_decode_balanced", "c3_decode_skewed", "c4_decode_fp8", "c5_prefill"]
