@@ -166,8 +166,9 @@ size_t moe_ffn_workspace_size(const moe_shape* shape);
  * s_x[r] * s_w[e, n].  FP8_BLOCK: x_hat and the bf16 intermediate are
  * quantised per row and 128-element group; each 128-wide K group of a
  * product is accumulated on its own and scaled by s_a[r, g] * s_w[e, n/128, g]
- * before the groups are added in K order (one persistent launch for FC1 and
- * FC2 on every batch size).
+ * before the groups are added in K order (decode engine: one persistent
+ * launch for FC1 and FC2; prefill engine: FC1 tiles, the group quantisation
+ * of the intermediate, FC2 tiles).
  * Errors: INVALID_ARG (null/misaligned/both or neither router input),
  * UNSUPPORTED_SHAPE (H or I not a multiple of 64, top_k > 8 or > E,
  * E > 256, the FP8_BLOCK limits above), WORKSPACE_TOO_SMALL,
@@ -321,7 +322,8 @@ size_t moe_grouped_ffn_workspace_size(const moe_shape* shape);
  * xp [R, H] (+ xp_scale [R] for FP8), act bf16 [R, I], y bf16 [R, H] in
  * (token, slot) order, R = T * top_k).  On the decode engine with bf16
  * weights both GEMMs run in one persistent launch whose FC2 units wait per
- * expert for that expert's FC1 units.  FP8_BLOCK (always one launch): xp
+ * expert for that expert's FC1 units.  FP8_BLOCK (one launch on the decode
+ * engine, three on the prefill engine): xp
  * e4m3 [R, H] with xp_scale fp32 [R, H/128] (one scale per row and group,
  * as moe_quantize_fp8_blocks with block_rows = 1 writes them), act e4m3
  * [R, I] receives the quantised intermediate (its group scales stay in the

@@ -287,14 +287,24 @@ moe_status ffn_impl(const moe_shape* s, int engine, bool fuse, const void* xp,
   const bool f8 = s->wdtype == MOE_W_FP8_E4M3;
   const int T = s->T, H = s->H, E = s->E, I = s->I, R = s->T * s->top_k;
   if (s->wdtype == MOE_W_FP8_BLOCK) {
-    // block-wise FP8: one persistent launch on every batch size; the
-    // intermediate is E4M3 codes (actq) with one scale per 128 columns
-    MOE_CUDA(moe::launch_decode_ffn_fp8b(static_cast<const uint8_t*>(xp), xp_scale,
-                                         static_cast<const uint8_t*>(w13), w13_scale,
-                                         static_cast<const uint8_t*>(w2), w2_scale, actq, act_scale,
-                                         y, offsets, row_src, tw, sched, E, H, I, R, T, dev->sms,
-                                         dev->status, st),
-             "block-wise FP8 FFN launch");
+    // block-wise FP8; the FC2 input is E4M3 codes (actq) with one scale per
+    // 128 columns.  Decode engine: one persistent launch (FC1 quantises in
+    // its epilogue).  Prefill engine: FC1 tiles -> bf16 act, quantisation,
+    // FC2 tiles.
+    if (engine == MOE_ENGINE_PREFILL)
+      MOE_CUDA(moe::launch_prefill_ffn_fp8b(static_cast<const uint8_t*>(xp), xp_scale,
+                                            static_cast<const uint8_t*>(w13), w13_scale,
+                                            static_cast<const uint8_t*>(w2), w2_scale, act, actq,
+                                            act_scale, y, offsets, row_src, tw, E, H, I, R,
+                                            dev->sms, dev->status, st),
+               "block-wise FP8 FFN launch");
+    else
+      MOE_CUDA(moe::launch_decode_ffn_fp8b(static_cast<const uint8_t*>(xp), xp_scale,
+                                           static_cast<const uint8_t*>(w13), w13_scale,
+                                           static_cast<const uint8_t*>(w2), w2_scale, actq,
+                                           act_scale, y, offsets, row_src, tw, sched, E, H, I, R, T,
+                                           dev->sms, dev->status, st),
+               "block-wise FP8 FFN launch");
     return MOE_OK;
   }
   if (fuse) {
@@ -720,7 +730,8 @@ size_t moe_grouped_ffn_workspace_size(const moe_shape* shape) {
   const size_t R = (size_t)shape->T * shape->top_k;
   size_t n = up256((size_t)(2 * shape->E + 1) * 4);
   if (shape->wdtype == MOE_W_FP8_E4M3) n += up256(R * shape->I) + up256(R * 4);
-  if (shape->wdtype == MOE_W_FP8_BLOCK) n += up256(R * (shape->I / 128) * 4);
+  if (shape->wdtype == MOE_W_FP8_BLOCK)  // group scales of act, and its bf16 values
+    n += up256(R * (shape->I / 128) * 4) + up256(R * shape->I * 2);
   return n;
 }
 
@@ -754,9 +765,13 @@ moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* 
   int32_t* sched = at<int32_t>(workspace, 0);
   uint8_t* actq = f8 ? at<uint8_t>(workspace, up256(sched_bytes)) : nullptr;
   float* act_scale = f8 ? at<float>(workspace, up256(sched_bytes) + up256(R * shape->I)) : nullptr;
-  if (fb) {  // the E4M3 intermediate goes to the caller's act, its scales to the workspace
+  void* act_mid = act;
+  if (fb) {
+    // the E4M3 intermediate goes to the caller's act; its group scales and
+    // (prefill engine) its bf16 values to the workspace
     actq = static_cast<uint8_t*>(act);
     act_scale = at<float>(workspace, up256(sched_bytes));
+    act_mid = at<void>(workspace, up256(sched_bytes) + up256(R * (shape->I / 128) * 4));
     MOE_CUDA(cudaMemsetAsync(sched, 0, sched_bytes, st), "scheduler reset");
   }
   const int engine = pick_engine(shape);
@@ -764,7 +779,7 @@ moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* 
   const bool fuse = fuse_decode(shape, engine);
   if (fuse) MOE_CUDA(cudaMemsetAsync(sched, 0, sched_bytes, st), "scheduler reset");
   return ffn_impl(shape, engine, fuse, xp, xp_scale, w13, w13_scale, w2, w2_scale, offsets,
-                  row_src, topk_w, act, y, sched, actq, act_scale, dev, st);
+                  row_src, topk_w, act_mid, y, sched, actq, act_scale, dev, st);
 }
 
 moe_status moe_grouped_ffn_nvfp4(const moe_shape* shape, const void* xp, const uint8_t* w13,

@@ -108,6 +108,16 @@ cudaError_t launch_decode_ffn_fp8b(const uint8_t* xp, const float* xp_scale, con
                                    int H, int I, int R_max, int T, int sms, int* status,
                                    cudaStream_t st);
 
+// Block-wise FP8 for many rows per expert: FC1 tiles (128 tokens x 64 gate
+// + 64 up rows) -> bf16 act, group quantisation of act, FC2 tiles (128
+// tokens x 128 rows of W2) -> bf16 rows at row_src; three launches.
+cudaError_t launch_prefill_ffn_fp8b(const uint8_t* xp, const float* xp_scale, const uint8_t* w13,
+                                    const float* w13_scale, const uint8_t* w2,
+                                    const float* w2_scale, void* act, uint8_t* actq,
+                                    float* act_scale, void* y, const int32_t* offsets,
+                                    const int32_t* row_src, const float* topk_w, int E, int H,
+                                    int I, int R_max, int sms, int* status, cudaStream_t st);
+
 // Bounded-wait self-test: a kernel that waits on an mbarrier nothing arrives
 // on for at most limit_cycles SM cycles and records MOE_ERR_TIMEOUT.
 cudaError_t launch_wait_selftest(long long limit_cycles, int* status, cudaStream_t st);

@@ -657,6 +657,329 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
   if (warp == 1) tmem_dealloc(tmem, kTmemColsB);
 }
 
+
+// ------------------------------------------- prefill tile kernel (FC1 / FC2) --
+// For batches with many rows per expert the weight-streaming layout above
+// re-reads each expert's weights once per 64-token chunk.  This kernel tiles
+// the tokens instead: a unit is 128 token rows (MMA M, TMEM lanes) x 128
+// weight rows (MMA N) of one expert over all of K, one 128-wide K group per
+// 32 KB stage.  FC1 (MODE 1) takes 64 gate rows and the matching 64 up rows
+// and writes bf16 a = silu(g) u; FC2 (MODE 3) takes 128 rows of W2 and writes
+// bf16 (routing weight x y) at row row_src[r].  The forward quantises a per
+// 128-column group between the two launches.
+//
+// Each K group's product goes to its own 128-column TMEM slot (ring of four).
+// Eight epilogue warps, two per TMEM lane quarter, each own 64 accumulator
+// columns of their 32 token rows in registers: a thread's group scale is one
+// activation scale (its token row) times one weight-tile scale per 32
+// columns, so the fold is a scalar multiply-add per element.  The warps never
+// synchronise with one another.
+constexpr int kThreadsT = 320;       // warp 0 TMA, 1 MMA (+ TMEM owner), 2-9 epilogue
+constexpr int kTileBytesT = 128 * 128;
+constexpr int kStageBytesT = 2 * kTileBytesT;  // token tile + weight tile of one K group
+constexpr int kSlotsT = 4;
+constexpr int kMaxStagesT = 6;
+
+struct TParams {
+  const int32_t* offsets;
+  int E, I, R_max;
+  int N_w;                  // weight rows per expert
+  int nt;                   // N tiles per (expert, token tile)
+  int kg;                   // K groups
+  int stages;
+  const float* a_scale;     // [R, kg] activation group scales
+  const float* w_scale;     // [E, N_w / 128, kg] weight tile scales
+  const int32_t* row_src;   // FC2: destination row of row r
+  const float* topk_w;      // FC2: routing weight of pair row_src[r]
+  void* out;                // bf16 rows
+  int ldo;
+  int* status;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
+    const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
+    const TParams p) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_up[kMaxExperts + 1];
+  __shared__ __align__(8) uint64_t sfull[kMaxStagesT];
+  __shared__ __align__(8) uint64_t sempty[kMaxStagesT];
+  __shared__ __align__(8) uint64_t kfull[kSlotsT];
+  __shared__ __align__(8) uint64_t kempty[kSlotsT];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~(uintptr_t)1023);
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sempty[s], 1);
+    }
+    for (int q = 0; q < kSlotsT; ++q) {
+      mbar_init(&kfull[q], 1);
+      mbar_init(&kempty[q], 8);  // lane 0 of each epilogue warp
+    }
+    mbar_init(&drain_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_w);
+  } else if (warp == 1) {
+    tmem_alloc(&s_tmem, kTmemColsB);
+    tmem_relinquish();
+  }
+  pdl_trigger();
+  pdl_wait();
+  for (int e = threadIdx.x; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
+  __syncthreads();
+  if (threadIdx.x == 0) {  // offsets must be monotone within [0, R_max]
+    int prev = 0;
+    bool bad = false;
+    for (int e = 0; e <= p.E; ++e) {
+      int v = s_off[e];
+      if (v < prev || v > p.R_max || (e == 0 && v != 0)) {
+        bad = true;
+        v = v < prev ? prev : (v > p.R_max ? p.R_max : v);
+        if (e == 0) v = 0;
+      }
+      s_off[e] = v;
+      prev = v;
+    }
+    if (bad && blockIdx.x == 0) flag_status(p.status, MOE_ERR_INVALID_ARG);
+  }
+  __syncthreads();
+  if (warp == 0) {  // unit prefix: ceil(rows / 128) token tiles x nt per expert
+    int carry = 0;
+    for (int base = 0; base < p.E; base += 32) {
+      const int e = base + lane;
+      const int cnt = (e < p.E) ? s_off[e + 1] - s_off[e] : 0;
+      const int v = ((cnt + 127) / 128) * p.nt;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e < p.E) s_up[e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_up[p.E] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int U = s_up[p.E];
+
+  if (warp == 0) {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_last();  // re-read by the expert's other token tiles
+      const uint64_t pol_a = l2_policy_evict_first();
+      int s = 0;
+      uint32_t ph = 0, armed = 0, armed_ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
+        const Unit un = unit_of(u, s_off, s_up, p.E, p.nt, 128);
+        const int wrow = un.e * p.N_w;
+        // FC1: gate rows nt*64.. and the matching up rows; FC2: 128 rows
+        const int r0 = MODE == 1 ? wrow + un.nt * 64 : wrow + un.nt * 128;
+        const int r1 = MODE == 1 ? wrow + p.I + un.nt * 64 : r0 + 64;
+        for (int g = 0; g < p.kg; ++g) {
+          if (!mbar_wait_spin(&sempty[s], ph ^ 1, &s_abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sfull[s], (uint32_t)kStageBytesT);
+          uint8_t* st = ring + (size_t)s * kStageBytesT;
+          tma_load_2d(st, &tm_a, &sfull[s], g * kGroup, un.row0, pol_a);
+          tma_load_2d(st + kTileBytesT, &tm_w, &sfull[s], g * kGroup, r0, pol_w);
+          tma_load_2d(st + kTileBytesT + kTileBytesT / 2, &tm_w, &sfull[s], g * kGroup, r1, pol_w);
+          armed |= 1u << s;
+          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+          if (++s == p.stages) { s = 0; ph ^= 1; }
+        }
+      }
+      if (ok) ok = producer_tail(sempty, p.stages, s, ph, &s_abort);
+      if (!ok) {
+        flag_status(p.status, MOE_ERR_TIMEOUT);
+        drain_armed(sfull, p.stages, armed, armed_ph);
+      }
+    }
+  } else if (warp == 1) {
+    // ====================================================== MMA issuer
+    if (lane == 0) {
+      int s = 0, q = 0;
+      uint32_t ph = 0, qph = 0;
+      bool ok = true, issued = false;
+      const uint32_t idesc = make_idesc(128, 0u);  // M = N = 128, E4M3 A and B
+      for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
+        for (int g = 0; g < p.kg; ++g) {
+          if (!mbar_wait_spin(&sfull[s], ph, &s_abort) ||
+              !mbar_wait_spin(&kempty[q], qph ^ 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(ring + (size_t)s * kStageBytesT);
+          const uint32_t d = tmem + q * 128;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // each group starts a fresh sum
+            mma_e4m3(d, sw128_desc(a0 + kk * 32), sw128_desc(a0 + kTileBytesT + kk * 32), idesc,
+                     kk ? 1u : 0u);
+          issued = true;
+          mma_commit(&sempty[s]);
+          mma_commit(&kfull[q]);
+          if (++s == p.stages) { s = 0; ph ^= 1; }
+          if (++q == kSlotsT) { q = 0; qph ^= 1; }
+        }
+      }
+      for (int i = 0; ok && i < kSlotsT; ++i) {  // tail: every slot handed back
+        ok = mbar_wait(&kempty[q], qph ^ 1, &s_abort);
+        if (++q == kSlotsT) { q = 0; qph ^= 1; }
+      }
+      if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
+      if (issued) {
+        mma_commit(&drain_bar);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&drain_bar, 0) && clock64() - t0 < kSpinLimitCycles) {
+        }
+      }
+    }
+  } else {
+    // ======================================================== epilogue
+    // Warp w (2..9): token rows 32 (w % 4) .. +31 of the tile (its TMEM lane
+    // quarter) and half h = (w - 2) / 4 of the columns: FC1 gate columns
+    // 32h .. 32h + 31 with the matching up columns 64 + 32h ..; FC2 columns
+    // 64h .. 64h + 63.  acc[0..31] and acc[32..63] are those two 32-column runs.
+    const int h = (warp - 2) >> 2;
+    const int qtr = warp & 3;
+    const int lrow = qtr * 32 + lane;
+    const uint32_t tlane = (uint32_t)(qtr * 32) << 16;
+    const int c_lo = MODE == 1 ? 32 * h : 64 * h;
+    const int c_hi = MODE == 1 ? 64 + 32 * h : 64 * h + 32;
+    const int nblk = p.N_w / kGroup;
+    int q = 0;
+    uint32_t qph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
+      const Unit un = unit_of(u, s_off, s_up, p.E, p.nt, 128);
+      const bool rvalid = lrow < un.rows;
+      const int r = un.row0 + lrow;
+      // weight tiles of the two column runs
+      const int rb_lo = MODE == 1 ? (un.nt * 64) / kGroup : un.nt;
+      const int rb_hi = MODE == 1 ? (p.I + un.nt * 64) / kGroup : un.nt;
+      const float* sw_lo = p.w_scale + ((size_t)un.e * nblk + rb_lo) * p.kg;
+      const float* sw_hi = p.w_scale + ((size_t)un.e * nblk + rb_hi) * p.kg;
+      const float* sa_row = p.a_scale + (size_t)(rvalid ? r : 0) * p.kg;
+      float acc[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+      float sa = rvalid ? sa_row[0] : 0.f, wl = sw_lo[0], wh = sw_hi[0];
+      for (int g = 0; g < p.kg; ++g) {
+        // next group's scales load while this group's product is awaited
+        const int gn = g + 1 < p.kg ? g + 1 : g;
+        const float sa_n = rvalid ? sa_row[gn] : 0.f, wl_n = sw_lo[gn], wh_n = sw_hi[gn];
+        int wok = 1;
+        if (lane == 0) wok = mbar_wait(&kfull[q], qph, &s_abort);
+        wok = __shfl_sync(0xffffffffu, wok, 0);
+        if (!wok) { ok = false; break; }
+        tc_fence_after();
+        float v[64];
+        const uint32_t ta = tmem + tlane + q * 128;
+        tmem_ld16(ta + c_lo, v);
+        tmem_ld16(ta + c_lo + 16, v + 16);
+        tmem_ld16(ta + c_hi, v + 32);
+        tmem_ld16(ta + c_hi + 16, v + 48);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&kempty[q]);
+        if (++q == kSlotsT) { q = 0; qph ^= 1; }
+        const float fl = sa * wl, fh = sa * wh;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          acc[c] = fmaf(v[c], fl, acc[c]);
+          acc[32 + c] = fmaf(v[32 + c], fh, acc[32 + c]);
+        }
+        sa = sa_n;
+        wl = wl_n;
+        wh = wh_n;
+      }
+      if (!ok) break;
+      if (!rvalid) continue;
+      bf16* out = reinterpret_cast<bf16*>(p.out);
+      if (MODE == 1) {
+        // a = bf16(silu(g) u): 32 columns from nt*64 + 32h, 64 bytes
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2)
+          pk[c / 2] = pack2_bf16(silu_f(acc[c]) * acc[32 + c], silu_f(acc[c + 1]) * acc[33 + c]);
+        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * p.ldo + un.nt * 64 + 32 * h);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      } else {
+        // routing weight x y, bf16, at row row_src[r]: 64 columns from nt*128 + 64h
+        const int orow = p.row_src[r];
+        const float tw = p.topk_w[orow];
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) pk[c / 2] = pack2_bf16(acc[c] * tw, acc[c + 1] * tw);
+        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)orow * p.ldo + un.nt * 128 + 64 * h);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+    if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemColsB);
+}
+
+template <int MODE>
+cudaError_t launch_tile(const void* a, const float* a_scale, const uint8_t* w, const float* w_scale,
+                        int K, int N_w, int nt, const int32_t* offsets, const int32_t* row_src,
+                        const float* topk_w, void* out, int ldo, int E, int I, int R_max, int sms,
+                        int* status, cudaStream_t st) {
+  TParams p{};
+  p.offsets = offsets;
+  p.E = E;
+  p.I = I;
+  p.R_max = R_max;
+  p.N_w = N_w;
+  p.nt = nt;
+  p.kg = K / kGroup;
+  p.a_scale = a_scale;
+  p.w_scale = w_scale;
+  p.row_src = row_src;
+  p.topk_w = topk_w;
+  p.out = out;
+  p.ldo = ldo;
+  p.status = status;
+  auto k = moe_tc_fp8b_tile_kernel<MODE>;
+  cudaFuncAttributes fa{};
+  cudaError_t e = cudaFuncGetAttributes(&fa, k);
+  if (e != cudaSuccess) return e;
+  int stages = (int)((kSmemLimitB - (int)fa.sharedSizeBytes - 1024) / kStageBytesT);
+  if (stages > kMaxStagesT) stages = kMaxStagesT;
+  p.stages = stages;
+  const size_t smem = 1024 + (size_t)stages * kStageBytesT;
+  CUtensorMap ma, mw;
+  if (!tc::encode_map(&ma, a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, R_max, K, kGroup, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::encode_map(&mw, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (int64_t)E * N_w, K, kGroup, 64,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorNotSupported;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(k, dim3(sms), dim3(kThreadsT), smem, st, ma, mw, p);
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ host --
@@ -741,6 +1064,26 @@ cudaError_t launch_decode_ffn_fp8b(const uint8_t* xp, const float* xp_scale, con
   e = cudaFuncSetAttribute(moe_tc_fp8b_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(moe_tc_fp8b_kernel, dim3(sms), dim3(kThreadsB), smem, st, m[0], m[1], bx, p);
+}
+
+cudaError_t launch_prefill_ffn_fp8b(const uint8_t* xp, const float* xp_scale, const uint8_t* w13,
+                                    const float* w13_scale, const uint8_t* w2,
+                                    const float* w2_scale, void* act, uint8_t* actq,
+                                    float* act_scale, void* y, const int32_t* offsets,
+                                    const int32_t* row_src, const float* topk_w, int E, int H,
+                                    int I, int R_max, int sms, int* status, cudaStream_t st) {
+  if (R_max == 0) return cudaSuccess;
+  if (!fp8b_decode_covers(H, I, E)) return cudaErrorNotSupported;
+  // FC1 + silu_and_mul -> bf16 act [R, I]
+  cudaError_t e = launch_tile<1>(xp, xp_scale, w13, w13_scale, H, 2 * I, I / 64, offsets, nullptr,
+                                 nullptr, act, I, E, I, R_max, sms, status, st);
+  if (e != cudaSuccess) return e;
+  // act -> E4M3 codes with one scale per row and 128 columns
+  e = launch_quantize_fp8_blocks(act, R_max, I, 1, actq, act_scale, st);
+  if (e != cudaSuccess) return e;
+  // FC2 + routing weight -> bf16 rows at row_src
+  return launch_tile<3>(actq, act_scale, w2, w2_scale, I, H, H / 128, offsets, row_src, topk_w, y,
+                        H, E, I, R_max, sms, status, st);
 }
 
 }  // namespace moe

@@ -61,9 +61,10 @@ def quantize_weights(M, inp):
     return quantize_gpu(M, inp["w13"], 128), quantize_gpu(M, inp["w2"], 128)
 
 
-def run_forward(M, inp, wq, routed=None):
+def run_forward(M, inp, wq, routed=None, engine=None):
     T, H, E, k, I = inp["T"], inp["H"], inp["E"], inp["k"], inp["I"]
-    shape = M.make_shape(T, H, E, I, k, inp["eps"], fp8="block")
+    shape = M.make_shape(T, H, E, I, k, inp["eps"], fp8="block",
+                         engine=M.ENGINE_AUTO if engine is None else engine)
     ws = M.alloc_workspace(M.moe_ffn_workspace_size(shape), DEV)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
     (q13, s13), (q2, s2) = wq
@@ -82,11 +83,11 @@ def run_forward(M, inp, wq, routed=None):
     return out, ids, tw
 
 
-def check_fp8_block(M, inp, sample=None, seed=0):
+def check_fp8_block(M, inp, sample=None, seed=0, engine=None):
     T, k, I = inp["T"], inp["k"], inp["I"]
     wq = quantize_weights(M, inp)
     M.device_status(clear=True)
-    out, ids, tw = run_forward(M, inp, wq)
+    out, ids, tw = run_forward(M, inp, wq, engine=engine)
     xhat = O.rms_norm(f64(inp["x"]), f64(inp["norm_w"]), inp["eps"])
     if inp["router_logits"] is not None:
         l64 = f64(inp["router_logits"])
@@ -120,12 +121,16 @@ SHAPES = {
 }
 
 
+@pytest.mark.parametrize("engine", ["auto", "decode", "prefill"])
 @pytest.mark.parametrize("name", list(SHAPES))
-def test_forward_fp8_block_small(M, name):
+def test_forward_fp8_block_small(M, name, engine):
+    """Both engines: the weight-streaming launch (decode) and the token tiles
+    with a separate group quantisation (prefill)."""
     cfg, shape, routing = SHAPES[name]
     inp = workloads.make_inputs(cfg, DEV, shape=shape, routing=routing, seed=19)
-    inp["name"] = name
-    check_fp8_block(M, inp)
+    inp["name"] = f"{name}/{engine}"
+    eng = {"auto": None, "decode": M.ENGINE_DECODE, "prefill": M.ENGINE_PREFILL}[engine]
+    check_fp8_block(M, inp, engine=eng)
 
 
 def test_forward_fp8_block_full_decode_workload(M):
@@ -140,8 +145,8 @@ def test_forward_fp8_block_full_decode_workload(M):
 
 
 def test_forward_fp8_block_prefill_workload(M):
-    """Block-wise FP8 at the prefill size (T=4096, H=4096, E=64, k=8, I=1536):
-    token chunks of 64 rows; 8 sampled tokens recomputed by the oracle."""
+    """Block-wise FP8 at the prefill size (T=4096, H=4096, E=64, k=8, I=1536,
+    token tiles); 8 sampled tokens recomputed by the oracle."""
     inp = workloads.make_inputs("c9_prefill_fp8_block", DEV)
     inp["name"] = "c9_prefill_fp8_block"
     _, m, _ = check_fp8_block(M, inp, sample=8)
@@ -180,13 +185,15 @@ def test_routed_forward_fp8_block_matches_routed_oracle(M):
     assert_close(f64(out), res["out"], TOL_FP8, "routed fp8 block")
 
 
-def test_grouped_ffn_fp8_block_matches_forward(M):
+@pytest.mark.parametrize("engine", ["decode", "prefill"])
+def test_grouped_ffn_fp8_block_matches_forward(M, engine):
     """The FFN step entry point on the forward's own routing and gathered
     E4M3 rows gives the forward's output after the combine."""
     inp = workloads.make_inputs("c1_tiny", DEV, shape=SHAPES["learned_small"][1], seed=29)
     T, H, E, k, I = inp["T"], inp["H"], inp["E"], inp["k"], inp["I"]
+    eng = M.ENGINE_DECODE if engine == "decode" else M.ENGINE_PREFILL
     wq = quantize_weights(M, inp)
-    out, ids, tw = run_forward(M, inp, wq)
+    out, ids, tw = run_forward(M, inp, wq, engine=eng)
     R = T * k
     xhat = torch.empty_like(inp["x"])
     M.moe_rmsnorm(inp["x"], inp["norm_w"], inp["eps"], xhat)
@@ -200,7 +207,7 @@ def test_grouped_ffn_fp8_block_matches_forward(M):
     xps = xs[tok].contiguous()
     act = torch.empty((R, I), dtype=torch.uint8, device=DEV)
     y = torch.empty((R, H), dtype=torch.bfloat16, device=DEV)
-    shape = M.make_shape(T, H, E, I, k, inp["eps"], fp8="block")
+    shape = M.make_shape(T, H, E, I, k, inp["eps"], fp8="block", engine=eng)
     ws = M.alloc_workspace(M.moe_grouped_ffn_workspace_size(shape), DEV)
     (q13, s13), (q2, s2) = wq
     M.moe_grouped_ffn(shape, xp, q13, q2, offsets, row_src, tw, act, y, ws, xp_scale=xps,
