@@ -674,6 +674,15 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
 // activation scale (its token row) times one weight-tile scale per 32
 // columns, so the fold is a scalar multiply-add per element.  The warps never
 // synchronise with one another.
+// a0 += v0 * f, a1 += v1 * f in one paired fp32 instruction (each half an
+// IEEE fused multiply-add, round to nearest: the same bits as two fmaf).
+MOE_DEV void fma2(float& a0, float& a1, float v0, float v1, float f) {
+  asm("{\n .reg .b64 a, v, s;\n mov.b64 a, {%0, %1};\n mov.b64 v, {%2, %3};\n"
+      " mov.b64 s, {%4, %4};\n fma.rn.f32x2 a, v, s, a;\n mov.b64 {%0, %1}, a;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(v0), "f"(v1), "f"(f));
+}
+
 constexpr int kThreadsT = 320;       // warp 0 TMA, 1 MMA (+ TMEM owner), 2-9 epilogue
 constexpr int kTileBytesT = 128 * 128;
 constexpr int kStageBytesT = 2 * kTileBytesT;  // token tile + weight tile of one K group
@@ -790,7 +799,9 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
         const int r0 = MODE == 1 ? wrow + un.nt * 64 : wrow + un.nt * 128;
         const int r1 = MODE == 1 ? wrow + p.I + un.nt * 64 : r0 + 64;
         for (int g = 0; g < p.kg; ++g) {
-          if (!mbar_wait_spin(&sempty[s], ph ^ 1, &s_abort)) { ok = false; break; }
+          // suspending waits here and in the MMA thread: both share an SM
+          // sub-partition with epilogue warps, whose fold is the busy part
+          if (!mbar_wait(&sempty[s], ph ^ 1, &s_abort)) { ok = false; break; }
           mbar_arrive_expect_tx(&sfull[s], (uint32_t)kStageBytesT);
           uint8_t* st = ring + (size_t)s * kStageBytesT;
           tma_load_2d(st, &tm_a, &sfull[s], g * kGroup, un.row0, pol_a);
@@ -816,8 +827,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
       const uint32_t idesc = make_idesc(128, 0u);  // M = N = 128, E4M3 A and B
       for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
         for (int g = 0; g < p.kg; ++g) {
-          if (!mbar_wait_spin(&sfull[s], ph, &s_abort) ||
-              !mbar_wait_spin(&kempty[q], qph ^ 1, &s_abort)) {
+          if (!mbar_wait(&sfull[s], ph, &s_abort) || !mbar_wait(&kempty[q], qph ^ 1, &s_abort)) {
             ok = false;
             break;
           }
@@ -899,9 +909,9 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
         if (++q == kSlotsT) { q = 0; qph ^= 1; }
         const float fl = sa * wl, fh = sa * wh;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          acc[c] = fmaf(v[c], fl, acc[c]);
-          acc[32 + c] = fmaf(v[32 + c], fh, acc[32 + c]);
+        for (int c = 0; c < 32; c += 2) {
+          fma2(acc[c], acc[c + 1], v[c], v[c + 1], fl);
+          fma2(acc[32 + c], acc[33 + c], v[32 + c], v[33 + c], fh);
         }
         sa = sa_n;
         wl = wl_n;
