@@ -13,9 +13,12 @@
 // fp16 tile, 3.5 times the bytes of its codes, never passes through shared
 // memory.  The fp32 matrix scale is applied in the epilogue.
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 #include <stdlib.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "engine.h"
@@ -171,12 +174,19 @@ struct NvJob {
   int kst;                  // K stages
 };
 
-// Token-row (B) tensor maps per job with box heights 2, 4, 8 and 16 rows: a
-// unit loads only as many rows as it has (the MMA's N is a multiple of 16;
-// the columns of rows not loaded are ignored by the epilogue).
-struct NvBMaps {
-  CUtensorMap m[2][4];
-};
+// Every stage is three TMA loads (the per-load issue cost, not the bytes,
+// bounded the first versions): one 3D box of all four 64-element atoms of
+// the token rows, one 3D box of the unit's two 64-row weight slices of codes
+// (FC1: gate rows and the matching up rows, I rows apart; FC2: 64 + 64
+// consecutive rows), one of their block scales.
+MOE_DEV void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar, int x, int y, int z,
+                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
 
 struct NvParams {
   const int32_t* offsets;
@@ -209,7 +219,8 @@ MOE_DEV uint32_t e4m3_to_h2(uint32_t code) {
 __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
     const __grid_constant__ CUtensorMap tm_q0, const __grid_constant__ CUtensorMap tm_s0,
     const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_s1,
-    const __grid_constant__ NvBMaps bx, const NvParams p) {
+    const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
+    const NvParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_up[2][kMaxExperts + 1];
@@ -257,8 +268,8 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
     prefetch_tmap(&tm_s0);
     prefetch_tmap(&tm_q1);
     prefetch_tmap(&tm_s1);
-    for (int jb = 0; jb < 2; ++jb)
-      for (int bi = 0; bi < 4; ++bi) prefetch_tmap(&bx.m[jb][bi]);
+    prefetch_tmap(&tm_b0);
+    prefetch_tmap(&tm_b1);
   } else if (warp == 1) {
     tmem_alloc(&s_tmem, kTmemColsNv);
     tmem_relinquish();
@@ -361,32 +372,24 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
           if (!ok) break;
           fence_proxy_async_global();
         }
-        // B boxes: the smallest height of 2, 4, 8, 16 rows covering the unit
-        const int bi = un.rows > 8 ? 3 : (un.rows > 4 ? 2 : (un.rows > 2 ? 1 : 0));
-        const int brows = 2 << bi;
-        const int nb = bi == 3 ? (un.rows + kBoxRowsNv - 1) / kBoxRowsNv : 1;
-        const uint32_t tx = (uint32_t)(kFp4Bytes + kSbBytes + 4 * nb * brows * 128);
+        // all chunk token rows are loaded (rows of other experts or past the
+        // end are ignored by the epilogue; the box is zero-filled past R_max)
+        const uint32_t tx = (uint32_t)(kFp4Bytes + kSbBytes + p.b_bytes);
         const CUtensorMap* tq = un.job ? &tm_q1 : &tm_q0;
         const CUtensorMap* ts = un.job ? &tm_s1 : &tm_s0;
-        const CUtensorMap* tx_map = &bx.m[un.job][bi];
-        const int wrow = un.e * j.N_w;
-        // FC1: 64 gate rows then the matching 64 up rows; FC2: 128 rows
-        const int r0 = un.job == 0 ? wrow + un.nt * 64 : wrow + un.nt * 128;
-        const int r1 = un.job == 0 ? wrow + p.I + un.nt * 64 : r0 + 64;
+        const CUtensorMap* tb = un.job ? &tm_b1 : &tm_b0;
+        // FC1: 64 gate rows and the matching 64 up rows (the map's third
+        // dimension steps I rows); FC2: 128 consecutive rows (steps of 64)
+        const int r0 = un.e * j.N_w + (un.job == 0 ? un.nt * 64 : un.nt * 128);
         for (int ks = 0; ks < j.kst; ++ks) {
           if (!mbar_wait_spin(&sempty[s], ph ^ 1, &s_abort)) { ok = false; break; }
           mbar_arrive_expect_tx(&sfull[s], tx);
           uint8_t* st = ring + (size_t)s * p.stage_bytes;
           uint8_t* codes = st + p.b_bytes;
           uint8_t* scales = codes + kFp4Bytes;
-          tma_load_2d(codes, tq, &sfull[s], ks * (kKStage / 2), r0, pol_w);
-          tma_load_2d(codes + 64 * (kKStage / 2), tq, &sfull[s], ks * (kKStage / 2), r1, pol_w);
-          tma_load_2d(scales, ts, &sfull[s], ks * (kKStage / 16), r0, pol_w);
-          tma_load_2d(scales + 64 * (kKStage / 16), ts, &sfull[s], ks * (kKStage / 16), r1, pol_w);
-          for (int a = 0; a < 4; ++a)
-            for (int bb = 0; bb < nb; ++bb)
-              tma_load_2d(st + (size_t)a * p.chunk * 128 + bb * kBoxRowsNv * 128, tx_map, &sfull[s],
-                          ks * kKStage + a * 64, un.row0 + bb * kBoxRowsNv, pol_x);
+          tma_load_3d(codes, tq, &sfull[s], ks * (kKStage / 2), r0, 0, pol_w);
+          tma_load_3d(scales, ts, &sfull[s], ks * (kKStage / 16), r0, 0, pol_w);
+          tma_load_3d(st, tb, &sfull[s], 0, un.row0, ks * 4, pol_x);
           armed |= 1u << s;
           armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
           if (++s == p.stages) { s = 0; ph ^= 1; }
@@ -626,6 +629,38 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
 }  // namespace
 
 // ------------------------------------------------------------------ host --
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode3 = nullptr;
+std::once_flag g_encode3_once;
+
+void load_encode3() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode3 = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+// 3D tensor map: extents e0 (contiguous), e1, e2; byte strides s1, s2 of
+// dimensions 1 and 2; box b0 x b1 x b2, zero fill out of range.
+bool encode_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t e0,
+                   uint64_t e1, uint64_t e2, uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1,
+                   uint32_t b2, CUtensorMapSwizzle sw) {
+  std::call_once(g_encode3_once, load_encode3);
+  if (!g_encode3) return false;
+  cuuint64_t dims[3] = {e0, e1, e2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode3(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_quantize_nvfp4(const void* w, int M, int N, int K, uint8_t* q, uint8_t* sb,
                                   float* sg, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
@@ -689,29 +724,29 @@ cudaError_t launch_decode_ffn_nvfp4(const void* xp, const uint8_t* w13_q, const 
   // job 0: FC1 + silu_and_mul, fp16 rows [R, I]; job 1: FC2 + routing weight, bf16 rows at row_src
   p.job[0] = NvJob{w13_sg, row_src, nullptr, act, 2 * I, I, I / 64, H / kKStage};
   p.job[1] = NvJob{w2_sg, row_src, topk_w, y, H, H, (H + 127) / 128, I / kKStage};
-  CUtensorMap m[4];
-  NvBMaps bx;
-  const int64_t rows13 = (int64_t)E * 2 * I, rows2 = (int64_t)E * H;
-  for (int bi = 0; bi < 4; ++bi)
-    if (!tc::encode_map(&bx.m[0][bi], xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, R_max, H, 64, 2 << bi,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tc::encode_map(&bx.m[1][bi], act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, R_max, I, 64, 2 << bi,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorNotSupported;
-  if (!tc::encode_map(&m[0], w13_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows13, H / 2, kKStage / 2, 64,
-                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc::encode_map(&m[1], w13_sb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows13, H / 16, kKStage / 16, 64,
-                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !tc::encode_map(&m[2], w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows2, I / 2, kKStage / 2, 64,
-                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc::encode_map(&m[3], w2_sb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows2, I / 16, kKStage / 16, 64,
-                      CU_TENSOR_MAP_SWIZZLE_NONE))
+  // maps[0..3]: FC1 codes, FC1 scales, FC2 codes, FC2 scales as [half][64
+  // rows][K bytes] boxes; maps[4..5]: token rows as [atom][chunk rows][64
+  // fp16 elements] boxes
+  CUtensorMap m[6];
+  const uint64_t rows13 = (uint64_t)E * 2 * I, rows2 = (uint64_t)E * H;
+  if (!encode_map_3d(&m[0], w13_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, H / 2, rows13, 2, H / 2,
+                     (uint64_t)I * (H / 2), kKStage / 2, 64, 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map_3d(&m[1], w13_sb, CU_TENSOR_MAP_DATA_TYPE_UINT8, H / 16, rows13, 2, H / 16,
+                     (uint64_t)I * (H / 16), kKStage / 16, 64, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_map_3d(&m[2], w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, I / 2, rows2, 2, I / 2,
+                     (uint64_t)64 * (I / 2), kKStage / 2, 64, 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map_3d(&m[3], w2_sb, CU_TENSOR_MAP_DATA_TYPE_UINT8, I / 16, rows2, 2, I / 16,
+                     (uint64_t)64 * (I / 16), kKStage / 16, 64, 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_map_3d(&m[4], xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 64, (uint64_t)R_max, H / 64,
+                     (uint64_t)H * 2, 128, 64, chunk, 4, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map_3d(&m[5], act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 64, (uint64_t)R_max, I / 64,
+                     (uint64_t)I * 2, 128, 64, chunk, 4, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(moe_tc_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(moe_tc_nvfp4_kernel, dim3(sms), dim3(kNvThreads), smem, st, m[0], m[1], m[2],
-                       m[3], bx, p);
+                       m[3], m[4], m[5], p);
 }
 
 }  // namespace moe
