@@ -443,6 +443,7 @@ def main_native(args):
     act16 = torch.empty((R, I), dtype=torch.float16, device=dev) if nvfp4 else None
     fws = M.alloc_workspace(max(256, M.moe_grouped_ffn_workspace_size(shape)), dev)
     stages = (["rmsnorm", "route", "permute", "ffn", "combine"] if fused else
+              ["rmsnorm", "route", "permute", "fc1", "quant", "fc2", "combine"] if fp8 else
               ["rmsnorm", "route", "permute", "fc1", "fc2", "combine"])
 
     def step_b(evs=None):
@@ -481,10 +482,11 @@ def main_native(args):
         else:
             M.moe_grouped_gemm(shape, M.GEMM_FC1_SILU, xp, w13, offsets, act, a_scale=xps,
                                w_scale=s13)
+            mark(4)
             if fp8:
                 M.lib.moe_quantize_fp8_rows(act.data_ptr(), R, I, actq.data_ptr(),
                                             acts.data_ptr(), st.cuda_stream)
-            mark(4)
+                mark(5)
             M.moe_grouped_gemm(shape, M.GEMM_FC2_BF16, actq if fp8 else act, w2, offsets, y,
                                a_scale=acts, w_scale=s2, row_src=row_src, topk_w=tw)
         mark(len(stages) - 1)

@@ -845,48 +845,84 @@ cudaError_t launch_combine(const void* y, bool y_bf16, bool pair_order,
 }
 
 // ========================================================== row E4M3 quantiser
-// One CTA per row: s = absmax / 448 (1 for a zero row); q = e4m3(x / s).
-// Rows at or beyond *nrows_dev (when given) are skipped.
+// One warp per row: s = absmax / 448 (1 for a zero row); q = e4m3(x / s).
+// Rows of up to 2048 columns stay in registers between the absmax and the
+// quantisation (one read of x); longer rows are read twice.  Rows at or
+// beyond *nrows_dev (when given) are skipped.
+constexpr int kQuantRegVec = 8;  // 16-byte vectors per lane held in registers
+
+MOE_DEV uint2 quant8_e4m3(const float (&f)[8], float s) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) lo |= (uint32_t)f_to_e4m3(__fdiv_rn(f[i], s)) << (8 * i);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) hi |= (uint32_t)f_to_e4m3(__fdiv_rn(f[4 + i], s)) << (8 * i);
+  return make_uint2(lo, hi);
+}
+
 __global__ void __launch_bounds__(256) quant_rows_kernel(const bf16* __restrict__ x, int64_t rows,
                                                          int cols, uint8_t* __restrict__ q,
                                                          float* __restrict__ scale,
                                                          const int32_t* __restrict__ nrows_dev) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float red[32];
+  const int lane = threadIdx.x & 31;
   const int64_t nr = nrows_dev ? min(rows, (int64_t)*nrows_dev) : rows;
   const int nv = cols >> 3;
-  for (int64_t r = blockIdx.x; r < nr; r += gridDim.x) {
+  const int64_t wpb = blockDim.x >> 5;
+  for (int64_t r = blockIdx.x * wpb + (threadIdx.x >> 5); r < nr; r += (int64_t)gridDim.x * wpb) {
     const uint4* xr = reinterpret_cast<const uint4*>(x + r * cols);
-    float amax = 0.f;
-    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-      float f[8];
-      unpack8_bf16(xr[v], f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    }
-    amax = block_max(amax, red);
-    const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
     uint2* qr = reinterpret_cast<uint2*>(q + r * cols);
-    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-      float f[8];
-      unpack8_bf16(xr[v], f);
-      uint32_t lo = 0, hi = 0;
+    float amax = 0.f;
+    if (nv <= 32 * kQuantRegVec) {
+      uint4 buf[kQuantRegVec];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) lo |= (uint32_t)f_to_e4m3(__fdiv_rn(f[i], s)) << (8 * i);
+      for (int i = 0; i < kQuantRegVec; ++i) {
+        const int v = lane + 32 * i;
+        if (v < nv) {
+          buf[i] = xr[v];
+          float f[8];
+          unpack8_bf16(buf[i], f);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) hi |= (uint32_t)f_to_e4m3(__fdiv_rn(f[4 + i], s)) << (8 * i);
-      qr[v] = make_uint2(lo, hi);
+          for (int t = 0; t < 8; ++t) amax = fmaxf(amax, fabsf(f[t]));
+        }
+      }
+      amax = warp_max(amax);
+      const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+#pragma unroll
+      for (int i = 0; i < kQuantRegVec; ++i) {
+        const int v = lane + 32 * i;
+        if (v < nv) {
+          float f[8];
+          unpack8_bf16(buf[i], f);
+          qr[v] = quant8_e4m3(f, s);
+        }
+      }
+      if (lane == 0) scale[r] = s;
+    } else {
+      for (int v = lane; v < nv; v += 32) {
+        float f[8];
+        unpack8_bf16(xr[v], f);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) amax = fmaxf(amax, fabsf(f[t]));
+      }
+      amax = warp_max(amax);
+      const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      for (int v = lane; v < nv; v += 32) {
+        float f[8];
+        unpack8_bf16(xr[v], f);
+        qr[v] = quant8_e4m3(f, s);
+      }
+      if (lane == 0) scale[r] = s;
     }
-    if (threadIdx.x == 0) scale[r] = s;
-    __syncthreads();  // red[] is reused by the next row
   }
 }
 
 cudaError_t launch_quant_rows(const void* x, int64_t rows, int cols, void* q, float* scale,
                               const int32_t* nrows_dev, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
-  int64_t blocks = rows < 152 * 64 ? rows : 152 * 64;
+  int64_t blocks = (rows + 7) / 8;  // eight rows (warps) per CTA
+  if (blocks > 152 * 16) blocks = 152 * 16;
   return launch_kernel(quant_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, (const bf16*)x,
                        rows, cols, (uint8_t*)q, scale, nrows_dev);
 }
