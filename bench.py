@@ -393,6 +393,7 @@ def main_native(args):
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
+    lc0 = M.lib.moe_launch_count()  # the library's own host-side launch counter
     for i in range(args.steps):
         if flush is not None:
             flush.zero_()
@@ -400,6 +401,7 @@ def main_native(args):
         fwd()
         ev[i][1].record(st)
     torch.cuda.synchronize()
+    launches_timed = M.lib.moe_launch_count() - lc0
     wall_a = time.perf_counter() - t_wall
     step_ms = [a.elapsed_time(b) for a, b in ev]
     # keep the same load for a moment so the clock sampler sees it
@@ -589,11 +591,6 @@ def main_native(args):
     h2d = x_h.numel() * 2 + (lg_h.numel() * 4 if lg_h is not None else 0)
     d2h = out_h.numel() * 2
 
-    # rmsnorm, [router], top-k, permute (1, or 3 for large batches), gather,
-    # FC1 + FC2 (one fused launch or two), [FP8 quant], combine
-    launches_per_step = (1 + (1 if inp["router_w"] is not None else 0) + 1 +
-                         (3 if T * k > 4096 else 1) + 1 + (1 if fused else 2) +
-                         (1 if fp8 and not fb else 0) + 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = args.cpu_tokens or auto_cpu_tokens(args.workload)
@@ -626,7 +623,8 @@ def main_native(args):
             "stage_path_equals_forward": same,
             "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches": launches_timed,
+            "launches_per_step": launches_timed / args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
             "wall_s_region_a": wall_a,

@@ -108,6 +108,11 @@ typedef void* moe_stream_t; /* cudaStream_t */
 /* MOE_ABI_VERSION of the built library. */
 int32_t moe_abi_version(void);
 
+/* Number of kernels the library has enqueued in this process so far, on every
+ * device and stream (memsets excluded).  A host-side counter for launch
+ * accounting (e.g. kernels per forward); no device synchronisation. */
+int64_t moe_launch_count(void);
+
 /* Thread-local description of the last non-MOE_OK status on this thread
  * (empty string if none).  Never NULL; valid until the next call. */
 const char* moe_last_error(void);

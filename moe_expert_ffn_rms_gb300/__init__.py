@@ -52,6 +52,7 @@ _SZ = ctypes.c_size_t
 
 _SIGS = {
     "moe_abi_version": (_I32, []),
+    "moe_launch_count": (ctypes.c_int64, []),
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_check_device": (ctypes.c_int, []),

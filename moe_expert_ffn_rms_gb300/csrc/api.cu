@@ -493,6 +493,8 @@ extern "C" {
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
 
+int64_t moe_launch_count(void) { return (int64_t)launch_count(); }
+
 const char* moe_last_error(void) { return g_err.c_str(); }
 
 const char* moe_status_string(moe_status s) {

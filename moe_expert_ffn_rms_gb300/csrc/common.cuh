@@ -127,6 +127,11 @@ MOE_DEV void warp_topk(const float (&v)[kTopkPer], int E, int k, int lane, int32
 // MOE_PDL=0 or the calling thread is inside a PdlOff scope with off = true.
 bool pdl_enabled();
 
+// Host-side count of the kernels the library has enqueued (every launch site
+// calls count_launch() after a successful launch).
+void count_launch();
+long long launch_count();
+
 class PdlOff {
  public:
   explicit PdlOff(bool off = true);
@@ -155,7 +160,9 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
-  return e != cudaSuccess ? e : cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 // ------------------------------------------------------------- reductions --

@@ -1301,7 +1301,9 @@ cudaError_t launch_pair(const CUtensorMap& tw, const CUtensorMap& tx, const Para
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, k, tw, tx, p);
-  return e != cudaSuccess ? e : cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 // Prefill on CTA pairs; cudaErrorNotSupported when not covered or not
@@ -1360,7 +1362,9 @@ __global__ void wait_selftest_kernel(long long limit, int* status) {
 
 cudaError_t launch_wait_selftest(long long limit_cycles, int* status, cudaStream_t st) {
   wait_selftest_kernel<<<1, 32, 0, st>>>(limit_cycles, status);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 void engine_init_device() { std::call_once(g_encode_once, load_encode); }
@@ -1514,7 +1518,9 @@ cudaError_t launch_decode_forward_mega(bool fp8, const DecodeForward& f, const v
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], p, f);
-  return e != cudaSuccess ? e : cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 }  // namespace moe

@@ -8,9 +8,15 @@
 #include <float.h>
 #include <stdlib.h>
 
+#include <atomic>
+
 namespace {
 thread_local bool t_pdl_off = false;
+std::atomic<long long> g_launch_count{0};
 }  // namespace
+
+void count_launch() { g_launch_count.fetch_add(1, std::memory_order_relaxed); }
+long long launch_count() { return g_launch_count.load(std::memory_order_relaxed); }
 
 bool pdl_enabled() {
   static const bool on = [] {

@@ -42,6 +42,14 @@ def test_library_resolves_every_symbol_at_load(M):
     ctypes.CDLL(M.LIB_PATH, mode=os.RTLD_NOW)
 
 
+def test_launch_counter_host_only(M):
+    # host-side counter: readable without a GPU, and nothing launched here
+    n = M.lib.moe_launch_count()
+    assert n >= 0
+    assert M.lib.moe_rmsnorm(None, None, 4, 256, 1e-6, None, None, None, None) == 1
+    assert M.lib.moe_launch_count() == n  # a rejected call enqueues nothing
+
+
 def test_abi_version_and_status_strings(M):
     assert M.abi_version() == 1
     assert M.lib.moe_status_string(0) == b"MOE_OK"

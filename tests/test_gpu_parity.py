@@ -551,6 +551,19 @@ def test_forward_reference_workloads(M, cfg, sample):
     torch.cuda.empty_cache()
 
 
+def test_launch_counter_counts_the_forward(M):
+    """The forward of the tiny workload enqueues the same number of kernels
+    every call: rms_norm, router + top-k, permute, gather, fused FFN, combine."""
+    inp = workloads.make_inputs("c1_tiny", DEV)
+    _run_forward(M, inp)
+    n0 = M.lib.moe_launch_count()
+    _run_forward(M, inp)
+    n1 = M.lib.moe_launch_count()
+    _run_forward(M, inp)
+    n2 = M.lib.moe_launch_count()
+    assert n1 - n0 == n2 - n1 == 6
+
+
 def test_forward_is_deterministic(M):
     inp = workloads.make_inputs("c1_tiny", DEV, shape=SMALL["ragged_b"], seed=3)
     o1, i1, w1 = _run_forward(M, inp)
