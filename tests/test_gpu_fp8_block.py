@@ -118,6 +118,9 @@ SHAPES = {
     "two_chunks": ("c1_tiny", workloads.Shape(T=300, H=256, E=2, k=1, I=384), "learned"),
     "single_token": ("c1_tiny", workloads.Shape(T=1, H=768, E=8, k=4, I=128), "learned"),
     "odd_groups": ("c1_tiny", workloads.Shape(T=7, H=512, E=4, k=2, I=640), "learned"),
+    # the largest K of each GEMM: 64 scale groups (H or I = 8192)
+    "max_groups_fc1": ("c1_tiny", workloads.Shape(T=6, H=8192, E=4, k=2, I=256), "learned"),
+    "max_groups_fc2": ("c1_tiny", workloads.Shape(T=6, H=256, E=4, k=2, I=8192), "learned"),
 }
 
 

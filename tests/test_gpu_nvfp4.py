@@ -106,6 +106,7 @@ SHAPES = {
     "rows_64": ("c1_tiny", workloads.Shape(T=64, H=256, E=4, k=2, I=256), "learned"),
     "two_chunks": ("c1_tiny", workloads.Shape(T=300, H=256, E=2, k=1, I=512), "learned"),
     "single_token": ("c1_tiny", workloads.Shape(T=1, H=768, E=8, k=4, I=256), "learned"),
+    "wide_hidden": ("c3_decode_skewed", workloads.Shape(T=8, H=7168, E=16, k=4, I=512), "zipf"),
 }
 
 
