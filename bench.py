@@ -693,8 +693,9 @@ def kernel_source_sha(workload):
 def read_traffic(kernel, workload):
     """DRAM traffic per launch from a committed ncu summary, if it was taken on
     the current kernel source; else None."""
+    import workloads
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    if not os.path.exists(p):
+    if not os.path.exists(p) or workload not in workloads.CONFIGS:
         return None
     sha = kernel_source_sha(workload)
     with open(p) as f:
