@@ -22,8 +22,11 @@
  *           over expert weights streamed from HBM, split by columns (split-N).
  *   [SM]    "vLLM's adaptation to different GPU SM architectures", sections
  *           3.1/3.2 (W8A8 scaled GEMM, FP8 E4M3, output-first signature
- *           cutlass_scaled_mm(c, ...)) and 4.3 (experts take hidden_states,
- *           w1, w2; small batches want few launches).
+ *           cutlass_scaled_mm(c, ...)), 4.3 (experts take hidden_states,
+ *           w1, w2; small batches want few launches), 4.4 and the MoE GEMM
+ *           support table (FP8 block-wise and NVFP4 expert weights), and the
+ *           Hopper data-flow figure (block-wise FP8 dequantised inside the
+ *           GEMM loop).
  *
  * Conventions shared by every entry point:
  *   - Every tensor pointer is a DEVICE pointer owned by the caller, unless a
@@ -110,7 +113,8 @@ int32_t moe_abi_version(void);
 
 /* Number of kernels the library has enqueued in this process so far, on every
  * device and stream (memsets excluded).  A host-side counter for launch
- * accounting (e.g. kernels per forward); no device synchronisation. */
+ * accounting (e.g. kernels per forward); no device synchronisation.  The
+ * pages describe no such call; it has no counterpart there. */
 int64_t moe_launch_count(void);
 
 /* Thread-local description of the last non-MOE_OK status on this thread
