@@ -227,7 +227,7 @@ int route_splits(int T, int H, int E) {
   const int tiles = ((T + rt.tt - 1) / rt.tt) * ((E + rt.te - 1) / rt.te);
   const int steps = H / RT_K;
   int ks = (4 * 152 + tiles - 1) / tiles;  // about four CTAs per SM
-  const int min_steps = 8;                 // at least 256 K per chunk
+  const int min_steps = 4;                 // at least 128 K per chunk
   if (ks > steps / min_steps) ks = steps / min_steps;
   if (ks < 1) ks = 1;
   const int per = (steps + ks - 1) / ks;  // K steps per chunk
@@ -271,14 +271,30 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
   float v[kTopkPer];
 #pragma unroll
   for (int i = 0; i < kTopkPer; ++i) v[i] = 0.f;
-  // Partial sums: chunk z outer, experts inner, so a lane has up to
-  // kTopkPer loads in flight; each logit is still summed in z order.
+  // Partial sums: four chunks are loaded before they are added (4 x
+  // kTopkPer loads in flight per lane); each logit is still summed in z order.
   const float* pt = part + (size_t)t * tstride;
-  for (int z = 0; z < ks; ++z) {
+  int z = 0;
+  for (; z + 4 <= ks; z += 4) {
+    float l[4][kTopkPer];
+#pragma unroll
+    for (int zz = 0; zz < 4; ++zz)
+#pragma unroll
+      for (int i = 0; i < kTopkPer; ++i) {
+        const int e = lane + 32 * i;
+        l[zz][i] = e < E ? pt[(size_t)(z + zz) * zstride + e] : 0.f;
+      }
+#pragma unroll
+    for (int zz = 0; zz < 4; ++zz)
+#pragma unroll
+      for (int i = 0; i < kTopkPer; ++i)
+        if (lane + 32 * i < E) v[i] += l[zz][i];
+  }
+  for (; z < ks; ++z) {
 #pragma unroll
     for (int i = 0; i < kTopkPer; ++i) {
       const int e = lane + 32 * i;
-      if (e < E) v[i] += pt[z * zstride + e];
+      if (e < E) v[i] += pt[(size_t)z * zstride + e];
     }
   }
 #pragma unroll
