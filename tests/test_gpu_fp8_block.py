@@ -121,6 +121,7 @@ SHAPES = {
     # the largest K of each GEMM: 64 scale groups (H or I = 8192)
     "max_groups_fc1": ("c1_tiny", workloads.Shape(T=6, H=8192, E=4, k=2, I=256), "learned"),
     "max_groups_fc2": ("c1_tiny", workloads.Shape(T=6, H=256, E=4, k=2, I=8192), "learned"),
+    "max_experts": ("c3_decode_skewed", workloads.Shape(T=40, H=256, E=256, k=8, I=256), "zipf"),
 }
 
 

@@ -107,6 +107,7 @@ SHAPES = {
     "two_chunks": ("c1_tiny", workloads.Shape(T=300, H=256, E=2, k=1, I=512), "learned"),
     "single_token": ("c1_tiny", workloads.Shape(T=1, H=768, E=8, k=4, I=256), "learned"),
     "wide_hidden": ("c3_decode_skewed", workloads.Shape(T=8, H=7168, E=16, k=4, I=512), "zipf"),
+    "max_experts": ("c3_decode_skewed", workloads.Shape(T=40, H=256, E=256, k=8, I=256), "zipf"),
 }
 
 
@@ -156,3 +157,19 @@ def test_grouped_ffn_nvfp4_matches_forward(M):
     M.moe_combine(y, rop, T, k, out2, pair_order=True)
     torch.cuda.synchronize()
     assert torch.equal(out, out2)
+
+
+def test_forward_nvfp4_zero_tokens(M):
+    shape = M.make_shape(0, 256, 8, 256, 2, nvfp4=True)
+    ws = M.alloc_workspace(max(256, M.moe_ffn_workspace_size(shape)), DEV)
+    w = torch.ones((256,), dtype=torch.bfloat16, device=DEV)
+    q13 = torch.zeros((8, 512, 128), dtype=torch.uint8, device=DEV)
+    sb13 = torch.zeros((8, 512, 16), dtype=torch.uint8, device=DEV)
+    q2 = torch.zeros((8, 256, 128), dtype=torch.uint8, device=DEV)
+    sb2 = torch.zeros((8, 256, 16), dtype=torch.uint8, device=DEV)
+    sg = torch.ones((8,), dtype=torch.float32, device=DEV)
+    rw = torch.zeros((256, 8), dtype=torch.float32, device=DEV)
+    out = torch.empty((1, 256), dtype=torch.bfloat16, device=DEV)
+    M.moe_ffn_forward_nvfp4(shape, w, w, q13, sb13, sg, q2, sb2, sg, out, ws, router_w=rw)
+    torch.cuda.synchronize()
+    assert M.device_status() == 0
