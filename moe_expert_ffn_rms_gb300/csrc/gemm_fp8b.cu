@@ -683,11 +683,13 @@ MOE_DEV void fma2(float& a0, float& a1, float v0, float v1, float f) {
       : "f"(v0), "f"(v1), "f"(f));
 }
 
-constexpr int kThreadsT = 320;       // warp 0 TMA, 1 MMA (+ TMEM owner), 2-9 epilogue
+constexpr int kThreadsT = 352;       // warp 0 TMA, 1 MMA (+ TMEM owner), 2-9 epilogue, 10 MMA
+constexpr int kMma2WarpT = 10;
 constexpr int kTileBytesT = 128 * 128;
 constexpr int kStageBytesT = 2 * kTileBytesT;  // token tile + weight tile of one K group
 constexpr int kSlotsT = 4;
 constexpr int kMaxStagesT = 6;
+static_assert(kSlotsT % 2 == 0, "each TMEM slot belongs to one of the two MMA issuers");
 
 struct TParams {
   const int32_t* offsets;
@@ -705,6 +707,33 @@ struct TParams {
   int* status;
 };
 
+// What an epilogue thread needs of one unit: its token row and the scale
+// rows of its two 32-column runs.
+struct TileCtx {
+  int r, nt;
+  bool rvalid;
+  const float* sa_row;      // activation scales of row r, one per K group
+  const float* sw_lo;       // weight-tile scales of the two column runs
+  const float* sw_hi;
+};
+
+template <int MODE>
+MOE_DEV TileCtx tile_ctx(int u, const int* s_off, const int* s_up, const TParams& p, int lrow) {
+  const Unit un = unit_of(u, s_off, s_up, p.E, p.nt, 128);
+  const int nblk = p.N_w / kGroup;
+  // FC1: gate rows nt*64.. and the matching up rows I further; FC2: one tile
+  const int rb_lo = MODE == 1 ? (un.nt * 64) / kGroup : un.nt;
+  const int rb_hi = MODE == 1 ? (p.I + un.nt * 64) / kGroup : un.nt;
+  TileCtx c;
+  c.nt = un.nt;
+  c.rvalid = lrow < un.rows;
+  c.r = un.row0 + lrow;
+  c.sa_row = p.a_scale + (size_t)(c.rvalid ? c.r : 0) * p.kg;
+  c.sw_lo = p.w_scale + ((size_t)un.e * nblk + rb_lo) * p.kg;
+  c.sw_hi = p.w_scale + ((size_t)un.e * nblk + rb_hi) * p.kg;
+  return c;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
     const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
@@ -716,7 +745,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
   __shared__ __align__(8) uint64_t sempty[kMaxStagesT];
   __shared__ __align__(8) uint64_t kfull[kSlotsT];
   __shared__ __align__(8) uint64_t kempty[kSlotsT];
-  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t drain_bar[2];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -732,7 +761,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
       mbar_init(&kfull[q], 1);
       mbar_init(&kempty[q], 8);  // lane 0 of each epilogue warp
     }
-    mbar_init(&drain_bar, 1);
+    mbar_init(&drain_bar[0], 1);
+    mbar_init(&drain_bar[1], 1);
     s_abort = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_a);
@@ -818,42 +848,52 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
         drain_armed(sfull, p.stages, armed, armed_ph);
       }
     }
-  } else if (warp == 1) {
-    // ====================================================== MMA issuer
+  } else if (warp == 1 || warp == kMma2WarpT) {
+    // ===================================================== MMA issuers
+    // Two threads issue the MMAs: warp 1 the even K groups (counted over all
+    // units), warp 10 the odd ones, so one thread's per-instruction issue
+    // cost no longer paces the tensor pipe.  Each group has its own stage and
+    // TMEM slot, and both rings have even lengths, so every stage and every
+    // slot belongs to one issuer and is used in order.
     if (lane == 0) {
-      int s = 0, q = 0;
+      const int par = warp == 1 ? 0 : 1;
+      int s = 0, q = 0, gi = 0;
       uint32_t ph = 0, qph = 0;
       bool ok = true, issued = false;
       const uint32_t idesc = make_idesc(128, 0u);  // M = N = 128, E4M3 A and B
       for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
-        for (int g = 0; g < p.kg; ++g) {
-          if (!mbar_wait(&sfull[s], ph, &s_abort) || !mbar_wait(&kempty[q], qph ^ 1, &s_abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(ring + (size_t)s * kStageBytesT);
-          const uint32_t d = tmem + q * 128;
+        for (int g = 0; g < p.kg; ++g, ++gi) {
+          if ((gi & 1) == par) {
+            if (!mbar_wait(&sfull[s], ph, &s_abort) || !mbar_wait(&kempty[q], qph ^ 1, &s_abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(ring + (size_t)s * kStageBytesT);
+            const uint32_t d = tmem + q * 128;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // each group starts a fresh sum
-            mma_e4m3(d, sw128_desc(a0 + kk * 32), sw128_desc(a0 + kTileBytesT + kk * 32), idesc,
-                     kk ? 1u : 0u);
-          issued = true;
-          mma_commit(&sempty[s]);
-          mma_commit(&kfull[q]);
+            for (int kk = 0; kk < 4; ++kk)  // each group starts a fresh sum
+              mma_e4m3(d, sw128_desc(a0 + kk * 32), sw128_desc(a0 + kTileBytesT + kk * 32), idesc,
+                       kk ? 1u : 0u);
+            issued = true;
+            mma_commit(&sempty[s]);
+            mma_commit(&kfull[q]);
+          }
           if (++s == p.stages) { s = 0; ph ^= 1; }
           if (++q == kSlotsT) { q = 0; qph ^= 1; }
         }
       }
-      for (int i = 0; ok && i < kSlotsT; ++i) {  // tail: every slot handed back
-        ok = mbar_wait(&kempty[q], qph ^ 1, &s_abort);
+      // tail: this issuer's slots handed back (the next four ring positions
+      // are the last use of each slot)
+      for (int i = 0; ok && i < kSlotsT; ++i, ++gi) {
+        if ((gi & 1) == par) ok = mbar_wait(&kempty[q], qph ^ 1, &s_abort);
         if (++q == kSlotsT) { q = 0; qph ^= 1; }
       }
       if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
       if (issued) {
-        mma_commit(&drain_bar);
+        mma_commit(&drain_bar[par]);
         const long long t0 = clock64();
-        while (!mbar_try_wait(&drain_bar, 0) && clock64() - t0 < kSpinLimitCycles) {
+        while (!mbar_try_wait(&drain_bar[par], 0) && clock64() - t0 < kSpinLimitCycles) {
         }
       }
     }
@@ -863,34 +903,54 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
     // quarter) and half h = (w - 2) / 4 of the columns: FC1 gate columns
     // 32h .. 32h + 31 with the matching up columns 64 + 32h ..; FC2 columns
     // 64h .. 64h + 63.  acc[0..31] and acc[32..63] are those two 32-column runs.
+    // The MMA thread runs at most four K groups ahead, so the global loads a
+    // unit needs are issued early: the next group's scales during this one
+    // (at a unit's last group, the next unit's first), FC2's destination row
+    // one unit ahead and its routing weight halfway through the unit.
     const int h = (warp - 2) >> 2;
     const int qtr = warp & 3;
     const int lrow = qtr * 32 + lane;
     const uint32_t tlane = (uint32_t)(qtr * 32) << 16;
     const int c_lo = MODE == 1 ? 32 * h : 64 * h;
     const int c_hi = MODE == 1 ? 64 + 32 * h : 64 * h + 32;
-    const int nblk = p.N_w / kGroup;
     int q = 0;
     uint32_t qph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
-      const Unit un = unit_of(u, s_off, s_up, p.E, p.nt, 128);
-      const bool rvalid = lrow < un.rows;
-      const int r = un.row0 + lrow;
-      // weight tiles of the two column runs
-      const int rb_lo = MODE == 1 ? (un.nt * 64) / kGroup : un.nt;
-      const int rb_hi = MODE == 1 ? (p.I + un.nt * 64) / kGroup : un.nt;
-      const float* sw_lo = p.w_scale + ((size_t)un.e * nblk + rb_lo) * p.kg;
-      const float* sw_hi = p.w_scale + ((size_t)un.e * nblk + rb_hi) * p.kg;
-      const float* sa_row = p.a_scale + (size_t)(rvalid ? r : 0) * p.kg;
+    int u = blockIdx.x;
+    TileCtx cur{}, nxt{};
+    float sa = 0.f, wl = 0.f, wh = 0.f;
+    int orow = 0, orow_n = 0;
+    if (u < U) {
+      cur = tile_ctx<MODE>(u, s_off, s_up, p, lrow);
+      sa = cur.rvalid ? cur.sa_row[0] : 0.f;
+      wl = cur.sw_lo[0];
+      wh = cur.sw_hi[0];
+      if (MODE == 3 && cur.rvalid) orow = p.row_src[cur.r];
+    }
+    for (; ok && u < U; u += gridDim.x) {
+      const bool has_next = u + (int)gridDim.x < U;
+      if (has_next) {
+        nxt = tile_ctx<MODE>(u + gridDim.x, s_off, s_up, p, lrow);
+        if (MODE == 3 && nxt.rvalid) orow_n = p.row_src[nxt.r];
+      }
+      float tw = 0.f;
       float acc[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) acc[c] = 0.f;
-      float sa = rvalid ? sa_row[0] : 0.f, wl = sw_lo[0], wh = sw_hi[0];
       for (int g = 0; g < p.kg; ++g) {
-        // next group's scales load while this group's product is awaited
-        const int gn = g + 1 < p.kg ? g + 1 : g;
-        const float sa_n = rvalid ? sa_row[gn] : 0.f, wl_n = sw_lo[gn], wh_n = sw_hi[gn];
+        // the scales of the group after this one load while this group's
+        // product is awaited
+        float sa_n = 0.f, wl_n = 0.f, wh_n = 0.f;
+        if (g + 1 < p.kg) {
+          sa_n = cur.rvalid ? cur.sa_row[g + 1] : 0.f;
+          wl_n = cur.sw_lo[g + 1];
+          wh_n = cur.sw_hi[g + 1];
+        } else if (has_next) {
+          sa_n = nxt.rvalid ? nxt.sa_row[0] : 0.f;
+          wl_n = nxt.sw_lo[0];
+          wh_n = nxt.sw_hi[0];
+        }
+        if (MODE == 3 && g == (p.kg >> 1) && cur.rvalid) tw = p.topk_w[orow];
         int wok = 1;
         if (lane == 0) wok = mbar_wait(&kfull[q], qph, &s_abort);
         wok = __shfl_sync(0xffffffffu, wok, 0);
@@ -918,28 +978,33 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
         wh = wh_n;
       }
       if (!ok) break;
-      if (!rvalid) continue;
-      bf16* out = reinterpret_cast<bf16*>(p.out);
-      if (MODE == 1) {
-        // a = bf16(silu(g) u): 32 columns from nt*64 + 32h, 64 bytes
-        uint32_t pk[16];
+      if (cur.rvalid) {
+        bf16* out = reinterpret_cast<bf16*>(p.out);
+        if (MODE == 1) {
+          // a = bf16(silu(g) u): 32 columns from nt*64 + 32h, 64 bytes; silu
+          // with the fast exponential and divide, as in the decode epilogue
+          uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2)
-          pk[c / 2] = pack2_bf16(silu_f(acc[c]) * acc[32 + c], silu_f(acc[c + 1]) * acc[33 + c]);
-        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * p.ldo + un.nt * 64 + 32 * h);
+          for (int c = 0; c < 32; c += 2) {
+            const float g0 = acc[c], g1 = acc[c + 1];
+            pk[c / 2] = pack2_bf16(__fdividef(g0, 1.0f + __expf(-g0)) * acc[32 + c],
+                                   __fdividef(g1, 1.0f + __expf(-g1)) * acc[33 + c]);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(out + (size_t)cur.r * p.ldo + cur.nt * 64 + 32 * h);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-      } else {
-        // routing weight x y, bf16, at row row_src[r]: 64 columns from nt*128 + 64h
-        const int orow = p.row_src[r];
-        const float tw = p.topk_w[orow];
-        uint32_t pk[32];
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        } else {
+          // routing weight x y, bf16, at row row_src[r]: 64 columns from nt*128 + 64h
+          uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) pk[c / 2] = pack2_bf16(acc[c] * tw, acc[c + 1] * tw);
-        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)orow * p.ldo + un.nt * 128 + 64 * h);
+          for (int c = 0; c < 64; c += 2) pk[c / 2] = pack2_bf16(acc[c] * tw, acc[c + 1] * tw);
+          uint4* dst = reinterpret_cast<uint4*>(out + (size_t)orow * p.ldo + cur.nt * 128 + 64 * h);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 8; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
       }
+      cur = nxt;
+      orow = orow_n;
     }
     if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
   }
@@ -977,6 +1042,8 @@ cudaError_t launch_tile(const void* a, const float* a_scale, const uint8_t* w, c
   if (e != cudaSuccess) return e;
   int stages = (int)((kSmemLimitB - (int)fa.sharedSizeBytes - 1024) / kStageBytesT);
   if (stages > kMaxStagesT) stages = kMaxStagesT;
+  stages &= ~1;  // even: each stage belongs to one of the two MMA issuers
+  if (stages < 2) return cudaErrorNotSupported;
   p.stages = stages;
   const size_t smem = 1024 + (size_t)stages * kStageBytesT;
   CUtensorMap ma, mw;
