@@ -140,7 +140,8 @@ __global__ void __launch_bounds__(256) gather_rows_f16_kernel(const int32_t* __r
 }
 
 // ------------------------------------------------------- fused FFN kernel --
-constexpr int kNvThreads = 448;   // warp 0 TMA, 1 MMA, 2-5 epilogue, 6-13 dequantise
+constexpr int kNvThreads = 480;   // warp 0 TMA, 1 MMA, 2-5 epilogue, 6-13 dequantise, 14 MMA
+constexpr int kMma2WarpNv = 14;
 constexpr int kDqWarps = 8;       // two per TMEM lane quarter: each takes two of a stage's four atoms
 constexpr int kKStage = 256;      // K elements per stage: 128 B of codes, 16 B of scales per row
 constexpr int kRowsNv = 128;      // weight rows per unit (MMA M)
@@ -150,7 +151,9 @@ constexpr int kMaxStagesNv = 8;
 constexpr int kBoxRowsNv = 16;    // token rows per TMA box
 constexpr int kRingNv = 4;        // claimed-unit slots
 constexpr int kMaxChunkNv = 64;   // token rows per unit (MMA N)
-// TMEM columns: two fp32 accumulators of kMaxChunkNv columns, then kASlots
+// TMEM columns: two fp32 accumulators of kMaxChunkNv columns (each, for
+// chunks of at most 32 token rows, two banks of chunk columns: one per MMA
+// issuer), then kASlots
 // slots of one stage's fp16 A (128 lanes x 256 K elements = 128 columns: four
 // 64-element atoms of 32 columns).  The dequantising warps and the MMA hand
 // over whole stages, so each side waits on one barrier per stage.
@@ -186,6 +189,22 @@ MOE_DEV void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar, int x,
       ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
       "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
       : "memory");
+}
+
+// 16 accumulator columns at taddr: bank 0's, bank 1's (chunk columns
+// further), or their sum.
+MOE_DEV void load_acc16(uint32_t taddr, int chunk, bool bank0, bool bank1, float* v) {
+  if (bank0 && bank1) {
+    float w[16];
+    tmem_ld16(taddr, v);
+    tmem_ld16(taddr + chunk, w);
+    tmem_ld_wait();
+#pragma unroll
+    for (int t = 0; t < 16; ++t) v[t] += w[t];
+  } else {
+    tmem_ld16(bank1 ? taddr + chunk : taddr, v);
+    tmem_ld_wait();
+  }
 }
 
 struct NvParams {
@@ -232,7 +251,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
   __shared__ __align__(8) uint64_t tempty[2];
   __shared__ __align__(8) uint64_t ufull[kRingNv];
   __shared__ __align__(8) uint64_t uempty[kRingNv];
-  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t drain_bar[2];
   __shared__ __align__(8) uint64_t xch_bar;
   __shared__ int s_uring[kRingNv];
   __shared__ uint32_t s_tmem;
@@ -242,6 +261,9 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~(uintptr_t)1023);
+  // two MMA issuers, each summing alternate K stages into its own bank of
+  // chunk columns, when two banks fit an accumulator; else warp 1 alone
+  const bool dual = 2 * p.chunk <= kAccColsNv;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -253,14 +275,15 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
       mbar_init(&aempty[q], 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
+      mbar_init(&tfull[a], dual ? 2 : 1);  // a commit of each issuer
       mbar_init(&tempty[a], 128);
     }
     for (int i = 0; i < kRingNv; ++i) {
       mbar_init(&ufull[i], 1);
-      mbar_init(&uempty[i], 1 + 4 + kDqWarps);  // MMA thread, epilogue and dequantising warps
+      mbar_init(&uempty[i], 2 + 4 + kDqWarps);  // MMA threads, epilogue and dequantising warps
     }
-    mbar_init(&drain_bar, 1);
+    mbar_init(&drain_bar[0], 1);
+    mbar_init(&drain_bar[1], 1);
     mbar_init(&xch_bar, 128);
     s_abort = 0;
     fence_mbar_init();
@@ -401,11 +424,19 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         drain_armed(sfull, p.stages, armed, armed_ph);
       }
     }
-  } else if (warp == 1) {
-    // ====================================================== MMA issuer
+  } else if (warp == 1 || warp == kMma2WarpNv) {
+    // ===================================================== MMA issuers
+    // With two issuers, warp 1 takes the CTA's even K stages (counted over
+    // all units) and warp 14 the odd ones, each into its own bank.  A stage,
+    // an A slot and a ring slot may pass between the issuers, but every wait
+    // stays in order: an issuer reaches stage n only after its own stage
+    // n - 2, so the loads and conversions up to n - 2 (in order) are done and
+    // no barrier it waits on can be a whole phase behind; and none can be a
+    // phase ahead, since that needs this issuer's own stage n released.
     if (lane == 0) {
+      const int par = warp == 1 ? 0 : 1;
       int s = 0, q = 0, acc = 0;
-      uint32_t ph = 0, qph = 0, aph = 0;
+      uint32_t ph = 0, qph = 0, aph = 0, n = 0;
       bool ok = true;
       bool issued = false;
       for (int i = 0; ok; ++i) {
@@ -417,40 +448,46 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         const int kst = p.job[un.job].kst;
         if (!mbar_wait(&tempty[acc], aph ^ 1, &s_abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d = tmem + acc * kAccColsNv;
+        const uint32_t d = tmem + acc * kAccColsNv + (dual ? par * p.chunk : 0);
         const uint32_t idesc = make_idesc(((un.rows + 15) / 16) * 16, 0u);  // fp16 A and B
-        for (int ks = 0; ks < kst && ok; ++ks) {
-          if (!mbar_wait_spin(&sfull[s], ph, &s_abort) || !mbar_wait_spin(&afull[q], qph, &s_abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t b0 = smem_u32(ring + (size_t)s * p.stage_bytes);
-          const uint32_t a0 = tmem + kACol0 + q * kAColsPerStage;
-          for (int a = 0; a < 4; ++a) {
-            const uint32_t bb = b0 + a * p.chunk * 128;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {  // four 16-element K steps (8 columns) per atom
-              const uint32_t accum = (ks | a | kk) ? 1u : 0u;
-              mma_f16_ts(d, a0 + a * kAColsPerAtom + kk * 8, sw128_desc(bb + kk * 32), idesc, accum);
+        bool first = true;  // this issuer's first stage of the unit starts its sum
+        for (int ks = 0; ks < kst && ok; ++ks, ++n) {
+          if (dual ? (int)(n & 1) == par : par == 0) {
+            if (!mbar_wait_spin(&sfull[s], ph, &s_abort) ||
+                !mbar_wait_spin(&afull[q], qph, &s_abort)) {
+              ok = false;
+              break;
             }
+            tc_fence_after();
+            const uint32_t b0 = smem_u32(ring + (size_t)s * p.stage_bytes);
+            const uint32_t a0 = tmem + kACol0 + q * kAColsPerStage;
+            for (int a = 0; a < 4; ++a) {
+              const uint32_t bb = b0 + a * p.chunk * 128;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {  // four 16-element K steps (8 columns) per atom
+                const uint32_t accum = (!first || a || kk) ? 1u : 0u;
+                mma_f16_ts(d, a0 + a * kAColsPerAtom + kk * 8, sw128_desc(bb + kk * 32), idesc,
+                           accum);
+              }
+            }
+            first = false;
+            issued = true;
+            mma_commit(&aempty[q]);
+            mma_commit(&sempty[s]);
           }
-          issued = true;
-          mma_commit(&aempty[q]);
           if (++q == kASlots) { q = 0; qph ^= 1; }
-          mma_commit(&sempty[s]);
           if (++s == p.stages) { s = 0; ph ^= 1; }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
+        if (dual || par == 0) mma_commit(&tfull[acc]);
         if (++acc == 2) { acc = 0; aph ^= 1; }
       }
       if (ok) ok = accumulator_tail(tempty, acc, aph, &s_abort);
       if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
       if (issued) {
-        mma_commit(&drain_bar);
+        mma_commit(&drain_bar[par]);
         const long long t0 = clock64();
-        while (!mbar_try_wait(&drain_bar, 0) && clock64() - t0 < kSpinLimitCycles) {
+        while (!mbar_try_wait(&drain_bar[par], 0) && clock64() - t0 < kSpinLimitCycles) {
         }
       }
     }
@@ -460,7 +497,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
     const int qw = warp & 3;
     const int lrow = qw * 32 + lane;
     int acc = 0;
-    uint32_t aph = 0, xph = 0;
+    uint32_t aph = 0, xph = 0, n0 = 0;
     for (int i = 0;; ++i) {
       const int u = next_unit(i);
       __syncwarp();
@@ -472,6 +509,12 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
       if (u < 0) break;
       const Unit un = decode_unit(u);
       const NvJob& j = p.job[un.job];
+      // banks holding this unit's sums: bank b has the stages n0 + ks with
+      // n0 + ks = b (mod 2)
+      const int kst = j.kst;
+      const bool bank0 = !dual || kst >= 2 || (n0 & 1) == 0;
+      const bool bank1 = dual && (kst >= 2 || (n0 & 1) == 1);
+      n0 += (uint32_t)kst;
       if (!mbar_wait(&tfull[acc], aph, &s_abort)) {
         flag_status(p.status, MOE_ERR_TIMEOUT);
         break;
@@ -487,8 +530,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         const int n = un.nt * 64 + (lrow & 63);
         for (int c = 0; c < ncols && ok; c += 16) {
           float v[16];
-          tmem_ld16(tbase + c, v);
-          tmem_ld_wait();
+          load_acc16(tbase + c, p.chunk, bank0, bank1, v);
           if (!is_gate) {
 #pragma unroll
             for (int t = 0; t < 16; ++t) s_xch[(lrow - 64) * 17 + t] = v[t] * sg;
@@ -515,8 +557,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         const int n = un.nt * 128 + lrow;
         for (int c = 0; c < ncols; c += 16) {
           float v[16];
-          tmem_ld16(tbase + c, v);
-          tmem_ld_wait();
+          load_acc16(tbase + c, p.chunk, bank0, bank1, v);
           if (n < j.n_out) {
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
