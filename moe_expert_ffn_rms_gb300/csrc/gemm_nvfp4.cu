@@ -140,8 +140,8 @@ __global__ void __launch_bounds__(256) gather_rows_f16_kernel(const int32_t* __r
 }
 
 // ------------------------------------------------------- fused FFN kernel --
-constexpr int kNvThreads = 480;   // warp 0 TMA, 1 MMA, 2-5 epilogue, 6-13 dequantise, 14 MMA
-constexpr int kMma2WarpNv = 14;
+constexpr int kNvThreads = 512;   // warp 0 TMA, 1 MMA, 2-5 epilogue, 6-13 dequantise, 14-15 MMA
+constexpr int kMaxIssuersNv = 3;  // MMA threads: warp 1, then warps 14, 15
 constexpr int kDqWarps = 8;       // two per TMEM lane quarter: each takes two of a stage's four atoms
 constexpr int kKStage = 256;      // K elements per stage: 128 B of codes, 16 B of scales per row
 constexpr int kRowsNv = 128;      // weight rows per unit (MMA M)
@@ -151,9 +151,8 @@ constexpr int kMaxStagesNv = 8;
 constexpr int kBoxRowsNv = 16;    // token rows per TMA box
 constexpr int kRingNv = 4;        // claimed-unit slots
 constexpr int kMaxChunkNv = 64;   // token rows per unit (MMA N)
-// TMEM columns: two fp32 accumulators of kMaxChunkNv columns (each, for
-// chunks of at most 32 token rows, two banks of chunk columns: one per MMA
-// issuer), then kASlots
+// TMEM columns: two fp32 accumulators of kMaxChunkNv columns (each split
+// into one bank of chunk columns per MMA issuer), then kASlots
 // slots of one stage's fp16 A (128 lanes x 256 K elements = 128 columns: four
 // 64-element atoms of 32 columns).  The dequantising warps and the MMA hand
 // over whole stages, so each side waits on one barrier per stage.
@@ -165,6 +164,9 @@ constexpr int kASlots = 3;
 constexpr int kTmemColsNv = 512;  // >= kACol0 + kASlots * kAColsPerStage, a power of two
 constexpr int kSmemLimitNv = 227 * 1024;
 static_assert(kACol0 + kASlots * kAColsPerStage <= kTmemColsNv, "TMEM budget");
+// an issuer's own previous stage must be at least kASlots back for its A-slot
+// waits to stay in order (see the MMA issuers)
+static_assert(kMaxIssuersNv <= kASlots, "A slots per issuer");
 
 struct NvJob {
   const float* sg;          // [E] fp32 matrix scales
@@ -191,19 +193,23 @@ MOE_DEV void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar, int x,
       : "memory");
 }
 
-// 16 accumulator columns at taddr: bank 0's, bank 1's (chunk columns
-// further), or their sum.
-MOE_DEV void load_acc16(uint32_t taddr, int chunk, bool bank0, bool bank1, float* v) {
-  if (bank0 && bank1) {
-    float w[16];
-    tmem_ld16(taddr, v);
-    tmem_ld16(taddr + chunk, w);
-    tmem_ld_wait();
+// 16 accumulator columns at taddr summed over the banks in the mask (bank b
+// b * chunk columns further), in bank order.
+MOE_DEV void load_acc16(uint32_t taddr, int chunk, uint32_t banks, float* v) {
+  bool any = false;
+  for (int b = 0; b < kMaxIssuersNv; ++b) {
+    if (!((banks >> b) & 1u)) continue;
+    if (!any) {
+      tmem_ld16(taddr + b * chunk, v);
+      tmem_ld_wait();
+      any = true;
+    } else {
+      float w[16];
+      tmem_ld16(taddr + b * chunk, w);
+      tmem_ld_wait();
 #pragma unroll
-    for (int t = 0; t < 16; ++t) v[t] += w[t];
-  } else {
-    tmem_ld16(bank1 ? taddr + chunk : taddr, v);
-    tmem_ld_wait();
+      for (int t = 0; t < 16; ++t) v[t] += w[t];
+    }
   }
 }
 
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
   __shared__ __align__(8) uint64_t tempty[2];
   __shared__ __align__(8) uint64_t ufull[kRingNv];
   __shared__ __align__(8) uint64_t uempty[kRingNv];
-  __shared__ __align__(8) uint64_t drain_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar[kMaxIssuersNv];
   __shared__ __align__(8) uint64_t xch_bar;
   __shared__ int s_uring[kRingNv];
   __shared__ uint32_t s_tmem;
@@ -261,9 +267,13 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~(uintptr_t)1023);
-  // two MMA issuers, each summing alternate K stages into its own bank of
-  // chunk columns, when two banks fit an accumulator; else warp 1 alone
-  const bool dual = 2 * p.chunk <= kAccColsNv;
+  // ni MMA issuers, issuer b summing the K stages n = b (mod ni) into its
+  // own bank of chunk columns: as many as fit an accumulator, at most
+  // kMaxIssuersNv and at most the ring's stages
+  int ni = kAccColsNv / p.chunk;
+  ni = ni < kMaxIssuersNv ? ni : kMaxIssuersNv;
+  ni = ni < p.stages ? ni : p.stages;
+  const int mma_par = warp == 1 ? 0 : (warp >= 14 ? warp - 13 : -1);  // issuer index
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -275,15 +285,14 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
       mbar_init(&aempty[q], 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], dual ? 2 : 1);  // a commit of each issuer
+      mbar_init(&tfull[a], ni);  // a commit of each active issuer
       mbar_init(&tempty[a], 128);
     }
     for (int i = 0; i < kRingNv; ++i) {
       mbar_init(&ufull[i], 1);
-      mbar_init(&uempty[i], 2 + 4 + kDqWarps);  // MMA threads, epilogue and dequantising warps
+      mbar_init(&uempty[i], kMaxIssuersNv + 4 + kDqWarps);  // MMA threads, epilogue, dequantisers
     }
-    mbar_init(&drain_bar[0], 1);
-    mbar_init(&drain_bar[1], 1);
+    for (int b = 0; b < kMaxIssuersNv; ++b) mbar_init(&drain_bar[b], 1);
     mbar_init(&xch_bar, 128);
     s_abort = 0;
     fence_mbar_init();
@@ -424,17 +433,18 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         drain_armed(sfull, p.stages, armed, armed_ph);
       }
     }
-  } else if (warp == 1 || warp == kMma2WarpNv) {
+  } else if (mma_par >= 0) {
     // ===================================================== MMA issuers
-    // With two issuers, warp 1 takes the CTA's even K stages (counted over
-    // all units) and warp 14 the odd ones, each into its own bank.  A stage,
-    // an A slot and a ring slot may pass between the issuers, but every wait
-    // stays in order: an issuer reaches stage n only after its own stage
-    // n - 2, so the loads and conversions up to n - 2 (in order) are done and
-    // no barrier it waits on can be a whole phase behind; and none can be a
-    // phase ahead, since that needs this issuer's own stage n released.
+    // Issuer b takes the CTA's K stages n = b (mod ni), counted over all
+    // units, into its own bank.  A stage ring slot and an A slot pass between
+    // the issuers, but every wait stays in order: an issuer reaches stage n
+    // only after its own stage n - ni, so the loads and conversions up to
+    // n - ni (in order) are done, and ni <= min(stages, kASlots) means no
+    // barrier it waits on can be a whole phase behind; none can be a phase
+    // ahead, since that needs this issuer's own stage n released.  Issuers
+    // past ni only follow the units.
     if (lane == 0) {
-      const int par = warp == 1 ? 0 : 1;
+      const int par = mma_par;
       int s = 0, q = 0, acc = 0;
       uint32_t ph = 0, qph = 0, aph = 0, n = 0;
       bool ok = true;
@@ -448,11 +458,11 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         const int kst = p.job[un.job].kst;
         if (!mbar_wait(&tempty[acc], aph ^ 1, &s_abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d = tmem + acc * kAccColsNv + (dual ? par * p.chunk : 0);
+        const uint32_t d = tmem + acc * kAccColsNv + par * p.chunk;
         const uint32_t idesc = make_idesc(((un.rows + 15) / 16) * 16, 0u);  // fp16 A and B
         bool first = true;  // this issuer's first stage of the unit starts its sum
         for (int ks = 0; ks < kst && ok; ++ks, ++n) {
-          if (dual ? (int)(n & 1) == par : par == 0) {
+          if ((int)(n % (uint32_t)ni) == par) {
             if (!mbar_wait_spin(&sfull[s], ph, &s_abort) ||
                 !mbar_wait_spin(&afull[q], qph, &s_abort)) {
               ok = false;
@@ -479,7 +489,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
           if (++s == p.stages) { s = 0; ph ^= 1; }
         }
         if (!ok) break;
-        if (dual || par == 0) mma_commit(&tfull[acc]);
+        if (par < ni) mma_commit(&tfull[acc]);
         if (++acc == 2) { acc = 0; aph ^= 1; }
       }
       if (ok) ok = accumulator_tail(tempty, acc, aph, &s_abort);
@@ -510,10 +520,12 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
       const Unit un = decode_unit(u);
       const NvJob& j = p.job[un.job];
       // banks holding this unit's sums: bank b has the stages n0 + ks with
-      // n0 + ks = b (mod 2)
+      // n0 + ks = b (mod ni), none if there is no such ks < kst
       const int kst = j.kst;
-      const bool bank0 = !dual || kst >= 2 || (n0 & 1) == 0;
-      const bool bank1 = dual && (kst >= 2 || (n0 & 1) == 1);
+      uint32_t banks = 0;
+      for (int b = 0; b < ni; ++b)
+        if (kst >= ni || (int)(((uint32_t)b + (uint32_t)ni - n0 % (uint32_t)ni) % (uint32_t)ni) < kst)
+          banks |= 1u << b;
       n0 += (uint32_t)kst;
       if (!mbar_wait(&tfull[acc], aph, &s_abort)) {
         flag_status(p.status, MOE_ERR_TIMEOUT);
@@ -530,7 +542,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         const int n = un.nt * 64 + (lrow & 63);
         for (int c = 0; c < ncols && ok; c += 16) {
           float v[16];
-          load_acc16(tbase + c, p.chunk, bank0, bank1, v);
+          load_acc16(tbase + c, p.chunk, banks, v);
           if (!is_gate) {
 #pragma unroll
             for (int t = 0; t < 16; ++t) s_xch[(lrow - 64) * 17 + t] = v[t] * sg;
@@ -557,7 +569,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         const int n = un.nt * 128 + lrow;
         for (int c = 0; c < ncols; c += 16) {
           float v[16];
-          load_acc16(tbase + c, p.chunk, bank0, bank1, v);
+          load_acc16(tbase + c, p.chunk, banks, v);
           if (n < j.n_out) {
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
