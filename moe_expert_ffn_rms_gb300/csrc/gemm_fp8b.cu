@@ -829,7 +829,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
         const int r0 = MODE == 1 ? wrow + un.nt * 64 : wrow + un.nt * 128;
         const int r1 = MODE == 1 ? wrow + p.I + un.nt * 64 : r0 + 64;
         for (int g = 0; g < p.kg; ++g) {
-          // suspending waits here and in the MMA thread: both share an SM
+          // suspending waits here and in the MMA threads: each shares an SM
           // sub-partition with epilogue warps, whose fold is the busy part
           if (!mbar_wait(&sempty[s], ph ^ 1, &s_abort)) { ok = false; break; }
           mbar_arrive_expect_tx(&sfull[s], (uint32_t)kStageBytesT);
@@ -903,7 +903,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
     // quarter) and half h = (w - 2) / 4 of the columns: FC1 gate columns
     // 32h .. 32h + 31 with the matching up columns 64 + 32h ..; FC2 columns
     // 64h .. 64h + 63.  acc[0..31] and acc[32..63] are those two 32-column runs.
-    // The MMA thread runs at most four K groups ahead, so the global loads a
+    // The MMA threads run at most four K groups ahead, so the global loads a
     // unit needs are issued early: the next group's scales during this one
     // (at a unit's last group, the next unit's first), FC2's destination row
     // one unit ahead and its routing weight halfway through the unit.

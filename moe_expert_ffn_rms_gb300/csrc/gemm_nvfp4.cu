@@ -193,23 +193,20 @@ MOE_DEV void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar, int x,
       : "memory");
 }
 
-// 16 accumulator columns at taddr summed over the banks in the mask (bank b
-// b * chunk columns further), in bank order.
-MOE_DEV void load_acc16(uint32_t taddr, int chunk, uint32_t banks, float* v) {
-  bool any = false;
-  for (int b = 0; b < kMaxIssuersNv; ++b) {
-    if (!((banks >> b) & 1u)) continue;
-    if (!any) {
-      tmem_ld16(taddr + b * chunk, v);
-      tmem_ld_wait();
-      any = true;
-    } else {
-      float w[16];
-      tmem_ld16(taddr + b * chunk, w);
-      tmem_ld_wait();
+// 16 accumulator columns at taddr summed over the nclass stage classes:
+// class c (c = 0, 1, .. in that order) is in bank (first + c) mod ni, which
+// lies b * chunk columns further for bank b.
+MOE_DEV void load_acc16(uint32_t taddr, int chunk, int ni, int first, int nclass, float* v) {
+  tmem_ld16(taddr + first * chunk, v);
+  tmem_ld_wait();
+  for (int c = 1; c < nclass; ++c) {
+    int b = first + c;
+    if (b >= ni) b -= ni;
+    float w[16];
+    tmem_ld16(taddr + b * chunk, w);
+    tmem_ld_wait();
 #pragma unroll
-      for (int t = 0; t < 16; ++t) v[t] += w[t];
-    }
+    for (int t = 0; t < 16; ++t) v[t] += w[t];
   }
 }
 
@@ -519,13 +516,13 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
       if (u < 0) break;
       const Unit un = decode_unit(u);
       const NvJob& j = p.job[un.job];
-      // banks holding this unit's sums: bank b has the stages n0 + ks with
-      // n0 + ks = b (mod ni), none if there is no such ks < kst
+      // the unit's stages ks = c (mod ni) are in bank (n0 + c) mod ni; the
+      // epilogue adds the classes c = 0, 1, .. in that order, so the sum does
+      // not depend on where the unit fell in the CTA's stage count (which
+      // the dynamic unit claims change from run to run)
       const int kst = j.kst;
-      uint32_t banks = 0;
-      for (int b = 0; b < ni; ++b)
-        if (kst >= ni || (int)(((uint32_t)b + (uint32_t)ni - n0 % (uint32_t)ni) % (uint32_t)ni) < kst)
-          banks |= 1u << b;
+      const int bank_first = (int)(n0 % (uint32_t)ni);
+      const int nclass = kst < ni ? kst : ni;
       n0 += (uint32_t)kst;
       if (!mbar_wait(&tfull[acc], aph, &s_abort)) {
         flag_status(p.status, MOE_ERR_TIMEOUT);
@@ -542,7 +539,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         const int n = un.nt * 64 + (lrow & 63);
         for (int c = 0; c < ncols && ok; c += 16) {
           float v[16];
-          load_acc16(tbase + c, p.chunk, banks, v);
+          load_acc16(tbase + c, p.chunk, ni, bank_first, nclass, v);
           if (!is_gate) {
 #pragma unroll
             for (int t = 0; t < 16; ++t) s_xch[(lrow - 64) * 17 + t] = v[t] * sg;
@@ -569,7 +566,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         const int n = un.nt * 128 + lrow;
         for (int c = 0; c < ncols; c += 16) {
           float v[16];
-          load_acc16(tbase + c, p.chunk, banks, v);
+          load_acc16(tbase + c, p.chunk, ni, bank_first, nclass, v);
           if (n < j.n_out) {
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
