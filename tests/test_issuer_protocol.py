@@ -1,5 +1,6 @@
-"""Host-side model of the stage hand-offs in the NVFP4 decode kernel with
-several MMA issuer threads (csrc/gemm_nvfp4.cu).
+"""Host-side models of the stage hand-offs in the kernels with several MMA
+issuer threads: the NVFP4 decode kernel (csrc/gemm_nvfp4.cu) and the
+block-wise FP8 prefill tiles (csrc/gemm_fp8b.cu, `run_tiles` below).
 
 K stages n = 0, 1, .. of a CTA flow through two rings: the TMA producer fills
 stage slot n % S (barriers sfull / sempty), the converting warps turn it into
@@ -183,3 +184,108 @@ def test_class_order_sum_is_independent_of_the_first_bank():
                     v += banks[(first + c) % ni]
                 totals.add(v.tobytes())
             assert len(totals) == 1
+
+
+def run_tiles(n_groups, ring_s, ring_q, ni, seed, max_delay=6):
+    """The block-wise FP8 prefill tiles: TMA stages (ring S, released by the
+    MMA commit), one TMEM slot per K group (ring Q: the MMA commit fills it,
+    the in-order epilogue drains it), K group g issued by thread g % ni."""
+    rng = random.Random(seed)
+    sfull = [Barrier(1) for _ in range(ring_s)]
+    sempty = [Barrier(1) for _ in range(ring_s)]
+    kfull = [Barrier(1) for _ in range(ring_q)]
+    kempty = [Barrier(1) for _ in range(ring_q)]
+    slot_s = [None] * ring_s
+    slot_q = [None] * ring_q  # group whose product a TMEM slot holds
+    done, drained = set(), set()
+    prod, epi = [0], [0]
+    iss = [b for b in range(ni)]
+    inflight = []
+
+    def producer():
+        g = prod[0]
+        if g >= n_groups:
+            return False
+        s = g % ring_s
+        if not sempty[s].try_wait_parity(((g // ring_s) & 1) ^ 1):
+            return False
+        old = slot_s[s]
+        if old is not None and old not in done:
+            raise Violation(f"producer overwrote group {old} with {g}")
+        slot_s[s] = g
+        sfull[s].arrive()
+        prod[0] += 1
+        return True
+
+    def issuer(b):
+        g = iss[b]
+        if g >= n_groups:
+            return False
+        s, q = g % ring_s, g % ring_q
+        if not (sfull[s].try_wait_parity((g // ring_s) & 1) and
+                kempty[q].try_wait_parity(((g // ring_q) & 1) ^ 1)):
+            return False
+        if slot_s[s] != g:
+            raise Violation(f"issuer {b} read stage slot {s} for {g}, holds {slot_s[s]}")
+        old = slot_q[q]
+        if old is not None and old not in drained:
+            raise Violation(f"issuer {b} overwrote the product of group {old} with {g}")
+        slot_q[q] = g
+        inflight.append([rng.randint(0, max_delay), g])
+        iss[b] += ni
+        return True
+
+    def complete():
+        ready = [m for m in inflight if m[0] <= 0]
+        if not ready:
+            for m in inflight:
+                m[0] -= 1
+            return bool(inflight)
+        m = rng.choice(ready)
+        inflight.remove(m)
+        g = m[1]
+        done.add(g)
+        sempty[g % ring_s].arrive()
+        kfull[g % ring_q].arrive()
+        return True
+
+    def epilogue():
+        g = epi[0]
+        if g >= n_groups:
+            return False
+        q = g % ring_q
+        if not kfull[q].try_wait_parity((g // ring_q) & 1):
+            return False
+        if slot_q[q] != g or g not in done:
+            raise Violation(f"epilogue read slot {q} for {g}, holds {slot_q[q]}")
+        drained.add(g)
+        kempty[q].arrive()
+        epi[0] += 1
+        return True
+
+    roles = [producer, complete, epilogue] + [lambda b=b: issuer(b) for b in range(ni)]
+    while len(drained) < n_groups:
+        order = roles[:]
+        rng.shuffle(order)
+        if not any(r() for r in order):
+            raise Violation(f"deadlock with {len(drained)} of {n_groups} groups drained")
+    return True
+
+
+@pytest.mark.parametrize("ring_s,ring_q,ni", [(6, 4, 2), (6, 4, 1), (5, 3, 2), (4, 4, 4), (2, 2, 2)])
+def test_tile_issuers_within_the_slot_count_never_misread(ring_s, ring_q, ni):
+    # the kernel runs six stages, four slots and two issuers; it keeps both
+    # rings even, which is enough, though ni <= both ring lengths already is
+    for seed in range(300):
+        run_tiles(48, ring_s, ring_q, ni, seed)
+
+
+@pytest.mark.parametrize("ring_s,ring_q,ni", [(6, 2, 3), (6, 4, 5)])
+def test_tile_issuers_beyond_the_slot_count_misread_somewhere(ring_s, ring_q, ni):
+    failures = 0
+    for seed in range(300):
+        try:
+            run_tiles(48, ring_s, ring_q, ni, seed)
+        except Violation:
+            failures += 1
+    assert failures > 0
