@@ -247,6 +247,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (0 = auto)")
+    ap.add_argument("--no-more", action="store_true",
+                    help="measure only --workload (no prefill entries under \"more\")")
     return ap.parse_args()
 
 
@@ -306,23 +308,22 @@ def main_reference(args):
         "data": "synthetic",
         "config": {"workload": args.workload, "T": cfg["T"], "H": cfg["H"], "E": cfg["E"],
                    "top_k": cfg["k"], "I": cfg["I"], "fp8": cfg["fp8"]},
-        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": 1,
+                         "host_cores": os.cpu_count(), "kind": "oracle",
                          "sample": desc + f"; each step = one pass over the sample"},
         "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def main_native(args):
+def run_workload(args, workload, dev, rank, world, local, steps, warmup, cpu_ok):
+    """Measures one workload (regions A, B and e2e); returns rank 0's JSON
+    record (None on other ranks)."""
     import torch
-    rank, world, local = dist_setup(args)
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
     import moe_expert_ffn_rms_gb300 as M
     import workloads
 
-    M.check_device()
-    inp = workloads.make_inputs(args.workload, dev)
+    inp = workloads.make_inputs(workload, dev)
     T, H, E, k, I, fp8 = inp["T"], inp["H"], inp["E"], inp["k"], inp["I"], inp["fp8"]
     nvfp4 = bool(inp.get("nvfp4"))
     fb = fp8 == "block"
@@ -381,12 +382,12 @@ def main_native(args):
                               w13_scale=s13, w2_scale=s2, topk_ids_out=ids, topk_w_out=tw)
 
     # ---- region A: the product call, device-resident inputs
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         fwd()
     torch.cuda.synchronize()
     offsets_np = None
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+          for _ in range(steps)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -394,7 +395,7 @@ def main_native(args):
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
     lc0 = M.lib.moe_launch_count()  # the library's own host-side launch counter
-    for i in range(args.steps):
+    for i in range(steps):
         if flush is not None:
             flush.zero_()
         ev[i][0].record(st)
@@ -495,14 +496,14 @@ def main_native(args):
         M.moe_combine(y, rop, T, k, out_b, pair_order=True)
         mark(len(stages))
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step_b()
     torch.cuda.synchronize()
     fwd()
     torch.cuda.synchronize()
-    same = bool(torch.equal(out, out_b)) if args.warmup > 0 else None
+    same = bool(torch.equal(out, out_b)) if warmup > 0 else None
     evs_all = []
-    for i in range(args.steps):
+    for i in range(steps):
         if flush is not None:
             flush.zero_()
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
@@ -524,7 +525,7 @@ def main_native(args):
         ffn_bytes = work["fc1_bytes"] + work["fc2_bytes"]
         achieved = ffn_bytes / (stage_ms["ffn"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": read_traffic("ffn", args.workload),
+                "frac": achieved / peaks["hbm_gbs"], "traffic": read_traffic("ffn", workload),
                 "kernel": "fused decode FFN (FC1 + silu_and_mul + FC2 + routing weight, one launch)",
                 "peak_source": peaks["source"],
                 "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
@@ -532,7 +533,7 @@ def main_native(args):
     elif decode:
         achieved = work["fc1_bytes"] / (stage_ms["fc1"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": read_traffic("fc1", args.workload),
+                "frac": achieved / peaks["hbm_gbs"], "traffic": read_traffic("fc1", workload),
                 "kernel": "grouped GEMM FC1 + silu_and_mul",
                 "peak_source": peaks["source"],
                 "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
@@ -546,7 +547,7 @@ def main_native(args):
         flops = work["fc1_flops"] + work["fc2_flops"]
         achieved = flops / (stage_ms["ffn"] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
-                "frac": achieved / tpeak, "traffic": read_traffic("ffn", args.workload),
+                "frac": achieved / tpeak, "traffic": read_traffic("ffn", workload),
                 "kernel": "block-wise FP8 FFN: FC1 tiles + silu_and_mul, 1x128 group quantiser, "
                           "FC2 tiles + routing weight (three launches timed together)",
                 "peak_source": tsrc, "frac_of_sustained": achieved / tpeak_sus,
@@ -557,13 +558,15 @@ def main_native(args):
         achieved = work["fc1_flops"] / (stage_ms["fc1"] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak,
                 "unit": "TFLOP/s", "frac": achieved / tpeak,
-                "traffic": read_traffic("fc1", args.workload),
+                "traffic": read_traffic("fc1", workload),
                 "kernel": "grouped GEMM FC1 + silu_and_mul", "peak_source": tsrc,
                 "frac_of_sustained": achieved / tpeak_sus,
                 "fc2_TFLOPs": work["fc2_flops"] / (stage_ms["fc2"] * 1e-3) / 1e12,
                 "ffn_TFLOPs": (work["fc1_flops"] + work["fc2_flops"]) /
                               ((stage_ms["fc1"] + stage_ms["fc2"]) * 1e-3) / 1e12,
                 "algorithmic_flops_per_launch": work["fc1_flops"]}
+        roof["fc2_frac"] = roof["fc2_TFLOPs"] / tpeak
+        roof["ffn_frac"] = roof["ffn_TFLOPs"] / tpeak
 
     # ---- e2e: host buffers in, host buffer out, copies inside the timed region.
     # Every step uploads its inputs from pinned host memory, runs the forward
@@ -613,41 +616,42 @@ def main_native(args):
             out_h[b].copy_(out_d[b], non_blocking=True)
             ev_down[b].record(down)
 
-    for i in range(args.warmup):
+    for i in range(warmup):
         e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
     up.wait_event(e0)
-    for i in range(args.steps):
+    for i in range(steps):
         e2e_step(i)
-    st.wait_event(ev_down[(args.steps - 1) & 1])
+    st.wait_event(ev_down[(steps - 1) & 1])
     e1.record(st)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
-    e2e_same = bool(torch.equal(out_h[(args.steps - 1) & 1], out.cpu()))
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    e2e_same = bool(torch.equal(out_h[(steps - 1) & 1], out.cpu()))
     h2d = x_h.numel() * 2 + (lg_h.numel() * 4 if lg_h is not None else 0)
     d2h = out_h[0].numel() * 2
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n = args.cpu_tokens or auto_cpu_tokens(args.workload)
+    if rank == 0 and world == 1 and cpu_ok and not args.no_cpu_baseline:
+        n = args.cpu_tokens or auto_cpu_tokens(workload)
         # FP8 workloads: the oracle gets the bf16 originals and quantises them itself
         tps, secs, desc = run_oracle_sample(inp, n)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc,
-               "seconds": secs}
+        cpu = {"value": tps, "unit": "tokens/s", "cores": 1, "host_cores": os.cpu_count(),
+               "kind": "oracle", "sample": desc, "seconds": secs}
+    line = None
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
+            "steps": steps, "warmup": warmup, "ms_per_step": mean_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ("fp16 x fp16 -> f32 (NVFP4 weights dequantised exactly, bf16 activations)"
                       if nvfp4 else
                       "fp8-e4m3 x fp8-e4m3 -> f32 per 128-wide K group, scaled and summed in f32"
                       if fb else "fp8-e4m3 x fp8-e4m3 -> f32" if fp8 else "bf16 x bf16 -> f32"),
             "data": "synthetic (seeded torch generator; random-init weights)",
-            "config": {"workload": args.workload, "T": T, "H": H, "E": E, "top_k": k, "I": I,
+            "config": {"workload": workload, "T": T, "H": H, "E": E, "top_k": k, "I": I,
                        "fp8": fp8,
                        "weights": ("nvfp4" if nvfp4 else "e4m3, 128x128 tile scales" if fb else
                                    ("e4m3" if fp8 else "bf16")),
@@ -666,11 +670,47 @@ def main_native(args):
                                if overlap else "on the compute stream (forward under 0.1 ms)"),
                     "output_equals_forward": e2e_same},
             "gpu_launches": launches_timed,
-            "launches_per_step": launches_timed / args.steps,
+            "launches_per_step": launches_timed / steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
             "wall_s_region_a": wall_a,
         }
+    del inp, ws
+    torch.cuda.empty_cache()
+    return line
+
+
+# Workloads measured after the headline one in a default single-GPU run: the
+# prefill (T = 4096) half of the metric, bf16 and FP8 W8A8.
+MORE_WORKLOADS = ("c5_prefill", "c8_prefill_fp8")
+MORE_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config", "roofline",
+             "stages_ms", "e2e", "clocks", "launches_per_step", "stage_path_equals_forward")
+
+
+def main_native(args):
+    import torch
+    rank, world, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import moe_expert_ffn_rms_gb300 as M
+    M.check_device()
+    line = run_workload(args, args.workload, dev, rank, world, local, args.steps, args.warmup,
+                        cpu_ok=True)
+    if rank == 0 and line is not None and line["roofline"]["bound"] == "hbm":
+        # The measured HBM peak is a copy (read + write bytes counted); a
+        # decode FFN only reads, and a read stream can run a little faster
+        # than a copy, so the fraction can read slightly above 1.  The
+        # fraction of the nominal 8 TB/s sits beside it.
+        line["roofline"]["peak_kind"] = "copy bandwidth (read + write bytes), measured"
+    more = [w for w in MORE_WORKLOADS if w != args.workload] if (
+        world == 1 and args.workload == DEFAULT_WORKLOAD and not args.no_more) else []
+    if more and rank == 0:
+        line["more"] = {}
+        for w in more:
+            sub = run_workload(args, w, dev, rank, world, local, min(args.steps, 100),
+                               max(3, min(args.warmup, 10)), cpu_ok=False)
+            line["more"][w] = {k: sub[k] for k in MORE_KEYS if k in sub}
+    if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -214,6 +214,10 @@ moe_status moe_ffn_forward_routed(const moe_shape* shape, const void* x, const v
  *   Set-up: the first call on a device (with that device current) looks up
  *   the array's device address; make that first call before any stream
  *   capture.
+ *   The address belongs to the device's primary context (the one the CUDA
+ *   runtime uses) and is kept for the life of the process: after
+ *   cudaDeviceReset(), or from a different driver-API context on the same
+ *   device, do not call this entry point.
  *   All calls on a device share the one array and it keeps the last call's
  *   contents (nothing in it needs to start at zero).  Calls whose work
  *   overlaps on the GPU (other streams, other host threads) race on it:
@@ -265,7 +269,16 @@ moe_status moe_rmsnorm(const void* x, const void* w, int32_t T, int32_t H, float
 /* Device workspace bytes moe_route_topk needs (router partial sums). */
 size_t moe_route_workspace_size(int32_t T, int32_t H, int32_t E);
 
-/* Router softmax and renormalised top-k.
+/* Router softmax and renormalised top-k.  [RUBIN] "Hardware grows..."
+ * names the router softmax (exp-bound); the pages are silent on the router
+ * layer, the selection rule and the renormalisation, so the plain reading is
+ * used: a linear router over x_hat, softmax over all E, the k largest
+ * probabilities (ties to the lower expert index), renormalised over the k.
+ * Errors: MOE_ERR_INVALID_ARG for NULL or misaligned pointers, or when both
+ * or neither of router_w and logits_in are given; UNSUPPORTED_SHAPE outside
+ * the limits below.  A NaN logit ranks as -inf (below every finite logit,
+ * ties to the lower index), so every slot holds a distinct expert in [0, E);
+ * a token whose selected logits are all -inf gets weights 0.
  *   logits = xhat W_r + b   (fp32; skipped when logits_in != NULL, then
  *                            logits = logits_in + b)
  *   ids[t, :]  = the top_k experts by logit, descending, ties to the lower
@@ -287,7 +300,12 @@ moe_status moe_route_topk(const void* xhat, const float* router_w, const float* 
 size_t moe_permute_workspace_size(int32_t T, int32_t E, int32_t k);
 
 /* Token -> expert grouping (stable counting sort of the T*k (t, j) pairs by
- * expert; rows ordered by expert, then token).
+ * expert; rows ordered by expert, then token).  [SM] 4.2/4.3 describe grouped
+ * GEMM MoE backends that consume expert-grouped rows; the pages are silent on
+ * the grouping itself, so the plain reading (a stable sort by expert) is used.
+ * Errors: MOE_ERR_INVALID_ARG for NULL or misaligned pointers or a workspace
+ * below moe_permute_workspace_size(); ids outside [0, E) are skipped on the
+ * device and flagged (MOE_ERR_INVALID_ARG in the device status word).
  *   ids int32 [T, k]            routing (each row: distinct experts)
  *   offsets int32 [E + 1]       expert e owns rows offsets[e] .. offsets[e+1]-1
  *   row_src int32 [T*k]         row r holds pair t*k + j
@@ -363,7 +381,11 @@ moe_status moe_grouped_ffn_nvfp4(const moe_shape* shape, const void* xp, const u
 moe_status moe_silu_and_mul(const void* h, int32_t R, int32_t I, void* a, moe_stream_t stream);
 
 /* Weighted combine: out[t, :] = bf16( sum_{j=0..k-1} y_{t,j} ) summed in fp32
- * in j order (the routing weight is already in y), where y_{t,j} is row
+ * in j order (the routing weight is already in y).  The pages are silent on
+ * the combine; the plain reading is used (a weighted sum of the token's k
+ * expert outputs, no residual and no shared expert, one bf16 rounding).
+ * Errors: MOE_ERR_INVALID_ARG for NULL or misaligned pointers or H % 8 != 0.
+ * y_{t,j} is row
  * row_of_pair[t*k+j] of y (y_pair_order = 0: rows in expert order, as
  * MOE_GEMM_FC2 writes them) or row t*k+j (y_pair_order = 1: rows in
  * (token, slot) order, as MOE_GEMM_FC2_BF16 writes them).  Pairs whose

@@ -70,7 +70,10 @@ MOE_DEV float silu_f(float z) { return z / (1.0f + expf(-z)); }
 // ... in v (-FLT_MAX past E).  The k winners are taken one at a time by a warp
 // arg-max (larger logit first, lower index on ties); the weights are the
 // softmax over the selected logits (= full softmax renormalised).  Lane 0
-// writes ids[0..k) and w[0..k).
+// writes ids[0..k) and w[0..k).  A NaN logit ranks as -inf (below every
+// finite logit, ties to the lower index as usual), so each of the k slots
+// always receives a distinct expert in [0, E) (k <= E); when every selected
+// logit is -inf the softmax is undefined and the token's weights are 0.
 constexpr int kTopkPer = kMaxExperts / 32;
 
 MOE_DEV void warp_topk(const float (&v)[kTopkPer], int E, int k, int lane, int32_t* ids,
@@ -86,8 +89,9 @@ MOE_DEV void warp_topk(const float (&v)[kTopkPer], int E, int k, int lane, int32
 #pragma unroll
     for (int i = 0; i < kTopkPer; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !(taken & (1u << i)) && (v[i] > bv || (v[i] == bv && e < be))) {
-        bv = v[i];
+      const float vi = (v[i] != v[i]) ? -INFINITY : v[i];  // NaN ranks as -inf
+      if (e < E && !(taken & (1u << i)) && (vi > bv || (vi == bv && e < be))) {
+        bv = vi;
         be = e;
       }
     }
@@ -106,19 +110,20 @@ MOE_DEV void warp_topk(const float (&v)[kTopkPer], int E, int k, int lane, int32
   }
   if (lane == 0) {
     const float m = sel_v[0];
+    const bool finite_max = m > -INFINITY;
     float p[kMaxTopK];
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
       if (j >= k) break;
-      p[j] = expf(sel_v[j] - m);
+      p[j] = finite_max ? expf(sel_v[j] - m) : 0.f;
       s += p[j];
     }
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
       if (j >= k) break;
       ids[j] = sel_e[j];
-      w[j] = p[j] / s;
+      w[j] = finite_max ? p[j] / s : 0.f;
     }
   }
 }

@@ -578,7 +578,10 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
         // 16 tokens a pass; each token's absmax over the unit's 128 columns
         // (one K group of FC2) from a warp reduction and four per-warp
         // maxima (double-buffered, so one barrier a pass); then the E4M3
-        // codes and the group scale.
+        // codes and the group scale.  Each code is decided from a / s with
+        // the correctly rounded divide: a and s carry few significant bits,
+        // so a / s often lands exactly on a midpoint between two E4M3
+        // values, where a * (1 / s) can round to the other side.
         const int n = un.nt * 128 + l;
         uint8_t* outq = reinterpret_cast<uint8_t*>(j.out);
         const int kg_out = j.n_out / kGroup;
@@ -603,7 +606,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
               const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
               if (c < un.rows) {
                 const size_t r = (size_t)(un.row0 + c);
-                outq[r * j.n_out + n] = f_to_e4m3(a[t] * __frcp_rn(s));
+                outq[r * j.n_out + n] = f_to_e4m3(__fdiv_rn(a[t], s));
                 if (l == 0) j.out_scale[r * kg_out + un.nt] = s;
               }
             }

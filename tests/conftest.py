@@ -26,3 +26,20 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    # Routing-exemption counts per workload (tokens whose routing was accepted
+    # inside a tie band, or re-derived from the GPU's x_hat), one JSON line so
+    # that the tail of a quiet run keeps them.
+    try:
+        from tests.parity_util import RECORDS
+    except Exception:  # pragma: no cover
+        return
+    if RECORDS:
+        import json
+        short = {name: {k: v for k, v in c.items()
+                        if k in ("tokens", "set_ties", "set_ties_routed_apart", "order_ties_routed_apart",
+                                 "xhat_rows_differ", "rerouted_by_xhat", "max_logit_err")}
+                 for name, c in sorted(RECORDS.items())}
+        terminalreporter.write_line("routing exemptions: " + json.dumps(short, separators=(",", ":")))

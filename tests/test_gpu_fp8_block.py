@@ -7,7 +7,8 @@ import torch
 
 import oracle as O
 import workloads
-from tests.parity_util import TOL_FP8, assert_close, check_routing, f64
+from tests.parity_util import (TOL_FP8, assert_close, check_routing_e2e, covering_tokens, f64,
+                               forward_xhat, o1_weights)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -61,11 +62,12 @@ def quantize_weights(M, inp):
     return quantize_gpu(M, inp["w13"], 128), quantize_gpu(M, inp["w2"], 128)
 
 
-def run_forward(M, inp, wq, routed=None, engine=None):
+def run_forward(M, inp, wq, routed=None, engine=None, ws=None):
     T, H, E, k, I = inp["T"], inp["H"], inp["E"], inp["k"], inp["I"]
     shape = M.make_shape(T, H, E, I, k, inp["eps"], fp8="block",
                          engine=M.ENGINE_AUTO if engine is None else engine)
-    ws = M.alloc_workspace(M.moe_ffn_workspace_size(shape), DEV)
+    if ws is None:
+        ws = M.alloc_workspace(M.moe_ffn_workspace_size(shape), DEV)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
     (q13, s13), (q2, s2) = wq
     if routed is not None:
@@ -83,26 +85,33 @@ def run_forward(M, inp, wq, routed=None, engine=None):
     return out, ids, tw
 
 
-def check_fp8_block(M, inp, sample=None, seed=0, engine=None):
-    T, k, I = inp["T"], inp["k"], inp["I"]
+def check_fp8_block(M, inp, sample=None, seed=0, engine=None, name=""):
+    """sample: None = every token, "tiles" = tokens reaching every (expert,
+    128-row token tile), an int = that many random tokens."""
+    T, H, E, k, I = inp["T"], inp["H"], inp["E"], inp["k"], inp["I"]
     wq = quantize_weights(M, inp)
     M.device_status(clear=True)
-    out, ids, tw = run_forward(M, inp, wq, engine=engine)
-    xhat = O.rms_norm(f64(inp["x"]), f64(inp["norm_w"]), inp["eps"])
-    if inp["router_logits"] is not None:
-        l64 = f64(inp["router_logits"])
-    else:
-        l64 = O.router_logits(xhat, f64(inp["router_w"]),
-                              None if inp["router_bias"] is None else f64(inp["router_bias"]))
+    shape = M.make_shape(T, H, E, I, k, inp["eps"], fp8="block",
+                         engine=M.ENGINE_AUTO if engine is None else engine)
+    ws = M.alloc_workspace(M.moe_ffn_workspace_size(shape), DEV)
+    out, ids, tw = run_forward(M, inp, wq, engine=engine, ws=ws)
     ids_g = ids.cpu().numpy()
-    _, w_use, _ = check_routing(ids_g, tw.cpu().double().numpy(), l64, k)
+    xg = f64(forward_xhat(M, ws, T, H))
+    ids_use, w_use, xhat, _ = check_routing_e2e(
+        ids_g, tw.cpu().double().numpy(), f64(inp["x"]), f64(inp["norm_w"]), inp["eps"], k,
+        xhat_gpu=xg, router_w=None if inp["router_w"] is None else f64(inp["router_w"]),
+        router_bias=None if inp["router_bias"] is None else f64(inp["router_bias"]),
+        logits=None if inp["router_logits"] is None else f64(inp["router_logits"]), name=name)
     toks = np.arange(T)
-    if sample is not None and sample < T:
+    if sample == "tiles":
+        toks, ntiles = covering_tokens(ids_use, E, k, tile=128, n_min=256, seed=seed)
+        print(f"{inp['name']}: {len(toks)} tokens cover all {ntiles} (expert, token tile) pairs")
+    elif sample is not None and sample < T:
         toks = np.sort(np.random.default_rng(seed).choice(T, size=sample, replace=False))
-    used = np.unique(ids_g[toks])
+    used = np.unique(ids_use[toks])
     b13 = {int(e): O.quantize_blocks_e4m3(f64(inp["w13"][e]), 128) for e in used}
     b2 = {int(e): O.quantize_blocks_e4m3(f64(inp["w2"][e]), 128) for e in used}
-    ref = O.ffn_token_outputs(xhat[toks], ids_g[toks], w_use[toks], None, None, I, fp8="block",
+    ref = O.ffn_token_outputs(xhat[toks], ids_use[toks], w_use[toks], None, None, I, fp8="block",
                               wq13_of=b13.get, wq2_of=b2.get)
     m = assert_close(f64(out)[toks], ref, TOL_FP8, inp["name"] + " fp8 block")
     assert M.device_status() == 0
@@ -129,19 +138,23 @@ SHAPES = {
 @pytest.mark.parametrize("name", list(SHAPES))
 def test_forward_fp8_block_small(M, name, engine):
     """Both engines: the weight-streaming launch (decode) and the token tiles
-    with a separate group quantisation (prefill)."""
+    with a separate group quantisation (prefill); the workloads' own weights
+    and weights rescaled to outputs of order one."""
     cfg, shape, routing = SHAPES[name]
-    inp = workloads.make_inputs(cfg, DEV, shape=shape, routing=routing, seed=19)
-    inp["name"] = f"{name}/{engine}"
     eng = {"auto": None, "decode": M.ENGINE_DECODE, "prefill": M.ENGINE_PREFILL}[engine]
-    check_fp8_block(M, inp, engine=eng)
+    for o1 in (False, True):
+        inp = workloads.make_inputs(cfg, DEV, shape=shape, routing=routing, seed=19)
+        inp["name"] = f"{name}/{engine}" + (" o1" if o1 else "")
+        if o1:
+            o1_weights(inp)
+        check_fp8_block(M, inp, engine=eng)
 
 
 def test_forward_fp8_block_full_decode_workload(M):
     """The block-wise FP8 decode workload (T=16, H=4096, E=64, k=8, I=1536),
-    two tokens recomputed by the oracle; the run is deterministic."""
+    every token recomputed by the oracle; the run is deterministic."""
     inp = workloads.make_inputs("c7_decode_fp8_block", DEV)
-    out, m, wq = check_fp8_block(M, inp, sample=2)
+    out, m, wq = check_fp8_block(M, inp, name="c7_decode_fp8_block")
     o1, i1, _ = run_forward(M, inp, wq)
     o2, i2, _ = run_forward(M, inp, wq)
     assert torch.equal(o1, o2) and torch.equal(i1, i2) and torch.equal(o1, out)
@@ -150,10 +163,11 @@ def test_forward_fp8_block_full_decode_workload(M):
 
 def test_forward_fp8_block_prefill_workload(M):
     """Block-wise FP8 at the prefill size (T=4096, H=4096, E=64, k=8, I=1536,
-    token tiles); 8 sampled tokens recomputed by the oracle."""
+    token tiles); the oracle recomputes tokens that reach every (expert,
+    128-row token tile)."""
     inp = workloads.make_inputs("c9_prefill_fp8_block", DEV)
     inp["name"] = "c9_prefill_fp8_block"
-    _, m, _ = check_fp8_block(M, inp, sample=8)
+    _, m, _ = check_fp8_block(M, inp, sample="tiles", name="c9_prefill_fp8_block")
     print(f"c9_prefill_fp8_block: max scaled error {m:.3e}")
     del inp
     torch.cuda.empty_cache()

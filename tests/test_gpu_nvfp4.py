@@ -8,7 +8,8 @@ import torch
 
 import oracle as O
 import workloads
-from tests.parity_util import TOL_BF16, assert_close, check_routing, f64
+from tests.parity_util import (TOL_BF16, assert_close, check_routing_e2e, f64, forward_xhat,
+                               o1_weights)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -55,10 +56,11 @@ def test_quantize_nvfp4_bit_exact(M):
     assert sg[2].item() == 1.0 and int(q[2].max()) == 0 and int(sb[2].max()) == 0
 
 
-def run_forward(M, inp, wq):
+def run_forward(M, inp, wq, ws=None):
     T, H, E, k, I = inp["T"], inp["H"], inp["E"], inp["k"], inp["I"]
     shape = M.make_shape(T, H, E, I, k, inp["eps"], nvfp4=True)
-    ws = M.alloc_workspace(M.moe_ffn_workspace_size(shape), DEV)
+    if ws is None:
+        ws = M.alloc_workspace(M.moe_ffn_workspace_size(shape), DEV)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
     ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
     tw = torch.empty((T, k), dtype=torch.float32, device=DEV)
@@ -70,19 +72,20 @@ def run_forward(M, inp, wq):
     return out, ids, tw
 
 
-def check_nvfp4(M, inp, sample=None, seed=0):
-    T, k, I = inp["T"], inp["k"], inp["I"]
+def check_nvfp4(M, inp, sample=None, seed=0, name=""):
+    T, H, E, k, I = inp["T"], inp["H"], inp["E"], inp["k"], inp["I"]
     wq = (quantize_gpu(M, inp["w13"]), quantize_gpu(M, inp["w2"]))
     M.device_status(clear=True)
-    out, ids, tw = run_forward(M, inp, wq)
-    xhat = O.rms_norm(f64(inp["x"]), f64(inp["norm_w"]), inp["eps"])
-    if inp["router_logits"] is not None:
-        l64 = f64(inp["router_logits"])
-    else:
-        l64 = O.router_logits(xhat, f64(inp["router_w"]),
-                              None if inp["router_bias"] is None else f64(inp["router_bias"]))
+    shape = M.make_shape(T, H, E, I, k, inp["eps"], nvfp4=True)
+    ws = M.alloc_workspace(M.moe_ffn_workspace_size(shape), DEV)
+    out, ids, tw = run_forward(M, inp, wq, ws=ws)
     ids_g = ids.cpu().numpy()
-    _, w_use, ndiff = check_routing(ids_g, tw.cpu().double().numpy(), l64, k)
+    xg = f64(forward_xhat(M, ws, T, H))
+    ids_use, w_use, xhat, _ = check_routing_e2e(
+        ids_g, tw.cpu().double().numpy(), f64(inp["x"]), f64(inp["norm_w"]), inp["eps"], k,
+        xhat_gpu=xg, router_w=None if inp["router_w"] is None else f64(inp["router_w"]),
+        router_bias=None if inp["router_bias"] is None else f64(inp["router_bias"]),
+        logits=None if inp["router_logits"] is None else f64(inp["router_logits"]), name=name)
     toks = np.arange(T)
     if sample is not None and sample < T:
         toks = np.sort(np.random.default_rng(seed).choice(T, size=sample, replace=False))
@@ -92,7 +95,7 @@ def check_nvfp4(M, inp, sample=None, seed=0):
 
     def w2_of(e):
         return O.dequantize_nvfp4(*O.quantize_nvfp4(f64(inp["w2"][e])))
-    ref = O.ffn_token_outputs(xhat[toks], ids_g[toks], w_use[toks], w13_of, w2_of, I)
+    ref = O.ffn_token_outputs(xhat[toks], ids_use[toks], w_use[toks], w13_of, w2_of, I)
     m = assert_close(f64(out)[toks], ref, TOL_BF16, inp["name"] + " nvfp4")
     assert M.device_status() == 0
     return out, m
@@ -114,16 +117,19 @@ SHAPES = {
 @pytest.mark.parametrize("name", list(SHAPES))
 def test_forward_nvfp4_small(M, name):
     cfg, shape, routing = SHAPES[name]
-    inp = workloads.make_inputs(cfg, DEV, shape=shape, routing=routing, seed=13)
-    inp["name"] = name
-    check_nvfp4(M, inp)
+    for o1 in (False, True):
+        inp = workloads.make_inputs(cfg, DEV, shape=shape, routing=routing, seed=13)
+        inp["name"] = name + (" o1" if o1 else "")
+        if o1:
+            o1_weights(inp)
+        check_nvfp4(M, inp)
 
 
 def test_forward_nvfp4_full_decode_workload(M):
-    """The decode NVFP4 workload (T=16, H=4096, E=64, k=8, I=1536), two
-    tokens recomputed by the oracle; the run is deterministic."""
+    """The decode NVFP4 workload (T=16, H=4096, E=64, k=8, I=1536), every
+    token recomputed by the oracle; the run is deterministic."""
     inp = workloads.make_inputs("c6_decode_nvfp4", DEV)
-    out, m = check_nvfp4(M, inp, sample=2)
+    out, m = check_nvfp4(M, inp, name="c6_decode_nvfp4")
     wq = (quantize_gpu(M, inp["w13"]), quantize_gpu(M, inp["w2"]))
     o1, i1, _ = run_forward(M, inp, wq)
     o2, i2, _ = run_forward(M, inp, wq)

@@ -226,6 +226,79 @@ def test_fp8_gemm_equals_bf16_gemm_on_representable_inputs():
     np.testing.assert_allclose(y8, y16, rtol=1e-13, atol=0)
 
 
+def _rep_rows(rng, shape, exps):
+    """Rows of E4M3 values, each row scaled by its own power of two 2^exps[r]
+    and holding one element of magnitude 448 (so its absmax/448 scale is
+    exactly 2^exps[r])."""
+    grid = np.array(sorted(set(O.e4m3_decode(c) for c in range(0x7F))))
+    grid = np.concatenate([-grid[1:], grid])
+    m = rng.choice(grid, size=shape)
+    m[np.arange(shape[0]), rng.integers(0, shape[1], shape[0])] = 448.0
+    return m * np.ldexp(1.0, np.asarray(exps))[:, None]
+
+
+def test_fp8_per_channel_scales_pin_their_axes():
+    """The W8A8 scales belong to different axes: one per token row of the
+    activations (s_a) and one per output channel of the weights (s_w); the
+    SM-architecture article's scaled GEMM c = (a*s_a)(b*s_b).  With a
+    different power of two on every row and every output channel, the FP8
+    FC1 and FC2 equal the bf16 ones exactly only if each scale multiplies its
+    own axis: a transposed or shifted scale vector fails."""
+    rng = np.random.default_rng(33)
+    H, I, E, rows = 64, 48, 2, 7
+    offsets = np.array([0, 3, rows])
+    x = _rep_rows(rng, (rows, H), rng.integers(-9, -4, rows))
+    w13 = [_rep_rows(rng, (2 * I, H), rng.integers(-14, -9, 2 * I)) for _ in range(E)]
+    w2 = [_rep_rows(rng, (H, I), rng.integers(-13, -8, H)) for _ in range(E)]
+    xq, sx = O.quantize_rows_e4m3(x)
+    q13 = [O.quantize_rows_e4m3(w) for w in w13]
+    q2 = [O.quantize_rows_e4m3(w) for w in w2]
+    assert len(set(sx.tolist())) > 1 and len(set(q13[0][1].tolist())) > 1
+    a8 = O.grouped_fc1_fp8(xq, sx, offsets, lambda e: q13[e][0], lambda e: q13[e][1], I)
+    a16 = O.grouped_fc1(x, offsets, lambda e: w13[e], I)
+    np.testing.assert_array_equal(a8, a16)
+    rw = rng.random(rows)
+    aq, sa = O.quantize_rows_e4m3(a16)
+    y8 = O.grouped_fc2_fp8(a16, offsets, lambda e: q2[e][0], lambda e: q2[e][1], rw)
+    y16 = O.grouped_fc2(aq * sa[:, None], offsets, lambda e: w2[e], rw)
+    np.testing.assert_allclose(y8, y16, rtol=1e-13, atol=0)
+    # a planted mistake: the FC2 channel scales reversed
+    y_bad = O.grouped_fc2_fp8(a16, offsets, lambda e: q2[e][0], lambda e: q2[e][1][::-1], rw)
+    assert not np.allclose(y_bad, y16, rtol=1e-6, atol=0)
+
+
+def test_fp8_forward_token_definition_matches_grouped_form():
+    """ffn_token_outputs(fp8=True), the per-token definition the sampled GPU
+    checks of the W8A8 workloads use, equals the grouped W8A8 forward on the
+    tiny workload: all columns and a column subset (whose channel scales must
+    follow the columns)."""
+    inp = workloads.make_inputs("c1_tiny", "cpu")
+    x = inp["x"].double().numpy()
+    nw = inp["norm_w"].double().numpy()
+    Wr = inp["router_w"].double().numpy()
+    w13 = inp["w13"].double().numpy()
+    w2 = inp["w2"].double().numpy()
+    res = O.moe_ffn_forward(x, nw, 1e-6, 2, w13, w2, router_w=Wr, fp8=True)
+    q13 = {e: O.quantize_rows_e4m3(w13[e]) for e in range(8)}
+    q2 = {e: O.quantize_rows_e4m3(w2[e]) for e in range(8)}
+    assert len(set(q2[0][1].tolist())) > 30             # the channel scales differ
+    direct = O.ffn_token_outputs(res["xhat"], res["ids"], res["topk_w"], None, None, 512,
+                                 fp8=True, wq13_of=q13.get, wq2_of=q2.get)
+    np.testing.assert_array_equal(direct, res["out"])
+    cols = np.array([0, 5, 77, 128, 255])
+    direct_c = O.ffn_token_outputs(res["xhat"], res["ids"], res["topk_w"], None, None, 512,
+                                   cols=cols, fp8=True, wq13_of=q13.get, wq2_of=q2.get)
+    np.testing.assert_array_equal(direct_c, res["out"][:, cols])
+    # a planted mistake: the column subset taken with the scales of other columns
+    bad2 = {e: (q2[e][0], np.roll(q2[e][1], 1)) for e in range(8)}
+    bad_c = O.ffn_token_outputs(res["xhat"], res["ids"], res["topk_w"], None, None, 512,
+                                cols=cols, fp8=True, wq13_of=q13.get, wq2_of=bad2.get)
+    assert not np.array_equal(bad_c, res["out"][:, cols])
+    # W8A8 stays close to the bf16 forward (E4M3 carries 3 mantissa bits)
+    ref = O.moe_ffn_forward(x, nw, 1e-6, 2, w13, w2, router_w=Wr)["out"]
+    assert np.max(np.abs(res["out"] - ref)) < 6e-2 * max(1.0, np.max(np.abs(ref)))
+
+
 # ---------------------------------------------------------------------------
 # block-wise FP8 (128 x 128 weight tiles, 1 x 128 activation groups)
 # ---------------------------------------------------------------------------
