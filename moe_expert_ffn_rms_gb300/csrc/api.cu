@@ -254,10 +254,11 @@ int pick_engine(const moe_shape* s) {
 }
 
 // Grouped GEMM dispatch: tcgen05 engines where the shape allows, else SIMT.
+// `sched`: NULL, or a zeroed int the token-tile engine claims its units from.
 moe_status run_gemm(const moe_shape* s, int mode, int engine, const void* a, const float* a_scale,
                     const void* w, const float* w_scale, const int32_t* offsets,
                     const int32_t* row_src, const float* topk_w, void* c, int R_max, int sms,
-                    int* status, cudaStream_t st) {
+                    int* status, cudaStream_t st, int32_t* sched = nullptr) {
   const bool f8 = s->wdtype == MOE_W_FP8_E4M3;
   const bool fc2 = mode >= MOE_GEMM_FC2;
   const int K = fc2 ? s->I : s->H;
@@ -268,7 +269,7 @@ moe_status run_gemm(const moe_shape* s, int mode, int engine, const void* a, con
   if (!simt_only)
     e = moe::launch_gemm_tc(mode, f8, engine == MOE_ENGINE_DECODE, a, a_scale, w, w_scale,
                             offsets, row_src, topk_w, c, s->E, K, s->I, N_out, R_max, s->T, sms,
-                            status, st);
+                            status, st, sched);
   if (e == cudaErrorNotSupported)
     e = moe::launch_gemm_simt(mode, f8, a, a_scale, w, w_scale, offsets, row_src, topk_w, c, s->E,
                               K, s->I, N_out, R_max, st);
@@ -277,8 +278,9 @@ moe_status run_gemm(const moe_shape* s, int mode, int engine, const void* a, con
 }
 
 // FC1 + silu_and_mul then FC2 + routing weight (bf16 rows in (token, slot)
-// order).  `sched` (1 + E ints) must be zero when the fused decode launch is
-// used; actq / act_scale are the FP8 path's scratch.
+// order).  `sched` (1 + 2E ints) must be zero: the fused decode launch uses
+// all of it, the token-tile engine sched[0] (FC1) and sched[1] (FC2) as unit
+// counters; actq / act_scale are the FP8 path's scratch.
 moe_status ffn_impl(const moe_shape* s, int engine, bool fuse, const void* xp,
                     const float* xp_scale, const void* w13, const float* w13_scale, const void* w2,
                     const float* w2_scale, const int32_t* offsets, const int32_t* row_src,
@@ -315,8 +317,10 @@ moe_status ffn_impl(const moe_shape* s, int engine, bool fuse, const void* xp,
     if (e == cudaSuccess) return MOE_OK;
     if (e != cudaErrorNotSupported) return cuda_fail(e, "fused decode FFN launch");
   }
+  int32_t* sched_fc1 = (engine == MOE_ENGINE_PREFILL && sched) ? sched : nullptr;
+  int32_t* sched_fc2 = sched_fc1 ? sched + 1 : nullptr;
   moe_status rc = run_gemm(s, MOE_GEMM_FC1_SILU, engine, xp, xp_scale, w13, w13_scale, offsets,
-                           row_src, nullptr, act, R, dev->sms, dev->status, st);
+                           row_src, nullptr, act, R, dev->sms, dev->status, st, sched_fc1);
   if (rc != MOE_OK) return rc;
   // FP8: per-row quantisation of the bf16 intermediate before FC2
   const void* a2 = act;
@@ -325,7 +329,7 @@ moe_status ffn_impl(const moe_shape* s, int engine, bool fuse, const void* xp,
     a2 = actq;
   }
   return run_gemm(s, MOE_GEMM_FC2_BF16, engine, a2, act_scale, w2, w2_scale, offsets, row_src, tw,
-                  y, R, dev->sms, dev->status, st);
+                  y, R, dev->sms, dev->status, st, sched_fc2);
 }
 
 bool fuse_decode(const moe_shape* s, int engine) {
@@ -779,7 +783,9 @@ moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* 
   const int engine = pick_engine(shape);
   PdlOff no_pdl(engine == MOE_ENGINE_PREFILL);  // as in the forward
   const bool fuse = fuse_decode(shape, engine);
-  if (fuse) MOE_CUDA(cudaMemsetAsync(sched, 0, sched_bytes, st), "scheduler reset");
+  // the fused decode launch and the token tiles' unit counters start at zero
+  if (!fb && (fuse || engine == MOE_ENGINE_PREFILL))
+    MOE_CUDA(cudaMemsetAsync(sched, 0, sched_bytes, st), "scheduler reset");
   return ffn_impl(shape, engine, fuse, xp, xp_scale, w13, w13_scale, w2, w2_scale, offsets,
                   row_src, topk_w, act_mid, y, sched, actq, act_scale, dev, st);
 }

@@ -692,13 +692,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
   const int U0 = s_up[0][p.E];
   const int U = U0 + (NJ == 2 ? s_up[NJ - 1][p.E] : 0);
 
+  // token tiles: the token chunks of one weight tile are consecutive units,
+  // so the CTAs that share the tile start it together
   auto decode_unit = [&](int u) -> Unit {
     if (NJ == 2 && u >= U0) {
-      Unit un = unit_of(u - U0, s_off, s_up[NJ - 1], p.E, p.job[NJ - 1].nt, p.chunk);
+      Unit un = unit_of(u - U0, s_off, s_up[NJ - 1], p.E, p.job[NJ - 1].nt, p.chunk, !SWAP);
       un.job = 1;
       return un;
     }
-    return unit_of(u, s_off, s_up[0], p.E, p.job[0].nt, p.chunk);
+    return unit_of(u, s_off, s_up[0], p.E, p.job[0].nt, p.chunk, !SWAP);
   };
   // Consumers read claimed units in order from the unit ring.
   auto next_unit = [&](int i) -> int {
@@ -1306,15 +1308,15 @@ cudaError_t launch_pair(const CUtensorMap& tw, const CUtensorMap& tx, const Para
   return e;
 }
 
-// Prefill on CTA pairs; cudaErrorNotSupported when not covered or not
-// enabled.  Off unless MOE_PREFILL_PAIR=1: prefill runs with this kernel
-// stalled intermittently on GB300 and the cause has not been found, so the
-// single-CTA tiles are the default.
+// Prefill on CTA pairs.  Not launched: prefill runs with this kernel stalled
+// intermittently on GB300 and the cause has not been found, so it stays off
+// the GPU (cudaErrorNotSupported) and the single-CTA tiles run instead.
+constexpr bool kPrefillPairEnabled = false;
+
 cudaError_t launch_prefill_pair(int mode, bool fp8, const Params& base, const JobP& job,
                                 const CUtensorMap& tw, const CUtensorMap& tx, int sms,
                                 cudaStream_t st) {
-  const char* env = getenv("MOE_PREFILL_PAIR");
-  if (!(env && env[0] == '1')) return cudaErrorNotSupported;
+  if (!kPrefillPairEnabled) return cudaErrorNotSupported;
   Params p = base;
   p.job[0] = job;
   p.njobs = 1;
@@ -1373,7 +1375,7 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
                            const void* w, const float* w_scale, const int32_t* offsets,
                            const int32_t* row_src, const float* topk_w, void* c, int E, int K,
                            int I, int N_out, int R_max, int T, int sms, int* status,
-                           cudaStream_t st) {
+                           cudaStream_t st, int* sched) {
   std::call_once(g_encode_once, load_encode);
   if (R_max == 0) return cudaSuccess;
   if (!g_encode || E > kMaxExperts) return cudaErrorNotSupported;
@@ -1385,7 +1387,7 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
   p.I = I;
   p.R_max = R_max;
   p.njobs = 1;
-  p.sched = nullptr;
+  p.sched = decode ? nullptr : sched;  // one launch, one job: only the unit counter is used
   p.status = status;
   CUtensorMap maps[4];
   if (!make_job(&p.job[0], &maps[0], &maps[1], mode, fp8, decode, a, a_scale, w, w_scale, row_src,

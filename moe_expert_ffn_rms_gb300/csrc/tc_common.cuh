@@ -19,19 +19,30 @@ struct Unit {
 };
 
 // Unit u of a job: expert e has ceil(cnt/chunk) token chunks, each with nt N
-// tiles; s_up[e] is the exclusive prefix of units.
-MOE_DEV Unit unit_of(int u, const int* s_off, const int* s_up, int E, int nt, int chunk) {
+// tiles; s_up[e] is the exclusive prefix of units.  Within an expert the N
+// tile varies fastest (mt_fast = false), or the token chunk does (mt_fast =
+// true: consecutive units share one weight tile).
+MOE_DEV Unit unit_of(int u, const int* s_off, const int* s_up, int E, int nt, int chunk,
+                     bool mt_fast = false) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (s_up[mid] <= u) lo = mid; else hi = mid - 1;
   }
   const int local = u - s_up[lo];
-  const int mt = local / nt;
+  int mt, n;
+  if (mt_fast) {
+    const int chunks = (s_off[lo + 1] - s_off[lo] + chunk - 1) / chunk;
+    n = local / chunks;
+    mt = local - n * chunks;
+  } else {
+    mt = local / nt;
+    n = local - mt * nt;
+  }
   Unit un;
   un.job = 0;
   un.e = lo;
-  un.nt = local - mt * nt;
+  un.nt = n;
   un.row0 = s_off[lo] + mt * chunk;
   un.rows = min(chunk, s_off[lo + 1] - un.row0);
   return un;
