@@ -34,8 +34,8 @@
  *     memory; scratch comes from the caller's `workspace`.
  *   - Layouts are row-major with the last index contiguous.  bf16 is
  *     __nv_bfloat16 (2 bytes), e4m3 is OCP FP8 E4M3FN (1 byte).
- *   - Device pointers must be 16-byte aligned; row lengths must keep every
- *     row 16-byte aligned (H and I multiples of 64).
+ *   - Device pointers must be 16-byte aligned (weight scales included); row
+ *     lengths must keep every row 16-byte aligned (H and I multiples of 64).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *     only enqueue work on it and never synchronise the host.
  *   - Inputs are read only.  A return of MOE_OK means the work was enqueued;

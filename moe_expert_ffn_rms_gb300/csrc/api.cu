@@ -375,6 +375,8 @@ moe_status forward_impl(const moe_shape* s, const void* x, const void* norm_w, c
   MOE_REQ(!f8 || (w13_scale && w2_scale), MOE_ERR_INVALID_ARG, "FP8 weights need w13_scale and w2_scale");
   MOE_REQ(aligned16(x) && aligned16(norm_w) && aligned16(w13) && aligned16(w2) && aligned16(out),
           MOE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  MOE_REQ(!f8 || (aligned16(w13_scale) && aligned16(w2_scale)), MOE_ERR_INVALID_ARG,
+          "FP8 weight scales must be 16-byte aligned");
   MOE_REQ(((uintptr_t)workspace & 255u) == 0, MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   const Ws L = layout(s);
   MOE_REQ(ws_bytes >= L.total, MOE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", ws_bytes,
@@ -722,6 +724,7 @@ moe_status moe_grouped_gemm(const moe_shape* shape, int32_t mode, const void* a,
   MOE_REQ(aligned16(a) && aligned16(w) && aligned16(c), MOE_ERR_INVALID_ARG, "misaligned pointer");
   const bool f8 = shape->wdtype == MOE_W_FP8_E4M3;
   MOE_REQ(!f8 || (a_scale && w_scale), MOE_ERR_INVALID_ARG, "FP8 needs a_scale and w_scale");
+  MOE_REQ(!f8 || aligned16(w_scale), MOE_ERR_INVALID_ARG, "FP8 weight scales must be 16-byte aligned");
   MOE_REQ(!(topk_w && !row_src), MOE_ERR_INVALID_ARG, "topk_w needs row_src");
   DevInfo* d = nullptr;
   if ((rc = device_info(&d)) != MOE_OK) return rc;
@@ -756,6 +759,8 @@ moe_status moe_grouped_ffn(const moe_shape* shape, const void* xp, const float* 
           MOE_ERR_INVALID_ARG, "xp, w13, w2, offsets, row_src, topk_w, act, y and workspace must be non-NULL");
   MOE_REQ(!f8 || (xp_scale && w13_scale && w2_scale), MOE_ERR_INVALID_ARG,
           "FP8 needs xp_scale, w13_scale and w2_scale");
+  MOE_REQ(!f8 || (aligned16(w13_scale) && aligned16(w2_scale)), MOE_ERR_INVALID_ARG,
+          "FP8 weight scales must be 16-byte aligned");
   MOE_REQ(aligned16(xp) && aligned16(w13) && aligned16(w2) && aligned16(act) && aligned16(y),
           MOE_ERR_INVALID_ARG, "misaligned pointer");
   MOE_REQ(((uintptr_t)workspace & 255u) == 0, MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");

@@ -47,6 +47,9 @@ using namespace ptx;
 using namespace tc;
 
 constexpr int kThreads = 192;
+// Wide token tiles (256 token rows per unit): the producer, the MMA thread and
+// eight epilogue warps (four per 128-row half).
+constexpr int kThreadsWide = 320;
 constexpr int kRowBytes = 128;       // one swizzle row: K slice of a stage
 constexpr int kTileRows = 128;       // MMA M
 constexpr int kTileBytes = kTileRows * kRowBytes;  // 16 KB
@@ -132,15 +135,17 @@ MOE_DEV void issue_stage(uint8_t* a, uint8_t* b, uint64_t* bar, const CUtensorMa
   }
 }
 
-// Epilogue of one unit: TMEM -> registers -> fused op -> global memory.
-// Returns false if a bounded wait ran out.
+// Epilogue of one weight-streaming unit: TMEM -> registers -> fused op ->
+// global memory (token tiles use epilogue_tile below).  Returns false if a
+// bounded wait ran out.
 template <bool SWAP, int MODE, bool FP8>
 MOE_DEV bool epilogue_unit(const Unit& un, const JobP& j, int I, uint32_t tbase, int lrow,
                            float* s_xch, uint64_t* xch_bar, uint32_t& xph, volatile int* abort) {
   constexpr bool IS_FC2 = (MODE == 2 || MODE == 3);  // routing-weight epilogue
   constexpr bool OUT_F32 = (MODE == 2);              // fp32 output (else bf16)
+  static_assert(SWAP, "token tiles use epilogue_tile");
   const int wrow0 = un.e * j.N_w;
-  if (SWAP) {
+  {
     // lane = weight row of the slice, columns = the unit's token rows
     const int ncols = ((un.rows + 15) / 16) * 16;
     if (MODE == 1) {
@@ -204,107 +209,197 @@ MOE_DEV bool epilogue_unit(const Unit& un, const JobP& j, int I, uint32_t tbase,
         }
       }
     }
-  } else {
-    // lane = token row of the tile, columns = weight rows
-    const int r = un.row0 + lrow;
-    const bool rvalid = lrow < un.rows;
-    const float sa = (FP8 && rvalid) ? j.a_scale[r] : 1.f;
-    if (MODE == 1) {
-      for (int c2 = 0; c2 < 128; c2 += 32) {
-        // two 16-column chunks of gate and up per TMEM round trip
-        float gg[32], uu[32];
-        tmem_ld16(tbase + c2, gg);
-        tmem_ld16(tbase + c2 + 16, gg + 16);
-        tmem_ld16(tbase + 128 + c2, uu);
-        tmem_ld16(tbase + 128 + c2 + 16, uu + 16);
-        tmem_ld_wait();
-#pragma unroll
-        for (int cc = 0; cc < 32; cc += 16) {
-        const float* g = gg + cc;
-        const float* up = uu + cc;
-        const int c = c2 + cc;
-        const int n0 = un.nt * 128 + c;
-        if (rvalid) {
-          uint32_t pk[8];
-#pragma unroll
-          for (int t = 0; t < 16; t += 2) {
-            float o[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int n = min(n0 + t + h, I - 1);
-              const float gs = FP8 ? sa * j.w_scale[wrow0 + n] : 1.f;
-              const float us = FP8 ? sa * j.w_scale[wrow0 + I + n] : 1.f;
-              o[h] = silu_f(g[t + h] * gs) * (up[t + h] * us);
-            }
-            pk[t / 2] = pack2_bf16(o[0], o[1]);
-          }
-          bf16* dst = reinterpret_cast<bf16*>(j.out) + (size_t)r * j.ldo + n0;
-          if (n0 + 16 <= I) {
-            reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          } else {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-              if (n0 + t < I) {
-                const uint32_t w2 = pk[t / 2];
-                const uint16_t h = (t & 1) ? (uint16_t)(w2 >> 16) : (uint16_t)(w2 & 0xffffu);
-                reinterpret_cast<uint16_t*>(dst)[t] = h;
-              }
-            }
-          }
-        }
-        }
-      }
-    } else {
-      const float tw = (IS_FC2 && rvalid && j.topk_w) ? j.topk_w[j.row_src[r]] : 1.f;
-      // FC2 bf16 rows go back to (token, slot) order
-      const int orow = (MODE == 3 && rvalid && j.row_src) ? j.row_src[r] : r;
-      for (int c4 = 0; c4 < 256; c4 += 64) {
-        // four 16-column chunks per TMEM round trip
-        float vv[64];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld16(tbase + c4 + 16 * q, vv + 16 * q);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-        float* v = vv + 16 * q;
-        const int c = c4 + 16 * q;
-        const int n0 = un.nt * 256 + c;
-        if (rvalid && n0 < j.n_out) {
-#pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const float ws = FP8 ? j.w_scale[wrow0 + min(n0 + t, j.n_out - 1)] : 1.f;
-            v[t] = v[t] * ws * sa * tw;
-          }
-          if (OUT_F32) {
-            float* dst = reinterpret_cast<float*>(j.out) + (size_t)r * j.ldo + n0;
-            if (n0 + 16 <= j.n_out) {
-#pragma unroll
-              for (int t = 0; t < 16; t += 4)
-                reinterpret_cast<float4*>(dst)[t / 4] = make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]);
-            } else {
-              for (int t = 0; t < 16 && n0 + t < j.n_out; ++t) dst[t] = v[t];
-            }
-          } else {
-            bf16* dst = reinterpret_cast<bf16*>(j.out) + (size_t)orow * j.ldo + n0;
-            if (n0 + 16 <= j.n_out) {
-              uint32_t pk[8];
-#pragma unroll
-              for (int t = 0; t < 16; t += 2) pk[t / 2] = pack2_bf16(v[t], v[t + 1]);
-              reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            } else {
-              for (int t = 0; t < 16 && n0 + t < j.n_out; ++t) dst[t] = __float2bfloat16_rn(v[t]);
-            }
-          }
-        }
-        }
-      }
-    }
   }
   return true;
 }
 
+
+// ------------------------------------------------ token-tile epilogue --
+// What a token-tile epilogue thread needs besides the accumulator: its row,
+// the row's FP8 activation scale, the routing weight and the output row of
+// FC2.  Loaded before the thread waits for the accumulator, so these
+// dependent global loads overlap the unit's main loop.
+struct TileRow {
+  int r;        // activation row
+  int orow;     // output row
+  bool valid;   // the row belongs to the unit
+  float sa;     // E4M3 activation scale (1 for bf16)
+  float tw;     // routing weight (FC2; else 1)
+};
+
+template <int MODE, bool FP8>
+MOE_DEV TileRow tile_row(const Unit& un, const JobP& j, int lrow) {
+  constexpr bool IS_FC2 = (MODE == 2 || MODE == 3);
+  TileRow t;
+  t.r = un.row0 + lrow;
+  t.valid = lrow < un.rows;
+  t.sa = (FP8 && t.valid) ? j.a_scale[t.r] : 1.f;
+  const int src = (IS_FC2 && t.valid && j.row_src) ? j.row_src[t.r] : t.r;
+  t.tw = (IS_FC2 && t.valid && j.topk_w) ? j.topk_w[src] : 1.f;
+  t.orow = (MODE == 3) ? src : t.r;  // FC2 bf16 rows go back to (token, slot) order
+  return t;
+}
+
+// Shared-memory staging of one epilogue warp: 32 rows x 32 bf16 columns.
+constexpr int kStageWords = 32 * 4;  // uint4 per warp (2 KB)
+// E4M3 token tiles: the unit's 256 weight-channel scales, per epilogue warp.
+constexpr int kTileScales = 256;
+
+// Loads the E4M3 channel scales of a token-tile unit into the warp's slot
+// (FC1: the 128 gate then the 128 up channels of the N tile; else the N
+// tile's 256 channels; 0 past the matrix), before the warp waits for the
+// accumulator.  Scale rows are 16-byte aligned (the boundary checks it).
+template <int MODE>
+MOE_DEV void load_tile_scales(const Unit& un, const JobP& j, int I, int lane, float* wsc) {
+  const float* base = j.w_scale + (size_t)un.e * j.N_w;
+#pragma unroll
+  for (int i = lane * 4; i < kTileScales; i += 128) {
+    int col, lim;
+    if (MODE == 1) {
+      col = (i < 128 ? 0 : I) + un.nt * 128 + (i & 127);
+      lim = (i < 128 ? 0 : I) + I;
+      if (un.nt * 128 + (i & 127) >= I) col = lim;  // past the intermediate
+    } else {
+      col = un.nt * 256 + i;
+      lim = j.n_out;
+    }
+    const float4 v = col < lim ? *reinterpret_cast<const float4*>(base + col)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(wsc + i) = v;
+  }
+  __syncwarp();
+}
+
+// Writes a warp's 32 rows x 32 bf16 columns to global memory in 64-byte row
+// runs: each lane holds its row's 32 values as 16 packed words (pk); they go
+// through the warp's shared-memory buffer (16-byte chunks XOR-swizzled by row
+// pair, so neither side has bank conflicts) and come back as 8 rows x 64 bytes
+// per store instruction -- instead of 32 rows x 16 bytes, a quarter of each
+// sector.  dst(row) is the row's first column; rows whose `valid` is false
+// are not written.
+MOE_DEV void store_rows32(uint4* stg, int lane, const uint32_t (&pk)[16], bool valid, bf16* dst) {
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    stg[lane * 4 + (c ^ sw)] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+  __syncwarp();
+  const unsigned long long my = reinterpret_cast<unsigned long long>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = i * 8 + (lane >> 2), c = lane & 3;
+    const uint4 v = stg[row * 4 + (c ^ ((row >> 1) & 3))];
+    const unsigned long long base = __shfl_sync(0xffffffffu, my, row);
+    const int ok = __shfl_sync(0xffffffffu, valid ? 1 : 0, row);
+    if (ok) reinterpret_cast<uint4*>(base)[c] = v;
+  }
+  __syncwarp();
+}
+
+// silu(z) = z / (1 + e^-z) with the fast exponential and divide (the token
+// tiles' FC1 epilogue is on the critical path; the result is rounded to bf16).
+MOE_DEV float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// Epilogue of one token-tile unit: lane = token row of the tile, columns =
+// weight rows.  TMEM is read in rounds of 128 columns (64 with E4M3 scales,
+// whose per-column loads need registers too), one wait per round; bf16 rows
+// leave through store_rows32 (stg: this warp's staging buffer).
+template <int MODE, bool FP8>
+MOE_DEV void epilogue_tile(const Unit& un, const JobP& j, int I, uint32_t tbase,
+                           const TileRow& t, int lane, uint4* stg, const float* wsc) {
+  if (MODE == 1) {
+    for (int c2 = 0; c2 < 128; c2 += 64) {
+      float gg[64], uu[64];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        tmem_ld16(tbase + c2 + 16 * q, gg + 16 * q);
+        tmem_ld16(tbase + 128 + c2 + 16 * q, uu + 16 * q);
+      }
+      tmem_ld_wait();
+#pragma unroll
+      for (int cc = 0; cc < 64; cc += 32) {
+        const int n0 = un.nt * 128 + c2 + cc;  // I % 64 == 0: 32 columns are all in or all out
+        if (n0 >= I) continue;
+        uint32_t pk[16];
+#pragma unroll
+        for (int t16 = 0; t16 < 32; t16 += 16) {
+          // E4M3: the 16 gate and 16 up channel scales of these columns
+          // (16-byte aligned rows; the same addresses in every lane)
+          float gs[16], us[16];
+#pragma unroll
+          for (int v4 = 0; v4 < 16; v4 += 4) {
+            if (FP8) {
+              const int ci = c2 + cc + t16 + v4;  // column within the N tile
+              const float4 a = *reinterpret_cast<const float4*>(wsc + ci);
+              const float4 b = *reinterpret_cast<const float4*>(wsc + 128 + ci);
+              gs[v4] = a.x * t.sa; gs[v4 + 1] = a.y * t.sa; gs[v4 + 2] = a.z * t.sa; gs[v4 + 3] = a.w * t.sa;
+              us[v4] = b.x * t.sa; us[v4 + 1] = b.y * t.sa; us[v4 + 2] = b.z * t.sa; us[v4 + 3] = b.w * t.sa;
+            } else {
+              gs[v4] = gs[v4 + 1] = gs[v4 + 2] = gs[v4 + 3] = 1.f;
+              us[v4] = us[v4 + 1] = us[v4 + 2] = us[v4 + 3] = 1.f;
+            }
+          }
+#pragma unroll
+          for (int tt = 0; tt < 16; tt += 2) {
+            const int c = cc + t16 + tt;
+            pk[(t16 + tt) / 2] = pack2_bf16(silu_fast(gg[c] * gs[tt]) * (uu[c] * us[tt]),
+                                            silu_fast(gg[c + 1] * gs[tt + 1]) * (uu[c + 1] * us[tt + 1]));
+          }
+        }
+        store_rows32(stg, lane, pk, t.valid,
+                     reinterpret_cast<bf16*>(j.out) + (size_t)t.r * j.ldo + n0);
+      }
+    }
+  } else {
+    constexpr int RC = FP8 ? 64 : 128;  // columns per round
+    const float f = t.sa * t.tw;
+    for (int c4 = 0; c4 < 256; c4 += RC) {
+      float vv[RC];
+#pragma unroll
+      for (int q = 0; q < RC / 16; ++q) tmem_ld16(tbase + c4 + 16 * q, vv + 16 * q);
+      tmem_ld_wait();
+#pragma unroll
+      for (int cc = 0; cc < RC; cc += 32) {
+        float* v = vv + cc;
+        // bf16 outputs (FC1 raw 2I, FC2 H columns) are multiples of 64 columns,
+        // so 32 columns are all in or all out; fp32 outputs (the router's 3E
+        // logit columns among them) may end inside a chunk
+        const int n0 = un.nt * 256 + c4 + cc;
+        if (n0 >= j.n_out) continue;
+        if (FP8) {
+          // channel scales from the warp's slot (the same address in every lane)
+#pragma unroll
+          for (int tt = 0; tt < 32; tt += 4) {
+            const float4 w = *reinterpret_cast<const float4*>(wsc + c4 + cc + tt);
+            v[tt] *= w.x * f; v[tt + 1] *= w.y * f; v[tt + 2] *= w.z * f; v[tt + 3] *= w.w * f;
+          }
+        } else {
+#pragma unroll
+          for (int tt = 0; tt < 32; ++tt) v[tt] *= f;
+        }
+        if (MODE == 2) {  // fp32 rows
+          if (t.valid) {
+            float* dst = reinterpret_cast<float*>(j.out) + (size_t)t.r * j.ldo + n0;
+            // vector stores need a 16-byte row pitch (the router's 3E may not give one)
+            if (n0 + 32 <= j.n_out && (j.ldo & 3) == 0) {
+#pragma unroll
+              for (int tt = 0; tt < 32; tt += 4)
+                reinterpret_cast<float4*>(dst)[tt / 4] =
+                    make_float4(v[tt], v[tt + 1], v[tt + 2], v[tt + 3]);
+            } else {
+              for (int tt = 0; tt < 32 && n0 + tt < j.n_out; ++tt) dst[tt] = v[tt];
+            }
+          }
+        } else {
+          uint32_t pk[16];
+#pragma unroll
+          for (int tt = 0; tt < 32; tt += 2) pk[tt / 2] = pack2_bf16(v[tt], v[tt + 1]);
+          store_rows32(stg, lane, pk, t.valid,
+                       reinterpret_cast<bf16*>(j.out) + (size_t)t.orow * j.ldo + n0);
+        }
+      }
+    }
+  }
+}
 
 // ------------------------------------------ whole decode forward phases --
 // Grid-wide barrier of a cooperative launch.  bar[0] counts arrivals, bar[1]
@@ -576,12 +671,21 @@ MOE_DEV void mega_combine(const MegaP& mp) {
 // MEGA: the whole decode forward in this launch (cooperative, one CTA per SM):
 // rms_norm, routing, permute and row gather before the FFN, the combine after
 // it, each phase separated by a grid barrier (MegaP).
-template <bool SWAP, bool FP8, int M0, int M1, bool MEGA = false>
-__global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
+// WIDE (token tiles only): a unit is 256 token rows x the N tile, computed as
+// two M = 128 MMAs per K step that share the weight slice in shared memory --
+// per flop 2/3 of the operand bytes of the 128-row tile.  The two 256-column
+// accumulators fill TMEM, so one unit's accumulators are live at a time and
+// eight epilogue warps drain both halves at once.
+template <bool SWAP, bool FP8, int M0, int M1, bool MEGA = false, bool WIDE = false>
+__global__ void __launch_bounds__(WIDE ? kThreadsWide : kThreads, 1) moe_tc_gemm_kernel(
     const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_x0,
     const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_x1,
     const Params p, const MegaP mp) {
+  static_assert(!WIDE || (!SWAP && !MEGA && M1 < 0), "wide tiles are single-job token tiles");
+  static_assert(SWAP || M1 < 0, "token-tile launches run one job");
   constexpr int NJ = (M1 >= 0) ? 2 : 1;
+  constexpr int NE = WIDE ? 8 : 4;     // epilogue warps
+  constexpr int NACC = WIDE ? 1 : 2;   // accumulator buffers (each kAccCols; WIDE: both halves)
   extern __shared__ uint8_t dyn_smem[];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_up[NJ][kMaxExperts + 1];
@@ -598,6 +702,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ float s_xch[SWAP && (M0 == 1 || M1 == 1) ? 64 * 17 : 1];  // decode FC1: up values
+  __shared__ uint4 s_stg[SWAP ? 1 : NE * kStageWords];  // token tiles: epilogue row staging
+  __shared__ __align__(16) float s_wsc[(!SWAP && FP8) ? NE * kTileScales : 4];  // E4M3 channel scales
   __shared__ volatile int s_gok;  // MEGA: grid barrier result
   unsigned mega_gen = 0;          // MEGA: grid barrier generation (thread 0)
 
@@ -614,11 +720,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], 128);
+      mbar_init(&tempty_bar[a], 32 * NE);
     }
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(&ufull_bar[i], 1);
-      mbar_init(&uempty_bar[i], 1 + 4);  // MMA thread + the four epilogue warps
+      mbar_init(&uempty_bar[i], 1 + NE);  // MMA thread + the epilogue warps
     }
     mbar_init(&drain_bar, 1);
     mbar_init(&xch_bar, 128);
@@ -751,9 +857,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
           fence_proxy_async_global();
         }
         const int nb = SWAP ? (un.rows + kDecodeBoxRows - 1) / kDecodeBoxRows : 0;
+        // WIDE: the second 128-row half of the token rows is loaded only when
+        // the unit has rows there
+        const bool half2 = WIDE && un.rows > kTileRows;
         const uint32_t tx = (uint32_t)p.kw *
                             (SWAP ? (uint32_t)(p.a_atom + nb * kDecodeBoxRows * kRowBytes)
-                                  : (uint32_t)(kTileBytes + 2 * kTileBytes));
+                                  : (uint32_t)((half2 ? 2 : 1) * kTileBytes + 2 * kTileBytes));
         const CUtensorMap* tw = un.job ? &tm_w1 : &tm_w0;
         const CUtensorMap* tx_map = un.job ? &tm_x1 : &tm_x0;
         for (int ks = 0; ks < j.kst; ++ks) {
@@ -770,6 +879,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
             else
               issue_stage<SWAP, 0>(a + w * p.a_atom, b + w * p.b_atom, &full_bar[s], tw, tx_map, un,
                                    kx, wrow, p.I, nb, pol_w, pol_x);
+            if (half2)  // token rows 128..255 of the unit, after the first half
+              tma_load_2d(a + w * p.a_atom + kTileBytes, tx_map, &full_bar[s], kx,
+                          un.row0 + kTileRows, pol_x);
           }
           armed |= 1u << s;
           armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
@@ -803,6 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
         const uint32_t d = tmem + acc * kAccCols;
         const int n = SWAP ? ((un.rows + 15) / 16) * 16 : 256;
         const uint32_t idesc = make_idesc(n, FP8 ? 0u : 1u);
+        const bool half2 = WIDE && un.rows > kTileRows;  // WIDE: rows 128..255 -> d + kAccCols
         for (int ks = 0; ks < kst; ++ks) {
           if (!mbar_wait(&full_bar[s], ph, &s_abort)) { ok = false; break; }
           tc_fence_after();
@@ -817,6 +930,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
               const uint32_t accum = (ks | w | kk) ? 1u : 0u;
               if (FP8) mma_e4m3(d, ad, bd, idesc, accum);
               else mma_bf16(d, ad, bd, idesc, accum);
+              if (half2) {
+                const uint64_t ad2 = sw128_desc(a + kTileBytes + kk * 32);
+                if (FP8) mma_e4m3(d + kAccCols, ad2, bd, idesc, accum);
+                else mma_bf16(d + kAccCols, ad2, bd, idesc, accum);
+              }
             }
           }
           issued = true;
@@ -825,9 +943,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
         }
         if (!ok) break;
         mma_commit(&tfull_bar[acc]);
-        if (++acc == 2) { acc = 0; aph ^= 1; }
+        if (++acc == NACC) { acc = 0; aph ^= 1; }
       }
-      if (ok) ok = accumulator_tail(tempty_bar, acc, aph, &s_abort);
+      if (ok) ok = accumulator_tail(tempty_bar, acc, aph, &s_abort, NACC);
       if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
       if (issued) {  // all issued MMAs complete before TMEM can be released
         mma_commit(&drain_bar);
@@ -840,6 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
     // ======================================================== epilogue
     const int q = warp & 3;            // TMEM lane quarter of this warp
     const int lrow = q * 32 + lane;    // accumulator row (TMEM lane)
+    const int half = WIDE ? (warp - 2) >> 2 : 0;  // WIDE: token rows 128 * half ..
     int acc = 0;
     uint32_t aph = 0;
     uint32_t xph = 0;  // phase of xch_bar (decode FC1 exchange)
@@ -852,27 +971,46 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_gemm_kernel(
         break;
       }
       if (u < 0) break;
-      const Unit un = decode_unit(u);
+      Unit un = decode_unit(u);
+      if (WIDE) {  // this warp's 128-row half of the unit (possibly empty)
+        un.row0 += half * kTileRows;
+        un.rows = max(0, min(kTileRows, un.rows - half * kTileRows));
+      }
+      // token tiles: the row's scale, routing weight and output row first
+      TileRow trow{};
+      float* wsc = s_wsc + ((!SWAP && FP8) ? (warp - 2) * kTileScales : 0);
+      if constexpr (!SWAP) {
+        if (un.rows > 0) {
+          trow = tile_row<M0, FP8>(un, p.job[0], lrow);
+          if constexpr (FP8) load_tile_scales<M0>(un, p.job[0], p.I, lane, wsc);
+        }
+      }
       if (!mbar_wait(&tfull_bar[acc], aph, &s_abort)) {
         flag_status(p.status, MOE_ERR_TIMEOUT);
         break;
       }
       tc_fence_after();
-      const uint32_t tbase = tmem + acc * kAccCols + ((uint32_t)(q * 32) << 16);
-      bool ok;
-      if (un.job == 0)
+      const uint32_t tbase =
+          tmem + acc * kAccCols + (uint32_t)(half * kAccCols) + ((uint32_t)(q * 32) << 16);
+      bool ok = true;
+      if constexpr (!SWAP) {
+        if (un.rows > 0)
+          epilogue_tile<M0, FP8>(un, p.job[0], p.I, tbase, trow, lane,
+                                 s_stg + (warp - 2) * kStageWords, wsc);
+      } else if (un.job == 0) {
         ok = epilogue_unit<SWAP, M0, FP8>(un, p.job[0], p.I, tbase, lrow, s_xch, &xch_bar, xph,
                                           &s_abort);
-      else
+      } else {
         ok = epilogue_unit<SWAP, (M1 >= 0 ? M1 : M0), FP8>(un, p.job[1], p.I, tbase, lrow, s_xch,
                                                            &xch_bar, xph, &s_abort);
+      }
       if (!ok) {
         flag_status(p.status, MOE_ERR_TIMEOUT);
         break;
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
-      if (++acc == 2) { acc = 0; aph ^= 1; }
+      if (++acc == NACC) { acc = 0; aph ^= 1; }
       if (NJ == 2 && un.job == 0 && p.sched && !FP8) {
         // publish this warp's rows of the FC1 output to later TMA readers
         fence_proxy_async_global();
@@ -969,6 +1107,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_pair_kernel(
   __shared__ __align__(8) uint64_t xch_bar;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
+  __shared__ uint4 s_stg[4 * kStageWords];  // epilogue row staging
+  __shared__ __align__(16) float s_wsc[FP8 ? 4 * kTileScales : 4];  // E4M3 channel scales
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -1131,7 +1271,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_pair_kernel(
     const int lrow = q * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
-    uint32_t xph = 0;
     for (int u = pair; u < U; u += npairs) {
       Unit un = unit_of(u, s_off, s_up, p.E, j.nt, p.chunk);
       if (!mbar_wait(&tfull_bar[acc], aph, &s_abort)) {
@@ -1143,10 +1282,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_tc_pair_kernel(
       un.row0 += (int)rank * kTileRows;
       un.rows = max(0, min(kTileRows, un.rows - (int)rank * kTileRows));
       const uint32_t tbase = tmem + acc * kAccCols + ((uint32_t)(q * 32) << 16);
-      if (!epilogue_unit<false, MODE, FP8>(un, j, p.I, tbase, lrow, nullptr, &xch_bar, xph,
-                                           &s_abort)) {
-        flag_status(p.status, MOE_ERR_TIMEOUT);
-        break;
+      if (un.rows > 0) {
+        float* wsc = s_wsc + (FP8 ? (warp - 2) * kTileScales : 0);
+        if (FP8) load_tile_scales<MODE>(un, j, p.I, lane, wsc);
+        epilogue_tile<MODE, FP8>(un, j, p.I, tbase, tile_row<MODE, FP8>(un, j, lrow), lane,
+                                 s_stg + (warp - 2) * kStageWords, wsc);
       }
       tc_fence_before();
       __syncwarp();
@@ -1201,23 +1341,23 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, int64_t rows, int64_t 
                         elem, rows, cols, kRowBytes / elem, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <bool SWAP, bool FP8, int M0, int M1>
+template <bool SWAP, bool FP8, int M0, int M1, bool WIDE = false>
 cudaError_t launch_k(const CUtensorMap* maps, const Params& p, int grid, size_t smem,
                      cudaStream_t st) {
-  auto k = moe_tc_gemm_kernel<SWAP, FP8, M0, M1>;
+  auto k = moe_tc_gemm_kernel<SWAP, FP8, M0, M1, false, WIDE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(k, dim3(grid), dim3(kThreads), smem, st, maps[0], maps[1], maps[2], maps[3],
-                       p, MegaP{});
+  return launch_kernel(k, dim3(grid), dim3(WIDE ? kThreadsWide : kThreads), smem, st, maps[0],
+                       maps[1], maps[2], maps[3], p, MegaP{});
 }
 
-template <bool SWAP, bool FP8>
+template <bool SWAP, bool FP8, bool WIDE = false>
 cudaError_t launch_mode(int mode, const CUtensorMap* maps, const Params& p, int grid, size_t smem,
                         cudaStream_t st) {
-  if (mode == 0) return launch_k<SWAP, FP8, 0, -1>(maps, p, grid, smem, st);
-  if (mode == 1) return launch_k<SWAP, FP8, 1, -1>(maps, p, grid, smem, st);
-  if (mode == 2) return launch_k<SWAP, FP8, 2, -1>(maps, p, grid, smem, st);
-  return launch_k<SWAP, FP8, 3, -1>(maps, p, grid, smem, st);
+  if (mode == 0) return launch_k<SWAP, FP8, 0, -1, WIDE>(maps, p, grid, smem, st);
+  if (mode == 1) return launch_k<SWAP, FP8, 1, -1, WIDE>(maps, p, grid, smem, st);
+  if (mode == 2) return launch_k<SWAP, FP8, 2, -1, WIDE>(maps, p, grid, smem, st);
+  return launch_k<SWAP, FP8, 3, -1, WIDE>(maps, p, grid, smem, st);
 }
 
 // Token rows per decode unit: an expert normally holds <= T rows (distinct
@@ -1255,11 +1395,15 @@ bool make_job(JobP* j, CUtensorMap* tw, CUtensorMap* tx, int mode, bool fp8, boo
 }
 
 // Ring geometry shared by the launches; converts each job's K bytes into
-// stages of kw atoms.
-bool set_ring(Params* p, bool decode, int T, size_t* smem) {
-  const int static_smem = 8 * 1024;
-  p->chunk = decode ? decode_chunk(T) : kTileRows;
-  p->a_atom = kTileBytes;
+// stages of kw atoms.  wide: 256-row token tiles (two 16 KB token-row boxes
+// and the 32 KB weight slice per K slice).
+bool set_ring(Params* p, bool decode, int T, size_t* smem, bool wide = false) {
+  // static shared memory: barriers and tables, plus the token tiles'
+  // epilogue staging (2 KB per epilogue warp)
+  const int static_smem =
+      8 * 1024 + (decode ? 0 : (wide ? 8 : 4) * (kStageWords * 16 + kTileScales * 4));
+  p->chunk = decode ? decode_chunk(T) : (wide ? 2 * kTileRows : kTileRows);
+  p->a_atom = wide ? 2 * kTileBytes : kTileBytes;
   p->b_atom = decode ? p->chunk * kRowBytes : 2 * kTileBytes;
   int kw = 1;
   if (decode) {
@@ -1326,7 +1470,7 @@ cudaError_t launch_prefill_pair(int mode, bool fp8, const Params& base, const Jo
   p.b_atom = kTileBytes;    // this CTA's half of the 256 weight rows
   p.a_bytes = p.a_atom;
   p.stage_bytes = p.a_atom + p.b_atom;
-  const int static_smem = 8 * 1024;
+  const int static_smem = 8 * 1024 + 4 * (kStageWords * 16 + kTileScales * 4);
   int stages = (kSmemLimit - static_smem - 1024) / p.stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   p.stages = stages;
@@ -1399,8 +1543,18 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
     cudaError_t e = launch_prefill_pair(mode, fp8, p, p.job[0], maps[0], maps[1], sms, st);
     if (e != cudaErrorNotSupported) return e;
   }
+  // Token tiles of 256 rows when the batch gives every SM at least two of
+  // them (256-row units in the plain rows-per-expert estimate); else 128.
+  bool wide = false;
+  if (!decode) {
+    const int64_t est = ((int64_t)R_max / (2 * kTileRows)) * p.job[0].nt;
+    wide = est >= 2LL * sms;
+    const char* env = getenv("MOE_WIDE_TILES");
+    if (env && env[0] == '0') wide = false;
+    if (env && env[0] == '1') wide = true;
+  }
   size_t smem = 0;
-  if (!set_ring(&p, decode, T, &smem)) return cudaErrorNotSupported;
+  if (!set_ring(&p, decode, T, &smem, wide)) return cudaErrorNotSupported;
   p.job[1] = p.job[0];
   // upper bound on units: every expert's token chunks times the N tiles
   const int64_t chunks = (int64_t)(R_max + p.chunk - 1) / p.chunk + E;
@@ -1410,6 +1564,9 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
   if (decode)
     return fp8 ? launch_mode<true, true>(mode, maps, p, grid, smem, st)
                : launch_mode<true, false>(mode, maps, p, grid, smem, st);
+  if (wide)
+    return fp8 ? launch_mode<false, true, true>(mode, maps, p, grid, smem, st)
+               : launch_mode<false, false, true>(mode, maps, p, grid, smem, st);
   return fp8 ? launch_mode<false, true>(mode, maps, p, grid, smem, st)
              : launch_mode<false, false>(mode, maps, p, grid, smem, st);
 }

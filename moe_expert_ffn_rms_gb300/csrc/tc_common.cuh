@@ -77,11 +77,13 @@ MOE_DEV bool producer_tail(uint64_t* empty_bar, int stages, int s, uint32_t ph,
   return true;
 }
 
-// MMA tail: waits until the epilogues have released both accumulators.
-MOE_DEV bool accumulator_tail(uint64_t* tempty_bar, int acc, uint32_t aph, volatile int* abort) {
-  for (int i = 0; i < 2; ++i) {
+// MMA tail: waits until the epilogues have released every accumulator (nacc
+// buffers used round-robin).
+MOE_DEV bool accumulator_tail(uint64_t* tempty_bar, int acc, uint32_t aph, volatile int* abort,
+                              int nacc = 2) {
+  for (int i = 0; i < nacc; ++i) {
     if (!mbar_wait(&tempty_bar[acc], aph ^ 1, abort)) return false;
-    if (++acc == 2) { acc = 0; aph ^= 1; }
+    if (++acc == nacc) { acc = 0; aph ^= 1; }
   }
   return true;
 }

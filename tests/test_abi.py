@@ -98,6 +98,12 @@ def test_forward_rejects_bad_arguments_on_host(M):
     f8 = M.make_shape(4, 256, 8, 512, 2, fp8=True)
     assert M.lib.moe_ffn_forward(ctypes.byref(f8), fake, fake, fake, None, None, fake, fake, None,
                                  None, fake, None, None, fake, 1 << 40, None) == 1
+    # FP8 weight scales must be 16-byte aligned (the tile epilogues read them as float4)
+    assert M.lib.moe_ffn_forward(ctypes.byref(f8), fake, fake, fake, None, None, fake, fake,
+                                 fake + 4, fake, fake, None, None, fake, 1 << 40, None) == 1
+    assert "scales must be 16-byte aligned" in M.last_error()
+    assert M.lib.moe_grouped_gemm(ctypes.byref(f8), 1, fake, fake, fake, fake + 8, fake, None, None,
+                                  fake, None) == 1
 
 
 def test_step_entry_points_reject_bad_arguments_on_host(M):

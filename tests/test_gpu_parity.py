@@ -40,14 +40,18 @@ SMALL = {
     "wide_e": workloads.Shape(T=45, H=320, E=256, k=8, I=192),
     "prefill_like": workloads.Shape(T=300, H=384, E=4, k=2, I=256),
     "single": workloads.Shape(T=1, H=128, E=8, k=4, I=128),
+    # > 256 rows per expert: a full 256-row wide tile and a one-half tail
+    "two_wide_chunks": workloads.Shape(T=700, H=256, E=2, k=1, I=256),
 }
 
-ENGINES = ["auto", "decode", "prefill", "simt"]
+ENGINES = ["auto", "decode", "prefill", "prefill_wide", "simt"]
 # decode: FC1 and FC2 fused in one persistent launch; decode_mega: the whole
 # forward in one cooperative launch where it is covered (MOE_MEGA=1);
 # decode_unfused: FC1 and FC2 in two launches
 FWD_ENGINES = ENGINES + ["decode_mega", "decode_unfused"]
-ENV_SWITCHES = ("MOE_FORCE_SIMT", "MOE_FUSE", "MOE_ROUTER_TC", "MOE_MEGA")
+# prefill: 128-row token tiles; prefill_wide: 256-row token tiles (two M = 128
+# MMAs per K step), which the engine picks by itself at large batches
+ENV_SWITCHES = ("MOE_FORCE_SIMT", "MOE_FUSE", "MOE_ROUTER_TC", "MOE_MEGA", "MOE_WIDE_TILES")
 
 
 def _set_engine(shape_obj, engine, M):
@@ -62,6 +66,11 @@ def _set_engine(shape_obj, engine, M):
     if engine == "decode_unfused":
         os.environ["MOE_FUSE"] = "0"
         return M.ENGINE_DECODE
+    if engine == "prefill":
+        os.environ["MOE_WIDE_TILES"] = "0"
+    if engine == "prefill_wide":
+        os.environ["MOE_WIDE_TILES"] = "1"
+        return M.ENGINE_PREFILL
     return {"auto": M.ENGINE_AUTO, "decode": M.ENGINE_DECODE, "prefill": M.ENGINE_PREFILL}[engine]
 
 
@@ -141,7 +150,7 @@ def test_route_topk_given_logits_bit_exact(M, T, E, k):
 
 @pytest.mark.parametrize("tc", ["1", "0"])
 @pytest.mark.parametrize("cfg", ["c1_tiny", "c3_decode_skewed", "c5_prefill", "wide_prefill",
-                                 "small_uneven", "small_bias"])
+                                 "small_uneven", "small_bias", "odd_e_prefill"])
 def test_route_topk_router(M, cfg, tc):
     """Router logits from x_hat and W_r (tensor-core bf16x3 split for >= 256
     tokens unless MOE_ROUTER_TC=0; a one-CTA-per-token router fused with top-k
@@ -156,6 +165,9 @@ def test_route_topk_router(M, cfg, tc):
     elif cfg == "small_bias":    # Zipf bias on a small router, H * E at the size limit
         inp = workloads.make_inputs("c3_decode_skewed", DEV,
                                     shape=workloads.Shape(T=9, H=256, E=256, k=8, I=256))
+    elif cfg == "odd_e_prefill":  # tensor-core router with 3E = 21 logit columns (odd row pitch)
+        inp = workloads.make_inputs("c1_tiny", DEV,
+                                    shape=workloads.Shape(T=300, H=512, E=7, k=2, I=256))
     else:
         inp = workloads.make_inputs(cfg, DEV)
     T, H, E, k = inp["T"], inp["H"], inp["E"], inp["k"]
@@ -285,7 +297,8 @@ def _grouped_inputs(shape, seed, fp8=False, hot=False):
 
 
 @pytest.mark.parametrize("engine", ENGINES)
-@pytest.mark.parametrize("name", ["ragged_a", "ragged_b", "prefill_like", "single", "hot"])
+@pytest.mark.parametrize("name", ["ragged_a", "ragged_b", "prefill_like", "single", "hot",
+                                  "two_wide_chunks"])
 def test_grouped_gemm_modes(M, engine, name):
     shape = SMALL.get(name, workloads.Shape(T=150, H=256, E=5, k=2, I=192))
     d = _grouped_inputs(shape, 21, hot=(name == "hot"))
@@ -365,7 +378,7 @@ def test_grouped_gemm_fp8(M, engine):
 
 
 @pytest.mark.parametrize("fp8", [False, True])
-@pytest.mark.parametrize("engine", ["decode", "prefill"])
+@pytest.mark.parametrize("engine", ["decode", "prefill", "prefill_wide"])
 @pytest.mark.parametrize("name", ["ragged_a", "prefill_like", "hot"])
 def test_grouped_ffn_matches_steps(M, engine, name, fp8):
     """moe_grouped_ffn (fused on the decode engine for bf16) gives the same bits
