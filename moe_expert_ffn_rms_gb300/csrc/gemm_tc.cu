@@ -1083,226 +1083,6 @@ __global__ void __launch_bounds__(WIDE ? kThreadsWide : kThreads, 1) moe_tc_gemm
   if (warp == 1) tmem_dealloc(tmem, 2 * kAccCols);
 }
 
-// Prefill grouped GEMM on CTA pairs (cta_group::2).  A pair computes a
-// 256-token x 256-column tile: each CTA loads its own 128 token rows and one
-// half of the 256 weight rows (FC1 + silu: CTA 0 the 128 gate rows, CTA 1 the
-// matching 128 up rows; otherwise rows 0..127 / 128..255 of the N tile), so a
-// CTA moves 32 KB per K slice instead of 48 KB and the ring holds six slices.
-// Only the even CTA issues MMAs (M = 256, N = 256); TMA loads of both CTAs
-// complete on the even CTA's full barrier; MMA commits arrive on both CTAs'
-// barriers; each CTA's epilogue drains its own TMEM (its 128 rows x 256
-// columns) and releases the accumulator with remote arrives on the even CTA.
-template <int MODE, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1) moe_tc_pair_kernel(
-    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-    const Params p) {
-  extern __shared__ uint8_t dyn_smem[];
-  __shared__ int s_off[kMaxExperts + 1];
-  __shared__ int s_up[kMaxExperts + 1];
-  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t tfull_bar[2];
-  __shared__ __align__(8) uint64_t tempty_bar[2];
-  __shared__ __align__(8) uint64_t drain_bar;
-  __shared__ __align__(8) uint64_t xch_bar;
-  __shared__ uint32_t s_tmem;
-  __shared__ volatile int s_abort;
-  __shared__ uint4 s_stg[4 * kStageWords];  // epilogue row staging
-  __shared__ __align__(16) float s_wsc[FP8 ? 4 * kTileScales : 4];  // E4M3 channel scales
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  uint8_t* ring = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~(uintptr_t)1023);
-  const JobP& j = p.job[0];
-
-  if (warp == 0 && lane == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], 2 * 4);  // the four epilogue warps of both CTAs
-    }
-    mbar_init(&drain_bar, 1);
-    mbar_init(&xch_bar, 128);
-    s_abort = 0;
-    fence_mbar_init();
-    prefetch_tmap(&tm_w);
-    prefetch_tmap(&tm_x);
-  } else if (warp == 1) {
-    tmem_alloc_pair(&s_tmem, 2 * kAccCols);
-    tmem_relinquish_pair();
-  }
-  pdl_trigger();
-  pdl_wait();
-  for (int e = threadIdx.x; e <= p.E; e += blockDim.x) s_off[e] = p.offsets[e];
-  __syncthreads();
-  if (threadIdx.x == 0) {  // offsets must be monotone within [0, R_max]
-    int prev = 0;
-    bool bad = false;
-    for (int e = 0; e <= p.E; ++e) {
-      int v = s_off[e];
-      if (v < prev || v > p.R_max || (e == 0 && v != 0)) {
-        bad = true;
-        v = v < prev ? prev : (v > p.R_max ? p.R_max : v);
-        if (e == 0) v = 0;
-      }
-      s_off[e] = v;
-      prev = v;
-    }
-    if (bad && blockIdx.x == 0) flag_status(p.status, MOE_ERR_INVALID_ARG);
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int carry = 0;
-    for (int base = 0; base < p.E; base += 32) {
-      const int e = base + lane;
-      const int cnt = (e < p.E) ? s_off[e + 1] - s_off[e] : 0;
-      const int v = ((cnt + p.chunk - 1) / p.chunk) * j.nt;
-      int incl = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-      }
-      if (e < p.E) s_up[e] = carry + incl - v;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) s_up[p.E] = carry;
-  }
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // the peer's barriers are initialised before any remote use
-  tc_fence_after();
-  const uint32_t tmem = s_tmem;
-  const int U = s_up[p.E];
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-
-  if (warp == 0) {
-    // ===================================================== TMA producer
-    if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_last();
-      const uint64_t pol_x = l2_policy_evict_last();
-      int s = 0;
-      uint32_t ph = 0;
-      uint32_t armed = 0, armed_ph = 0;
-      bool ok = true;
-      const uint32_t bytes_pair = 2u * (uint32_t)(p.a_atom + p.b_atom);
-      for (int u = pair; u < U && ok; u += npairs) {
-        const Unit un = unit_of(u, s_off, s_up, p.E, j.nt, p.chunk);
-        const int wrow = un.e * j.N_w;
-        const int arow = un.row0 + (int)rank * kTileRows;
-        const int brow = (MODE == 1) ? wrow + (rank ? p.I : 0) + un.nt * 128
-                                     : wrow + un.nt * 256 + (int)rank * 128;
-        for (int ks = 0; ks < j.kst; ++ks) {
-          if (!mbar_wait(&empty_bar[s], ph ^ 1, &s_abort)) { ok = false; break; }
-          if (leader) mbar_arrive_expect_tx(&full_bar[s], bytes_pair);
-          const uint32_t fb = mapa_shared(smem_u32(&full_bar[s]), 0);
-          uint8_t* a = ring + (size_t)s * p.stage_bytes;
-          uint8_t* b = a + p.a_bytes;
-          const int kx = ks * (FP8 ? 128 : 64);
-          tma_load_2d_pair(a, &tm_x, fb, kx, arow, pol_x);
-          tma_load_2d_pair(b, &tm_w, fb, kx, brow, pol_w);
-          armed |= 1u << s;
-          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
-          if (++s == p.stages) { s = 0; ph ^= 1; }
-        }
-      }
-      // both CTAs: the even CTA's commits arrive on this CTA's empty barriers
-      if (ok) ok = producer_tail(empty_bar, p.stages, s, ph, &s_abort);
-      if (!ok) {
-        flag_status(p.status, MOE_ERR_TIMEOUT);
-        // the even CTA's full barriers count both CTAs' copies
-        if (leader) drain_armed(full_bar, p.stages, armed, armed_ph);
-      }
-    }
-  } else if (warp == 1) {
-    // ============================================ MMA issuer (even CTA)
-    if (lane == 0 && leader) {
-      int s = 0;
-      uint32_t ph = 0;
-      int acc = 0;
-      uint32_t aph = 0;
-      bool ok = true;
-      bool issued = false;
-      const uint32_t idesc = make_idesc_m(256, 256, FP8 ? 0u : 1u);
-      for (int u = pair; u < U && ok; u += npairs) {
-        if (!mbar_wait(&tempty_bar[acc], aph ^ 1, &s_abort)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d = tmem + acc * kAccCols;
-        for (int ks = 0; ks < j.kst; ++ks) {
-          if (!mbar_wait(&full_bar[s], ph, &s_abort)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t a = smem_u32(ring + (size_t)s * p.stage_bytes);
-          const uint32_t b = a + p.a_bytes;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sw128_desc(a + kk * 32);
-            const uint64_t bd = sw128_desc(b + kk * 32);
-            const uint32_t accum = (ks | kk) ? 1u : 0u;
-            if (FP8) mma_e4m3_pair(d, ad, bd, idesc, accum);
-            else mma_bf16_pair(d, ad, bd, idesc, accum);
-          }
-          issued = true;
-          mma_commit_pair(&empty_bar[s], 0x3);
-          if (++s == p.stages) { s = 0; ph ^= 1; }
-        }
-        if (!ok) break;
-        mma_commit_pair(&tfull_bar[acc], 0x3);
-        if (++acc == 2) { acc = 0; aph ^= 1; }
-      }
-      // both CTAs' epilogues (remote arrivals from the odd CTA) have released
-      // the accumulators before teardown
-      if (ok) ok = accumulator_tail(tempty_bar, acc, aph, &s_abort);
-      if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
-      if (issued) {
-        mma_commit_pair(&drain_bar, 0x1);
-        const long long t0 = clock64();
-        while (!mbar_try_wait(&drain_bar, 0) && clock64() - t0 < kSpinLimitCycles) {
-        }
-      }
-    }
-  } else {
-    // ======================================================== epilogue
-    const int q = warp & 3;
-    const int lrow = q * 32 + lane;
-    int acc = 0;
-    uint32_t aph = 0;
-    for (int u = pair; u < U; u += npairs) {
-      Unit un = unit_of(u, s_off, s_up, p.E, j.nt, p.chunk);
-      if (!mbar_wait(&tfull_bar[acc], aph, &s_abort)) {
-        flag_status(p.status, MOE_ERR_TIMEOUT);
-        break;
-      }
-      tc_fence_after();
-      // this CTA's 128 token rows of the pair's 256
-      un.row0 += (int)rank * kTileRows;
-      un.rows = max(0, min(kTileRows, un.rows - (int)rank * kTileRows));
-      const uint32_t tbase = tmem + acc * kAccCols + ((uint32_t)(q * 32) << 16);
-      if (un.rows > 0) {
-        float* wsc = s_wsc + (FP8 ? (warp - 2) * kTileScales : 0);
-        if (FP8) load_tile_scales<MODE>(un, j, p.I, lane, wsc);
-        epilogue_tile<MODE, FP8>(un, j, p.I, tbase, tile_row<MODE, FP8>(un, j, lrow), lane,
-                                 s_stg + (warp - 2) * kStageWords, wsc);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
-      if (++acc == 2) { acc = 0; aph ^= 1; }
-    }
-  }
-
-  // ---- teardown: both CTAs are done with each other's shared memory
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc_pair(tmem, 2 * kAccCols);
-}
-
 // ------------------------------------------------------------------ host --
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -1426,71 +1206,6 @@ bool set_ring(Params* p, bool decode, int T, size_t* smem, bool wide = false) {
   return true;
 }
 
-template <int MODE, bool FP8>
-cudaError_t launch_pair(const CUtensorMap& tw, const CUtensorMap& tx, const Params& p, int grid,
-                        size_t smem, cudaStream_t st) {
-  auto k = moe_tc_pair_kernel<MODE, FP8>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, k, tw, tx, p);
-  if (e == cudaSuccess) e = cudaGetLastError();
-  if (e == cudaSuccess) count_launch();
-  return e;
-}
-
-// Prefill on CTA pairs.  Not launched: prefill runs with this kernel stalled
-// intermittently on GB300 and the cause has not been found, so it stays off
-// the GPU (cudaErrorNotSupported) and the single-CTA tiles run instead.
-constexpr bool kPrefillPairEnabled = false;
-
-cudaError_t launch_prefill_pair(int mode, bool fp8, const Params& base, const JobP& job,
-                                const CUtensorMap& tw, const CUtensorMap& tx, int sms,
-                                cudaStream_t st) {
-  if (!kPrefillPairEnabled) return cudaErrorNotSupported;
-  Params p = base;
-  p.job[0] = job;
-  p.njobs = 1;
-  p.chunk = 2 * kTileRows;  // token rows per pair unit
-  p.kw = 1;
-  p.a_atom = kTileBytes;
-  p.b_atom = kTileBytes;    // this CTA's half of the 256 weight rows
-  p.a_bytes = p.a_atom;
-  p.stage_bytes = p.a_atom + p.b_atom;
-  const int static_smem = 8 * 1024 + 4 * (kStageWords * 16 + kTileScales * 4);
-  int stages = (kSmemLimit - static_smem - 1024) / p.stage_bytes;
-  if (stages > kMaxStages) stages = kMaxStages;
-  p.stages = stages;
-  p.job[0].kst = (job.kst + kRowBytes - 1) / kRowBytes;  // job.kst holds K bytes here
-  p.job[1] = p.job[0];
-  const size_t smem = (size_t)stages * p.stage_bytes + 1024;
-  const int64_t chunks = (int64_t)(p.R_max + p.chunk - 1) / p.chunk + p.E;
-  const int64_t units = chunks * job.nt;
-  int npairs = (int)(units < sms / 2 ? units : sms / 2);
-  if (npairs < 1) npairs = 1;
-  if (mode == 0) return fp8 ? launch_pair<0, true>(tw, tx, p, 2 * npairs, smem, st)
-                            : launch_pair<0, false>(tw, tx, p, 2 * npairs, smem, st);
-  if (mode == 1) return fp8 ? launch_pair<1, true>(tw, tx, p, 2 * npairs, smem, st)
-                            : launch_pair<1, false>(tw, tx, p, 2 * npairs, smem, st);
-  if (mode == 2) return fp8 ? launch_pair<2, true>(tw, tx, p, 2 * npairs, smem, st)
-                            : launch_pair<2, false>(tw, tx, p, 2 * npairs, smem, st);
-  return fp8 ? launch_pair<3, true>(tw, tx, p, 2 * npairs, smem, st)
-             : launch_pair<3, false>(tw, tx, p, 2 * npairs, smem, st);
-}
-
 // Self-test of the bounded waits: one thread waits on an mbarrier that no
 // thread arrives on, for at most `limit` cycles, and records the timeout.
 __global__ void wait_selftest_kernel(long long limit, int* status) {
@@ -1539,10 +1254,6 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
     return cudaErrorNotSupported;
   maps[2] = maps[0];
   maps[3] = maps[1];
-  if (!decode) {
-    cudaError_t e = launch_prefill_pair(mode, fp8, p, p.job[0], maps[0], maps[1], sms, st);
-    if (e != cudaErrorNotSupported) return e;
-  }
   // Token tiles of 256 rows when the batch gives every SM at least two of
   // them (256-row units in the plain rows-per-expert estimate); else 128.
   bool wide = false;

@@ -59,11 +59,10 @@ MOE_DEV void fence_proxy_async_global() {
 }
 
 // ------------------------------------------------------ pipeline tails --
-// tcgen05.commit arrives on its mbarriers asynchronously, and with a CTA pair
-// the even CTA's commits also arrive on the odd CTA's barriers.  A CTA must
-// not exit while such an arrival is still on its way to its shared memory
-// (the next CTA on the SM reuses it), so before teardown each role waits for
-// the arrivals it has not consumed yet.
+// tcgen05.commit arrives on its mbarriers asynchronously.  A CTA must not exit
+// while such an arrival is still on its way to its shared memory (the next CTA
+// on the SM reuses it), so before teardown each role waits for the arrivals it
+// has not consumed yet.
 
 // Producer tail: waits until the MMAs have released the last use of every
 // ring slot.  (s, ph) is the producer's position after its last slot; a slot

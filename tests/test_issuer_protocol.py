@@ -1,7 +1,6 @@
 """Host-side models of the stage hand-offs in the kernels with several MMA
 issuer threads: the NVFP4 decode kernel (csrc/gemm_nvfp4.cu) and the
-block-wise FP8 prefill tiles (csrc/gemm_fp8b.cu, `run_tiles` below); and of
-the cross-CTA protocol of the CTA-pair prefill tiles (`run_pair`).
+block-wise FP8 prefill tiles (csrc/gemm_fp8b.cu, `run_tiles` below).
 
 K stages n = 0, 1, .. of a CTA flow through two rings: the TMA producer fills
 stage slot n % S (barriers sfull / sempty), the converting warps turn it into
@@ -290,179 +289,3 @@ def test_tile_issuers_beyond_the_slot_count_misread_somewhere(ring_s, ring_q, ni
         except Violation:
             failures += 1
     assert failures > 0
-
-
-class TxBarrier(Barrier):
-    """An mbarrier with a transaction count: a phase completes when its
-    arrivals are in and its expected bytes have landed.  Bytes may land
-    before they are expected (the count goes negative)."""
-
-    def __init__(self, count):
-        super().__init__(count)
-        self.tx = 0
-
-    def _check(self):
-        if self.pending == 0 and self.tx == 0:
-            self.phase += 1
-            self.pending = self.count
-
-    def arrive(self):
-        self.pending -= 1
-        self._check()
-
-    def arrive_expect_tx(self, nbytes):
-        self.tx += nbytes
-        self.arrive()
-
-    def complete_tx(self, nbytes):
-        self.tx -= nbytes
-        self._check()
-
-
-def run_pair(n_units, kst, ring_s, seed, max_delay=5):
-    """The CTA-pair prefill tiles (csrc/gemm_tc.cu, moe_tc_pair_kernel): both
-    CTAs load half of each stage; only the even CTA's producer expects the
-    pair's bytes on its full barrier, and both CTAs' copies land there; the
-    even CTA's MMA commits arrive on both CTAs' empty and accumulator-full
-    barriers (multicast); both epilogues release the accumulator on the even
-    CTA's barrier.  Ground truth checks every wait that passes."""
-    rng = random.Random(seed)
-    half = 3  # bytes per CTA per stage, in units
-    full = [TxBarrier(1) for _ in range(ring_s)]  # the even CTA's
-    empty = [[Barrier(1) for _ in range(ring_s)] for _ in range(2)]
-    tfull = [[Barrier(1) for _ in range(2)] for _ in range(2)]
-    tempty = [Barrier(2) for _ in range(2)]  # both CTAs' epilogues
-    slot = [[None] * ring_s for _ in range(2)]
-    landed = set()  # (cta, stage) copies that have landed
-    consumed, unit_done = set(), set()
-    n_stages = n_units * kst
-    prod = [0, 0]
-    mma = {"n": 0, "u": 0, "started": False}
-    epi = [0, 0]
-    copies = []  # [delay, cta, stage]
-    mma_q = []   # in-order completions: [delay, kind, value]
-
-    def producer(c):
-        n = prod[c]
-        if n >= n_stages:
-            return False
-        s = n % ring_s
-        if not empty[c][s].try_wait_parity(((n // ring_s) & 1) ^ 1):
-            return False
-        old = slot[c][s]
-        if old is not None and old not in consumed:
-            raise Violation(f"CTA {c} producer overwrote stage {old} with {n}")
-        if c == 0:
-            full[s].arrive_expect_tx(2 * half)
-        slot[c][s] = n
-        copies.append([rng.randint(0, max_delay), c, n])
-        prod[c] += 1
-        return True
-
-    def land():
-        ready = [m for m in copies if m[0] <= 0]
-        for m in copies:
-            m[0] -= 1
-        if not ready:
-            return bool(copies)
-        m = rng.choice(ready)
-        copies.remove(m)
-        _, c, n = m
-        landed.add((c, n))
-        full[n % ring_s].complete_tx(half)
-        return True
-
-    def mma_issue():
-        u, n = mma["u"], mma["n"]
-        if u >= n_units:
-            return False
-        acc = u & 1
-        if not mma["started"]:
-            if not tempty[acc].try_wait_parity(((u // 2) & 1) ^ 1):
-                return False
-            if any(x >= u - 2 and x not in unit_done for x in range(max(0, u - 2), u - 1)):
-                raise Violation(f"MMA reused accumulator {acc} for unit {u} before it drained")
-            mma["started"] = True
-        s = n % ring_s
-        if not full[s].try_wait_parity((n // ring_s) & 1):
-            return False
-        for c in (0, 1):
-            if slot[c][s] != n or (c, n) not in landed:
-                raise Violation(f"MMA read CTA {c}'s stage slot {s} for {n} too early")
-        mma_q.append([rng.randint(0, max_delay), "stage", n])
-        mma["n"] += 1
-        if mma["n"] % kst == 0:
-            mma_q.append([0, "unit", u])
-            mma["u"] += 1
-            mma["started"] = False
-        return True
-
-    def mma_complete():
-        if not mma_q:
-            return False
-        head = mma_q[0]
-        if head[0] > 0:
-            head[0] -= 1
-            return True
-        mma_q.pop(0)
-        _, kind, v = head
-        if kind == "stage":
-            consumed.add(v)
-            for c in (0, 1):
-                empty[c][v % ring_s].arrive()
-        else:
-            for c in (0, 1):
-                tfull[c][v & 1].arrive()
-        return True
-
-    def epilogue(c):
-        u = epi[c]
-        if u >= n_units:
-            return False
-        acc = u & 1
-        if not tfull[c][acc].try_wait_parity((u // 2) & 1):
-            return False
-        if any(k not in consumed for k in range(u * kst, (u + 1) * kst)):
-            raise Violation(f"CTA {c} epilogue read unit {u} before its MMAs completed")
-        if c == 1:
-            unit_done.add(u)
-        tempty[acc].arrive()
-        epi[c] += 1
-        return True
-
-    roles = [lambda: producer(0), lambda: producer(1), land, mma_issue, mma_complete,
-             lambda: epilogue(0), lambda: epilogue(1)]
-    while min(epi) < n_units:
-        order = roles[:]
-        rng.shuffle(order)
-        if not any(r() for r in order):
-            raise Violation(f"deadlock at epilogue units {epi} of {n_units}")
-    return True
-
-
-@pytest.mark.parametrize("kst,ring_s", [(4, 6), (1, 6), (7, 6), (3, 2), (12, 6)])
-def test_cta_pair_protocol_never_misreads_or_deadlocks(kst, ring_s):
-    # the pair kernel's barrier protocol is sound under any interleaving, early
-    # peer bytes included; its intermittent stall must lie elsewhere
-    for seed in range(200):
-        run_pair(6, kst, ring_s, seed)
-
-
-def test_pair_model_catches_a_missing_peer_byte_count():
-    # planted in the model: the even CTA expects only its own half of the
-    # bytes, so a phase can complete before the peer's copy lands
-    orig = TxBarrier.arrive_expect_tx
-
-    def short(self, nbytes):
-        orig(self, nbytes // 2)
-    TxBarrier.arrive_expect_tx = short
-    try:
-        failures = 0
-        for seed in range(200):
-            try:
-                run_pair(6, 4, 6, seed)
-            except Violation:
-                failures += 1
-        assert failures > 0
-    finally:
-        TxBarrier.arrive_expect_tx = orig
