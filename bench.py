@@ -247,6 +247,9 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (0 = auto)")
+    ap.add_argument("--shape", default=None,
+                    help="T,H,E,k,I: the workload's recipe at another shape (smaller cases for "
+                         "profiling); the JSON line names it in config")
     ap.add_argument("--no-more", action="store_true",
                     help="measure only --workload (no prefill entries under \"more\")")
     return ap.parse_args()
@@ -323,7 +326,13 @@ def run_workload(args, workload, dev, rank, world, local, steps, warmup, cpu_ok)
     import moe_expert_ffn_rms_gb300 as M
     import workloads
 
-    inp = workloads.make_inputs(workload, dev)
+    shape_over = None
+    if args.shape and workload == args.workload:
+        T_, H_, E_, k_, I_ = (int(v) for v in args.shape.split(","))
+        shape_over = workloads.Shape(T=T_, H=H_, E=E_, k=k_, I=I_)
+    inp = workloads.make_inputs(workload, dev, shape=shape_over)
+    # committed DRAM traffic records are per full-size workload
+    traffic_key = workload if shape_over is None else None
     T, H, E, k, I, fp8 = inp["T"], inp["H"], inp["E"], inp["k"], inp["I"], inp["fp8"]
     nvfp4 = bool(inp.get("nvfp4"))
     fb = fp8 == "block"
@@ -525,7 +534,7 @@ def run_workload(args, workload, dev, rank, world, local, steps, warmup, cpu_ok)
         ffn_bytes = work["fc1_bytes"] + work["fc2_bytes"]
         achieved = ffn_bytes / (stage_ms["ffn"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": read_traffic("ffn", workload),
+                "frac": achieved / peaks["hbm_gbs"], "traffic": read_traffic("ffn", traffic_key),
                 "kernel": "fused decode FFN (FC1 + silu_and_mul + FC2 + routing weight, one launch)",
                 "peak_source": peaks["source"],
                 "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
@@ -533,7 +542,7 @@ def run_workload(args, workload, dev, rank, world, local, steps, warmup, cpu_ok)
     elif decode:
         achieved = work["fc1_bytes"] / (stage_ms["fc1"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": read_traffic("fc1", workload),
+                "frac": achieved / peaks["hbm_gbs"], "traffic": read_traffic("fc1", traffic_key),
                 "kernel": "grouped GEMM FC1 + silu_and_mul",
                 "peak_source": peaks["source"],
                 "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
@@ -547,7 +556,7 @@ def run_workload(args, workload, dev, rank, world, local, steps, warmup, cpu_ok)
         flops = work["fc1_flops"] + work["fc2_flops"]
         achieved = flops / (stage_ms["ffn"] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
-                "frac": achieved / tpeak, "traffic": read_traffic("ffn", workload),
+                "frac": achieved / tpeak, "traffic": read_traffic("ffn", traffic_key),
                 "kernel": "block-wise FP8 FFN: FC1 tiles + silu_and_mul, 1x128 group quantiser, "
                           "FC2 tiles + routing weight (three launches timed together)",
                 "peak_source": tsrc, "frac_of_sustained": achieved / tpeak_sus,
@@ -558,7 +567,7 @@ def run_workload(args, workload, dev, rank, world, local, steps, warmup, cpu_ok)
         achieved = work["fc1_flops"] / (stage_ms["fc1"] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak,
                 "unit": "TFLOP/s", "frac": achieved / tpeak,
-                "traffic": read_traffic("fc1", workload),
+                "traffic": read_traffic("fc1", traffic_key),
                 "kernel": "grouped GEMM FC1 + silu_and_mul", "peak_source": tsrc,
                 "frac_of_sustained": achieved / tpeak_sus,
                 "fc2_TFLOPs": work["fc2_flops"] / (stage_ms["fc2"] * 1e-3) / 1e12,
@@ -651,7 +660,8 @@ def run_workload(args, workload, dev, rank, world, local, steps, warmup, cpu_ok)
                       "fp8-e4m3 x fp8-e4m3 -> f32 per 128-wide K group, scaled and summed in f32"
                       if fb else "fp8-e4m3 x fp8-e4m3 -> f32" if fp8 else "bf16 x bf16 -> f32"),
             "data": "synthetic (seeded torch generator; random-init weights)",
-            "config": {"workload": workload, "T": T, "H": H, "E": E, "top_k": k, "I": I,
+            "config": {"workload": workload + ("" if shape_over is None else " (reduced shape)"),
+                       "T": T, "H": H, "E": E, "top_k": k, "I": I,
                        "fp8": fp8,
                        "weights": ("nvfp4" if nvfp4 else "e4m3, 128x128 tile scales" if fb else
                                    ("e4m3" if fp8 else "bf16")),
@@ -703,7 +713,8 @@ def main_native(args):
         # fraction of the nominal 8 TB/s sits beside it.
         line["roofline"]["peak_kind"] = "copy bandwidth (read + write bytes), measured"
     more = [w for w in MORE_WORKLOADS if w != args.workload] if (
-        world == 1 and args.workload == DEFAULT_WORKLOAD and not args.no_more) else []
+        world == 1 and args.workload == DEFAULT_WORKLOAD and not args.no_more and
+        not args.shape) else []
     if more and rank == 0:
         line["more"] = {}
         for w in more:
@@ -737,7 +748,7 @@ def read_traffic(kernel, workload):
     the current kernel source; else None."""
     import workloads
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    if not os.path.exists(p) or workload not in workloads.CONFIGS:
+    if not os.path.exists(p) or workload is None or workload not in workloads.CONFIGS:
         return None
     sha = kernel_source_sha(workload)
     with open(p) as f:
