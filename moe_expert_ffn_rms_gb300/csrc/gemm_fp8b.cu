@@ -762,7 +762,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
     }
     for (int q = 0; q < kSlotsT; ++q) {
       mbar_init(&kfull[q], 1);
-      mbar_init(&kempty[q], 8);  // lane 0 of each epilogue warp
+      mbar_init(&kempty[q], 8 * 32);  // every thread of the eight epilogue warps
     }
     mbar_init(&drain_bar[0], 1);
     mbar_init(&drain_bar[1], 1);
@@ -819,86 +819,99 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
 
   if (warp == 0) {
     // ===================================================== TMA producer
-    if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_last();  // re-read by the expert's other token tiles
-      const uint64_t pol_a = l2_policy_evict_first();
-      int s = 0;
-      uint32_t ph = 0, armed = 0, armed_ph = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
-        const Unit un = unit_of(u, s_off, s_up, p.E, p.nt, 128);
-        const int wrow = un.e * p.N_w;
-        // FC1: gate rows nt*64.. and the matching up rows; FC2: 128 rows
-        const int r0 = MODE == 1 ? wrow + un.nt * 64 : wrow + un.nt * 128;
-        const int r1 = MODE == 1 ? wrow + p.I + un.nt * 64 : r0 + 64;
-        for (int g = 0; g < p.kg; ++g) {
-          // suspending waits here and in the MMA threads: each shares an SM
-          // sub-partition with epilogue warps, whose fold is the busy part
-          if (!mbar_wait(&sempty[s], ph ^ 1, &s_abort)) { ok = false; break; }
+    // The whole warp runs the loop and waits; one elected lane arms the
+    // stage and issues its loads.
+    const uint64_t pol_w = l2_policy_evict_last();  // re-read by the expert's other token tiles
+    const uint64_t pol_a = l2_policy_evict_first();
+    int s = 0;
+    uint32_t ph = 0, armed = 0, armed_ph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
+      const Unit un = unit_of(u, s_off, s_up, p.E, p.nt, 128);
+      const int wrow = un.e * p.N_w;
+      // FC1: gate rows nt*64.. and the matching up rows; FC2: 128 rows
+      const int r0 = MODE == 1 ? wrow + un.nt * 64 : wrow + un.nt * 128;
+      const int r1 = MODE == 1 ? wrow + p.I + un.nt * 64 : r0 + 64;
+      for (int g = 0; g < p.kg; ++g) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sempty[s], ph ^ 1, &s_abort))) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
           mbar_arrive_expect_tx(&sfull[s], (uint32_t)kStageBytesT);
           uint8_t* st = ring + (size_t)s * kStageBytesT;
           tma_load_2d(st, &tm_a, &sfull[s], g * kGroup, un.row0, pol_a);
           tma_load_2d(st + kTileBytesT, &tm_w, &sfull[s], g * kGroup, r0, pol_w);
           tma_load_2d(st + kTileBytesT + kTileBytesT / 2, &tm_w, &sfull[s], g * kGroup, r1, pol_w);
-          armed |= 1u << s;
-          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
-          if (++s == p.stages) { s = 0; ph ^= 1; }
         }
+        __syncwarp();
+        armed |= 1u << s;
+        armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+        if (++s == p.stages) { s = 0; ph ^= 1; }
       }
-      if (ok) ok = producer_tail(sempty, p.stages, s, ph, &s_abort);
-      if (!ok) {
-        flag_status(p.status, MOE_ERR_TIMEOUT);
-        drain_armed(sfull, p.stages, armed, armed_ph);
-      }
+    }
+    if (ok) ok = __all_sync(0xffffffffu, producer_tail(sempty, p.stages, s, ph, &s_abort));
+    if (!ok && lane == 0) {
+      flag_status(p.status, MOE_ERR_TIMEOUT);
+      drain_armed(sfull, p.stages, armed, armed_ph);
     }
   } else if (warp == 1 || warp == kMma2WarpT) {
     // ===================================================== MMA issuers
-    // Two threads issue the MMAs: warp 1 the even K groups (counted over all
+    // Two warps issue the MMAs: warp 1 the even K groups (counted over all
     // units), warp 10 the odd ones, so one thread's per-instruction issue
     // cost no longer paces the tensor pipe.  Each group has its own stage and
     // TMEM slot, and both rings have even lengths, so every stage and every
-    // slot belongs to one issuer and is used in order.
-    if (lane == 0) {
-      const int par = warp == 1 ? 0 : 1;
-      int s = 0, q = 0, gi = 0;
-      uint32_t ph = 0, qph = 0;
-      bool ok = true, issued = false;
-      const uint32_t idesc = make_idesc(128, 0u);  // M = N = 128, E4M3 A and B
-      for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
-        for (int g = 0; g < p.kg; ++g, ++gi) {
-          if ((gi & 1) == par) {
-            if (!mbar_wait(&sfull[s], ph, &s_abort) || !mbar_wait(&kempty[q], qph ^ 1, &s_abort)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a0 = smem_u32(ring + (size_t)s * kStageBytesT);
-            const uint32_t d = tmem + q * 128;
+    // slot belongs to one issuer and is used in order.  The whole warp runs
+    // the loop and waits, and one elected lane issues, so the descriptors and
+    // TMEM addresses stay warp-uniform (a loop run by one divergent lane paid
+    // about 100 cycles per tcgen05 instruction).
+    const int par = warp == 1 ? 0 : 1;
+    int s = 0, q = 0, gi = 0;
+    uint32_t ph = 0, qph = 0;
+    bool ok = true, issued = false;
+    const uint32_t idesc = make_idesc(128, 0u);  // M = N = 128, E4M3 A and B
+    for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
+      for (int g = 0; g < p.kg; ++g, ++gi) {
+        if ((gi & 1) == par) {
+          const bool w = mbar_wait(&sfull[s], ph, &s_abort) && mbar_wait(&kempty[q], qph ^ 1, &s_abort);
+          if (!__all_sync(0xffffffffu, w)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(ring + (size_t)s * kStageBytesT);
+          const uint32_t d = tmem + q * 128;
+          if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)  // each group starts a fresh sum
               mma_e4m3(d, sw128_desc(a0 + kk * 32), sw128_desc(a0 + kTileBytesT + kk * 32), idesc,
                        kk ? 1u : 0u);
-            issued = true;
             mma_commit(&sempty[s]);
             mma_commit(&kfull[q]);
           }
-          if (++s == p.stages) { s = 0; ph ^= 1; }
-          if (++q == kSlotsT) { q = 0; qph ^= 1; }
+          __syncwarp();
+          issued = true;
         }
-      }
-      // tail: this issuer's slots handed back (the next four ring positions
-      // are the last use of each slot)
-      for (int i = 0; ok && i < kSlotsT; ++i, ++gi) {
-        if ((gi & 1) == par) ok = mbar_wait(&kempty[q], qph ^ 1, &s_abort);
+        if (++s == p.stages) { s = 0; ph ^= 1; }
         if (++q == kSlotsT) { q = 0; qph ^= 1; }
       }
-      if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
-      if (issued) {
-        mma_commit(&drain_bar[par]);
+    }
+    // tail: this issuer's slots handed back (the next four ring positions
+    // are the last use of each slot)
+    for (int i = 0; ok && i < kSlotsT; ++i, ++gi) {
+      if ((gi & 1) == par) ok = __all_sync(0xffffffffu, mbar_wait(&kempty[q], qph ^ 1, &s_abort));
+      if (++q == kSlotsT) { q = 0; qph ^= 1; }
+    }
+    if (!ok && lane == 0) flag_status(p.status, MOE_ERR_TIMEOUT);
+    if (issued) {
+      if (elect_one()) mma_commit(&drain_bar[par]);
+      __syncwarp();
+      if (lane == 0) {
         const long long t0 = clock64();
         while (!mbar_try_wait(&drain_bar[par], 0) && clock64() - t0 < kSpinLimitCycles) {
         }
       }
+      __syncwarp();
     }
   } else {
     // ======================================================== epilogue
@@ -954,10 +967,12 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
           wh_n = nxt.sw_hi[0];
         }
         if (MODE == 3 && g == (p.kg >> 1) && cur.rvalid) tw = p.topk_w[orow];
-        int wok = 1;
-        if (lane == 0) wok = mbar_wait(&kfull[q], qph, &s_abort);
-        wok = __shfl_sync(0xffffffffu, wok, 0);
-        if (!wok) { ok = false; break; }
+        // every lane waits and every lane hands the slot back: no divergent
+        // branch in the loop
+        if (!__all_sync(0xffffffffu, mbar_wait(&kfull[q], qph, &s_abort))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         float v[64];
         const uint32_t ta = tmem + tlane + q * 128;
@@ -967,8 +982,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
         tmem_ld16(ta + c_hi + 16, v + 48);
         tmem_ld_wait();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&kempty[q]);
+        mbar_arrive(&kempty[q]);
         if (++q == kSlotsT) { q = 0; qph ^= 1; }
         const float fl = sa * wl, fh = sa * wh;
 #pragma unroll

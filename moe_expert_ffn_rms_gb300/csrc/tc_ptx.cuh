@@ -120,6 +120,17 @@ MOE_DEV void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar, int x,
       : "memory");
 }
 
+// True in exactly one lane of the (converged) warp.  A role loop run by the
+// whole warp, with its single-thread instructions under this predicate, keeps
+// the operands of those instructions warp-uniform.
+MOE_DEV bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(e));
+  return e != 0;
+}
+
 // -------------------------------------------------------------- tcgen05 --
 MOE_DEV void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
