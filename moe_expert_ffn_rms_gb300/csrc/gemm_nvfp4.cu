@@ -275,10 +275,10 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&sfull[s], 1);
-      mbar_init(&sempty[s], 1 + kDqWarps);  // the MMA commit (B read) + the dequantising warps
+      mbar_init(&sempty[s], 1 + kDqWarps * 32);  // the MMA commit (B read) + every dequantiser
     }
     for (int q = 0; q < kASlots; ++q) {
-      mbar_init(&afull[q], kDqWarps);
+      mbar_init(&afull[q], kDqWarps * 32);
       mbar_init(&aempty[q], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -364,29 +364,37 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
 
   if (warp == 0) {
     // ===================================================== TMA producer
-    if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
-      const uint64_t pol_x = l2_policy_evict_last();
-      int s = 0;
-      uint32_t ph = 0;
-      uint32_t armed = 0, armed_ph = 0;
-      bool ok = true;
-      for (int i = 0; ok; ++i) {
-        const int slot = i % kRingNv;
-        if (!mbar_wait(&uempty[slot], (uint32_t)(((i / kRingNv) & 1) ^ 1), &s_abort)) {
-          ok = false;
-          break;
-        }
-        int u = atomicAdd(p.sched, 1);
+    // The whole warp runs the loop and waits; lane 0 claims the units, waits
+    // for FC1's rows and issues the loads.
+    const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
+    const uint64_t pol_x = l2_policy_evict_last();
+    int s = 0;
+    uint32_t ph = 0;
+    uint32_t armed = 0, armed_ph = 0;
+    bool ok = true;
+    for (int i = 0; ok; ++i) {
+      const int slot = i % kRingNv;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&uempty[slot], (uint32_t)(((i / kRingNv) & 1) ^ 1), &s_abort))) {
+        ok = false;
+        break;
+      }
+      int u = 0;
+      if (lane == 0) {
+        u = atomicAdd(p.sched, 1);
         if (u >= U) u = -1;
         s_uring[slot] = u;
         mbar_arrive(&ufull[slot]);
-        if (u < 0) break;
-        const Unit un = decode_unit(u);
-        const NvJob& j = p.job[un.job];
-        if (un.job == 1) {
-          // FC2 of expert e reads its FC1 rows: wait until every FC1 epilogue
-          // warp of e has published them (FC1 units are all claimed first)
+      }
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u < 0) break;
+      const Unit un = decode_unit(u);
+      const NvJob& j = p.job[un.job];
+      if (un.job == 1) {
+        // FC2 of expert e reads its FC1 rows: wait until every FC1 epilogue
+        // warp of e has published them (FC1 units are all claimed first)
+        int fok = 1;
+        if (lane == 0) {
           const int cnt = s_off[un.e + 1] - s_off[un.e];
           const int need = ((cnt + p.chunk - 1) / p.chunk) * p.job[0].nt * 4;
           const int* flag = p.sched + 1 + un.e;
@@ -394,24 +402,32 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
           while (ld_acquire(flag) < need) {
             if (s_abort || clock64() - t0 > kSpinLimitCycles) {
               s_abort = 1;
-              ok = false;
+              fok = 0;
               break;
             }
           }
-          if (!ok) break;
-          fence_proxy_async_global();
+          if (fok) fence_proxy_async_global();
         }
-        // all chunk token rows are loaded (rows of other experts or past the
-        // end are ignored by the epilogue; the box is zero-filled past R_max)
-        const uint32_t tx = (uint32_t)(kFp4Bytes + kSbBytes + p.b_bytes);
-        const CUtensorMap* tq = un.job ? &tm_q1 : &tm_q0;
-        const CUtensorMap* ts = un.job ? &tm_s1 : &tm_s0;
-        const CUtensorMap* tb = un.job ? &tm_b1 : &tm_b0;
-        // FC1: 64 gate rows and the matching 64 up rows (the map's third
-        // dimension steps I rows); FC2: 128 consecutive rows (steps of 64)
-        const int r0 = un.e * j.N_w + (un.job == 0 ? un.nt * 64 : un.nt * 128);
-        for (int ks = 0; ks < j.kst; ++ks) {
-          if (!mbar_wait_spin(&sempty[s], ph ^ 1, &s_abort)) { ok = false; break; }
+        if (!__shfl_sync(0xffffffffu, fok, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      // all chunk token rows are loaded (rows of other experts or past the
+      // end are ignored by the epilogue; the box is zero-filled past R_max)
+      const uint32_t tx = (uint32_t)(kFp4Bytes + kSbBytes + p.b_bytes);
+      const CUtensorMap* tq = un.job ? &tm_q1 : &tm_q0;
+      const CUtensorMap* ts = un.job ? &tm_s1 : &tm_s0;
+      const CUtensorMap* tb = un.job ? &tm_b1 : &tm_b0;
+      // FC1: 64 gate rows and the matching 64 up rows (the map's third
+      // dimension steps I rows); FC2: 128 consecutive rows (steps of 64)
+      const int r0 = un.e * j.N_w + (un.job == 0 ? un.nt * 64 : un.nt * 128);
+      for (int ks = 0; ks < j.kst; ++ks) {
+        if (!__all_sync(0xffffffffu, mbar_wait_spin(&sempty[s], ph ^ 1, &s_abort))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
           mbar_arrive_expect_tx(&sfull[s], tx);
           uint8_t* st = ring + (size_t)s * p.stage_bytes;
           uint8_t* codes = st + p.b_bytes;
@@ -419,16 +435,17 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
           tma_load_3d(codes, tq, &sfull[s], ks * (kKStage / 2), r0, 0, pol_w);
           tma_load_3d(scales, ts, &sfull[s], ks * (kKStage / 16), r0, 0, pol_w);
           tma_load_3d(st, tb, &sfull[s], 0, un.row0, ks * 4, pol_x);
-          armed |= 1u << s;
-          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
-          if (++s == p.stages) { s = 0; ph ^= 1; }
         }
+        __syncwarp();
+        armed |= 1u << s;
+        armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+        if (++s == p.stages) { s = 0; ph ^= 1; }
       }
-      if (ok) ok = producer_tail(sempty, p.stages, s, ph, &s_abort);
-      if (!ok) {
-        flag_status(p.status, MOE_ERR_TIMEOUT);
-        drain_armed(sfull, p.stages, armed, armed_ph);
-      }
+    }
+    if (ok) ok = __all_sync(0xffffffffu, producer_tail(sempty, p.stages, s, ph, &s_abort));
+    if (!ok && lane == 0) {
+      flag_status(p.status, MOE_ERR_TIMEOUT);
+      drain_armed(sfull, p.stages, armed, armed_ph);
     }
   } else if (mma_par >= 0) {
     // ===================================================== MMA issuers
@@ -439,63 +456,74 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
     // n - ni (in order) are done, and ni <= min(stages, kASlots) means no
     // barrier it waits on can be a whole phase behind; none can be a phase
     // ahead, since that needs this issuer's own stage n released.  Issuers
-    // past ni only follow the units.
-    if (lane == 0) {
+    // past ni only follow the units.  The whole warp runs the loop and
+    // waits; one elected lane issues.
+    {
       const int par = mma_par;
       int s = 0, q = 0, acc = 0;
       uint32_t ph = 0, qph = 0, aph = 0, n = 0;
       bool ok = true;
       bool issued = false;
       for (int i = 0; ok; ++i) {
-        const int u = next_unit(i);
+        const int u = __shfl_sync(0xffffffffu, next_unit(i), 0);  // every lane has read it
         if (u == -2) { ok = false; break; }
-        mbar_arrive(&uempty[i % kRingNv]);
+        if (lane == 0) mbar_arrive(&uempty[i % kRingNv]);
         if (u < 0) break;
         const Unit un = decode_unit(u);
         const int kst = p.job[un.job].kst;
-        if (!mbar_wait(&tempty[acc], aph ^ 1, &s_abort)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], aph ^ 1, &s_abort))) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + acc * kAccColsNv + par * p.chunk;
         const uint32_t idesc = make_idesc(((un.rows + 15) / 16) * 16, 0u);  // fp16 A and B
         bool first = true;  // this issuer's first stage of the unit starts its sum
         for (int ks = 0; ks < kst && ok; ++ks, ++n) {
           if ((int)(n % (uint32_t)ni) == par) {
-            if (!mbar_wait_spin(&sfull[s], ph, &s_abort) ||
-                !mbar_wait_spin(&afull[q], qph, &s_abort)) {
+            if (!__all_sync(0xffffffffu, mbar_wait_spin(&sfull[s], ph, &s_abort) &&
+                                             mbar_wait_spin(&afull[q], qph, &s_abort))) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t b0 = smem_u32(ring + (size_t)s * p.stage_bytes);
             const uint32_t a0 = tmem + kACol0 + q * kAColsPerStage;
-            for (int a = 0; a < 4; ++a) {
-              const uint32_t bb = b0 + a * p.chunk * 128;
+            if (elect_one()) {
+              for (int a = 0; a < 4; ++a) {
+                const uint32_t bb = b0 + a * p.chunk * 128;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {  // four 16-element K steps (8 columns) per atom
-                const uint32_t accum = (!first || a || kk) ? 1u : 0u;
-                mma_f16_ts(d, a0 + a * kAColsPerAtom + kk * 8, sw128_desc(bb + kk * 32), idesc,
-                           accum);
+                for (int kk = 0; kk < 4; ++kk) {  // four 16-element K steps (8 columns) per atom
+                  const uint32_t accum = (!first || a || kk) ? 1u : 0u;
+                  mma_f16_ts(d, a0 + a * kAColsPerAtom + kk * 8, sw128_desc(bb + kk * 32), idesc,
+                             accum);
+                }
               }
+              mma_commit(&aempty[q]);
+              mma_commit(&sempty[s]);
             }
+            __syncwarp();
             first = false;
             issued = true;
-            mma_commit(&aempty[q]);
-            mma_commit(&sempty[s]);
           }
           if (++q == kASlots) { q = 0; qph ^= 1; }
           if (++s == p.stages) { s = 0; ph ^= 1; }
         }
         if (!ok) break;
-        if (par < ni) mma_commit(&tfull[acc]);
+        if (par < ni) {
+          if (elect_one()) mma_commit(&tfull[acc]);
+          __syncwarp();
+        }
         if (++acc == 2) { acc = 0; aph ^= 1; }
       }
-      if (ok) ok = accumulator_tail(tempty, acc, aph, &s_abort);
-      if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
+      if (ok) ok = __all_sync(0xffffffffu, accumulator_tail(tempty, acc, aph, &s_abort));
+      if (!ok && lane == 0) flag_status(p.status, MOE_ERR_TIMEOUT);
       if (issued) {
-        mma_commit(&drain_bar[par]);
-        const long long t0 = clock64();
-        while (!mbar_try_wait(&drain_bar[par], 0) && clock64() - t0 < kSpinLimitCycles) {
+        if (elect_one()) mma_commit(&drain_bar[par]);
+        __syncwarp();
+        if (lane == 0) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(&drain_bar[par], 0) && clock64() - t0 < kSpinLimitCycles) {
+          }
         }
+        __syncwarp();
       }
     }
   } else if (warp < 6) {
@@ -621,15 +649,15 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
       const Unit un = decode_unit(u);
       const int kst = p.job[un.job].kst;
       for (int ks = 0; ks < kst; ++ks, ++n) {
-        // lane 0 waits for the staged codes and a free A slot; __syncwarp
-        // hands what it observed to the other lanes
+        // every lane waits for the staged codes and a free A slot, and every
+        // lane arrives below: the stage loop has no divergent branch
         const int slot = (int)(n % kASlots);
-        int wok = 1;
-        if (lane == 0)
-          wok = mbar_wait_spin(&sfull[s], ph, &s_abort) &&
-                mbar_wait_spin(&aempty[slot], ((n / kASlots) & 1) ^ 1, &s_abort);
-        wok = __shfl_sync(0xffffffffu, wok, 0);
-        if (!wok) { ok = false; break; }
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_spin(&sfull[s], ph, &s_abort) &&
+                            mbar_wait_spin(&aempty[slot], ((n / kASlots) & 1) ^ 1, &s_abort))) {
+          ok = false;
+          break;
+        }
         const uint8_t* st = ring + (size_t)s * p.stage_bytes + p.b_bytes;
         const uint8_t* crow = st + r * (kKStage / 2);
         const uint4 scales = *reinterpret_cast<const uint4*>(st + kFp4Bytes + r * (kKStage / 16));
@@ -655,11 +683,8 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         }
         tmem_st_wait();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&afull[slot]);
-          mbar_arrive(&sempty[s]);
-        }
+        mbar_arrive(&afull[slot]);
+        mbar_arrive(&sempty[s]);
         if (++s == p.stages) { s = 0; ph ^= 1; }
       }
     }
