@@ -233,9 +233,15 @@ MOE_DEV void e2m1x8_scaled(uint32_t w, uint32_t s2, uint32_t (&o)[4]) {
       : "r"(w), "r"(s2));
 }
 
-MOE_DEV uint32_t e4m3_to_h2(uint32_t code) {
-  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.x << 16);
+// The four E4M3 block scales of a 32-bit word, each as an fp16 pair (both
+// halves the scale): two paired conversions and four byte permutes.
+MOE_DEV void e4m3x4_to_h2(uint32_t w, uint32_t (&bs)[4]) {
+  asm("{\n .reg .b16 lo, hi;\n .reg .b32 h01, h23;\n mov.b32 {lo, hi}, %4;\n"
+      " cvt.rn.f16x2.e4m3x2 h01, lo;\n cvt.rn.f16x2.e4m3x2 h23, hi;\n"
+      " prmt.b32 %0, h01, 0, 0x1010;\n prmt.b32 %1, h01, 0, 0x3232;\n"
+      " prmt.b32 %2, h23, 0, 0x1010;\n prmt.b32 %3, h23, 0, 0x3232;\n}"
+      : "=r"(bs[0]), "=r"(bs[1]), "=r"(bs[2]), "=r"(bs[3])
+      : "r"(w));
 }
 
 __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
@@ -423,7 +429,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
       // dimension steps I rows); FC2: 128 consecutive rows (steps of 64)
       const int r0 = un.e * j.N_w + (un.job == 0 ? un.nt * 64 : un.nt * 128);
       for (int ks = 0; ks < j.kst; ++ks) {
-        if (!__all_sync(0xffffffffu, mbar_wait_spin(&sempty[s], ph ^ 1, &s_abort))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sempty[s], ph ^ 1, &s_abort))) {
           ok = false;
           break;
         }
@@ -478,8 +484,8 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         bool first = true;  // this issuer's first stage of the unit starts its sum
         for (int ks = 0; ks < kst && ok; ++ks, ++n) {
           if ((int)(n % (uint32_t)ni) == par) {
-            if (!__all_sync(0xffffffffu, mbar_wait_spin(&sfull[s], ph, &s_abort) &&
-                                             mbar_wait_spin(&afull[q], qph, &s_abort))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sfull[s], ph, &s_abort) &&
+                                             mbar_wait_sleep(&afull[q], qph, &s_abort))) {
               ok = false;
               break;
             }
@@ -669,8 +675,7 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
           const uint4 c1 = *reinterpret_cast<const uint4*>(crow + (((2 * a + 1) ^ (r & 7)) << 4));
           const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           uint32_t bs[4];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) bs[b] = e4m3_to_h2((swa >> (8 * b)) & 0xFFu);
+          e4m3x4_to_h2(swa, bs);
           uint32_t v[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {  // word c = elements 8c .. 8c + 7, block c / 2

@@ -65,6 +65,34 @@ MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   return mbar_wait_limit(bar, parity, abort, kSpinLimitCycles);
 }
 
+// mbar_wait whose probes suspend the thread for up to ~1 us each (the
+// try_wait suspend-time hint) instead of returning at once: for warps that
+// share an SM sub-partition with warps whose instruction issue is the
+// bottleneck.
+MOE_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)
+      : "memory");
+  return ok != 0;
+}
+
+MOE_DEV bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kSpinLimitCycles) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // Non-suspending probe of a phase (mbarrier.test_wait).
 MOE_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
