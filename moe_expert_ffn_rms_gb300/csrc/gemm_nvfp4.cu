@@ -637,14 +637,20 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
     // (rows are 128-byte swizzled: 16-byte chunk c of row r sits at chunk
     // c ^ (r % 8)) and one block scale per 16 elements, and stores its 64 fp16
     // values into 32 TMEM columns of atom a of stage slot n % kASlots, n = the
-    // stage count.
+    // stage count.  The loop is bound by instruction issue, so the slot and
+    // its phase are running counters and each thread loads only the 8 bytes
+    // of block scales of its two atoms.
     const int qtr = warp & 3;
     const int half = (warp - 6) >> 2;
     const int r = qtr * 32 + lane;
     const uint32_t tlane = (uint32_t)(qtr * 32) << 16;
-    int s = 0;
-    uint32_t ph = 0;
-    uint32_t n = 0;  // stages done by this CTA
+    const uint32_t c_off0 = (uint32_t)r * (kKStage / 2) + (((4 * half) ^ (r & 7)) << 4);
+    const uint32_t c_off1 = (uint32_t)r * (kKStage / 2) + (((4 * half + 1) ^ (r & 7)) << 4);
+    const uint32_t c_off2 = (uint32_t)r * (kKStage / 2) + (((4 * half + 2) ^ (r & 7)) << 4);
+    const uint32_t c_off3 = (uint32_t)r * (kKStage / 2) + (((4 * half + 3) ^ (r & 7)) << 4);
+    const uint32_t s_off8 = (uint32_t)kFp4Bytes + (uint32_t)r * (kKStage / 16) + 8u * half;
+    int s = 0, slot = 0;
+    uint32_t ph = 0, aph = 0;
     bool ok = true;
     for (int i = 0; ok; ++i) {
       const int u = next_unit(i);
@@ -654,25 +660,22 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
       if (u < 0) break;
       const Unit un = decode_unit(u);
       const int kst = p.job[un.job].kst;
-      for (int ks = 0; ks < kst; ++ks, ++n) {
+      for (int ks = 0; ks < kst; ++ks) {
         // every lane waits for the staged codes and a free A slot, and every
         // lane arrives below: the stage loop has no divergent branch
-        const int slot = (int)(n % kASlots);
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait_spin(&sfull[s], ph, &s_abort) &&
-                            mbar_wait_spin(&aempty[slot], ((n / kASlots) & 1) ^ 1, &s_abort))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_spin(&sfull[s], ph, &s_abort) &&
+                                         mbar_wait_spin(&aempty[slot], aph ^ 1, &s_abort))) {
           ok = false;
           break;
         }
         const uint8_t* st = ring + (size_t)s * p.stage_bytes + p.b_bytes;
-        const uint8_t* crow = st + r * (kKStage / 2);
-        const uint4 scales = *reinterpret_cast<const uint4*>(st + kFp4Bytes + r * (kKStage / 16));
+        const uint2 scales = *reinterpret_cast<const uint2*>(st + s_off8);
 #pragma unroll
         for (int aa = 0; aa < 2; ++aa) {
           const int a = 2 * half + aa;
-          const uint32_t swa = half ? (aa ? scales.w : scales.z) : (aa ? scales.y : scales.x);
-          const uint4 c0 = *reinterpret_cast<const uint4*>(crow + (((2 * a) ^ (r & 7)) << 4));
-          const uint4 c1 = *reinterpret_cast<const uint4*>(crow + (((2 * a + 1) ^ (r & 7)) << 4));
+          const uint32_t swa = aa ? scales.y : scales.x;
+          const uint4 c0 = *reinterpret_cast<const uint4*>(st + (aa ? c_off2 : c_off0));
+          const uint4 c1 = *reinterpret_cast<const uint4*>(st + (aa ? c_off3 : c_off1));
           const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           uint32_t bs[4];
           e4m3x4_to_h2(swa, bs);
@@ -691,11 +694,14 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         mbar_arrive(&afull[slot]);
         mbar_arrive(&sempty[s]);
         if (++s == p.stages) { s = 0; ph ^= 1; }
+        if (++slot == kASlots) { slot = 0; aph ^= 1; }
       }
     }
     // tail: the MMAs have released every A slot before the CTA exits
-    for (uint32_t nn = n; ok && nn < n + kASlots; ++nn)
-      ok = mbar_wait(&aempty[nn % kASlots], ((nn / kASlots) & 1) ^ 1, &s_abort);
+    for (int i = 0; ok && i < kASlots; ++i) {
+      ok = mbar_wait(&aempty[slot], aph ^ 1, &s_abort);
+      if (++slot == kASlots) { slot = 0; aph ^= 1; }
+    }
     if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
   }
 
