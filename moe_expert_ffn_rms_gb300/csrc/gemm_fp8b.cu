@@ -677,14 +677,8 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
 // activation scale (its token row) times one weight-tile scale per 32
 // columns, so the fold is a scalar multiply-add per element.  The warps never
 // synchronise with one another.
-// a0 += v0 * f, a1 += v1 * f in one paired fp32 instruction (each half an
-// IEEE fused multiply-add, round to nearest: the same bits as two fmaf).
-MOE_DEV void fma2(float& a0, float& a1, float v0, float v1, float f) {
-  asm("{\n .reg .b64 a, v, s;\n mov.b64 a, {%0, %1};\n mov.b64 v, {%2, %3};\n"
-      " mov.b64 s, {%4, %4};\n fma.rn.f32x2 a, v, s, a;\n mov.b64 {%0, %1}, a;\n}"
-      : "+f"(a0), "+f"(a1)
-      : "f"(v0), "f"(v1), "f"(f));
-}
+// The fold runs on register pairs (__ffma2_rn: each half an IEEE fused
+// multiply-add, round to nearest, the same bits as two fmaf).
 
 constexpr int kThreadsT = 352;       // warp 0 TMA, 1 MMA (+ TMEM owner), 2-9 epilogue, 10 MMA
 constexpr int kMma2WarpT = 10;
@@ -950,9 +944,9 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
         if (MODE == 3 && nxt.rvalid) orow_n = p.row_src[nxt.r];
       }
       float tw = 0.f;
-      float acc[64];
+      float2 acc[32];  // columns 2c, 2c + 1 of the lo run (c < 16), then of the hi run
 #pragma unroll
-      for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+      for (int c = 0; c < 32; ++c) acc[c] = make_float2(0.f, 0.f);
       for (int g = 0; g < p.kg; ++g) {
         // the scales of the group after this one load while this group's
         // product is awaited
@@ -976,19 +970,17 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
         tc_fence_after();
         float v[64];
         const uint32_t ta = tmem + tlane + q * 128;
-        tmem_ld16(ta + c_lo, v);
-        tmem_ld16(ta + c_lo + 16, v + 16);
-        tmem_ld16(ta + c_hi, v + 32);
-        tmem_ld16(ta + c_hi + 16, v + 48);
+        tmem_ld32(ta + c_lo, v);
+        tmem_ld32(ta + c_hi, v + 32);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&kempty[q]);
         if (++q == kSlotsT) { q = 0; qph ^= 1; }
-        const float fl = sa * wl, fh = sa * wh;
+        const float2 fl = make_float2(sa * wl, sa * wl), fh = make_float2(sa * wh, sa * wh);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          fma2(acc[c], acc[c + 1], v[c], v[c + 1], fl);
-          fma2(acc[32 + c], acc[33 + c], v[32 + c], v[33 + c], fh);
+        for (int c = 0; c < 16; ++c) {
+          acc[c] = __ffma2_rn(make_float2(v[2 * c], v[2 * c + 1]), fl, acc[c]);
+          acc[16 + c] = __ffma2_rn(make_float2(v[32 + 2 * c], v[33 + 2 * c]), fh, acc[16 + c]);
         }
         sa = sa_n;
         wl = wl_n;
@@ -1002,10 +994,10 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
           // with the fast exponential and divide, as in the decode epilogue
           uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float g0 = acc[c], g1 = acc[c + 1];
-            pk[c / 2] = pack2_bf16(__fdividef(g0, 1.0f + __expf(-g0)) * acc[32 + c],
-                                   __fdividef(g1, 1.0f + __expf(-g1)) * acc[33 + c]);
+          for (int c = 0; c < 16; ++c) {
+            const float g0 = acc[c].x, g1 = acc[c].y;
+            pk[c] = pack2_bf16(__fdividef(g0, 1.0f + __expf(-g0)) * acc[16 + c].x,
+                               __fdividef(g1, 1.0f + __expf(-g1)) * acc[16 + c].y);
           }
           uint4* dst = reinterpret_cast<uint4*>(out + (size_t)cur.r * p.ldo + cur.nt * 64 + 32 * h);
 #pragma unroll
@@ -1014,7 +1006,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
           // routing weight x y, bf16, at row row_src[r]: 64 columns from nt*128 + 64h
           uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) pk[c / 2] = pack2_bf16(acc[c] * tw, acc[c + 1] * tw);
+          for (int c = 0; c < 32; ++c) pk[c] = pack2_bf16(acc[c].x * tw, acc[c].y * tw);
           uint4* dst = reinterpret_cast<uint4*>(out + (size_t)orow * p.ldo + cur.nt * 128 + 64 * h);
 #pragma unroll
           for (int i = 0; i < 8; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
