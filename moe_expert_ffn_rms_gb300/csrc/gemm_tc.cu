@@ -301,7 +301,8 @@ MOE_DEV float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // Epilogue of one token-tile unit: lane = token row of the tile, columns =
 // weight rows.  TMEM is read in rounds of 128 columns (64 with E4M3 scales,
-// whose per-column loads need registers too), one wait per round; bf16 rows
+// whose per-column loads need registers too) with 32-column loads, one wait
+// per round; bf16 rows
 // leave through store_rows32 (stg: this warp's staging buffer).
 template <int MODE, bool FP8>
 MOE_DEV void epilogue_tile(const Unit& un, const JobP& j, int I, uint32_t tbase,
@@ -310,9 +311,9 @@ MOE_DEV void epilogue_tile(const Unit& un, const JobP& j, int I, uint32_t tbase,
     for (int c2 = 0; c2 < 128; c2 += 64) {
       float gg[64], uu[64];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        tmem_ld16(tbase + c2 + 16 * q, gg + 16 * q);
-        tmem_ld16(tbase + 128 + c2 + 16 * q, uu + 16 * q);
+      for (int q = 0; q < 2; ++q) {
+        tmem_ld32(tbase + c2 + 32 * q, gg + 32 * q);
+        tmem_ld32(tbase + 128 + c2 + 32 * q, uu + 32 * q);
       }
       tmem_ld_wait();
 #pragma unroll
@@ -355,7 +356,7 @@ MOE_DEV void epilogue_tile(const Unit& un, const JobP& j, int I, uint32_t tbase,
     for (int c4 = 0; c4 < 256; c4 += RC) {
       float vv[RC];
 #pragma unroll
-      for (int q = 0; q < RC / 16; ++q) tmem_ld16(tbase + c4 + 16 * q, vv + 16 * q);
+      for (int q = 0; q < RC / 32; ++q) tmem_ld32(tbase + c4 + 32 * q, vv + 32 * q);
       tmem_ld_wait();
 #pragma unroll
       for (int cc = 0; cc < RC; cc += 32) {
