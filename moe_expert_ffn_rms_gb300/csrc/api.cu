@@ -176,8 +176,24 @@ bool router_on_tensor_cores(int T) {
   return T >= 256;
 }
 
+// K splits of the tensor-core router GEMM.  Its [T, 3E] output gives few
+// token tiles (ceil(T / 128) units at 3E <= 256), each over all of K, so K is
+// split until the units about fill the SMs, keeping at least 8 K stages of 64
+// per split; top-k adds the splits' partial logits.
+constexpr int kMaxRouterSplits = 8;
+
+int router_ksplit(int T, int H, int E, int sms) {
+  const int tiles = ((T + 127) / 128) * ((3 * E + 255) / 256);
+  int s = sms / (tiles > 0 ? tiles : 1);
+  const int kst = (H + 63) / 64;
+  if (s > kst / 8) s = kst / 8;
+  if (s > kMaxRouterSplits) s = kMaxRouterSplits;
+  return s < 1 ? 1 : s;
+}
+
 size_t router_tc_bytes(int T, int H, int E) {
-  return up256((size_t)3 * E * H * 2) + up256(2 * 4) + up256((size_t)T * 3 * E * 4);
+  return up256((size_t)3 * E * H * 2) + up256(2 * 4) +
+         up256((size_t)T * 3 * E * kMaxRouterSplits * 4);
 }
 
 size_t router_ws_bytes(int T, int H, int E) {
@@ -200,14 +216,15 @@ moe_status compute_router_logits(const void* xhat, const float* router_w, int T,
     int32_t* seg = at<int32_t>(ws, up256((size_t)3 * E * H * 2));
     float* d = at<float>(ws, up256((size_t)3 * E * H * 2) + up256(2 * 4));
     MOE_CUDA(moe::launch_router_split(router_w, H, E, T, wt, seg, st), "router split launch");
+    const int S = router_ksplit(T, H, E, dev->sms);
     cudaError_t e = moe::launch_gemm_tc(MOE_GEMM_FC2, false, false, xhat, nullptr, wt, nullptr,
                                         seg, nullptr, nullptr, d, 1, H, H, 3 * E, T, T, dev->sms,
-                                        dev->status, st);
-    if (e == cudaSuccess) {
+                                        dev->status, st, nullptr, S);
+    if (e == cudaSuccess) {  // row t: S splits x (hi, mid, lo) x E partial logits
       *part = d;
-      *ks = 3;
+      *ks = 3 * S;
       *zstride = (size_t)E;
-      *tstride = (size_t)3 * E;
+      *tstride = (size_t)3 * E * S;
       return MOE_OK;
     }
     if (e != cudaErrorNotSupported) return cuda_fail(e, "router GEMM launch");

@@ -20,11 +20,15 @@ void engine_init_device();
 //          int that is zero when the kernel starts, from which the CTAs claim
 //          work units in order (so CTAs working on units that share a weight
 //          tile run close together in time and the tile is served by L2).
+//   ksplit token tiles, mode 2 only: split K into ksplit ranges, each unit
+//          once per range, split s writing fp32 columns s * N_out .. of rows
+//          N_out * ksplit wide (the caller sums the splits); at most the K
+//          stages (64 elements each).
 cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const float* a_scale,
                            const void* w, const float* w_scale, const int32_t* offsets,
                            const int32_t* row_src, const float* topk_w, void* c, int E, int K,
                            int I, int N_out, int R_max, int T, int sms, int* status,
-                           cudaStream_t st, int* sched = nullptr);
+                           cudaStream_t st, int* sched = nullptr, int ksplit = 1);
 
 // Decode FFN in one persistent launch: FC1 + silu_and_mul (xp -> act) and
 // FC2 + routing weight (act -> y, bf16 rows in (token, slot) order), with a

@@ -85,6 +85,10 @@ struct Params {
   int a_atom;   // bytes of one A atom (128 rows x 128 B)
   int b_atom;   // bytes of one B atom
   int njobs;    // 1, or 2 for FC1 -> FC2 in one launch
+  // Split-K (one job, fp32 rows): every unit is computed ksplit times, split
+  // s over K stages [s kst / ksplit, (s + 1) kst / ksplit), into output
+  // columns s * n_out ..; 1: no split.
+  int ksplit;
   // Dynamic scheduling (fused launch): sched[0] is the unit counter, sched[1 + e]
   // counts finished FC1 epilogue warps (bf16) or units (E4M3) of expert e, and
   // sched[1 + E + e] is set once expert e's FC1 rows are quantised (E4M3).
@@ -377,11 +381,12 @@ MOE_DEV void epilogue_tile(const Unit& un, const JobP& j, int I, uint32_t tbase,
 #pragma unroll
           for (int tt = 0; tt < 32; ++tt) v[tt] *= f;
         }
-        if (MODE == 2) {  // fp32 rows
+        if (MODE == 2) {  // fp32 rows (split s of a split-K launch: columns s * n_out ..)
           if (t.valid) {
-            float* dst = reinterpret_cast<float*>(j.out) + (size_t)t.r * j.ldo + n0;
+            const int c0 = un.split * j.n_out;
+            float* dst = reinterpret_cast<float*>(j.out) + (size_t)t.r * j.ldo + c0 + n0;
             // vector stores need a 16-byte row pitch (the router's 3E may not give one)
-            if (n0 + 32 <= j.n_out && (j.ldo & 3) == 0) {
+            if (n0 + 32 <= j.n_out && ((j.ldo | c0) & 3) == 0) {
 #pragma unroll
               for (int tt = 0; tt < 32; tt += 4)
                 reinterpret_cast<float4*>(dst)[tt / 4] =
@@ -797,7 +802,8 @@ __global__ void __launch_bounds__(WIDE ? kThreadsWide : kThreads, 1) moe_tc_gemm
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   const int U0 = s_up[0][p.E];
-  const int U = U0 + (NJ == 2 ? s_up[NJ - 1][p.E] : 0);
+  const int KS = (NJ == 1 && p.ksplit > 1) ? p.ksplit : 1;  // K splits
+  const int U = NJ == 2 ? U0 + s_up[NJ - 1][p.E] : U0 * KS;
 
   // token tiles: the token chunks of one weight tile are consecutive units,
   // so the CTAs that share the tile start it together
@@ -807,7 +813,20 @@ __global__ void __launch_bounds__(WIDE ? kThreadsWide : kThreads, 1) moe_tc_gemm
       un.job = 1;
       return un;
     }
+    if (KS > 1) {
+      const int sp = u / U0;
+      Unit un = unit_of(u - sp * U0, s_off, s_up[0], p.E, p.job[0].nt, p.chunk, !SWAP);
+      un.split = sp;
+      return un;
+    }
     return unit_of(u, s_off, s_up[0], p.E, p.job[0].nt, p.chunk, !SWAP);
+  };
+  // the unit's K stages [kb, ke)
+  auto k_begin = [&](const Unit& un, int kst) -> int {
+    return KS > 1 ? (int)(((int64_t)un.split * kst) / KS) : 0;
+  };
+  auto k_end = [&](const Unit& un, int kst) -> int {
+    return KS > 1 ? (int)(((int64_t)(un.split + 1) * kst) / KS) : kst;
   };
   // Consumers read claimed units in order from the unit ring.
   auto next_unit = [&](int i) -> int {
@@ -866,7 +885,8 @@ __global__ void __launch_bounds__(WIDE ? kThreadsWide : kThreads, 1) moe_tc_gemm
                                   : (uint32_t)((half2 ? 2 : 1) * kTileBytes + 2 * kTileBytes));
         const CUtensorMap* tw = un.job ? &tm_w1 : &tm_w0;
         const CUtensorMap* tx_map = un.job ? &tm_x1 : &tm_x0;
-        for (int ks = 0; ks < j.kst; ++ks) {
+        const int kb = k_begin(un, j.kst), ke = k_end(un, j.kst);
+        for (int ks = kb; ks < ke; ++ks) {
           if (!mbar_wait(&empty_bar[s], ph ^ 1, &s_abort)) { ok = false; break; }
           mbar_arrive_expect_tx(&full_bar[s], tx);
           uint8_t* a = ring + (size_t)s * p.stage_bytes;
@@ -911,13 +931,14 @@ __global__ void __launch_bounds__(WIDE ? kThreadsWide : kThreads, 1) moe_tc_gemm
         if (u < 0) break;
         const Unit un = decode_unit(u);
         const int kst = p.job[un.job].kst;
+        const int kb = k_begin(un, kst), ke = k_end(un, kst);
         if (!mbar_wait(&tempty_bar[acc], aph ^ 1, &s_abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + acc * kAccCols;
         const int n = SWAP ? ((un.rows + 15) / 16) * 16 : 256;
         const uint32_t idesc = make_idesc(n, FP8 ? 0u : 1u);
         const bool half2 = WIDE && un.rows > kTileRows;  // WIDE: rows 128..255 -> d + kAccCols
-        for (int ks = 0; ks < kst; ++ks) {
+        for (int ks = kb; ks < ke; ++ks) {
           if (!mbar_wait(&full_bar[s], ph, &s_abort)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a0 = smem_u32(ring + (size_t)s * p.stage_bytes);
@@ -928,7 +949,7 @@ __global__ void __launch_bounds__(WIDE ? kThreadsWide : kThreads, 1) moe_tc_gemm
             for (int kk = 0; kk < 4; ++kk) {  // four 32-byte K steps per 128-byte atom
               const uint64_t ad = sw128_desc(a + kk * 32);
               const uint64_t bd = sw128_desc(b + kk * 32);
-              const uint32_t accum = (ks | w | kk) ? 1u : 0u;
+              const uint32_t accum = ((ks - kb) | w | kk) ? 1u : 0u;
               if (FP8) mma_e4m3(d, ad, bd, idesc, accum);
               else mma_bf16(d, ad, bd, idesc, accum);
               if (half2) {
@@ -1235,10 +1256,11 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
                            const void* w, const float* w_scale, const int32_t* offsets,
                            const int32_t* row_src, const float* topk_w, void* c, int E, int K,
                            int I, int N_out, int R_max, int T, int sms, int* status,
-                           cudaStream_t st, int* sched) {
+                           cudaStream_t st, int* sched, int ksplit) {
   std::call_once(g_encode_once, load_encode);
   if (R_max == 0) return cudaSuccess;
   if (!g_encode || E > kMaxExperts) return cudaErrorNotSupported;
+  if (ksplit < 1 || (ksplit > 1 && (decode || mode != MOE_GEMM_FC2))) return cudaErrorNotSupported;
   // prefill tiles start only after their predecessor has completed
   PdlOff no_pdl(!decode);
   Params p{};
@@ -1247,6 +1269,7 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
   p.I = I;
   p.R_max = R_max;
   p.njobs = 1;
+  p.ksplit = 1;
   p.sched = decode ? nullptr : sched;  // one launch, one job: only the unit counter is used
   p.status = status;
   CUtensorMap maps[4];
@@ -1267,10 +1290,15 @@ cudaError_t launch_gemm_tc(int mode, bool fp8, bool decode, const void* a, const
   }
   size_t smem = 0;
   if (!set_ring(&p, decode, T, &smem, wide)) return cudaErrorNotSupported;
+  if (ksplit > 1) {
+    if (ksplit > p.job[0].kst) return cudaErrorNotSupported;  // every split has a K stage
+    p.ksplit = ksplit;
+    p.job[0].ldo = N_out * ksplit;
+  }
   p.job[1] = p.job[0];
   // upper bound on units: every expert's token chunks times the N tiles
   const int64_t chunks = (int64_t)(R_max + p.chunk - 1) / p.chunk + E;
-  const int64_t units = chunks * p.job[0].nt;
+  const int64_t units = chunks * p.job[0].nt * p.ksplit;
   int grid = (int)(units < sms ? units : sms);
   if (grid < 1) grid = 1;
   if (decode)

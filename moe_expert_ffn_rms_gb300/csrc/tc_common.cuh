@@ -16,6 +16,7 @@ using namespace ptx;
 
 struct Unit {
   int job, e, nt, row0, rows;
+  int split;  // K split of the unit (split-K launches; else 0)
 };
 
 // Unit u of a job: expert e has ceil(cnt/chunk) token chunks, each with nt N
@@ -41,6 +42,7 @@ MOE_DEV Unit unit_of(int u, const int* s_off, const int* s_up, int E, int nt, in
   }
   Unit un;
   un.job = 0;
+  un.split = 0;
   un.e = lo;
   un.nt = n;
   un.row0 = s_off[lo] + mt * chunk;
