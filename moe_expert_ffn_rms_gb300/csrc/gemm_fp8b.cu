@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
     }
     for (int q = 0; q < p.slots; ++q) {
       mbar_init(&kfull[q], 1);             // the MMA commit
-      mbar_init(&kempty[q], kEpiWarpsB);   // lane 0 of each epilogue warp
+      mbar_init(&kempty[q], kEpiWarpsB * 32);  // every thread of the epilogue warps
     }
     for (int i = 0; i < kRingB; ++i) {
       mbar_init(&ufull[i], 1);
@@ -333,29 +333,37 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
 
   if (warp == 0) {
     // ===================================================== TMA producer
-    if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
-      const uint64_t pol_x = l2_policy_evict_last();
-      int s = 0;
-      uint32_t ph = 0;
-      uint32_t armed = 0, armed_ph = 0;
-      bool ok = true;
-      for (int i = 0; ok; ++i) {
-        const int slot = i % kRingB;
-        if (!mbar_wait(&uempty[slot], (uint32_t)(((i / kRingB) & 1) ^ 1), &s_abort)) {
-          ok = false;
-          break;
-        }
-        int u = atomicAdd(p.sched, 1);
+    // The whole warp runs the loop and waits; lane 0 claims the units, waits
+    // for FC1's rows and issues the loads.
+    const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
+    const uint64_t pol_x = l2_policy_evict_last();
+    int s = 0;
+    uint32_t ph = 0;
+    uint32_t armed = 0, armed_ph = 0;
+    bool ok = true;
+    for (int i = 0; ok; ++i) {
+      const int slot = i % kRingB;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&uempty[slot], (uint32_t)(((i / kRingB) & 1) ^ 1), &s_abort))) {
+        ok = false;
+        break;
+      }
+      int u = 0;
+      if (lane == 0) {
+        u = atomicAdd(p.sched, 1);
         if (u >= U) u = -1;
         s_uring[slot] = u;
         mbar_arrive(&ufull[slot]);
-        if (u < 0) break;
-        const Unit un = decode_unit(u);
-        const BJob& j = p.job[un.job];
-        if (un.job == 1) {
-          // FC2 of expert e reads its FC1 rows: wait until every FC1 unit of
-          // e has been published (FC1 units are all claimed first)
+      }
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u < 0) break;
+      const Unit un = decode_unit(u);
+      const BJob& j = p.job[un.job];
+      if (un.job == 1) {
+        // FC2 of expert e reads its FC1 rows: wait until every FC1 unit of
+        // e has been published (FC1 units are all claimed first)
+        int fok = 1;
+        if (lane == 0) {
           const int cnt = s_off[un.e + 1] - s_off[un.e];
           const int need = ((cnt + p.chunk - 1) / p.chunk) * p.job[0].nt;
           const int* flag = p.sched + 1 + un.e;
@@ -363,26 +371,34 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
           while (ld_acquire(flag) < need) {
             if (s_abort || clock64() - t0 > kSpinLimitCycles) {
               s_abort = 1;
-              ok = false;
+              fok = 0;
               break;
             }
           }
-          if (!ok) break;
-          fence_proxy_async_global();
+          if (fok) fence_proxy_async_global();
         }
-        // B boxes: the smallest height of 2, 4, 8, 16 rows covering the unit
-        const int bi = un.rows > 8 ? 3 : (un.rows > 4 ? 2 : (un.rows > 2 ? 1 : 0));
-        const int brows = 2 << bi;
-        const int nb = bi == 3 ? (un.rows + kBoxRowsB - 1) / kBoxRowsB : 1;
-        const uint32_t tx = (uint32_t)(2 * kHalfBytes + nb * brows * 128);
-        const CUtensorMap* tw = un.job ? &tm_w1 : &tm_w0;
-        const CUtensorMap* tx_map = &bx.m[un.job][bi];
-        const int wrow = un.e * j.N_w;
-        // FC1: 128 gate rows and the matching 128 up rows; FC2: 256 rows
-        const int r0 = un.job == 0 ? wrow + un.nt * 128 : wrow + un.nt * 256;
-        const int r1 = un.job == 0 ? wrow + p.I + un.nt * 128 : r0 + 128;
-        for (int g = 0; g < j.kg; ++g) {
-          if (!mbar_wait_spin(&sempty[s], ph ^ 1, &s_abort)) { ok = false; break; }
+        if (!__shfl_sync(0xffffffffu, fok, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      // B boxes: the smallest height of 2, 4, 8, 16 rows covering the unit
+      const int bi = un.rows > 8 ? 3 : (un.rows > 4 ? 2 : (un.rows > 2 ? 1 : 0));
+      const int brows = 2 << bi;
+      const int nb = bi == 3 ? (un.rows + kBoxRowsB - 1) / kBoxRowsB : 1;
+      const uint32_t tx = (uint32_t)(2 * kHalfBytes + nb * brows * 128);
+      const CUtensorMap* tw = un.job ? &tm_w1 : &tm_w0;
+      const CUtensorMap* tx_map = &bx.m[un.job][bi];
+      const int wrow = un.e * j.N_w;
+      // FC1: 128 gate rows and the matching 128 up rows; FC2: 256 rows
+      const int r0 = un.job == 0 ? wrow + un.nt * 128 : wrow + un.nt * 256;
+      const int r1 = un.job == 0 ? wrow + p.I + un.nt * 128 : r0 + 128;
+      for (int g = 0; g < j.kg; ++g) {
+        if (!__all_sync(0xffffffffu, mbar_wait_spin(&sempty[s], ph ^ 1, &s_abort))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
           mbar_arrive_expect_tx(&sfull[s], tx);
           uint8_t* st = ring + (size_t)s * p.stage_bytes;
           tma_load_2d(st, tw, &sfull[s], g * kGroup, r0, pol_w);
@@ -390,40 +406,45 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
           for (int bb = 0; bb < nb; ++bb)
             tma_load_2d(st + 2 * kHalfBytes + bb * kBoxRowsB * 128, tx_map, &sfull[s], g * kGroup,
                         un.row0 + bb * kBoxRowsB, pol_x);
-          armed |= 1u << s;
-          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
-          if (++s == p.stages) { s = 0; ph ^= 1; }
         }
+        __syncwarp();
+        armed |= 1u << s;
+        armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+        if (++s == p.stages) { s = 0; ph ^= 1; }
       }
-      if (ok) ok = producer_tail(sempty, p.stages, s, ph, &s_abort);
-      if (!ok) {
-        flag_status(p.status, MOE_ERR_TIMEOUT);
-        drain_armed(sfull, p.stages, armed, armed_ph);
-      }
+    }
+    if (ok) ok = __all_sync(0xffffffffu, producer_tail(sempty, p.stages, s, ph, &s_abort));
+    if (!ok && lane == 0) {
+      flag_status(p.status, MOE_ERR_TIMEOUT);
+      drain_armed(sfull, p.stages, armed, armed_ph);
     }
   } else if (warp == 1) {
     // ====================================================== MMA issuer
-    if (lane == 0) {
-      int s = 0, q = 0;
-      uint32_t ph = 0, qph = 0;
-      bool ok = true, issued = false;
-      for (int i = 0; ok; ++i) {
-        const int u = next_unit(i);
-        if (u == -2) { ok = false; break; }
-        mbar_arrive(&uempty[i % kRingB]);
-        if (u < 0) break;
-        const Unit un = decode_unit(u);
-        const int kg = p.job[un.job].kg;
-        const uint32_t idesc = make_idesc(((un.rows + 15) / 16) * 16, 0u);  // E4M3 A and B
-        for (int g = 0; g < kg; ++g) {
-          if (!mbar_wait_spin(&sfull[s], ph, &s_abort) ||
-              !mbar_wait_spin(&kempty[q], qph ^ 1, &s_abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(ring + (size_t)s * p.stage_bytes);
-          const uint32_t b0 = a0 + 2 * kHalfBytes;
+    // The whole warp runs the loop and waits; one elected lane issues, so the
+    // descriptors and TMEM addresses stay warp-uniform (each group is eight
+    // small MMAs at decode's N, where a loop run by one divergent lane paid
+    // about 100 cycles per tcgen05 instruction).
+    int s = 0, q = 0;
+    uint32_t ph = 0, qph = 0;
+    bool ok = true, issued = false;
+    for (int i = 0; ok; ++i) {
+      const int u = __shfl_sync(0xffffffffu, next_unit(i), 0);  // every lane has read it
+      if (u == -2) { ok = false; break; }
+      if (lane == 0) mbar_arrive(&uempty[i % kRingB]);
+      if (u < 0) break;
+      const Unit un = decode_unit(u);
+      const int kg = p.job[un.job].kg;
+      const uint32_t idesc = make_idesc(((un.rows + 15) / 16) * 16, 0u);  // E4M3 A and B
+      for (int g = 0; g < kg; ++g) {
+        if (!__all_sync(0xffffffffu, mbar_wait_spin(&sfull[s], ph, &s_abort) &&
+                                         mbar_wait_spin(&kempty[q], qph ^ 1, &s_abort))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(ring + (size_t)s * p.stage_bytes);
+        const uint32_t b0 = a0 + 2 * kHalfBytes;
+        if (elect_one()) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint32_t d = tmem + q * p.slot_cols + h * p.chunk;
@@ -432,25 +453,30 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
               mma_e4m3(d, sw128_desc(a0 + h * kHalfBytes + kk * 32), sw128_desc(b0 + kk * 32), idesc,
                        kk ? 1u : 0u);
           }
-          issued = true;
           mma_commit(&sempty[s]);
           mma_commit(&kfull[q]);
-          if (++s == p.stages) { s = 0; ph ^= 1; }
-          if (++q == p.slots) { q = 0; qph ^= 1; }
         }
-      }
-      // tail: the epilogues have handed back every slot
-      for (int i = 0; ok && i < p.slots; ++i) {
-        ok = mbar_wait(&kempty[q], qph ^ 1, &s_abort);
+        __syncwarp();
+        issued = true;
+        if (++s == p.stages) { s = 0; ph ^= 1; }
         if (++q == p.slots) { q = 0; qph ^= 1; }
       }
-      if (!ok) flag_status(p.status, MOE_ERR_TIMEOUT);
-      if (issued) {  // all issued MMAs complete before TMEM is released
-        mma_commit(&drain_bar);
+    }
+    // tail: the epilogues have handed back every slot
+    for (int i = 0; ok && i < p.slots; ++i) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&kempty[q], qph ^ 1, &s_abort));
+      if (++q == p.slots) { q = 0; qph ^= 1; }
+    }
+    if (!ok && lane == 0) flag_status(p.status, MOE_ERR_TIMEOUT);
+    if (issued) {  // all issued MMAs complete before TMEM is released
+      if (elect_one()) mma_commit(&drain_bar);
+      __syncwarp();
+      if (lane == 0) {
         const long long t0 = clock64();
         while (!mbar_try_wait(&drain_bar, 0) && clock64() - t0 < kSpinLimitCycles) {
         }
       }
+      __syncwarp();
     }
   } else if (warp < 2 + kEpiWarpsB) {
     // ======================================================== epilogue
@@ -525,11 +551,12 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
       for (int g = 0; g < j.kg; ++g) {
         // a suspending wait: the epilogue has slack (the slot ring), while a
         // polling loop here would take issue slots from the TMA and MMA
-        // threads that share the SM's sub-partitions
-        int wok = 1;
-        if (lane == 0) wok = mbar_wait(&kfull[q], qph, &s_abort);
-        wok = __shfl_sync(0xffffffffu, wok, 0);
-        if (!wok) { ok = false; break; }
+        // threads that share the SM's sub-partitions.  Every lane waits and
+        // every lane arrives below: the group loop has no divergent branch.
+        if (!__all_sync(0xffffffffu, mbar_wait(&kfull[q], qph, &s_abort))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t ta = tmem + tlane + q * p.slot_cols;
         const float sw0 = s_ws[0][g], sw1 = s_ws[1][g];
@@ -556,8 +583,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) moe_tc_fp8b_kernel(
           }
         }
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&kempty[q]);
+        mbar_arrive(&kempty[q]);
         if (++q == p.slots) { q = 0; qph ^= 1; }
       }
       if (!ok) break;

@@ -670,25 +670,24 @@ __global__ void __launch_bounds__(kNvThreads, 1) moe_tc_nvfp4_kernel(
         }
         const uint8_t* st = ring + (size_t)s * p.stage_bytes + p.b_bytes;
         const uint2 scales = *reinterpret_cast<const uint2*>(st + s_off8);
+        uint32_t v[64];  // the warp's two atoms: 64 adjacent TMEM columns
 #pragma unroll
         for (int aa = 0; aa < 2; ++aa) {
-          const int a = 2 * half + aa;
           const uint32_t swa = aa ? scales.y : scales.x;
           const uint4 c0 = *reinterpret_cast<const uint4*>(st + (aa ? c_off2 : c_off0));
           const uint4 c1 = *reinterpret_cast<const uint4*>(st + (aa ? c_off3 : c_off1));
           const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           uint32_t bs[4];
           e4m3x4_to_h2(swa, bs);
-          uint32_t v[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {  // word c = elements 8c .. 8c + 7, block c / 2
             uint32_t o[4];
             e2m1x8_scaled(w[c], bs[c >> 1], o);
 #pragma unroll
-            for (int t = 0; t < 4; ++t) v[4 * c + t] = o[t];
+            for (int t = 0; t < 4; ++t) v[32 * aa + 4 * c + t] = o[t];
           }
-          tmem_st32(tmem + tlane + kACol0 + slot * kAColsPerStage + a * kAColsPerAtom, v);
         }
+        tmem_st64(tmem + tlane + kACol0 + slot * kAColsPerStage + 2 * half * kAColsPerAtom, v);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&afull[slot]);
