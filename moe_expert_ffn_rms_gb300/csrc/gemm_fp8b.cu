@@ -996,8 +996,12 @@ __global__ void __launch_bounds__(kThreadsT, 1) moe_tc_fp8b_tile_kernel(
         tc_fence_after();
         float v[64];
         const uint32_t ta = tmem + tlane + q * 128;
-        tmem_ld32(ta + c_lo, v);
-        tmem_ld32(ta + c_hi, v + 32);
+        if (MODE == 3) {  // FC2: the two runs are adjacent
+          tmem_ld64(ta + c_lo, v);
+        } else {
+          tmem_ld32(ta + c_lo, v);
+          tmem_ld32(ta + c_hi, v + 32);
+        }
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&kempty[q]);
