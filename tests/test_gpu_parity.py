@@ -150,7 +150,8 @@ def test_route_topk_given_logits_bit_exact(M, T, E, k):
 
 @pytest.mark.parametrize("tc", ["1", "0"])
 @pytest.mark.parametrize("cfg", ["c1_tiny", "c3_decode_skewed", "c5_prefill", "wide_prefill",
-                                 "small_uneven", "small_bias", "odd_e_prefill"])
+                                 "small_uneven", "small_bias", "odd_e_prefill", "split_k_uneven",
+                                 "split_k_odd_e"])
 def test_route_topk_router(M, cfg, tc):
     """Router logits from x_hat and W_r (tensor-core bf16x3 split for >= 256
     tokens unless MOE_ROUTER_TC=0; a one-CTA-per-token router fused with top-k
@@ -168,6 +169,12 @@ def test_route_topk_router(M, cfg, tc):
     elif cfg == "odd_e_prefill":  # tensor-core router with 3E = 21 logit columns (odd row pitch)
         inp = workloads.make_inputs("c1_tiny", DEV,
                                     shape=workloads.Shape(T=300, H=512, E=7, k=2, I=256))
+    elif cfg == "split_k_uneven":  # 25 K stages over 3 splits (8, 8, 9)
+        inp = workloads.make_inputs("c1_tiny", DEV,
+                                    shape=workloads.Shape(T=256, H=1600, E=24, k=2, I=256))
+    elif cfg == "split_k_odd_e":  # 4 splits of 3E = 21 columns: odd column offsets per split
+        inp = workloads.make_inputs("c1_tiny", DEV,
+                                    shape=workloads.Shape(T=400, H=2048, E=7, k=2, I=256))
     else:
         inp = workloads.make_inputs(cfg, DEV)
     T, H, E, k = inp["T"], inp["H"], inp["E"], inp["k"]
