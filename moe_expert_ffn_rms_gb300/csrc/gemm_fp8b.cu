@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "engine.h"
+#include "kernels.h"
 #include "tc_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -1117,9 +1118,9 @@ cudaError_t launch_rmsnorm_q128(const void* x, const void* w, int T, int H, floa
                                 uint8_t* yq, float* yscale, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   if (H % kGroup != 0) return cudaErrorInvalidValue;
-  const int nv = H / 8;
-  const int threads = nv >= 512 ? 512 : nv;  // nv is a multiple of 16
-  return launch_kernel(rmsnorm_q128_kernel, dim3(T), dim3(((threads + 31) / 32) * 32), 0, st,
+  // the rms_norm launch shape (a multiple of 32, so of 16 too)
+  const int threads = rmsnorm_threads(T, H / 8);
+  return launch_kernel(rmsnorm_q128_kernel, dim3(T), dim3(threads), 0, st,
                        (const bf16*)x, (const bf16*)w, H, eps, (bf16*)y, yq, yscale);
 }
 

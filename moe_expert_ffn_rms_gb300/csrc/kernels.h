@@ -10,6 +10,8 @@ namespace moe {
 // Router split-K: number of K chunks the router logits are split into.
 int route_splits(int T, int H, int E);
 
+// Threads per token row of the rms_norm launches (one CTA per token).
+int rmsnorm_threads(int T, int nv);
 cudaError_t launch_rmsnorm(const void* x, const void* w, int T, int H, float eps, void* y,
                            void* yq, float* yscale, cudaStream_t st);
 cudaError_t launch_router_logits(const void* xhat, const float* wr, int T, int H, int E, int ks,

@@ -96,11 +96,21 @@ __global__ void __launch_bounds__(512) rmsnorm_kernel(const bf16* __restrict__ x
   }
 }
 
+// Threads per token row (one CTA each).  Large batches: about four 16-byte
+// vectors per thread (128 threads at H = 4096), so an SM holds 16 tokens'
+// CTAs instead of 4 and overlaps their load -> reduce -> store chains
+// (prefill rms_norm 26 -> 19.5 us, with the E4M3 copy 41 -> 28 us).  Small
+// batches have fewer CTAs than SMs, where one vector per thread is faster.
+int rmsnorm_threads(int T, int nv) {
+  int threads = T >= 512 ? ((nv + 3) / 4 + 31) / 32 * 32 : ((nv + 31) / 32) * 32;
+  return threads < 32 ? 32 : (threads > 512 ? 512 : threads);
+}
+
 cudaError_t launch_rmsnorm(const void* x, const void* w, int T, int H, float eps, void* y,
                            void* yq, float* yscale, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  int nv = H / 8;
-  int threads = nv >= 512 ? 512 : ((nv + 31) / 32) * 32;
+  const int nv = H / 8;
+  int threads = rmsnorm_threads(T, nv);
   if (yq)
     return launch_kernel(rmsnorm_kernel<true>, dim3(T), dim3(threads), 0, st, (const bf16*)x,
                          (const bf16*)w, H, eps, (bf16*)y, (uint8_t*)yq, yscale);
