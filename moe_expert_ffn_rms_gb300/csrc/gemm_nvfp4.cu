@@ -140,8 +140,10 @@ __global__ void __launch_bounds__(256) gather_rows_f16_kernel(const int32_t* __r
 }
 
 // ------------------------------------------------------- fused FFN kernel --
-constexpr int kNvThreads = 512;   // warp 0 TMA, 1 MMA, 2-5 epilogue, 6-13 dequantise, 14-15 MMA
-constexpr int kMaxIssuersNv = 3;  // MMA threads: warp 1, then warps 14, 15
+constexpr int kNvThreads = 480;   // warp 0 TMA, 1 MMA, 2-5 epilogue, 6-13 dequantise, 14 MMA
+// MMA issuers: warp 1, then warp 14.  With the issue warp-uniform, a third
+// issuer (one more accumulator bank for the epilogue to add) was slower.
+constexpr int kMaxIssuersNv = 2;
 constexpr int kDqWarps = 8;       // two per TMEM lane quarter: each takes two of a stage's four atoms
 constexpr int kKStage = 256;      // K elements per stage: 128 B of codes, 16 B of scales per row
 constexpr int kRowsNv = 128;      // weight rows per unit (MMA M)
