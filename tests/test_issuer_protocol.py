@@ -272,7 +272,8 @@ def run_tiles(n_groups, ring_s, ring_q, ni, seed, max_delay=6):
     return True
 
 
-@pytest.mark.parametrize("ring_s,ring_q,ni", [(6, 4, 2), (6, 4, 1), (5, 3, 2), (4, 4, 4), (2, 2, 2)])
+@pytest.mark.parametrize("ring_s,ring_q,ni", [(6, 4, 2), (6, 4, 1), (6, 4, 3), (5, 3, 2), (4, 4, 4),
+                                              (2, 2, 2)])
 def test_tile_issuers_within_the_slot_count_never_misread(ring_s, ring_q, ni):
     # the kernel runs six stages, four slots and two issuers; it keeps both
     # rings even, which is enough, though ni <= both ring lengths already is
