@@ -74,9 +74,12 @@ MOE_DEV float silu_f(float z) { return z / (1.0f + expf(-z)); }
 // finite logit, ties to the lower index as usual), so each of the k slots
 // always receives a distinct expert in [0, E) (k <= E); when every selected
 // logit is -inf the softmax is undefined and the token's weights are 0.
+// PER values per lane (PER >= ceil(E / 32); a kernel instance for the
+// smallest PER that holds E keeps the scans short), at most kTopkPer.
 constexpr int kTopkPer = kMaxExperts / 32;
 
-MOE_DEV void warp_topk(const float (&v)[kTopkPer], int E, int k, int lane, int32_t* ids,
+template <int PER>
+MOE_DEV void warp_topk(const float (&v)[PER], int E, int k, int lane, int32_t* ids,
                        float* w) {
   unsigned taken = 0;
   float sel_v[kMaxTopK];
@@ -87,7 +90,7 @@ MOE_DEV void warp_topk(const float (&v)[kTopkPer], int E, int k, int lane, int32
     float bv = -INFINITY;
     int be = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < kTopkPer; ++i) {
+    for (int i = 0; i < PER; ++i) {
       const int e = lane + 32 * i;
       const float vi = (v[i] != v[i]) ? -INFINITY : v[i];  // NaN ranks as -inf
       if (e < E && !(taken & (1u << i)) && (vi > bv || (vi == bv && e < be))) {

@@ -267,6 +267,7 @@ cudaError_t launch_router_logits(const void* xhat, const float* wr, int T, int H
 
 // ==================================================== softmax / top-k / renorm
 // One warp per token.  Logit of expert e = sum_z part[z, t, e] (+ bias[e]).
+template <int PER>
 __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ part, int ks,
                                                    size_t zstride, size_t tstride,
                                                    const float* __restrict__ bias, int T, int E,
@@ -278,37 +279,38 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
-  float v[kTopkPer];
+  float v[PER];
 #pragma unroll
-  for (int i = 0; i < kTopkPer; ++i) v[i] = 0.f;
-  // Partial sums: four chunks are loaded before they are added (4 x
-  // kTopkPer loads in flight per lane); each logit is still summed in z order.
+  for (int i = 0; i < PER; ++i) v[i] = 0.f;
+  // Partial sums: four chunks are loaded before they are added (4 x PER
+  // loads in flight per lane, PER = ceil(E / 32) values of each logit row
+  // per lane); each logit is still summed in z order.
   const float* pt = part + (size_t)t * tstride;
   int z = 0;
   for (; z + 4 <= ks; z += 4) {
-    float l[4][kTopkPer];
+    float l[4][PER];
 #pragma unroll
     for (int zz = 0; zz < 4; ++zz)
 #pragma unroll
-      for (int i = 0; i < kTopkPer; ++i) {
+      for (int i = 0; i < PER; ++i) {
         const int e = lane + 32 * i;
         l[zz][i] = e < E ? pt[(size_t)(z + zz) * zstride + e] : 0.f;
       }
 #pragma unroll
     for (int zz = 0; zz < 4; ++zz)
 #pragma unroll
-      for (int i = 0; i < kTopkPer; ++i)
+      for (int i = 0; i < PER; ++i)
         if (lane + 32 * i < E) v[i] += l[zz][i];
   }
   for (; z < ks; ++z) {
 #pragma unroll
-    for (int i = 0; i < kTopkPer; ++i) {
+    for (int i = 0; i < PER; ++i) {
       const int e = lane + 32 * i;
       if (e < E) v[i] += pt[(size_t)z * zstride + e];
     }
   }
 #pragma unroll
-  for (int i = 0; i < kTopkPer; ++i) {
+  for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
       if (bias) v[i] += bias[e];
@@ -328,6 +330,7 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ par
 constexpr int kRouteSmallMaxHE = 65536;
 constexpr int kRouteSmallMaxH = 8192;
 
+template <int PER>
 __global__ void __launch_bounds__(256) route_small_kernel(const bf16* __restrict__ xhat,
                                                           const float* __restrict__ wr,
                                                           const float* __restrict__ bias, int T,
@@ -367,9 +370,9 @@ __global__ void __launch_bounds__(256) route_small_kernel(const bf16* __restrict
   }
   __syncthreads();
   if (tid < 32) {
-    float v[kTopkPer];
+    float v[PER];
 #pragma unroll
-    for (int i = 0; i < kTopkPer; ++i) {
+    for (int i = 0; i < PER; ++i) {
       const int ex = tid + 32 * i;
       v[i] = ex < E ? lg[ex] : -FLT_MAX;
     }
@@ -386,8 +389,15 @@ cudaError_t launch_route_small(const void* xhat, const float* wr, const float* b
                                cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   if (!route_small(H, E)) return cudaErrorInvalidValue;
-  return launch_kernel(route_small_kernel, dim3(T), dim3(256), 0, st, (const bf16*)xhat, wr, bias,
-                       T, H, E, k, ids, w, logits_out);
+  // the selection scans ceil(E / 32) values per lane (1, 2, 4 or 8)
+  auto go = [&](auto kern) {
+    return launch_kernel(kern, dim3(T), dim3(256), 0, st, (const bf16*)xhat, wr, bias, T, H, E, k,
+                         ids, w, logits_out);
+  };
+  if (E <= 32) return go(route_small_kernel<1>);
+  if (E <= 64) return go(route_small_kernel<2>);
+  if (E <= 128) return go(route_small_kernel<4>);
+  return go(route_small_kernel<kTopkPer>);
 }
 
 cudaError_t launch_topk(const float* part, int ks, const float* bias, int T, int E, int k,
@@ -396,8 +406,15 @@ cudaError_t launch_topk(const float* part, int ks, const float* bias, int T, int
   if (T == 0) return cudaSuccess;
   if (zstride == 0) zstride = (size_t)T * E;  // default: part[z][t][e]
   if (tstride == 0) tstride = (size_t)E;
-  return launch_kernel(topk_kernel, dim3((T + 3) / 4), dim3(128), 0, st, part, ks, zstride, tstride,
-                       bias, T, E, k, ids, w, logits_out);
+  // the selection scans ceil(E / 32) values per lane (1, 2, 4 or 8)
+  auto go = [&](auto kern) {
+    return launch_kernel(kern, dim3((T + 3) / 4), dim3(128), 0, st, part, ks, zstride, tstride,
+                         bias, T, E, k, ids, w, logits_out);
+  };
+  if (E <= 32) return go(topk_kernel<1>);
+  if (E <= 64) return go(topk_kernel<2>);
+  if (E <= 128) return go(topk_kernel<4>);
+  return go(topk_kernel<kTopkPer>);
 }
 
 // Router weights for the tensor-core router: W_r fp32 [H, E] -> three bf16
