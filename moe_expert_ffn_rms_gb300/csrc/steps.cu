@@ -696,37 +696,49 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restr
                                                           const uint4* __restrict__ src,
                                                           uint4* __restrict__ dst, int row_vec,
                                                           const float* __restrict__ sscale,
-                                                          float* __restrict__ dscale, int scols) {
+                                                          float* __restrict__ dscale, int scols,
+                                                          int parts) {
   pdl_trigger();
   pdl_wait();
   const int R = min(offsets[E], R_max);
   const int warps = blockDim.x >> 5, lane = threadIdx.x & 31;
-  for (int r = blockIdx.x * warps + (threadIdx.x >> 5); r < R; r += gridDim.x * warps) {
+  const int per = (row_vec + parts - 1) / parts;  // 16-byte vectors of one part of a row
+  const int64_t n = (int64_t)R * parts;
+  for (int64_t wi = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); wi < n;
+       wi += (int64_t)gridDim.x * warps) {
+    const int r = (int)(wi / parts), part = (int)(wi % parts);
     const int t = row_src[r] / k;
     const uint4* s = src + (size_t)t * row_vec;
     uint4* d = dst + (size_t)r * row_vec;
-    int v = lane;
-    for (; v + 96 < row_vec; v += 128) {  // four 16-byte loads in flight per lane
+    const int v1 = min(row_vec, (part + 1) * per);
+    int v = part * per + lane;
+    for (; v + 96 < v1; v += 128) {  // four 16-byte loads in flight per lane
       const uint4 a = s[v], b = s[v + 32], c = s[v + 64], e4 = s[v + 96];
       d[v] = a;
       d[v + 32] = b;
       d[v + 64] = c;
       d[v + 96] = e4;
     }
-    for (; v < row_vec; v += 32) d[v] = s[v];
-    if (dscale)
+    for (; v < v1; v += 32) d[v] = s[v];
+    if (dscale && part == 0)
       for (int c = lane; c < scols; c += 32) dscale[(size_t)r * scols + c] = sscale[(size_t)t * scols + c];
   }
 }
 
+// Small batches (decode: R <= 2048 rows) split each row over four warps, so a
+// row's loads go out in one round instead of four (the kernel sits between
+// the permute and the FFN on the decode chain); large batches keep one warp
+// per row.
 cudaError_t launch_gather_rows(const int32_t* offsets, int E, const int32_t* row_src, int k,
                                int R_max, const void* src, void* dst, int row_bytes,
                                const float* sscale, float* dscale, cudaStream_t st, int scols) {
   if (R_max == 0) return cudaSuccess;
-  int blocks = (R_max + 7) / 8;
+  const int parts = R_max <= 2048 ? 4 : 1;
+  int64_t blocks = ((int64_t)R_max * parts + 7) / 8;
   if (blocks > 152 * 8) blocks = 152 * 8;
-  return launch_kernel(gather_rows_kernel, dim3(blocks), dim3(256), 0, st, offsets, E, row_src, k,
-                       R_max, (const uint4*)src, (uint4*)dst, row_bytes / 16, sscale, dscale, scols);
+  return launch_kernel(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, offsets, E,
+                       row_src, k, R_max, (const uint4*)src, (uint4*)dst, row_bytes / 16, sscale,
+                       dscale, scols, parts);
 }
 
 // ================================================================ silu_and_mul
